@@ -1,0 +1,50 @@
+"""Plant one plausible mistake at a time in a copy of the oracle (on the CPU)
+and check that the pins in test_oracle_pins.py catch every one of them."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.py")
+
+# (name, original text, planted mistake)
+MUTATIONS = [
+    ("dropped bias term", "return s * q + b", "return s * q"),
+    ("nibble order", "out[..., 0::2] = packed & 0x0F", "out[..., 0::2] = packed >> 4"),
+    ("group index", "s = np.repeat(np.asarray(scale).astype(F64), group, axis=-1)",
+     "s = np.tile(np.asarray(scale).astype(F64), group)"),
+    ("router bias sign", "lg = lg + np.asarray(logit_bias, F64)[None, :]",
+     "lg = lg - np.asarray(logit_bias, F64)[None, :]"),
+    ("tie-break", "order = np.lexsort((ids, -lg), axis=-1)",
+     "order = np.lexsort((-ids, -lg), axis=-1)"),
+    ("softmax sign", "ex = np.exp(top - m)", "ex = np.exp(m - top)"),
+    ("renormalisation axis", "w = ex / ex.sum(axis=1, keepdims=True)", "w = ex / ex.sum()"),
+    ("gate/up roles", "return (silu(g) * u) @ w_down.T", "return (silu(u) * g) @ w_down.T"),
+    ("transposed down", "return (silu(g) * u) @ w_down.T", "return (silu(g) * u) @ w_down"),
+    ("silu sign", "return z * expit(z)", "return z * expit(-z)"),
+    ("gate/up halves", "return wgu[:I], wgu[I:],", "return wgu[I:], wgu[:I],"),
+    ("shared gate sign", "return expit(np.asarray(x, F64) @ np.asarray(w_shared_gate, F64))",
+     "return expit(-(np.asarray(x, F64) @ np.asarray(w_shared_gate, F64)))"),
+    ("slot index", "out += w[:, j:j + 1] * y[:, j]", "out += w[:, j:j + 1] * y[:, 0]"),
+    ("dropped shared term", "out += sigma[:, None] * swiglu_expert(x, wg, wu, wd)",
+     "out += 0.0 * swiglu_expert(x, wg, wu, wd)"),
+    ("perm index", "perm = (order // k).astype(np.int32)", "perm = (order % k).astype(np.int32)"),
+    ("offsets shift", "offsets[1:] = np.cumsum(counts)", "offsets[:-1] = np.cumsum(counts)"),
+    ("rms of v, not v^2", "np.mean(v * v, axis=-1, keepdims=True)", "np.mean(v, axis=-1, keepdims=True)"),
+]
+
+
+@pytest.mark.parametrize("name,orig,bad", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(name, orig, bad, tmp_path):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor not found once: {orig!r}"
+    mutant = tmp_path / "moe_oracle_mutant.py"
+    mutant.write_text(src.replace(orig, bad))
+    env = dict(os.environ, MOE_ORACLE_FILE=str(mutant))
+    r = subprocess.run(
+        [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"no pin caught the planted mistake '{name}'"
