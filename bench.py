@@ -1,0 +1,447 @@
+"""Benchmark of the sparse 4-bit MoE block on GB300.
+
+Default workload (one JSON line on rank 0): the Qwen-shaped 40-layer batch-1
+decode chain (d=2048, E=256, top-8, I=512, one sigmoid-gated shared expert,
+4-bit group-64 weights, RMS normalisation between layers).  One step = one
+token through all 40 layers (one kernel launch).  The same line carries the
+single-layer prefill case (T=4096 tokens, Zipf-skewed routing) under
+"prefill".  ``--workload prefill`` makes the prefill case the headline.
+
+Synthetic seeded inputs (synth/), random-init weights of that architecture.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (host cores).  Under torchrun every rank runs an independent
+replica (the path shards into independent batches; no collective on the data
+path); value = units of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+# workload constants
+D, E, K, I = 2048, 256, 8, 512
+DECODE_LAYERS = 40
+PREFILL_T = 4096
+EXPERT_BYTES = 1769472          # 4.5-bit gate/up + down of one expert (codes + fp16 s, beta)
+ROUTER_BYTES = E * D * 2
+LAYER_BYTES_DECODE = 9 * EXPERT_BYTES + ROUTER_BYTES + D * 2 + 2 * D * 2   # 16,986,112
+FLOP_PER_TOKEN = 2 * D * E + K * (2 * D * 2 * I + 2 * I * D) + (2 * D * 2 * I + 2 * I * D) + 2 * D
+GATEUP_FLOP_PER_ROW = 2 * D * 2 * I
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ ranks
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_info()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def l2_flush_buffer(torch, device):
+    return torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+
+def build_decode(torch, M, sd, gen, device):
+    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
+    layers = []
+    for l in range(DECODE_LAYERS):
+        w = sd.make_layer(0, l, shape, device=device)
+        layers.append(M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=1,
+                                        layouts=M.MOE_LAYOUT_DECODE), w))
+        del w
+    torch.cuda.empty_cache()
+    return layers
+
+
+def run_decode(args, torch, M, sd, gen, device, peaks):
+    layers = build_decode(torch, M, sd, gen, device)
+    nx = max(args.steps + args.warmup, 8)
+    xs = sd.make_x(1, nx, D, device=device)  # a different token every step
+    y = torch.empty(D, dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream(device)
+    for i in range(args.warmup):
+        M.decode(layers, xs[i % nx])
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clk = ClockSampler(device.index)
+    clk.start()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        M.decode(layers, xs[(args.warmup + i) % nx])
+        ends[i].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clocks = clk.stop()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_step = t_all0.elapsed_time(t_all1) / args.steps
+    ms_step = max_over_ranks(ms_step, device)
+    kernel_ms = statistics.mean(per)
+    bytes_launch = LAYER_BYTES_DECODE * DECODE_LAYERS
+    achieved = bytes_launch / (kernel_ms * 1e-3) / 1e9
+    # end to end through the C ABI with host buffers
+    xh = xs[:args.steps].cpu().pin_memory()
+    yh = torch.empty(D, dtype=torch.bfloat16).pin_memory()
+    for i in range(min(3, args.steps)):
+        M.decode_host(layers, xh[i], yh)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        M.decode_host(layers, xh[i], yh)
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_s = max_over_ranks(e2e_s, device)
+    err = layers[0].device_error()
+    return dict(
+        ms_per_step=ms_step, value=args.world * 1000.0 / ms_step, unit="tokens/s",
+        us_per_layer=ms_step * 1000.0 / DECODE_LAYERS,
+        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                  "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                  "traffic": None, "kernel": "decode_kernel",
+                  "algorithmic_bytes_per_launch": bytes_launch},
+        e2e={"value": args.world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": D * 2,
+             "d2h_bytes_per_step": D * 2},
+        gpu_launches=args.steps, clocks=clocks, device_error=err)
+
+
+def run_prefill(args, torch, M, sd, gen, device, peaks):
+    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
+    w = sd.make_layer(0, 0, shape, device=device)
+    layer = M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=PREFILL_T,
+                              layouts=M.MOE_LAYOUT_PREFILL), w)
+    del w
+    torch.cuda.empty_cache()
+    x = sd.make_x(0, PREFILL_T, D, device=device)
+    bias = torch.from_numpy(gen.zipf_bias(0, E)).to(device)
+    y = torch.empty_like(x)
+    flush = l2_flush_buffer(torch, device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        layer.forward(x, bias, out=y)
+    torch.cuda.synchronize(device)
+    layer.profile(True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clk = ClockSampler(device.index)
+    clk.start()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        starts[i].record(stream)
+        layer.forward(x, bias, out=y)
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clocks = clk.stop()
+    stages, calls = layer.profile_read()
+    layer.profile(False)
+    ms_step = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms_step = max_over_ranks(ms_step, device)
+    r = layer.route(x, bias)
+    counts = r["counts"].cpu()
+    rows = PREFILL_T * K + PREFILL_T
+    gu_ms = stages["gate_up"] / max(calls, 1)
+    gu_tflops = rows * GATEUP_FLOP_PER_ROW / (gu_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    total_flop = FLOP_PER_TOKEN * PREFILL_T
+    # end to end through the C ABI with host buffers
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    bh = bias.cpu().pin_memory()
+    layer.forward_host(xh, bh, yh)
+    t0 = time.perf_counter()
+    n_e2e = max(3, min(args.steps, 20))
+    for _ in range(n_e2e):
+        layer.forward_host(xh, bh, yh)
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    e2e_s = max_over_ranks(e2e_s, device)
+    err = layer.device_error()
+    return dict(
+        ms_per_step=ms_step, value=args.world * PREFILL_T * 1000.0 / ms_step, unit="tokens/s",
+        us_per_layer=ms_step * 1000.0,
+        stage_ms={k: round(v / max(calls, 1), 4) for k, v in stages.items()},
+        roofline={"bound": "tensor", "achieved": round(gu_tflops, 1), "peak": peak,
+                  "unit": "TFLOP/s", "frac": round(gu_tflops / peak, 4), "traffic": None,
+                  "kernel": "grouped_mma_kernel<gate/up>",
+                  "algorithmic_flop_per_launch": rows * GATEUP_FLOP_PER_ROW},
+        step_roofline_frac=round((total_flop / (peak * 1e12)) / (ms_step * 1e-3), 4),
+        experts_touched=int((counts > 0).sum()), max_expert_rows=int(counts.max()),
+        e2e={"value": args.world * PREFILL_T / e2e_s, "unit": "tokens/s",
+             "h2d_bytes_per_step": PREFILL_T * D * 2 + E * 4,
+             "d2h_bytes_per_step": PREFILL_T * D * 2},
+        gpu_launches=7 * args.steps, clocks=clocks, device_error=err)
+
+
+# ------------------------------------------------------------------ oracle arm
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def oracle_decode_sample(n_layers=2):
+    """fp64 oracle on the first n_layers of the decode chain (weights made
+    outside the timed region); returns (seconds, layers)."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    from synth import gen
+    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
+    x = O.bf16_values(gen.make_x(1, 1, D))
+    total = 0.0
+    for l in range(n_layers):
+        wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, l, 0, E, D, 0.02))
+        wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, l, 0, 1, D, 0.02)[0])
+        lg = O.router_logits(x, wr)
+        idx, _ = O.select_top_k(lg, K)
+        cache = {e: gen.expert_weights(0, l, e, shape) for e in list(idx[0]) + [E]}
+        vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr, w_shared_gate=wsg,
+                    experts=None, shared=None)
+        t0 = time.perf_counter()
+        out = O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"]
+        x = O.rms_norm(out)
+        total += time.perf_counter() - t0
+    return total, n_layers
+
+
+def oracle_prefill_sample(n_tok=256):
+    """fp64 oracle on n_tok tokens of the prefill workload (weights of the
+    experts they touch made outside the timed region)."""
+    from oracle import moe_oracle as O
+    from synth import gen
+    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
+    xb = gen.make_x(0, n_tok, D)
+    x = O.bf16_values(xb)
+    wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, 0, 0, E, D, 0.02))
+    wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, 0, 0, 1, D, 0.02)[0])
+    bias = gen.zipf_bias(0, E)
+    idx, _ = O.select_top_k(O.router_logits(x, wr, bias), K)
+    import numpy as np
+    cache = {int(e): gen.expert_weights(0, 0, int(e), shape) for e in np.unique(idx)}
+    cache[E] = gen.expert_weights(0, 0, E, shape)
+    vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr, w_shared_gate=wsg,
+                experts=None, shared=None)
+    t0 = time.perf_counter()
+    O.moe_layer(x, vals, logit_bias=bias, expert_source=lambda e: cache[e])
+    return time.perf_counter() - t0, n_tok
+
+
+def cpu_baseline(workload):
+    if workload == "decode":
+        sec, nl = oracle_decode_sample(2)
+        tok_s = 1.0 / (sec / nl * DECODE_LAYERS)
+        sample = f"fp64 oracle, layers 0-{nl - 1} of the 40-layer decode chain, scaled to 40 layers"
+    else:
+        sec, nt = oracle_prefill_sample(256)
+        tok_s = nt / sec
+        sample = f"fp64 oracle, {nt} tokens of the T=4096 Zipf prefill layer (dequantisation of touched experts included)"
+    return {"value": tok_s, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": sample}
+
+
+# ------------------------------------------------------------------ main
+def config_for(workload):
+    if workload == "decode":
+        return {"workload": "qwen-shaped MoE decode chain: 40 layers, T=1, d=2048, E=256, "
+                            "top-8, I=512 + shared expert, 4-bit g64",
+                "layers": DECODE_LAYERS, "tokens_per_step": 1,
+                "l2": "inputs larger than L2 (679 MB of weights read per step, a new token each step)"}
+    return {"workload": "qwen-shaped MoE prefill layer: T=4096, Zipf-skewed routing "
+                        "(b_e = 1.5 ln(1/rank_e)), d=2048, E=256, top-8, I=512 + shared, 4-bit g64",
+            "tokens_per_step": PREFILL_T, "l2": "flushed between timed steps (256 MB write)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
+    args = ap.parse_args()
+    ws, rank, local = dist_info()
+    args.world = ws
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cb = cpu_baseline(args.workload)
+        steps = []
+        for _ in range(args.steps):
+            steps.append(cpu_baseline(args.workload)["value"])
+        v = statistics.median(steps) if steps else cb["value"]
+        line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": v,
+                "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "higher_is_better": True, "dtype": "f64", "data": "synthetic",
+                "config": config_for(args.workload),
+                "cpu_baseline": dict(cb, value=v),
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import sparse_moe_bit_gb300 as M
+    from synth import device as sd
+    from synth import gen
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist("nccl")
+    peaks, peak_src = load_peaks()
+    primary = args.workload
+    secondary = None if args.no_secondary else ("prefill" if primary == "decode" else "decode")
+    runner = {"decode": run_decode, "prefill": run_prefill}
+    res = runner[primary](args, torch, M, sd, gen, device, peaks)
+    sec = runner[secondary](args, torch, M, sd, gen, device, peaks) if secondary else None
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "MoE-layer tokens/s (prefill T=4096; decode T=1) and % of HBM/tensor roofline",
+        "value": res["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+        "us_per_layer": res["us_per_layer"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16-operands/fp32-accumulate (prefill), fp32 CUDA-core (decode)",
+        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "config": dict(config_for(primary), parallelism=f"replicas x{ws}"),
+        "roofline": dict(res["roofline"], peak_source=peak_src),
+        "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+        "device_error": res["device_error"],
+    }
+    for key in ("stage_ms", "step_roofline_frac", "experts_touched", "max_expert_rows"):
+        if key in res:
+            line[key] = res[key]
+    if sec is not None:
+        line[secondary] = {k: sec[k] for k in ("value", "unit", "ms_per_step", "us_per_layer",
+                                               "roofline", "e2e", "gpu_launches")
+                           if k in sec}
+        for key in ("stage_ms", "step_roofline_frac", "experts_touched", "max_expert_rows"):
+            if key in sec:
+                line[secondary][key] = sec[key]
+    if ws == 1:
+        try:
+            line["cpu_baseline"] = cpu_baseline(primary)
+        except Exception as ex:  # the baseline is informative; never fail the bench on it
+            line["cpu_baseline"] = {"error": str(ex)}
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

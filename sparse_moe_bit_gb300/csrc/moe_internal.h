@@ -1,0 +1,125 @@
+// Internal structures shared by the translation units of libmoe.so.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 512;
+constexpr int kMaxK = 16;
+constexpr int kTokPerBlock = 64;  // tokens per block of the routing kernels
+constexpr int kTileRows = 256;    // largest token tile of the grouped GEMMs
+constexpr int kUnitRows = 256;    // weight rows per tensor-core work unit (2 x M=128)
+constexpr int kCodeChunk = 9216;  // 256 rows x (32 B codes + 4 B scale/bias)
+constexpr int kRouterChunk = 32768;  // 256 rows x 64 bf16, pre-swizzled
+
+// Per-handle scratch, sized for cfg.max_tokens tokens.
+struct Workspace {
+  int Tmax = 0;
+  size_t part_elems = 0;     // capacity of logit_part (floats)
+  float* logit_part = nullptr;  // router partial sums [KS][T][E]
+  float* logits = nullptr;      // [Tmax][E] final logits (bias included)
+  int32_t* idx = nullptr;       // [Tmax][k]
+  float* w = nullptr;           // [Tmax][k]
+  float* sigma = nullptr;       // [Tmax]
+  uint16_t* x16 = nullptr;      // [Tmax][d] fp16 copy of the activations
+  int32_t* hist = nullptr;      // [nblk][E]
+  int32_t* base = nullptr;      // [nblk][E]
+  int32_t* counts = nullptr;    // [E]
+  int32_t* offsets = nullptr;   // [E+1]
+  int32_t* perm = nullptr;      // [Tmax*(k+1)] grouped row -> token
+  int32_t* slot = nullptr;      // [Tmax][k]
+  int32_t* dst = nullptr;       // [Tmax*(k+1)] grouped row -> contribution row
+  float* wrow = nullptr;        // [Tmax*(k+1)] grouped row -> routing weight
+  int4* tiles = nullptr;        // [max_tiles] {expert, row0, nrows, npad}
+  int32_t* ntiles = nullptr;    // [1]
+  uint16_t* H = nullptr;        // [Tmax*(k+1)][I] fp16 SwiGLU activations
+  uint16_t* Y = nullptr;        // [Tmax*(k+1)][d] bf16 weighted contributions
+  int max_tiles = 0;
+  // staging for moe_forward_host
+  void* x_dev = nullptr;
+  void* y_dev = nullptr;
+  float* bias_dev = nullptr;
+};
+
+struct Handle {
+  moe_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int layouts = 0;
+  int n_exp = 0;  // E + has_shared (experts stored in the repacked arrays)
+  // prefill layouts (tensor-core path)
+  uint8_t* pf_gu = nullptr;      // [n_exp][I/128][d/64][kCodeChunk]
+  uint8_t* pf_dn = nullptr;      // [n_exp][d/256][I/64][kCodeChunk]
+  uint8_t* pf_router = nullptr;  // [ceil(E/256)][d/64][kRouterChunk]
+  // decode layouts (bandwidth path)
+  uint8_t* dc_gu = nullptr;      // [n_exp][I][2 rows][d/2 codes + d/64*4 s,b]
+  uint8_t* dc_dn = nullptr;      // [n_exp][d][I/2 codes + I/64*4 s,b]
+  uint16_t* dc_router_t = nullptr;  // bf16 [d][E] (transposed router)
+  uint16_t* w_router = nullptr;  // bf16 [E][d]
+  uint16_t* w_sg = nullptr;      // bf16 [d]
+  Workspace ws;
+  // per-stage timing (moe_profile_enable)
+  static constexpr int kStagesTimed = 7;
+  static constexpr int kProfCalls = 4096;
+  bool prof = false;
+  int prof_calls = 0;
+  cudaEvent_t* prof_ev = nullptr;  // [kProfCalls][kStagesTimed + 1]
+  int* dev_err = nullptr;
+  cudaStream_t last_stream = nullptr;
+};
+
+// ---- grouped tensor-core GEMM (grouped_mma.cu)
+enum MmaMode { MMA_ROUTER = 0, MMA_GATEUP = 1, MMA_DOWN = 2 };
+
+struct MmaParams {
+  int kb_per_unit;      // 64-wide K blocks per work unit
+  int m_units;          // 256-row weight units per tile
+  int units_per_tile;   // m_units * ksplit
+  int nunits_host;      // router only: total units
+  const int4* tiles;    // grouped modes: device tile list
+  const int32_t* ntiles_dev;
+  int router_n;         // router: tokens per tile
+  int rows_total;       // router: T
+  // A operand
+  const uint8_t* wA;
+  long long a_expert_stride;  // bytes per expert
+  long long a_unit_stride;    // bytes per 256-row unit
+  int a_chunk;                // bytes per K block
+  // B operand: 16-bit rows
+  const uint16_t* B;
+  int ldb;
+  const int32_t* b_rowmap;    // grouped row -> source row, or null
+  // epilogue
+  float* out_f32;             // router partials [KS][T][E]
+  int E;
+  uint16_t* H;
+  int ldh;
+  uint16_t* Y;
+  int ldy;
+  const int32_t* dst_row;
+  const float* row_scale;
+  int* err;
+};
+cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st);
+
+// ---- routing (routing.cu)
+cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
+                        const uint16_t* x, cudaStream_t st);
+cudaError_t launch_scan_tiles(const Handle* h, int T, cudaStream_t st);
+cudaError_t launch_scatter(const Handle* h, int T, cudaStream_t st);
+cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st);
+
+// ---- repack (repack.cu)
+cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st);
+
+// ---- decode (decode.cu)
+cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const float* bias,
+                          float eps, uint16_t* y, const moe_decode_trace* trace,
+                          cudaStream_t st);
+size_t decode_scratch_bytes(const Handle* h, int L);
+
+}  // namespace moe

@@ -1,0 +1,200 @@
+// One-time repacking of the canonical weights (moe_create) into the layouts
+// the kernels read.
+//
+// Prefill (tensor-core) layout: for every expert x, 256-row unit m and
+// 64-wide K block kb, one contiguous chunk of kCodeChunk bytes that a single
+// bulk copy brings into shared memory:
+//   bytes [0, 8192)     : 256 rows x 8 words of codes; in each 32-bit word the
+//                         code of K index 2j sits at bits 4j..4j+3 and the
+//                         code of K index 2j+1 at bits 16+4j..16+4j+3 (so the
+//                         pair (2j, 2j+1) comes out of one shift and mask as
+//                         the two halves of an fp16x2)
+//   bytes [8192, 9216)  : 256 rows x (scale fp16 | bias fp16 << 16)
+// Gate/up unit m holds gate rows m*128..m*128+127 then up rows of the same
+// features; down unit m holds output rows m*256..m*256+255.
+// Router prefill layout: unit m (experts m*256..m*256+255, zero rows past E),
+// block kb: two 128 x 64 bf16 tiles in the 128-byte swizzled K-major order of
+// the tensor-core operand (16-byte chunk c of row r stored at chunk c ^ (r%8)).
+//
+// Decode layout: codes as given (canonical), one array over all experts
+// (shared expert last), and scale/bias merged into one 32-bit word per group.
+#include <cuda_runtime.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+struct ExpertSrc {
+  const uint8_t* codes;
+  const uint16_t* scale;
+  const uint16_t* bias;
+  const uint8_t* sh_codes;
+  const uint16_t* sh_scale;
+  const uint16_t* sh_bias;
+  int E;
+  int R;  // rows per expert
+  int K;  // inner size
+};
+
+__device__ __forceinline__ void expert_ptrs(const ExpertSrc& s, int x, const uint8_t*& c,
+                                            const uint16_t*& sc, const uint16_t*& bi) {
+  if (x < s.E) {
+    c = s.codes + (long long)x * s.R * (s.K / 2);
+    sc = s.scale + (long long)x * s.R * (s.K / 64);
+    bi = s.bias + (long long)x * s.R * (s.K / 64);
+  } else {
+    c = s.sh_codes;
+    sc = s.sh_scale;
+    bi = s.sh_bias;
+  }
+}
+
+__device__ __forceinline__ uint32_t permute_word(uint32_t w) {
+  uint32_t o = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t b = (w >> (8 * j)) & 0xFFu;
+    o |= (b & 0xFu) << (4 * j);
+    o |= (b >> 4) << (16 + 4 * j);
+  }
+  return o;
+}
+
+// gate_up != 0: unit rows = gate m*128.. then up I + m*128..; else rows m*256..
+__global__ void repack_prefill_kernel(ExpertSrc s, int nexp, int MU, int gate_up, int I,
+                                      uint8_t* __restrict__ out) {
+  const int KB = s.K / 64;
+  const long long total = (long long)nexp * MU * KB * 256;
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(it & 255);
+    long long rest = it >> 8;
+    const int kb = (int)(rest % KB);
+    rest /= KB;
+    const int m = (int)(rest % MU);
+    const int x = (int)(rest / MU);
+    int row;
+    if (gate_up) row = (r < 128) ? m * 128 + r : I + m * 128 + (r - 128);
+    else row = m * 256 + r;
+    const uint8_t* c;
+    const uint16_t *sc, *bi;
+    expert_ptrs(s, x, c, sc, bi);
+    const uint4* src = reinterpret_cast<const uint4*>(c + (long long)row * (s.K / 2) + kb * 32);
+    const uint4 a = src[0], b = src[1];
+    uint8_t* chunk = out + (((long long)x * MU + m) * KB + kb) * kCodeChunk;
+    uint4* dst = reinterpret_cast<uint4*>(chunk + r * 32);
+    dst[0] = make_uint4(permute_word(a.x), permute_word(a.y), permute_word(a.z), permute_word(a.w));
+    dst[1] = make_uint4(permute_word(b.x), permute_word(b.y), permute_word(b.z), permute_word(b.w));
+    const long long gi = (long long)row * (s.K / 64) + kb;
+    reinterpret_cast<uint32_t*>(chunk + 8192)[r] = (uint32_t)sc[gi] | ((uint32_t)bi[gi] << 16);
+  }
+}
+
+__global__ void repack_router_prefill_kernel(const uint16_t* __restrict__ wr, int E, int d, int MU,
+                                             uint8_t* __restrict__ out) {
+  const int KB = d / 64;
+  const long long total = (long long)MU * KB * 256 * 8;
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(it & 7);
+    const int r = (int)((it >> 3) & 255);
+    const long long rest = it >> 11;
+    const int kb = (int)(rest % KB);
+    const int m = (int)(rest / KB);
+    const int e = m * 256 + r;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (e < E) v = *reinterpret_cast<const uint4*>(wr + (long long)e * d + kb * 64 + c * 8);
+    uint8_t* chunk = out + ((long long)m * KB + kb) * kRouterChunk;
+    *reinterpret_cast<uint4*>(chunk + (r >> 7) * 16384 + (r & 127) * 128 + ((c ^ (r & 7)) << 4)) =
+        v;
+  }
+}
+
+// decode layout: codes copied as they are, scale/bias merged per group
+__global__ void repack_decode_kernel(ExpertSrc s, int nexp, uint8_t* __restrict__ codes_out,
+                                     uint32_t* __restrict__ sb_out) {
+  const long long per_codes = (long long)s.R * (s.K / 2) / 16;  // uint4 per expert
+  const long long per_sb = (long long)s.R * (s.K / 64);
+  const long long total = (long long)nexp * (per_codes + per_sb);
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    if (it < nexp * per_codes) {
+      const int x = (int)(it / per_codes);
+      const long long i = it - x * per_codes;
+      const uint8_t* c;
+      const uint16_t *sc, *bi;
+      expert_ptrs(s, x, c, sc, bi);
+      reinterpret_cast<uint4*>(codes_out)[it] = reinterpret_cast<const uint4*>(c)[i];
+    } else {
+      const long long j = it - nexp * per_codes;
+      const int x = (int)(j / per_sb);
+      const long long i = j - x * per_sb;
+      const uint8_t* c;
+      const uint16_t *sc, *bi;
+      expert_ptrs(s, x, c, sc, bi);
+      sb_out[j] = (uint32_t)sc[i] | ((uint32_t)bi[i] << 16);
+    }
+  }
+}
+
+ExpertSrc make_src(const moe_weights* w, const moe_config& c, bool gu) {
+  ExpertSrc s;
+  s.E = c.E;
+  if (gu) {
+    s.codes = (const uint8_t*)w->gu_codes;
+    s.scale = (const uint16_t*)w->gu_scale;
+    s.bias = (const uint16_t*)w->gu_bias;
+    s.sh_codes = (const uint8_t*)w->sh_gu_codes;
+    s.sh_scale = (const uint16_t*)w->sh_gu_scale;
+    s.sh_bias = (const uint16_t*)w->sh_gu_bias;
+    s.R = 2 * c.I;
+    s.K = c.d;
+  } else {
+    s.codes = (const uint8_t*)w->dn_codes;
+    s.scale = (const uint16_t*)w->dn_scale;
+    s.bias = (const uint16_t*)w->dn_bias;
+    s.sh_codes = (const uint8_t*)w->sh_dn_codes;
+    s.sh_scale = (const uint16_t*)w->sh_dn_scale;
+    s.sh_bias = (const uint16_t*)w->sh_dn_bias;
+    s.R = c.d;
+    s.K = c.I;
+  }
+  return s;
+}
+
+}  // namespace
+
+cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const int grid = h->num_sms * 8;
+  const ExpertSrc gu = make_src(w, c, true);
+  const ExpertSrc dn = make_src(w, c, false);
+  if (h->layouts & MOE_LAYOUT_PREFILL) {
+    repack_prefill_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.I / 128, 1, c.I, h->pf_gu);
+    repack_prefill_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, c.d / 256, 0, c.I, h->pf_dn);
+    repack_router_prefill_kernel<<<grid, 256, 0, st>>>((const uint16_t*)w->w_router, c.E, c.d,
+                                                       (c.E + 255) / 256, h->pf_router);
+  }
+  if (h->layouts & MOE_LAYOUT_DECODE) {
+    const long long gu_codes = (long long)h->n_exp * 2 * c.I * (c.d / 2);
+    const long long dn_codes = (long long)h->n_exp * c.d * (c.I / 2);
+    repack_decode_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, h->dc_gu,
+                                               reinterpret_cast<uint32_t*>(h->dc_gu + gu_codes));
+    repack_decode_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, h->dc_dn,
+                                               reinterpret_cast<uint32_t*>(h->dc_dn + dn_codes));
+  }
+  cudaError_t e = cudaMemcpyAsync(h->w_router, w->w_router, (size_t)c.E * c.d * 2,
+                                  cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return e;
+  if (c.has_shared) {
+    e = cudaMemcpyAsync(h->w_sg, w->w_shared_gate, (size_t)c.d * 2, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    e = cudaMemsetAsync(h->w_sg, 0, (size_t)c.d * 2, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,345 @@
+// GPU-resident routing: softmax/top-k, histogram, prefix scan, scatter and
+// tile (block) map, and the deterministic combine.  No host round-trip: every
+// size the later kernels need stays in device memory.
+// Source: Perplexity, "Optimizing on-device inference for Apple Silicon",
+// §"Keep expert routing on the GPU" (histogram of assignments per expert,
+// prefix scan to start offsets, scatter of rows into their expert groups,
+// block map of the fixed-size blocks the grouped GEMM processes) and
+// §"Match tile size to expert load" (tiles sized from the expert's rows).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// (value, index) order of the selection: larger value first, then lower index.
+__device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) {
+  return va > vb || (va == vb && ea < eb);
+}
+
+// One warp per token.  Sums the router's K-split partial logits (fixed
+// order), adds the bias, keeps the top k by (logit desc, index asc) and
+// computes the renormalised softmax weights in fp64.  When x is given it
+// also writes the fp16 copy of the token's activations and the shared
+// expert's gate sigma = sigmoid(w_sg . x).  Each block counts its assignments
+// per expert (hist[block][e]).
+template <int VPL>
+__global__ void __launch_bounds__(256) topk_kernel(
+    const float* __restrict__ part, int KS, int T, int E, int k, const float* __restrict__ bias,
+    const uint16_t* __restrict__ x, int d, const uint16_t* __restrict__ w_sg, int has_shared,
+    float* __restrict__ logits, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+    float* __restrict__ sigma, uint16_t* __restrict__ x16, int32_t* __restrict__ hist,
+    int* __restrict__ err) {
+  __shared__ int cnt[kMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+
+  for (int tt = 0; tt < kTokPerBlock / 8; ++tt) {
+    const int t = blockIdx.x * kTokPerBlock + warp * (kTokPerBlock / 8) + tt;
+    if (t >= T) break;
+    float v[VPL];
+    bool nan_seen = false;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      float s = -INFINITY;
+      if (e < E) {
+        s = 0.0f;
+        for (int p = 0; p < KS; ++p) s += part[((long long)p * T + t) * E + e];
+        if (bias) s += bias[e];
+        logits[(long long)t * E + e] = s;
+        if (s != s) {
+          nan_seen = true;
+          s = -INFINITY;
+        }
+      }
+      v[j] = s;
+    }
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, MOE_DEVERR_NAN_LOGIT);
+
+    uint32_t taken = 0;
+    float sel_v[kMaxK];
+    int sel_e[kMaxK];
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int be = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && beats(v[j], e, bv, be)) {
+          bv = v[j];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (beats(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      sel_v[r] = bv;
+      sel_e[r] = be;
+    }
+    // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0)
+    const double m = (double)sel_v[0];
+    double den = 0.0;
+    for (int r = 0; r < k; ++r) den += (m == -INFINITY) ? 1.0 : exp((double)sel_v[r] - m);
+    for (int r = 0; r < k; ++r) {
+      if (lane == r) {
+        const double ex = (m == -INFINITY) ? 1.0 : exp((double)sel_v[r] - m);
+        idx_out[(long long)t * k + r] = sel_e[r];
+        w_out[(long long)t * k + r] = (float)(ex / den);
+        atomicAdd(&cnt[sel_e[r]], 1);
+      }
+    }
+
+    if (x) {
+      const uint16_t* xr = x + (long long)t * d;
+      uint16_t* xo = x16 + (long long)t * d;
+      float dot = 0.0f;
+      for (int c = lane * 8; c < d; c += 256) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(xr + c);
+        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t hv[4];
+        uint4 sg = make_uint4(0, 0, 0, 0);
+        if (has_shared) sg = *reinterpret_cast<const uint4*>(w_sg + c);
+        const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(wv[q] << 16);
+          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
+          dot = fmaf(lo, __uint_as_float(sv[q] << 16), dot);
+          dot = fmaf(hi, __uint_as_float(sv[q] & 0xFFFF0000u), dot);
+        }
+        *reinterpret_cast<uint4*>(xo + c) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+      if (has_shared) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        if (lane == 0) sigma[t] = 1.0f / (1.0f + expf(-dot));
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[(long long)blockIdx.x * E + e] = cnt[e];
+}
+
+// Single block.  Per expert: exclusive scan of the block histograms over
+// blocks (base[b][e]), the total count, the exclusive scan over experts
+// (offsets), and the tile map: full 256-row tiles first (expert order), then
+// each expert's remainder tile, larger remainders first.  The shared expert
+// (index E, all T tokens, rows T*k..T*k+T-1) takes part like any expert.
+__global__ void __launch_bounds__(1024) scan_tiles_kernel(
+    const int32_t* __restrict__ hist, int nblk, int T, int E, int k, int has_shared,
+    int32_t* __restrict__ base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int4* __restrict__ tiles, int32_t* __restrict__ ntiles) {
+  __shared__ int s_cnt[kMaxE + 1];
+  __shared__ int s_off[kMaxE + 2];
+  __shared__ int s_full[kMaxE + 2];
+  __shared__ int s_cls[kMaxE + 1];
+  __shared__ int s_clsn[17];
+  __shared__ int s_clsb[17];
+  const int tid = threadIdx.x;
+  const int nexp = E + (has_shared ? 1 : 0);
+
+  if (tid < E) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const int c = hist[(long long)b * E + tid];
+      base[(long long)b * E + tid] = run;
+      run += c;
+    }
+    s_cnt[tid] = run;
+    counts[tid] = run;
+  }
+  if (tid == E && has_shared) s_cnt[E] = T;
+  if (tid < 17) s_clsn[tid] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    // tiny serial scans (E <= 512)
+    int run = 0, runf = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = run;
+      run += s_cnt[e];
+    }
+    s_off[E] = run;
+    for (int e = 0; e < nexp; ++e) {
+      s_full[e] = runf;
+      runf += s_cnt[e] / kTileRows;
+    }
+    s_full[nexp] = runf;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+  if (tid < nexp) {
+    const int tail = s_cnt[tid] % kTileRows;
+    const int cls = tail ? ((tail + 15) >> 4) - 1 : -1;  // 0..15 (npad 16..256)
+    s_cls[tid] = cls;
+    if (cls >= 0) atomicAdd(&s_clsn[cls], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = s_full[nexp];
+    for (int c = 15; c >= 0; --c) {
+      s_clsb[c] = run;
+      run += s_clsn[c];
+    }
+    *ntiles = run;
+  }
+  __syncthreads();
+  if (tid < nexp) {
+    const int e = tid;
+    const int row_base = (e < E) ? s_off[e] : T * k;
+    const int nf = s_cnt[e] / kTileRows;
+    for (int i = 0; i < nf; ++i)
+      tiles[s_full[e] + i] = make_int4(e, row_base + i * kTileRows, kTileRows, kTileRows);
+    const int cls = s_cls[e];
+    if (cls >= 0) {
+      int rank = 0;
+      for (int f = 0; f < e; ++f) rank += (s_cls[f] == cls);
+      const int tail = s_cnt[e] - nf * kTileRows;
+      tiles[s_clsb[cls] + rank] =
+          make_int4(e, row_base + nf * kTileRows, tail, (tail + 15) & ~15);
+    }
+  }
+}
+
+// Scatter (stable counting sort by (expert, token)).  Row of assignment
+// (t, j) with expert e = offsets[e] + base[block][e] + (number of tokens
+// of this block before t that chose e).  Also fills, per grouped row, the
+// routing weight and the contribution row t*(k+has_shared)+j, and the rows of
+// the shared expert (T*k + t).
+__global__ void __launch_bounds__(256) scatter_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, const float* __restrict__ sigma,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ base, int T, int E, int k,
+    int has_shared, int32_t* __restrict__ perm, int32_t* __restrict__ slot,
+    int32_t* __restrict__ dst, float* __restrict__ wrow) {
+  __shared__ uint32_t mask[kMaxE][kTokPerBlock / 32];
+  const int b = blockIdx.x;
+  const int t0 = b * kTokPerBlock;
+  const int k1 = k + (has_shared ? 1 : 0);
+  for (int i = threadIdx.x; i < E * (kTokPerBlock / 32); i += blockDim.x)
+    (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  for (int a = threadIdx.x; a < kTokPerBlock * k; a += blockDim.x) {
+    const int tl = a / k;
+    const int t = t0 + tl;
+    if (t < T) {
+      const int e = idx[(long long)t * k + (a - tl * k)];
+      atomicOr(&mask[e][tl >> 5], 1u << (tl & 31));
+    }
+  }
+  __syncthreads();
+  for (int a = threadIdx.x; a < kTokPerBlock * k; a += blockDim.x) {
+    const int tl = a / k;
+    const int j = a - tl * k;
+    const int t = t0 + tl;
+    if (t < T) {
+      const int e = idx[(long long)t * k + j];
+      int rank = 0;
+      for (int wd = 0; wd < (tl >> 5); ++wd) rank += __popc(mask[e][wd]);
+      rank += __popc(mask[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+      const int row = offsets[e] + base[(long long)b * E + e] + rank;
+      perm[row] = t;
+      slot[(long long)t * k + j] = row;
+      wrow[row] = w[(long long)t * k + j];
+      dst[row] = t * k1 + j;
+    }
+  }
+  if (has_shared) {
+    for (int tl = threadIdx.x; tl < kTokPerBlock; tl += blockDim.x) {
+      const int t = t0 + tl;
+      if (t < T) {
+        const int row = T * k + t;
+        perm[row] = t;
+        wrow[row] = sigma[t];
+        dst[row] = t * k1 + k;
+      }
+    }
+  }
+}
+
+// out[t][f] = sum_{j=0}^{k1-1} Y[t*k1 + j][f], fp32 in slot order (the
+// shared expert's term last), rounded once to bf16.  The routing weights were
+// applied when the rows of Y were written.
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y, int k1,
+                                                     int d, uint16_t* __restrict__ out) {
+  const int t = blockIdx.x;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < k1; ++j) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(Y + ((long long)t * k1 + j) * d + c);
+      const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(v[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(v[q] & 0xFFFF0000u);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(out + (long long)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
+                        const uint16_t* x, cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const Workspace& ws = h->ws;
+  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
+  if (c.E <= 256)
+    topk_kernel<8><<<nblk, 256, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
+                                          c.has_shared, ws.logits, ws.idx, ws.w, ws.sigma,
+                                          ws.x16, ws.hist, h->dev_err);
+  else
+    topk_kernel<16><<<nblk, 256, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
+                                           c.has_shared, ws.logits, ws.idx, ws.w, ws.sigma,
+                                           ws.x16, ws.hist, h->dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan_tiles(const Handle* h, int T, cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const Workspace& ws = h->ws;
+  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
+  scan_tiles_kernel<<<1, 1024, 0, st>>>(ws.hist, nblk, T, c.E, c.k, c.has_shared, ws.base,
+                                        ws.counts, ws.offsets, ws.tiles, ws.ntiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const Handle* h, int T, cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const Workspace& ws = h->ws;
+  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
+  scatter_kernel<<<nblk, 256, 0, st>>>(ws.idx, ws.w, ws.sigma, ws.offsets, ws.base, T, c.E, c.k,
+                                       c.has_shared, ws.perm, ws.slot, ws.dst, ws.wrow);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const int threads = c.d / 8 < 256 ? c.d / 8 : 256;
+  combine_kernel<<<T, threads, 0, st>>>(h->ws.Y, c.k + (c.has_shared ? 1 : 0), c.d, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

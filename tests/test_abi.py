@@ -1,0 +1,86 @@
+"""The C-ABI library loads, exports every function include/moe.h declares,
+and rejects bad arguments before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch  # noqa: F401  (makes the CUDA runtime the library links against resolvable)
+    from sparse_moe_bit_gb300 import build, moe
+    if not os.path.exists(moe.LIB_PATH):
+        build.build()
+    return moe.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    from sparse_moe_bit_gb300 import moe
+    assert _declared() == sorted(moe.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.moe_version() == 1
+    assert lib.moe_status_string(0) == b"ok"
+    assert lib.moe_status_string(1) == b"invalid argument"
+    assert lib.moe_status_string(5) == b"device error"
+
+
+def _cfg(**kw):
+    from sparse_moe_bit_gb300 import moe
+    base = dict(d=256, E=16, k=2, I=128, group=64, scale_dtype=1, max_tokens=16,
+                has_shared=1, layouts=0)
+    base.update(kw)
+    return moe.MoEConfig(**base)._c()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=100), 1), (dict(d=0), 1), (dict(E=0), 1), (dict(E=513), 1), (dict(k=0), 1),
+    (dict(k=17, E=32), 1), (dict(k=3, E=2), 1), (dict(I=100), 1), (dict(group=32), 2),
+    (dict(scale_dtype=2), 2), (dict(scale_dtype=7), 1), (dict(max_tokens=0), 1),
+    (dict(has_shared=2), 1), (dict(layouts=9), 1)])
+def test_create_rejects_bad_config(lib, kw, status):
+    from sparse_moe_bit_gb300 import moe
+    w = moe._Weights()
+    h = ctypes.c_void_p()
+    assert lib.moe_create(ctypes.byref(_cfg(**kw)), ctypes.byref(w), None, ctypes.byref(h)) == status
+    assert h.value is None
+    assert len(lib.moe_last_error()) > 0
+
+
+def test_create_rejects_null_or_misaligned_weights(lib):
+    from sparse_moe_bit_gb300 import moe
+    h = ctypes.c_void_p()
+    w = moe._Weights()  # all NULL
+    assert lib.moe_create(ctypes.byref(_cfg()), ctypes.byref(w), None, ctypes.byref(h)) == 1
+    w = moe._Weights(*([0x1008] * 14))  # 8-byte aligned only
+    assert lib.moe_create(ctypes.byref(_cfg()), ctypes.byref(w), None, ctypes.byref(h)) == 1
+    assert lib.moe_create(None, ctypes.byref(w), None, ctypes.byref(h)) == 1
+    assert lib.moe_create(ctypes.byref(_cfg()), ctypes.byref(w), None, None) == 1
+
+
+def test_calls_on_null_handle_are_rejected(lib):
+    assert lib.moe_forward(None, None, 4, None, None, None) == 1
+    assert lib.moe_route(None, None, 4, None, None, None, None, None, None, None, None, None) == 1
+    assert lib.moe_route_from_logits(None, None, 4, None, None, None, None, None, None, None,
+                                     None) == 1
+    assert lib.moe_forward_host(None, None, 4, None, None, None) == 1
+    assert lib.moe_decode(None, 0, None, None, 1e-6, None, None, None) == 1
+    code = ctypes.c_int()
+    assert lib.moe_get_device_error(None, ctypes.byref(code)) == 1
+    assert lib.moe_destroy(None) == 0

@@ -1,0 +1,224 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle: router
+logits, routing and grouping (bit-exact given identical fp32 logits), and
+block outputs within rel-L2 <= 5e-3 and max-abs <= 3e-2 * max|oracle|."""
+import numpy as np
+import pytest
+import torch
+
+import sparse_moe_bit_gb300 as M
+from oracle import moe_oracle as O
+from synth import gen
+from tests.moe_cases import (MID, TINY, HostCase, bits_to_dev, check_output, dev_to_bits,
+                             near_tie_tokens)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return HostCase(TINY, seed=0)
+
+
+@pytest.fixture(scope="module")
+def mid():
+    return HostCase(MID, seed=1)
+
+
+def _x(case, T, row0=0, seed=0):
+    bits = gen.make_x(seed, T, case.shape.d, row0=row0)
+    return bits, bits_to_dev(bits)
+
+
+def _routing_matches(r_gpu, logits, k, E):
+    idx, w = O.select_top_k(logits.astype(np.float64), k)
+    counts, offsets, perm, slot = O.group_by_expert(idx, E)
+    assert np.array_equal(r_gpu["idx"].cpu().numpy(), idx)
+    assert np.array_equal(r_gpu["counts"].cpu().numpy(), counts)
+    assert np.array_equal(r_gpu["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(r_gpu["perm"].cpu().numpy(), perm)
+    assert np.array_equal(r_gpu["slot"].cpu().numpy(), slot)
+    wg = r_gpu["w"].cpu().numpy()
+    w32 = w.astype(np.float32)
+    ulp = np.spacing(np.abs(w32))
+    assert np.all(np.abs(wg - w32) <= ulp), "routing weights beyond 1 ulp of fp32"
+
+
+@pytest.mark.parametrize("T", [16, 200])
+def test_router_logits_vs_oracle(tiny, mid, T):
+    for case in (tiny, mid):
+        bits, x = _x(case, T)
+        r = case.moe.route(x)
+        torch.cuda.synchronize()
+        xv = O.bf16_values(bits)
+        ref = O.router_logits(xv, case.vals["w_router"])
+        absdot = np.abs(xv) @ np.abs(case.vals["w_router"]).T
+        got = r["logits"].cpu().numpy()
+        # fp32 accumulation of exact bf16 products: |err| <= d * 2^-24 * sum|x w|
+        tol = case.shape.d * 2.0 ** -24 * absdot + 1e-7
+        assert np.all(np.abs(got - ref) <= tol)
+
+
+@pytest.mark.parametrize("T", [16, 257, 1000])
+def test_routing_bit_exact_given_logits(tiny, mid, T):
+    for case in (tiny, mid):
+        bits, x = _x(case, T, seed=3)
+        r = case.moe.route(x)
+        torch.cuda.synchronize()
+        _routing_matches(r, r["logits"].cpu().numpy(), case.shape.k, case.shape.E)
+
+
+def test_route_from_crafted_logits_with_ties(mid):
+    rng = np.random.default_rng(11)
+    T, E, k = 300, MID.E, MID.k
+    lg = (np.round(rng.standard_normal((T, E)) * 2) / 2).astype(np.float32)  # many exact ties
+    lg[:10] = 0.0  # all experts tied
+    lg[10, :] = -np.inf
+    lg[11, :5] = np.inf
+    r = mid.moe.route_from_logits(torch.from_numpy(lg).cuda())
+    torch.cuda.synchronize()
+    _routing_matches(r, lg, k, E)
+
+
+def test_route_bias_is_added(mid):
+    bits, x = _x(mid, 64)
+    bias = torch.linspace(-1, 1, MID.E, device="cuda", dtype=torch.float32)
+    r0 = mid.moe.route(x)
+    r1 = mid.moe.route(x, bias)
+    torch.cuda.synchronize()
+    d = (r1["logits"] - r0["logits"]).cpu().numpy()
+    np.testing.assert_allclose(d, np.broadcast_to(bias.cpu().numpy(), d.shape), atol=2e-6)
+    _routing_matches(r1, r1["logits"].cpu().numpy(), MID.k, MID.E)
+
+
+@pytest.mark.parametrize("T", [2, 15, 16, 17, 64, 255, 256, 257, 1000])
+def test_forward_parity_tiny(tiny, T):
+    bits, x = _x(tiny, T, seed=T)
+    y = tiny.moe.forward(x)
+    r = tiny.moe.route(x)
+    torch.cuda.synchronize()
+    ref = tiny.oracle(bits, logits=r["logits"].cpu().numpy())
+    check_output(y.float().cpu().numpy(), ref["out"], f"tiny T={T}")
+    assert tiny.moe.device_error() == 0
+
+
+@pytest.mark.parametrize("T", [1, 33, 300])
+def test_forward_parity_mid(mid, T):
+    bits, x = _x(mid, T, seed=7)
+    if T == 1:  # prefill kernels at T = 1 need a handle without the decode layout
+        case = HostCase(MID, seed=1, layouts=M.MOE_LAYOUT_PREFILL)
+    else:
+        case = mid
+    y = case.moe.forward(x)
+    r = case.moe.route(x)
+    torch.cuda.synchronize()
+    ref = case.oracle(bits, logits=r["logits"].cpu().numpy())
+    check_output(y.float().cpu().numpy(), ref["out"], f"mid T={T}")
+
+
+def test_forward_independent_routing_mid(mid):
+    # the oracle routes from its own fp64 logits; near-tie tokens excluded
+    T = 400
+    bits, x = _x(mid, T, seed=5)
+    y = mid.moe.forward(x).float().cpu().numpy()
+    ref = mid.oracle(bits)
+    ok = ~near_tie_tokens(ref["logits"], MID.k)
+    check_output(y[ok], ref["out"][ok], "mid independent")
+
+
+def test_no_shared_expert():
+    case = HostCase(TINY, seed=4, has_shared=False)
+    bits, x = _x(case, 100)
+    y = case.moe.forward(x)
+    r = case.moe.route(x)
+    torch.cuda.synchronize()
+    ref = case.oracle(bits, logits=r["logits"].cpu().numpy())
+    check_output(y.float().cpu().numpy(), ref["out"], "no shared")
+
+
+def test_empty_experts_untouched_nan_poison():
+    case = HostCase(MID, seed=2)
+    T = 300
+    bits, x = _x(case, T, seed=9)
+    bias = torch.full((MID.E,), -1e4, device="cuda")
+    live = [1, 5, 6, 17, 30]
+    bias[live] = 0.0
+    y0 = case.moe.forward(x, bias)
+    r = case.moe.route(x, bias)
+    torch.cuda.synchronize()
+    counts = r["counts"].cpu().numpy()
+    assert set(np.nonzero(counts)[0].tolist()) <= set(live)
+    # same weights, but every expert without tokens gets NaN scales and biases
+    w2 = dict(case.w)
+    for key in ("gu_scale", "gu_bias", "dn_scale", "dn_bias"):
+        t = case.w[key].clone()
+        for e in range(MID.E):
+            if counts[e] == 0:
+                t[e] = float("nan")
+        w2[key] = t
+    poisoned = M.MoE(case.cfg, w2)
+    y1 = poisoned.forward(x, bias)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_to_bits_t(y0), dev_to_bits_t(y1))
+    ref = case.oracle(bits, logits=r["logits"].cpu().numpy())
+    check_output(y1.float().cpu().numpy(), ref["out"], "empty experts")
+
+
+def dev_to_bits_t(y):
+    return y.view(torch.int16)
+
+
+def test_one_hot_expert_many_tiles(mid):
+    T = 1000
+    bits, x = _x(mid, T, seed=12)
+    bias = torch.zeros(MID.E, device="cuda")
+    bias[3] = 60.0  # every token keeps expert 3: 1000 rows -> 3 full tiles + a tail
+    y = mid.moe.forward(x, bias)
+    r = mid.moe.route(x, bias)
+    torch.cuda.synchronize()
+    assert int(r["counts"][3]) == T
+    ref = mid.oracle(bits, logits=r["logits"].cpu().numpy())
+    check_output(y.float().cpu().numpy(), ref["out"], "hot expert")
+
+
+def test_deterministic_and_chunk_invariant():
+    a = HostCase(MID, seed=6, max_tokens=1024)
+    b = HostCase(MID, seed=6, max_tokens=96)
+    bits, x = _x(a, 1000, seed=13)
+    ya1 = a.moe.forward(x)
+    ya2 = a.moe.forward(x)
+    yb = b.moe.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(ya1.view(torch.int16), ya2.view(torch.int16)), "not deterministic"
+    r = a.moe.route(x)
+    ref = a.oracle(bits, logits=r["logits"].cpu().numpy())
+    check_output(yb.float().cpu().numpy(), ref["out"], "chunked")
+    assert torch.equal(ya1.view(torch.int16), yb.view(torch.int16)), "chunking changed the output"
+
+
+def test_forward_host_matches_device(mid):
+    T = 150
+    bits, x = _x(mid, T, seed=21)
+    bias = torch.randn(MID.E, generator=torch.Generator().manual_seed(0)) * 0.1
+    y_dev = mid.moe.forward(x, bias.cuda())
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    mid.moe.forward_host(xh, bias.pin_memory(), yh)
+    torch.cuda.synchronize()
+    assert torch.equal(y_dev.cpu().view(torch.int16), yh.view(torch.int16))
+
+
+def test_nan_logit_sets_device_error(mid):
+    lg = np.random.default_rng(1).standard_normal((20, MID.E)).astype(np.float32)
+    lg[4, 7] = np.nan
+    r = mid.moe.route_from_logits(torch.from_numpy(lg).cuda())
+    code = mid.moe.device_error()
+    assert code & 2
+    assert mid.moe.device_error() == 0  # reading clears it
+    # NaN is never selected (treated as -inf)
+    assert 7 not in r["idx"][4].cpu().numpy().tolist()
+
+
+def test_zero_tokens_is_a_no_op(mid):
+    x = torch.empty(0, MID.d, dtype=torch.bfloat16, device="cuda")
+    y = mid.moe.forward(x)
+    assert y.shape == (0, MID.d)
