@@ -91,10 +91,16 @@ def select_top_k(logits, k: int):
     with np.errstate(invalid="ignore"):
         ex = np.exp(top - m)
     w = ex / ex.sum(axis=1, keepdims=True)
-    # a token whose kept logits are all -inf: equal weights
-    bad = ~np.isfinite(m[:, 0])
-    if bad.any():
-        w[bad] = 1.0 / k
+    # Infinite logits (the pages are silent; the limit of the softmax): if the
+    # largest kept logit is +inf, the +inf experts share the weight equally;
+    # if every kept logit is -inf, the k experts share it equally.
+    pos = m[:, 0] == np.inf
+    if pos.any():
+        hit = (top[pos] == np.inf).astype(F64)
+        w[pos] = hit / hit.sum(axis=1, keepdims=True)
+    neg = m[:, 0] == -np.inf
+    if neg.any():
+        w[neg] = 1.0 / k
     return idx, w
 
 

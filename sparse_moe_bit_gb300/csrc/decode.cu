@@ -291,7 +291,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         double ex[kMaxK];
         double den = 0.0;
         for (int r = 0; r < k; ++r) {
-          ex[r] = (m == -INFINITY) ? 1.0 : exp((double)sel_w[r] - m);
+          // softmax limit for infinite logits (as in the prefill top-k)
+          if (m == INFINITY) ex[r] = (sel_w[r] == INFINITY) ? 1.0 : 0.0;
+          else if (m == -INFINITY) ex[r] = 1.0;
+          else ex[r] = exp((double)sel_w[r] - m);
           den += ex[r];
         }
         for (int r = 0; r < k; ++r) sel_w[r] = (float)(ex[r] / den);

@@ -22,6 +22,12 @@ __device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) {
   return va > vb || (va == vb && ea < eb);
 }
 
+__device__ __forceinline__ double softmax_term(float v, double m) {
+  if (m == INFINITY) return v == INFINITY ? 1.0 : 0.0;
+  if (m == -INFINITY) return 1.0;
+  return exp((double)v - m);
+}
+
 // One warp per token.  Sums the router's K-split partial logits (fixed
 // order), adds the bias, keeps the top k by (logit desc, index asc) and
 // computes the renormalised softmax weights in fp64.  When x is given it
@@ -90,13 +96,14 @@ __global__ void __launch_bounds__(256) topk_kernel(
       sel_v[r] = bv;
       sel_e[r] = be;
     }
-    // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0)
+    // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0); with infinite
+    // logits the limit: +inf experts share equally, all -inf share equally
     const double m = (double)sel_v[0];
     double den = 0.0;
-    for (int r = 0; r < k; ++r) den += (m == -INFINITY) ? 1.0 : exp((double)sel_v[r] - m);
+    for (int r = 0; r < k; ++r) den += softmax_term(sel_v[r], m);
     for (int r = 0; r < k; ++r) {
       if (lane == r) {
-        const double ex = (m == -INFINITY) ? 1.0 : exp((double)sel_v[r] - m);
+        const double ex = softmax_term(sel_v[r], m);
         idx_out[(long long)t * k + r] = sel_e[r];
         w_out[(long long)t * k + r] = (float)(ex / den);
         atomicAdd(&cnt[sel_e[r]], 1);

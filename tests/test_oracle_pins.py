@@ -150,6 +150,18 @@ def test_topk_weights_are_renormalised_full_softmax():
     assert np.all(np.diff(w, axis=1) <= 0)  # slots in descending logit order
 
 
+def test_topk_weights_infinite_logits_are_the_softmax_limit():
+    lg = np.array([[1.0, np.inf, 0.0, np.inf, -3.0],
+                   [-np.inf] * 5,
+                   [np.inf, 2.0, 1.0, 0.0, -1.0]])
+    idx, w = O.select_top_k(lg, 3)
+    assert idx.tolist() == [[1, 3, 0], [0, 1, 2], [0, 1, 2]]
+    assert w.tolist() == [[0.5, 0.5, 0.0], [1 / 3, 1 / 3, 1 / 3], [1.0, 0.0, 0.0]]
+    # the finite limit: logits c, c, a with c -> large give the same weights
+    idx2, w2 = O.select_top_k(np.array([[1.0, 800.0, 0.0, 800.0, -3.0]]), 3)
+    np.testing.assert_allclose(w2[0], [0.5, 0.5, 0.0], atol=1e-300)
+
+
 def test_router_logits_bias_and_orientation():
     # d != E so a transposed router matrix cannot go unnoticed
     rng = np.random.default_rng(4)
