@@ -203,10 +203,20 @@ def run_decode(args, torch, M, sd, gen, device, peaks):
         M.decode_host(layers, xh[i], yh)
     e2e_s = (time.perf_counter() - t0) / args.steps
     e2e_s = max_over_ranks(e2e_s, device)
+    # where a layer's time goes (GPU clock stamps of the first CTA, one traced token)
+    _, tr = M.decode(layers, xs[0], trace=True)
+    torch.cuda.synchronize(device)
+    ts = tr["timestamps"].cpu().numpy().astype("float64") / 1000.0
+    phases = {
+        "route_and_issue_copies": float((ts[:, 1] - ts[:, 0]).mean()),
+        "gate_up_and_barrier": float((ts[:, 2] - ts[:, 1]).mean()),
+        "down": float((ts[:, 3] - ts[:, 2]).mean()),
+        "router_partials_and_barrier": float((ts[1:, 0] - ts[:-1, 3]).mean()),
+    }
     err = layers[0].device_error()
     return dict(
         ms_per_step=ms_step, value=args.world * 1000.0 / ms_step, unit="tokens/s",
-        us_per_layer=ms_step * 1000.0 / DECODE_LAYERS,
+        us_per_layer=ms_step * 1000.0 / DECODE_LAYERS, phase_us=phases,
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                   "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                   "traffic": None, "kernel": "decode_kernel",
@@ -295,63 +305,70 @@ def cpu_threads():
         return os.cpu_count()
 
 
-def oracle_decode_sample(n_layers=2):
-    """fp64 oracle on the first n_layers of the decode chain (weights made
-    outside the timed region); returns (seconds, layers)."""
-    import numpy as np
-    from oracle import moe_oracle as O
-    from synth import gen
-    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
-    x = O.bf16_values(gen.make_x(1, 1, D))
-    total = 0.0
-    for l in range(n_layers):
-        wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, l, 0, E, D, 0.02))
-        wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, l, 0, 1, D, 0.02)[0])
-        lg = O.router_logits(x, wr)
-        idx, _ = O.select_top_k(lg, K)
-        cache = {e: gen.expert_weights(0, l, e, shape) for e in list(idx[0]) + [E]}
-        vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr, w_shared_gate=wsg,
-                    experts=None, shared=None)
+class OracleSample:
+    """A bounded sample of the workload for the fp64 oracle on host cores.
+    Weights are generated once (outside timing); run() times oracle work only.
+      decode : the first `n_layers` layers of the 40-layer chain, one token;
+               value scaled to a full 40-layer token
+      prefill: `n_tok` tokens of the T=4096 Zipf layer (router, top-k,
+               dequantisation of every touched expert, experts, combine)."""
+
+    def __init__(self, workload, n_layers=2, n_tok=256):
+        import numpy as np
+        from oracle import moe_oracle as O
+        from synth import gen
+        self.O, self.workload = O, workload
+        shape = gen.MoEShape(d=D, E=E, k=K, I=I)
+        if workload == "decode":
+            self.layers = []
+            x = O.bf16_values(gen.make_x(1, 1, D))
+            self.x0 = x
+            for l in range(n_layers):
+                wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, l, 0, E, D, 0.02))
+                wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, l, 0, 1, D, 0.02)[0])
+                idx, _ = O.select_top_k(O.router_logits(x, wr), K)
+                cache = {int(e): gen.expert_weights(0, l, int(e), shape) for e in idx[0]}
+                cache[E] = gen.expert_weights(0, l, E, shape)
+                vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr, w_shared_gate=wsg,
+                            experts=None, shared=None)
+                self.layers.append((vals, cache))
+                x = O.rms_norm(O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"])
+            self.units = n_layers
+            self.sample = (f"fp64 oracle, layers 0-{n_layers - 1} of the 40-layer decode chain "
+                           f"(one token), scaled to 40 layers")
+        else:
+            self.x = O.bf16_values(gen.make_x(0, n_tok, D))
+            wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, 0, 0, E, D, 0.02))
+            wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, 0, 0, 1, D, 0.02)[0])
+            self.bias = gen.zipf_bias(0, E)
+            idx, _ = O.select_top_k(O.router_logits(self.x, wr, self.bias), K)
+            self.cache = {int(e): gen.expert_weights(0, 0, int(e), shape) for e in np.unique(idx)}
+            self.cache[E] = gen.expert_weights(0, 0, E, shape)
+            self.vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr,
+                             w_shared_gate=wsg, experts=None, shared=None)
+            self.units = n_tok
+            self.sample = (f"fp64 oracle, {n_tok} tokens of the T=4096 Zipf prefill layer "
+                           f"(dequantisation of the {len(self.cache)} touched experts included)")
+
+    def run(self) -> float:
+        """One timed step; returns tokens/s."""
+        O = self.O
         t0 = time.perf_counter()
-        out = O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"]
-        x = O.rms_norm(out)
-        total += time.perf_counter() - t0
-    return total, n_layers
+        if self.workload == "decode":
+            x = self.x0
+            for vals, cache in self.layers:
+                x = O.rms_norm(O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"])
+            sec = time.perf_counter() - t0
+            return 1.0 / (sec / self.units * DECODE_LAYERS)
+        O.moe_layer(self.x, self.vals, logit_bias=self.bias, expert_source=lambda e: self.cache[e])
+        return self.units / (time.perf_counter() - t0)
 
 
-def oracle_prefill_sample(n_tok=256):
-    """fp64 oracle on n_tok tokens of the prefill workload (weights of the
-    experts they touch made outside the timed region)."""
-    from oracle import moe_oracle as O
-    from synth import gen
-    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
-    xb = gen.make_x(0, n_tok, D)
-    x = O.bf16_values(xb)
-    wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, 0, 0, E, D, 0.02))
-    wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, 0, 0, 1, D, 0.02)[0])
-    bias = gen.zipf_bias(0, E)
-    idx, _ = O.select_top_k(O.router_logits(x, wr, bias), K)
-    import numpy as np
-    cache = {int(e): gen.expert_weights(0, 0, int(e), shape) for e in np.unique(idx)}
-    cache[E] = gen.expert_weights(0, 0, E, shape)
-    vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr, w_shared_gate=wsg,
-                experts=None, shared=None)
-    t0 = time.perf_counter()
-    O.moe_layer(x, vals, logit_bias=bias, expert_source=lambda e: cache[e])
-    return time.perf_counter() - t0, n_tok
-
-
-def cpu_baseline(workload):
-    if workload == "decode":
-        sec, nl = oracle_decode_sample(2)
-        tok_s = 1.0 / (sec / nl * DECODE_LAYERS)
-        sample = f"fp64 oracle, layers 0-{nl - 1} of the 40-layer decode chain, scaled to 40 layers"
-    else:
-        sec, nt = oracle_prefill_sample(256)
-        tok_s = nt / sec
-        sample = f"fp64 oracle, {nt} tokens of the T=4096 Zipf prefill layer (dequantisation of touched experts included)"
-    return {"value": tok_s, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": sample}
+def cpu_baseline(workload, steps=1):
+    s = OracleSample(workload)
+    v = statistics.median([s.run() for _ in range(max(1, steps))])
+    return {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": s.sample}
 
 
 # ------------------------------------------------------------------ main
@@ -381,16 +398,18 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        cb = cpu_baseline(args.workload)
-        steps = []
-        for _ in range(args.steps):
-            steps.append(cpu_baseline(args.workload)["value"])
-        v = statistics.median(steps) if steps else cb["value"]
+        sample = OracleSample(args.workload)
+        for _ in range(args.warmup):
+            sample.run()
+        steps = [sample.run() for _ in range(args.steps)]
+        v = statistics.median(steps)
+        cb = {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+              "sample": sample.sample}
         line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": v,
                 "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
                 "higher_is_better": True, "dtype": "f64", "data": "synthetic",
                 "config": config_for(args.workload),
-                "cpu_baseline": dict(cb, value=v),
+                "cpu_baseline": cb,
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -424,14 +443,16 @@ def main():
         "e2e": res["e2e"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
         "device_error": res["device_error"],
     }
-    for key in ("stage_ms", "step_roofline_frac", "experts_touched", "max_expert_rows"):
+    for key in ("stage_ms", "phase_us", "step_roofline_frac", "experts_touched",
+                "max_expert_rows"):
         if key in res:
             line[key] = res[key]
     if sec is not None:
         line[secondary] = {k: sec[k] for k in ("value", "unit", "ms_per_step", "us_per_layer",
                                                "roofline", "e2e", "gpu_launches")
                            if k in sec}
-        for key in ("stage_ms", "step_roofline_frac", "experts_touched", "max_expert_rows"):
+        for key in ("stage_ms", "phase_us", "step_roofline_frac", "experts_touched",
+                    "max_expert_rows"):
             if key in sec:
                 line[secondary][key] = sec[key]
     if ws == 1:

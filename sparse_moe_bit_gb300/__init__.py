@@ -4,7 +4,7 @@ The compute lives in libmoe.so (CUDA kernels behind the C ABI of
 include/moe.h); this package is its thin Python binding.
 """
 from .moe import (MOE_LAYOUT_DECODE, MOE_LAYOUT_PREFILL, MOE_SCALE_F16, MoE, MoEConfig,
-                  MoEError, decode, load_library)
+                  MoEError, decode, decode_host, load_library)
 
-__all__ = ["MoE", "MoEConfig", "MoEError", "decode", "load_library", "MOE_SCALE_F16",
-           "MOE_LAYOUT_PREFILL", "MOE_LAYOUT_DECODE"]
+__all__ = ["MoE", "MoEConfig", "MoEError", "decode", "decode_host", "load_library",
+           "MOE_SCALE_F16", "MOE_LAYOUT_PREFILL", "MOE_LAYOUT_DECODE"]

@@ -10,7 +10,7 @@ namespace moe {
 
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 16;
-constexpr int kTokPerBlock = 64;  // tokens per block of the routing kernels
+constexpr int kTokPerBlock = 32;  // tokens per block of the routing kernels
 constexpr int kTileRows = 256;    // largest token tile of the grouped GEMMs
 constexpr int kUnitRows = 256;    // weight rows per tensor-core work unit (2 x M=128)
 constexpr int kCodeChunk = 9216;  // 256 rows x (32 B codes + 4 B scale/bias)
@@ -58,7 +58,7 @@ struct Handle {
   // decode layouts (bandwidth path)
   uint8_t* dc_gu = nullptr;      // [n_exp][I][2 rows][d/2 codes + d/64*4 s,b]
   uint8_t* dc_dn = nullptr;      // [n_exp][d][I/2 codes + I/64*4 s,b]
-  uint16_t* dc_router_t = nullptr;  // bf16 [d][E] (transposed router)
+  uint16_t* dc_router_t = nullptr;  // bf16 [d][Ep]: router transposed + w_sg column
   uint16_t* w_router = nullptr;  // bf16 [E][d]
   uint16_t* w_sg = nullptr;      // bf16 [d]
   Workspace ws;
@@ -71,6 +71,13 @@ struct Handle {
   int* dev_err = nullptr;
   cudaStream_t last_stream = nullptr;
 };
+
+// row pitch (elements) of the decode router layout: E router columns, the
+// shared-gate column, zero padding to a 16-byte multiple
+inline int decode_router_pitch(int E) { return ((E + 1) + 7) & ~7; }
+// 32-bit scale/bias words per row of the decode down layout: I/64 groups,
+// padded to a multiple of 4 (16-byte rows for bulk copies)
+inline int decode_dn_sb_pitch(int I) { return ((I / 64) + 3) & ~3; }
 
 // ---- grouped tensor-core GEMM (grouped_mma.cu)
 enum MmaMode { MMA_ROUTER = 0, MMA_GATEUP = 1, MMA_DOWN = 2 };

@@ -17,7 +17,8 @@
 // the tensor-core operand (16-byte chunk c of row r stored at chunk c ^ (r%8)).
 //
 // Decode layout: codes as given (canonical), one array over all experts
-// (shared expert last), and scale/bias merged into one 32-bit word per group.
+// (shared expert last), and scale/bias merged into one 32-bit word per group
+// (down rows padded to a multiple of four words).
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
@@ -112,10 +113,11 @@ __global__ void repack_router_prefill_kernel(const uint16_t* __restrict__ wr, in
 }
 
 // decode layout: codes copied as they are, scale/bias merged per group
-__global__ void repack_decode_kernel(ExpertSrc s, int nexp, uint8_t* __restrict__ codes_out,
+__global__ void repack_decode_kernel(ExpertSrc s, int nexp, int sb_pitch,
+                                     uint8_t* __restrict__ codes_out,
                                      uint32_t* __restrict__ sb_out) {
   const long long per_codes = (long long)s.R * (s.K / 2) / 16;  // uint4 per expert
-  const long long per_sb = (long long)s.R * (s.K / 64);
+  const long long per_sb = (long long)s.R * sb_pitch;
   const long long total = (long long)nexp * (per_codes + per_sb);
   for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
@@ -130,11 +132,36 @@ __global__ void repack_decode_kernel(ExpertSrc s, int nexp, uint8_t* __restrict_
       const long long j = it - nexp * per_codes;
       const int x = (int)(j / per_sb);
       const long long i = j - x * per_sb;
+      const long long row = i / sb_pitch;
+      const int g = (int)(i - row * sb_pitch);
       const uint8_t* c;
       const uint16_t *sc, *bi;
       expert_ptrs(s, x, c, sc, bi);
-      sb_out[j] = (uint32_t)sc[i] | ((uint32_t)bi[i] << 16);
+      if (g < s.K / 64) {
+        const long long gi = row * (s.K / 64) + g;
+        sb_out[j] = (uint32_t)sc[gi] | ((uint32_t)bi[gi] << 16);
+      } else {
+        sb_out[j] = 0u;
+      }
     }
+  }
+}
+
+// decode router layout: [d][Ep] bf16, Ep = round_up(E + 1, 8); row f holds
+// W_r[0..E-1][f], then w_sg[f], then zeros (16-byte rows: one bulk copy takes
+// a CTA's range of rows)
+__global__ void repack_router_decode_kernel(const uint16_t* __restrict__ wr,
+                                            const uint16_t* __restrict__ wsg, int E, int d,
+                                            int Ep, uint16_t* __restrict__ out) {
+  const long long total = (long long)d * Ep;
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const int f = (int)(it / Ep);
+    const int e = (int)(it - (long long)f * Ep);
+    uint16_t v = 0;
+    if (e < E) v = wr[(long long)e * d + f];
+    else if (e == E && wsg) v = wsg[f];
+    out[it] = v;
   }
 }
 
@@ -179,10 +206,13 @@ cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st) {
   if (h->layouts & MOE_LAYOUT_DECODE) {
     const long long gu_codes = (long long)h->n_exp * 2 * c.I * (c.d / 2);
     const long long dn_codes = (long long)h->n_exp * c.d * (c.I / 2);
-    repack_decode_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, h->dc_gu,
+    repack_decode_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.d / 64, h->dc_gu,
                                                reinterpret_cast<uint32_t*>(h->dc_gu + gu_codes));
-    repack_decode_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, h->dc_dn,
+    repack_decode_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, decode_dn_sb_pitch(c.I), h->dc_dn,
                                                reinterpret_cast<uint32_t*>(h->dc_dn + dn_codes));
+    repack_router_decode_kernel<<<grid, 256, 0, st>>>(
+        (const uint16_t*)w->w_router, c.has_shared ? (const uint16_t*)w->w_shared_gate : nullptr,
+        c.E, c.d, decode_router_pitch(c.E), h->dc_router_t);
   }
   cudaError_t e = cudaMemcpyAsync(h->w_router, w->w_router, (size_t)c.E * c.d * 2,
                                   cudaMemcpyDeviceToDevice, st);

@@ -34,8 +34,11 @@ __device__ __forceinline__ double softmax_term(float v, double m) {
 // also writes the fp16 copy of the token's activations and the shared
 // expert's gate sigma = sigmoid(w_sg . x).  Each block counts its assignments
 // per expert (hist[block][e]).
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+
 template <int VPL>
-__global__ void __launch_bounds__(256) topk_kernel(
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float* __restrict__ part, int KS, int T, int E, int k, const float* __restrict__ bias,
     const uint16_t* __restrict__ x, int d, const uint16_t* __restrict__ w_sg, int has_shared,
     float* __restrict__ logits, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
@@ -46,8 +49,8 @@ __global__ void __launch_bounds__(256) topk_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
 
-  for (int tt = 0; tt < kTokPerBlock / 8; ++tt) {
-    const int t = blockIdx.x * kTokPerBlock + warp * (kTokPerBlock / 8) + tt;
+  for (int tt = 0; tt < kTokPerBlock / kTopkWarps; ++tt) {
+    const int t = blockIdx.x * kTokPerBlock + warp * (kTokPerBlock / kTopkWarps) + tt;
     if (t >= T) break;
     float v[VPL];
     bool nan_seen = false;
@@ -98,22 +101,32 @@ __global__ void __launch_bounds__(256) topk_kernel(
     }
     // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0); with infinite
     // logits the limit: +inf experts share equally, all -inf share equally
+    // lane r owns slot r: one fp64 exp per kept expert, the sum by a fixed
+    // butterfly (the same order on every run)
     const double m = (double)sel_v[0];
-    double den = 0.0;
-    for (int r = 0; r < k; ++r) den += softmax_term(sel_v[r], m);
+    float my_v = -INFINITY;
+    int my_e = 0;
     for (int r = 0; r < k; ++r) {
       if (lane == r) {
-        const double ex = softmax_term(sel_v[r], m);
-        idx_out[(long long)t * k + r] = sel_e[r];
-        w_out[(long long)t * k + r] = (float)(ex / den);
-        atomicAdd(&cnt[sel_e[r]], 1);
+        my_v = sel_v[r];
+        my_e = sel_e[r];
       }
+    }
+    const double ex = (lane < k) ? softmax_term(my_v, m) : 0.0;
+    double den = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if (lane < k) {
+      idx_out[(long long)t * k + lane] = my_e;
+      w_out[(long long)t * k + lane] = (float)(ex / den);
+      atomicAdd(&cnt[my_e], 1);
     }
 
     if (x) {
       const uint16_t* xr = x + (long long)t * d;
       uint16_t* xo = x16 + (long long)t * d;
       float dot = 0.0f;
+#pragma unroll 4
       for (int c = lane * 8; c < d; c += 256) {
         const uint4 raw = *reinterpret_cast<const uint4*>(xr + c);
         const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -144,82 +157,109 @@ __global__ void __launch_bounds__(256) topk_kernel(
     hist[(long long)blockIdx.x * E + e] = cnt[e];
 }
 
+// Exclusive scan of one value per thread over the whole block (<= 1024
+// threads); returns the thread's prefix and writes the total to *total.
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;
+    if (lane == nw - 1) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
 // Single block.  Per expert: exclusive scan of the block histograms over
 // blocks (base[b][e]), the total count, the exclusive scan over experts
 // (offsets), and the tile map: full 256-row tiles first (expert order), then
-// each expert's remainder tile, larger remainders first.  The shared expert
-// (index E, all T tokens, rows T*k..T*k+T-1) takes part like any expert.
+// each expert's remainder tile, larger remainders first (ties in expert
+// order).  The shared expert (index E, all T tokens, rows T*k..T*k+T-1)
+// takes part like any expert.
 __global__ void __launch_bounds__(1024) scan_tiles_kernel(
     const int32_t* __restrict__ hist, int nblk, int T, int E, int k, int has_shared,
     int32_t* __restrict__ base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int4* __restrict__ tiles, int32_t* __restrict__ ntiles) {
-  __shared__ int s_cnt[kMaxE + 1];
-  __shared__ int s_off[kMaxE + 2];
-  __shared__ int s_full[kMaxE + 2];
+  __shared__ int warp_tot[32];
+  __shared__ int s_total;
   __shared__ int s_cls[kMaxE + 1];
-  __shared__ int s_clsn[17];
   __shared__ int s_clsb[17];
   const int tid = threadIdx.x;
   const int nexp = E + (has_shared ? 1 : 0);
 
+  int cnt = 0;
   if (tid < E) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
+    int b = 0;
+    for (; b + 8 <= nblk; b += 8) {
+      int c[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c[q] = hist[(long long)(b + q) * E + tid];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        base[(long long)(b + q) * E + tid] = cnt;
+        cnt += c[q];
+      }
+    }
+    for (; b < nblk; ++b) {
       const int c = hist[(long long)b * E + tid];
-      base[(long long)b * E + tid] = run;
-      run += c;
+      base[(long long)b * E + tid] = cnt;
+      cnt += c;
     }
-    s_cnt[tid] = run;
-    counts[tid] = run;
+    counts[tid] = cnt;
+  } else if (tid == E && has_shared) {
+    cnt = T;
   }
-  if (tid == E && has_shared) s_cnt[E] = T;
-  if (tid < 17) s_clsn[tid] = 0;
+  // offsets over the routed experts
+  const int off = block_exclusive_scan(tid < E ? cnt : 0, warp_tot, &s_total);
+  if (tid <= E) offsets[tid] = (tid < E) ? off : s_total;
+  // full tiles, all experts (shared last)
+  const int nf = (tid < nexp) ? cnt / kTileRows : 0;
+  const int full_off = block_exclusive_scan(nf, warp_tot, &s_total);
+  const int total_full = s_total;
+  // remainder tiles: class c = npad/16 - 1 (0..15), larger classes first
+  const int tail = (tid < nexp) ? cnt % kTileRows : 0;
+  const int cls = tail ? ((tail + 15) >> 4) - 1 : -1;
+  if (tid < nexp) s_cls[tid] = cls;
+  if (tid < 17) s_clsb[tid] = 0;
+  __syncthreads();
+  if (cls >= 0) atomicAdd(&s_clsb[cls], 1);
   __syncthreads();
   if (tid == 0) {
-    // tiny serial scans (E <= 512)
-    int run = 0, runf = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = run;
-      run += s_cnt[e];
-    }
-    s_off[E] = run;
-    for (int e = 0; e < nexp; ++e) {
-      s_full[e] = runf;
-      runf += s_cnt[e] / kTileRows;
-    }
-    s_full[nexp] = runf;
-  }
-  __syncthreads();
-  for (int e = tid; e <= E; e += blockDim.x) offsets[e] = s_off[e];
-  if (tid < nexp) {
-    const int tail = s_cnt[tid] % kTileRows;
-    const int cls = tail ? ((tail + 15) >> 4) - 1 : -1;  // 0..15 (npad 16..256)
-    s_cls[tid] = cls;
-    if (cls >= 0) atomicAdd(&s_clsn[cls], 1);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int run = s_full[nexp];
+    int run = total_full;
     for (int c = 15; c >= 0; --c) {
+      const int n = s_clsb[c];
       s_clsb[c] = run;
-      run += s_clsn[c];
+      run += n;
     }
     *ntiles = run;
   }
   __syncthreads();
   if (tid < nexp) {
     const int e = tid;
-    const int row_base = (e < E) ? s_off[e] : T * k;
-    const int nf = s_cnt[e] / kTileRows;
+    const int row_base = (e < E) ? off : T * k;
     for (int i = 0; i < nf; ++i)
-      tiles[s_full[e] + i] = make_int4(e, row_base + i * kTileRows, kTileRows, kTileRows);
-    const int cls = s_cls[e];
+      tiles[full_off + i] = make_int4(e, row_base + i * kTileRows, kTileRows, kTileRows);
     if (cls >= 0) {
       int rank = 0;
       for (int f = 0; f < e; ++f) rank += (s_cls[f] == cls);
-      const int tail = s_cnt[e] - nf * kTileRows;
-      tiles[s_clsb[cls] + rank] =
-          make_int4(e, row_base + nf * kTileRows, tail, (tail + 15) & ~15);
+      tiles[s_clsb[cls] + rank] = make_int4(e, row_base + nf * kTileRows, tail, (tail + 15) & ~15);
     }
   }
 }
@@ -258,7 +298,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(
       const int e = idx[(long long)t * k + j];
       int rank = 0;
       for (int wd = 0; wd < (tl >> 5); ++wd) rank += __popc(mask[e][wd]);
-      rank += __popc(mask[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+      rank += __popc(mask[e][tl >> 5] & ((1u << (tl & 31)) - 1u));  // tokens before t
       const int row = offsets[e] + base[(long long)b * E + e] + rank;
       perm[row] = t;
       slot[(long long)t * k + j] = row;
@@ -314,11 +354,11 @@ cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const
   const Workspace& ws = h->ws;
   const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
   if (c.E <= 256)
-    topk_kernel<8><<<nblk, 256, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
+    topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
                                           c.has_shared, ws.logits, ws.idx, ws.w, ws.sigma,
                                           ws.x16, ws.hist, h->dev_err);
   else
-    topk_kernel<16><<<nblk, 256, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
+    topk_kernel<16><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
                                            c.has_shared, ws.logits, ws.idx, ws.w, ws.sigma,
                                            ws.x16, ws.hist, h->dev_err);
   return cudaGetLastError();

@@ -53,7 +53,7 @@ class _Weights(ctypes.Structure):
 
 
 class _Trace(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "idx", "w", "sigma", "out")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("logits", "idx", "w", "sigma", "out", "timestamps")]
 
 
 _lib = None
@@ -242,8 +242,9 @@ def decode(layers: list, x: torch.Tensor, bias: torch.Tensor | None = None, eps:
                  idx=torch.empty(L, c.k, dtype=torch.int32, device=dev),
                  w=torch.empty(L, c.k, dtype=torch.float32, device=dev),
                  sigma=torch.empty(L, dtype=torch.float32, device=dev),
-                 out=torch.empty(L, c.d, dtype=torch.bfloat16, device=dev))
-        tr = _Trace(*[_ptr(t[n]) for n in ("logits", "idx", "w", "sigma", "out")])
+                 out=torch.empty(L, c.d, dtype=torch.bfloat16, device=dev),
+                 timestamps=torch.zeros(L, 4, dtype=torch.int64, device=dev))
+        tr = _Trace(*[_ptr(t[n]) for n in ("logits", "idx", "w", "sigma", "out", "timestamps")])
     _check(lib.moe_decode(arr, L, _ptr(x), _ptr(bias), float(eps), _ptr(y),
                           ctypes.byref(tr) if tr is not None else None, _stream(stream)))
     return (y, t) if trace else y
