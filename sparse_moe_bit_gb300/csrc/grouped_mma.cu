@@ -1,6 +1,7 @@
 // Grouped tensor-core GEMM for sm_103a: tcgen05.mma with TMEM accumulators,
-// operands staged in shared memory by bulk (TMA) copies and cp.async, 4-bit
-// weights dequantised tile by tile inside the pipeline.
+// operands staged in shared memory by the tensor memory accelerator (bulk
+// copies for the weight codes, 2-D tensor tiles and 4-row gathers for the
+// token rows), 4-bit weights dequantised tile by tile inside the pipeline.
 //
 // One work unit computes two 128-row weight tiles (A0, A1) against one token
 // tile of up to 256 rows (B), over K in blocks of 64 (one quantisation group
@@ -22,14 +23,16 @@
 // expert's row count: the token dimension N of each tile is the expert's
 // remaining row count rounded up to 16, at most 256).
 //
-// Warp roles (448 threads, one CTA per SM, persistent over the unit list):
-//   warp 0      lane 0: bulk copies of A (codes+scales, or router rows)
-//   warp 1      lane 0: tcgen05.mma issue; the warp owns the TMEM allocation
-//   warps 2..5  dequantise codes -> fp16 A tiles (128-byte swizzled, K-major)
-//   warps 6..9  gather B rows with cp.async into 128-byte swizzled tiles
-//   warps 10..13 epilogue: tcgen05.ld, activation / scaling, global stores
-// Pipelines: kStages stages of {codes, A, B}; TMEM holds two fp32
-// accumulators of 256 columns (A0 at column 0, A1 at column 256).
+// Warp roles (512 threads, one CTA per SM, persistent over the unit list):
+//   warp 0      B producer (lane 0 issues TMA; the warp stages row indices)
+//               and, for the router, the A bulk copies
+//   warp 1      lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
+//   warp 2      lane 0 issues the bulk copies of the weight codes
+//   warps 4..7  dequantise codes -> fp16 A tiles (128-byte swizzled, K-major)
+//   warps 8..15 epilogue: tcgen05.ld, activation / scaling, staging in shared
+//               memory, bulk stores of 64-byte row segments
+// Rings: A 2 stages, B 3 stages, codes 3 stages.  TMEM: two fp32 accumulators
+// of 256 columns (A0 at column 0, A1 at column 256).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -39,15 +42,19 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
+constexpr int kAStages = 2, kBStages = 3, kCStages = 3;
 constexpr int kAStage = 32768;  // two 128 x 64 x 16-bit tiles
 constexpr int kBStage = 32768;  // up to 256 x 64 x 16-bit
+constexpr int kEpiWarps = 8;
+constexpr int kStageBuf = 2048;  // per epilogue warp and buffer: 16 rows x 64 x 16-bit
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kAStage;
-constexpr int kOffCodes = kOffB + kStages * kBStage;
-constexpr int kOffBar = kOffCodes + kStages * kCodeChunk;
-constexpr int kNumBars = 5 * kStages + 3;
+constexpr int kOffB = kOffA + kAStages * kAStage;
+constexpr int kOffCodes = kOffB + kBStages * kBStage;
+constexpr int kOffStage = kOffCodes + kCStages * kCodeChunk;
+constexpr int kOffRows = kOffStage + kEpiWarps * 2 * kStageBuf;  // 256 gather row indices
+constexpr int kOffBar = kOffRows + 256 * 4;
+constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kCStages + 3;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -85,15 +92,21 @@ struct Smem {
   __device__ uint32_t a(int s) const { return base + kOffA + s * kAStage; }
   __device__ uint32_t b(int s) const { return base + kOffB + s * kBStage; }
   __device__ uint32_t codes(int s) const { return base + kOffCodes + s * kCodeChunk; }
+  __device__ uint32_t stage(int w, int i) const {
+    return base + kOffStage + (w * 2 + i) * kStageBuf;
+  }
   __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
-  __device__ uint32_t code_full(int s) const { return bar(s); }
-  __device__ uint32_t code_empty(int s) const { return bar(kStages + s); }
-  __device__ uint32_t a_full(int s) const { return bar(2 * kStages + s); }
-  __device__ uint32_t b_full(int s) const { return bar(3 * kStages + s); }
-  __device__ uint32_t ab_empty(int s) const { return bar(4 * kStages + s); }
-  __device__ uint32_t acc_full() const { return bar(5 * kStages); }
-  __device__ uint32_t acc_empty() const { return bar(5 * kStages + 1); }
-  __device__ uint32_t drain() const { return bar(5 * kStages + 2); }
+  __device__ uint32_t a_full(int s) const { return bar(s); }
+  __device__ uint32_t a_empty(int s) const { return bar(kAStages + s); }
+  __device__ uint32_t b_full(int s) const { return bar(2 * kAStages + s); }
+  __device__ uint32_t b_empty(int s) const { return bar(2 * kAStages + kBStages + s); }
+  __device__ uint32_t c_full(int s) const { return bar(2 * kAStages + 2 * kBStages + s); }
+  __device__ uint32_t c_empty(int s) const {
+    return bar(2 * kAStages + 2 * kBStages + kCStages + s);
+  }
+  __device__ uint32_t acc_full() const { return bar(kNumBars - 3); }
+  __device__ uint32_t acc_empty() const { return bar(kNumBars - 2); }
+  __device__ uint32_t drain() const { return bar(kNumBars - 1); }
 };
 
 __device__ __forceinline__ void record_timeout(volatile int* abort_flag, int* err) {
@@ -101,42 +114,53 @@ __device__ __forceinline__ void record_timeout(volatile int* abort_flag, int* er
   atomicOr(err, MOE_DEVERR_WAIT_TIMEOUT);
 }
 
-// All 32 lanes wait for the phase; the give-up decision is taken by lane 0 and
-// shared, so the warp leaves together.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err) {
-  const int lane = threadIdx.x & 31;
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    const bool done = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    if ((i & 63u) == 63u) {
-      int bail = 0;
-      if (lane == 0) {
-        const uint64_t now = globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        else if (now - t0 > kWaitLimitNs) bail = 1;
-        if (*abort_flag) bail = 1;
-      }
-      bail = __shfl_sync(0xffffffffu, bail, 0);
-      if (bail) {
-        if (lane == 0) record_timeout(abort_flag, err);
-        return false;
-      }
-    }
-  }
+// mbarrier wait that suspends the thread in hardware between checks
+__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                             int* err) {
-  if (mbar_wait_bounded(bar, parity, abort_flag, kWaitLimitNs)) return true;
-  record_timeout(abort_flag, err);
-  return false;
+  if (try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (try_wait_sleep(bar, parity)) return true;
+    if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_timeout(abort_flag, err);
+      return false;
+    }
+  }
 }
 
-// fp16 pair (1024 + q_lo, 1024 + q_hi) from the nibbles at bit 4j and 16+4j.
+// every lane waits (suspended); the give-up decision is the warp's together
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err) {
+  bool ok = try_wait_sleep(bar, parity);
+  if (__all_sync(0xffffffffu, ok)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    ok = ok || try_wait_sleep(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    int bail = 0;
+    if ((threadIdx.x & 31) == 0) bail = (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs);
+    if (__shfl_sync(0xffffffffu, bail, 0)) {
+      if ((threadIdx.x & 31) == 0) record_timeout(abort_flag, err);
+      return false;
+    }
+  }
+}
+
+// fp16 pair (q_lo, q_hi) * s + beta from the nibbles at bit 4j and 16+4j
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t v, int j, uint32_t s2, uint32_t b2) {
-  const uint32_t t = ((v >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+  const uint32_t t = ((v >> (4 * j)) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
   __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&t),
                       __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
   __half2 r = __hfma2(q, *reinterpret_cast<const __half2*>(&s2),
@@ -144,8 +168,30 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t v, int j, uint32_t s2,
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+__device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int4 rows,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const MmaParams p) {
+__global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_constant__ MmaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -159,17 +205,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const MmaParam
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* rows_s = reinterpret_cast<int*>(smem + kOffRows);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(S.code_full(s), 1);
-      mbar_init(S.code_empty(s), 4);
+    for (int s = 0; s < kAStages; ++s) {
       mbar_init(S.a_full(s), MODE == MMA_ROUTER ? 1 : 4);
-      mbar_init(S.b_full(s), 4);
-      mbar_init(S.ab_empty(s), 1);
+      mbar_init(S.a_empty(s), 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(S.b_full(s), 1);
+      mbar_init(S.b_empty(s), 1);
+    }
+    for (int s = 0; s < kCStages; ++s) {
+      mbar_init(S.c_full(s), 1);
+      mbar_init(S.c_empty(s), 4);
     }
     mbar_init(S.acc_full(), 1);
-    mbar_init(S.acc_empty(), 4);
+    mbar_init(S.acc_empty(), kEpiWarps);
     mbar_init(S.drain(), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -185,59 +237,90 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const MmaParam
   const int kbu = p.kb_per_unit;
 
   if (warp == 0) {
-    // ---------------------------------------------------------- A producer
-    if (lane == 0) {
-      uint32_t g = 0;
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-        const Unit t = get_unit(p, MODE, u);
-        const uint8_t* src = p.wA + (long long)t.expert * p.a_expert_stride +
-                             (long long)t.m * p.a_unit_stride +
-                             (long long)t.ks * kbu * p.a_chunk;
-        for (int kb = 0; kb < kbu; ++kb, ++g) {
-          const int s = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
-          if (MODE == MMA_ROUTER) {
-            if (!thread_wait(S.ab_empty(s), ph ^ 1, abort_flag, p.err)) goto a_done;
+    // ------------------------------------------------------ B (+ router A)
+    uint32_t gb = 0, ga = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const Unit t = get_unit(p, MODE, u);
+      if (MODE == MMA_GATEUP) {
+        // row indices of the unit's tokens; padding rows repeat a valid row
+        __syncwarp();
+        for (int i = lane; i < t.npad; i += 32)
+          rows_s[i] = p.b_rowmap[t.row0 + (i < t.nrows ? i : 0)];
+        __syncwarp();
+      }
+      const int k0 = t.ks * kbu;
+      const uint8_t* asrc = p.wA + (long long)t.m * p.a_unit_stride + (long long)k0 * p.a_chunk;
+      for (int kb = 0; kb < kbu; ++kb) {
+        if (MODE == MMA_ROUTER) {
+          const int s = ga % kAStages;
+          if (!warp_wait(S.a_empty(s), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
             mbar_arrive_expect_tx(S.a_full(s), kRouterChunk);
-            bulk_g2s(S.a(s), src + (long long)kb * p.a_chunk, kRouterChunk, S.a_full(s));
-          } else {
-            if (!thread_wait(S.code_empty(s), ph ^ 1, abort_flag, p.err)) goto a_done;
-            mbar_arrive_expect_tx(S.code_full(s), kCodeChunk);
-            bulk_g2s(S.codes(s), src + (long long)kb * p.a_chunk, kCodeChunk, S.code_full(s));
+            bulk_g2s(S.a(s), asrc + (long long)kb * p.a_chunk, kRouterChunk, S.a_full(s));
+          }
+          ++ga;
+        }
+        const int s = gb % kBStages;
+        if (!warp_wait(S.b_empty(s), ((gb / kBStages) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bs = S.b(s);
+        const int x = (k0 + kb) * 64;
+        if (MODE == MMA_GATEUP) {
+          // 4-row gathers, issued by 16 lanes (lane i: rows 4i, 4i + 64, ...)
+          if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
+          __syncwarp();
+          if (lane < 16) {
+            for (int n = 4 * lane; n < t.npad; n += 64) {
+              const int4 r4 = *reinterpret_cast<const int4*>(rows_s + n);
+              tma_gather4(bs + n * 128, &p.tmB, x, r4, S.b_full(s));
+            }
+          }
+        } else if (lane == 0) {
+          {
+            const int nbox = (t.npad + 31) >> 5;
+            mbar_arrive_expect_tx(S.b_full(s), (uint32_t)nbox * 4096);
+            for (int i = 0; i < nbox; ++i)
+              tma_tile_2d(bs + i * 4096, &p.tmB, x, t.row0 + 32 * i, S.b_full(s));
           }
         }
+        ++gb;
       }
-    a_done:;
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t g = 0, i = 0;
+      uint32_t ga = 0, gb = 0, i = 0;
       for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
         const Unit t = get_unit(p, MODE, u);
         if (!thread_wait(S.acc_empty(), (i & 1) ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
         bool ok = true;
-        for (int kb = 0; kb < kbu; ++kb, ++g) {
-          const int s = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
-          if (!thread_wait(S.a_full(s), ph, abort_flag, p.err) ||
-              !thread_wait(S.b_full(s), ph, abort_flag, p.err)) {
+        for (int kb = 0; kb < kbu; ++kb, ++ga, ++gb) {
+          const int sa = ga % kAStages, sb = gb % kBStages;
+          if (!thread_wait(S.a_full(sa), (ga / kAStages) & 1, abort_flag, p.err) ||
+              !thread_wait(S.b_full(sb), (gb / kBStages) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a0 = sdesc_k_sw128(S.a(s) + kk * 32);
-            const uint64_t a1 = sdesc_k_sw128(S.a(s) + 16384 + kk * 32);
-            const uint64_t bd = sdesc_k_sw128(S.b(s) + kk * 32);
+            const uint64_t a0 = sdesc_k_sw128(S.a(sa) + kk * 32);
+            const uint64_t a1 = sdesc_k_sw128(S.a(sa) + 16384 + kk * 32);
+            const uint64_t bd = sdesc_k_sw128(S.b(sb) + kk * 32);
             const uint32_t acc = (kb | kk) ? 1u : 0u;
             tc_mma_f16(tmem, a0, bd, idesc, acc);
             tc_mma_f16(tmem + 256, a1, bd, idesc, acc);
           }
-          tc_commit(S.ab_empty(s));
+          tc_commit(S.a_empty(sa));
+          tc_commit(S.b_empty(sb));
         }
         if (!ok) break;
         tc_commit(S.acc_full());
@@ -246,19 +329,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const MmaParam
       tc_commit(S.drain());
       mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
     }
-  } else if (warp < 6) {
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- codes
+    if (MODE != MMA_ROUTER && lane == 0) {
+      uint32_t gc = 0;
+      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+        const Unit t = get_unit(p, MODE, u);
+        const uint8_t* src = p.wA + (long long)t.expert * p.a_expert_stride +
+                             (long long)t.m * p.a_unit_stride;
+        for (int kb = 0; kb < kbu; ++kb, ++gc) {
+          const int s = gc % kCStages;
+          if (!thread_wait(S.c_empty(s), ((gc / kCStages) & 1) ^ 1, abort_flag, p.err)) goto c_done;
+          mbar_arrive_expect_tx(S.c_full(s), kCodeChunk);
+          bulk_g2s(S.codes(s), src + (long long)kb * p.a_chunk, kCodeChunk, S.c_full(s));
+        }
+      }
+    c_done:;
+    }
+  } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- dequantise
     if (MODE != MMA_ROUTER) {
-      const int dw = warp - 2;
-      uint32_t g = 0;
+      const int dw = warp - 4;
+      uint32_t ga = 0, gc = 0;
       for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-        for (int kb = 0; kb < kbu; ++kb, ++g) {
-          const int s = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
-          if (!warp_wait(S.code_full(s), ph, abort_flag, p.err)) goto dq_done;
-          if (!warp_wait(S.ab_empty(s), ph ^ 1, abort_flag, p.err)) goto dq_done;
-          const uint32_t codes = S.codes(s);
-          const uint32_t a = S.a(s);
+        for (int kb = 0; kb < kbu; ++kb, ++ga, ++gc) {
+          const int sc = gc % kCStages, sa = ga % kAStages;
+          if (!warp_wait(S.c_full(sc), (gc / kCStages) & 1, abort_flag, p.err)) goto dq_done;
+          if (!warp_wait(S.a_empty(sa), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) goto dq_done;
+          const uint32_t codes = S.codes(sc);
+          const uint32_t a = S.a(sa);
           const int c = lane & 7;
 #pragma unroll 4
           for (int it = 0; it < 16; ++it) {
@@ -277,98 +376,121 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const MmaParam
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(S.a_full(s));
-            mbar_arrive(S.code_empty(s));
+            mbar_arrive(S.a_full(sa));
+            mbar_arrive(S.c_empty(sc));
           }
         }
       }
     dq_done:;
     }
-  } else if (warp < 10) {
-    // ---------------------------------------------------------- B loader
-    const int bt = threadIdx.x - 192;
-    uint32_t g = 0;
-    int prev_s = -1;
-    bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const Unit t = get_unit(p, MODE, u);
-      const long long k0 = (long long)t.ks * kbu * 64;
-      for (int kb = 0; kb < kbu; ++kb, ++g) {
-        const int s = g % kStages;
-        const uint32_t ph = (g / kStages) & 1;
-        if (!warp_wait(S.ab_empty(s), ph ^ 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bs = S.b(s);
-        for (int i = bt; i < t.npad * 8; i += 128) {
-          const int n = i >> 3;
-          const int c = i & 7;
-          const bool valid = n < t.nrows;
-          const uint16_t* src = p.B;
-          if (valid) {
-            const int grow = t.row0 + n;
-            const long long srow = p.b_rowmap ? (long long)p.b_rowmap[grow] : (long long)grow;
-            src = p.B + srow * p.ldb + k0 + kb * 64 + c * 8;
-          }
-          cp_async16(bs + n * 128 + ((c ^ (n & 7)) << 4), src, valid ? 16u : 0u);
-        }
-        cp_async_commit();
-        if (prev_s >= 0) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(S.b_full(prev_s));
-        }
-        prev_s = s;
-      }
-    }
-    cp_async_wait<0>();
-    if (ok && prev_s >= 0) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(S.b_full(prev_s));
-    }
-  } else {
+  } else if (warp >= 8) {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int e = warp - 8;            // 0..7
+    const int q = warp & 3;            // TMEM lane quarter
+    const int half = e >> 2;           // columns [128*half, 128*half + 128)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t i = 0;
+    uint32_t i = 0, nst = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
       const Unit t = get_unit(p, MODE, u);
+      const int c0 = half * 128;
+      const int c1 = min(c0 + 128, t.npad);
+      // row data of the warp's 128 columns, fetched while the MMAs run:
+      // lane l holds rows c0 + l + 32 v, v = 0..3
+      float rsc4[4] = {0.f, 0.f, 0.f, 0.f};
+      int rdst4[4] = {0, 0, 0, 0};
+      if (MODE == MMA_DOWN) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int n = c0 + lane + 32 * v;
+          if (n < t.nrows) {
+            rsc4[v] = p.row_scale[t.row0 + n];
+            rdst4[v] = p.dst_row[t.row0 + n];
+          }
+        }
+      }
       if (!warp_wait(S.acc_full(), i & 1, abort_flag, p.err)) break;
       tc_fence_after();
-      for (int n0 = 0; n0 < t.npad; n0 += 16) {
+      for (int n0 = c0; n0 < c1; n0 += 16) {
         uint32_t r0[16], r1[16];
         tmem_ld16(tmem + lane_base + n0, r0);
         tmem_ld16(tmem + lane_base + 256 + n0, r1);
-        tmem_ld_wait();
+        const int nvalid = min(16, t.nrows - n0);
+        // this chunk's rows n0..n0+15 are held by lanes (n0 - c0) % 32 + j
+        // in register slot (n0 - c0) / 32
+        const int vsel = (n0 - c0) >> 5;
+        const int lsel = (n0 - c0) & 31;
+        float rsc_v = rsc4[0];
+        int rdst_v = rdst4[0];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = n0 + j;
-          if (n < t.nrows) {
+        for (int v = 1; v < 4; ++v) {
+          if (vsel == v) {
+            rsc_v = rsc4[v];
+            rdst_v = rdst4[v];
+          }
+        }
+        const float rsc = __shfl_sync(0xffffffffu, rsc_v, (lsel + lane) & 31);
+        const long long rdst = __shfl_sync(0xffffffffu, rdst_v, (lsel + lane) & 31);
+        tmem_ld_wait();
+        if (MODE == MMA_ROUTER) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j >= nvalid) break;
+            const int row = t.row0 + n0 + j;
+            const int ex = t.m * 256 + q * 32 + lane;
+            float* o = p.out_f32 + ((long long)t.ks * p.rows_total + row) * p.E;
+            if (ex < p.E) o[ex] = __uint_as_float(r0[j]);
+            if (ex + 128 < p.E) o[ex + 128] = __uint_as_float(r1[j]);
+          }
+          continue;
+        }
+        // stage [16 rows][32 or 64 values] in shared memory, then 16-byte
+        // vector stores of whole 64-byte row segments
+        const uint32_t sbuf = S.stage(e, nst & 1);
+        __syncwarp();  // the buffer's previous reads are done
+        if (nvalid > 0) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
             const float v0 = __uint_as_float(r0[j]);
             const float v1 = __uint_as_float(r1[j]);
-            const int row = t.row0 + n;
             if (MODE == MMA_GATEUP) {
               const float h = v0 / (1.0f + __expf(-v0)) * v1;
-              const int f = t.m * 128 + q * 32 + lane;
-              p.H[(long long)row * p.ldh + f] = __half_as_ushort(__float2half_rn(h));
-            } else if (MODE == MMA_DOWN) {
-              const float sc = p.row_scale[row];
-              const long long drow = p.dst_row[row];
-              const int f = t.m * 256 + q * 32 + lane;
-              uint16_t* yr = p.Y + drow * p.ldy;
-              yr[f] = __bfloat16_as_ushort(__float2bfloat16_rn(sc * v0));
-              yr[f + 128] = __bfloat16_as_ushort(__float2bfloat16_rn(sc * v1));
+              st_shared_u16(sbuf + j * 64 + lane * 2, __half_as_ushort(__float2half_rn(h)));
             } else {
-              const int e = t.m * 256 + q * 32 + lane;
-              float* o = p.out_f32 + ((long long)t.ks * p.rows_total + row) * p.E;
-              if (e < p.E) o[e] = v0;
-              if (e + 128 < p.E) o[e + 128] = v1;
+              const float sc = __shfl_sync(0xffffffffu, rsc, j);
+              st_shared_u16(sbuf + j * 128 + lane * 2,
+                            __bfloat16_as_ushort(__float2bfloat16_rn(sc * v0)));
+              st_shared_u16(sbuf + j * 128 + 64 + lane * 2,
+                            __bfloat16_as_ushort(__float2bfloat16_rn(sc * v1)));
             }
           }
         }
+        __syncwarp();
+        if (MODE == MMA_GATEUP) {
+          // 16 rows x 64 bytes: lane -> (row lane/4 + 8i, 16-byte piece lane%4)
+#pragma unroll
+          for (int it = 0; it < 2; ++it) {
+            const int j = (lane >> 2) + 8 * it;
+            if (j < nvalid) {
+              const uint4 v = ld_shared_v4(sbuf + j * 64 + (lane & 3) * 16);
+              const long long row = t.row0 + n0 + j;
+              *reinterpret_cast<uint4*>(p.H + row * p.ldh + t.m * 128 + q * 32 + (lane & 3) * 8) = v;
+            }
+          }
+        } else {
+          // 16 rows x 2 segments x 64 bytes: lane -> (row lane/8 + 4i, piece lane%8)
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int j = (lane >> 3) + 4 * it;
+            const long long dj = __shfl_sync(0xffffffffu, rdst, j);
+            if (j < nvalid) {
+              const int pc = lane & 7;  // pieces 0..3: first segment, 4..7: second
+              const uint4 v = ld_shared_v4(sbuf + j * 128 + pc * 16);
+              uint16_t* yr = p.Y + dj * p.ldy + t.m * 256 + q * 32 + (pc >> 2) * 128 + (pc & 3) * 8;
+              *reinterpret_cast<uint4*>(yr) = v;
+            }
+          }
+        }
+        ++nst;
       }
       tc_fence_before();
       __syncwarp();
@@ -397,7 +519,41 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
 }  // namespace
+
+cudaError_t make_tmap_16bit(CUtensorMap* map, const void* base, long long rows, long long cols,
+                            int box_rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st) {
   if (grid <= 0) return cudaSuccess;

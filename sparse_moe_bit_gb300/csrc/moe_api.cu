@@ -163,6 +163,8 @@ moe_status alloc_all(Handle* h) {
     CK(dalloc(&w.x16, (size_t)T * c.d * 2), "alloc");
     CK(dalloc(&w.H, (size_t)T * k1 * c.I * 2), "alloc");
     CK(dalloc(&w.Y, (size_t)T * k1 * c.d * 2), "alloc");
+    CK(make_tmap_16bit(&h->tm_x16, w.x16, T, c.d, 1, false), "tensor map (x16)");
+    CK(make_tmap_16bit(&h->tm_h, w.H, T * k1, c.I, 32, false), "tensor map (H)");
   }
   CK(dalloc(&w.x_dev, (size_t)T * c.d * 2), "alloc");
   CK(dalloc(&w.y_dev, (size_t)T * c.d * 2), "alloc");
@@ -195,8 +197,7 @@ moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int
     p.a_expert_stride = 0;
     p.a_unit_stride = (long long)(c.d / 64) * kRouterChunk;
     p.a_chunk = kRouterChunk;
-    p.B = x;
-    p.ldb = c.d;
+    CK(make_tmap_16bit(&p.tmB, x, T, c.d, 32, true), "tensor map (x)");
     p.b_rowmap = nullptr;
     p.out_f32 = h->ws.logit_part;
     p.E = c.E;
@@ -232,8 +233,7 @@ moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
   p.wA = h->pf_gu;
   p.a_unit_stride = (long long)(c.d / 64) * kCodeChunk;
   p.a_expert_stride = p.a_unit_stride * (c.I / 128);
-  p.B = w.x16;
-  p.ldb = c.d;
+  p.tmB = h->tm_x16;
   p.b_rowmap = w.perm;
   p.H = w.H;
   p.ldh = c.I;
@@ -248,8 +248,7 @@ moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
   p.wA = h->pf_dn;
   p.a_unit_stride = (long long)(c.I / 64) * kCodeChunk;
   p.a_expert_stride = p.a_unit_stride * (c.d / 256);
-  p.B = w.H;
-  p.ldb = c.I;
+  p.tmB = h->tm_h;
   p.b_rowmap = nullptr;
   p.Y = w.Y;
   p.ldy = c.d;

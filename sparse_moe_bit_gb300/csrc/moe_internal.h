@@ -1,5 +1,6 @@
 // Internal structures shared by the translation units of libmoe.so.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -62,6 +63,8 @@ struct Handle {
   uint16_t* w_router = nullptr;  // bf16 [E][d]
   uint16_t* w_sg = nullptr;      // bf16 [d]
   Workspace ws;
+  CUtensorMap tm_x16;  // gate/up B: x16 [Tmax][d], 1-row box (4-row gathers)
+  CUtensorMap tm_h;    // down B: H [Tmax*(k+1)][I], 32-row box
   // per-stage timing (moe_profile_enable)
   static constexpr int kStagesTimed = 7;
   static constexpr int kProfCalls = 4096;
@@ -83,6 +86,7 @@ inline int decode_dn_sb_pitch(int I) { return ((I / 64) + 3) & ~3; }
 enum MmaMode { MMA_ROUTER = 0, MMA_GATEUP = 1, MMA_DOWN = 2 };
 
 struct MmaParams {
+  CUtensorMap tmB;      // B operand: 2-D map, 64 x rows box, 128-byte swizzle
   int kb_per_unit;      // 64-wide K blocks per work unit
   int m_units;          // 256-row weight units per tile
   int units_per_tile;   // m_units * ksplit
@@ -96,9 +100,8 @@ struct MmaParams {
   long long a_expert_stride;  // bytes per expert
   long long a_unit_stride;    // bytes per 256-row unit
   int a_chunk;                // bytes per K block
-  // B operand: 16-bit rows
-  const uint16_t* B;
-  int ldb;
+  // B operand rows: gathered through b_rowmap (gate/up: 4-row TMA gathers) or
+  // contiguous from row0 (router, down: 32-row TMA tiles)
   const int32_t* b_rowmap;    // grouped row -> source row, or null
   // epilogue
   float* out_f32;             // router partials [KS][T][E]
@@ -112,6 +115,10 @@ struct MmaParams {
   int* err;
 };
 cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st);
+// 2-D tensor map over a row-major [rows][cols] 16-bit matrix, box {64, box_rows},
+// 128-byte swizzle (the tensor-core operand layout), zero fill out of bounds
+cudaError_t make_tmap_16bit(CUtensorMap* map, const void* base, long long rows, long long cols,
+                            int box_rows, bool bf16);
 
 // ---- routing (routing.cu)
 cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
