@@ -208,6 +208,31 @@ moe_status moe_decode_host(moe_handle* const* layers, int L, const void* x_host,
 moe_status moe_profile_enable(moe_handle* h, int enable);
 moe_status moe_profile_read(moe_handle* h, float* ms, int n, int* calls);
 
+/*
+ * Routing from given logits (as moe_route_from_logits, no handle, no shared
+ * expert) that allocates no device memory.  The pages have no counterpart of
+ * this entry point: it exists for callers that cannot call cudaMalloc -- code
+ * running inside a device memory allocator or its callbacks, serving loops
+ * that must never pay cudaMalloc's implicit device synchronisation, programs
+ * whose device memory is entirely owned by another framework.
+ *   Scratch: one file-scope device array of about 2.5 MB inside this library,
+ *   held by every GPU that loads the library until the process exits.  Limits:
+ *   T <= 2048, E <= 256, k <= 16 and k <= E; larger sizes return
+ *   MOE_ERR_INVALID_ARG before anything is enqueued.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (different
+ *   streams without ordering) race and give undefined results.
+ *   Inputs: logits fp32 [T][E] (device), logit_bias fp32 [E] or NULL.
+ *   Outputs (device, all required): idx int32 [T][k], w fp32 [T][k],
+ *   counts int32 [E], offsets int32 [E+1], perm int32 [T*k], slot int32 [T][k].
+ *   NaN logits are treated as -inf (not reported by this entry point).
+ */
+moe_status moe_route_from_logits_noalloc(const float* logits, int T, int E, int k,
+                                         const float* logit_bias, int32_t* idx, float* w,
+                                         int32_t* counts, int32_t* offsets, int32_t* perm,
+                                         int32_t* slot, void* stream);
+
 /* Synchronise the stream of the handle's last call and read (then clear) its
  * device error word (MOE_DEVERR_* bits).  Test and debugging aid. */
 moe_status moe_get_device_error(moe_handle* h, int* code);

@@ -11,6 +11,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "moe_internal.h"
 
@@ -389,4 +390,89 @@ cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st)
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// Routing from given logits with no device allocation.
+//
+// For callers that cannot call cudaMalloc: code running inside a device
+// memory allocator or its callbacks, serving loops that must never hit
+// cudaMalloc's implicit device synchronisation, and programs whose device
+// memory is entirely owned by another framework.  The kernels' scratch lives
+// in one file-scope device array of fixed size that every GPU loading this
+// library holds until the process exits.
+namespace {
+
+constexpr int kNaMaxT = 2048;  // tokens per call
+constexpr int kNaMaxE = 256;   // experts
+constexpr int kNaMaxK = kMaxK; // kept experts per token
+constexpr int kNaBlk = kNaMaxT / kTokPerBlock;
+constexpr int kNaTiles = kNaMaxT * kNaMaxK / kTileRows + kNaMaxE + 2;
+
+constexpr size_t na_align(size_t v) { return (v + 255) / 256 * 256; }
+constexpr size_t kNaLogits = 0;
+constexpr size_t kNaHist = na_align(kNaLogits + sizeof(float) * kNaMaxT * kNaMaxE);
+constexpr size_t kNaBase = na_align(kNaHist + sizeof(int32_t) * kNaBlk * kNaMaxE);
+constexpr size_t kNaDst = na_align(kNaBase + sizeof(int32_t) * kNaBlk * kNaMaxE);
+constexpr size_t kNaWrow = na_align(kNaDst + sizeof(int32_t) * kNaMaxT * kNaMaxK);
+constexpr size_t kNaTilesOff = na_align(kNaWrow + sizeof(float) * kNaMaxT * kNaMaxK);
+constexpr size_t kNaNtiles = na_align(kNaTilesOff + sizeof(int4) * kNaTiles);
+constexpr size_t kNaErr = na_align(kNaNtiles + 16);
+constexpr size_t kNaBytes = na_align(kNaErr + 16);  // about 2.5 MB
+
+// The scratch.  Host code must not pass &g_na_scratch to a kernel: on the host
+// the name is only a stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_na_scratch[kNaBytes];
+
+std::mutex g_na_mutex;
+unsigned char* g_na_ptr[64] = {};  // device address of g_na_scratch, per device
+
+cudaError_t na_scratch(unsigned char** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  if (!g_na_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_na_scratch);
+    if (e != cudaSuccess) return e;
+    g_na_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_na_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
 }  // namespace moe
+
+extern "C" moe_status moe_route_from_logits_noalloc(const float* logits, int T, int E, int k,
+                                                    const float* logit_bias, int32_t* idx,
+                                                    float* w, int32_t* counts, int32_t* offsets,
+                                                    int32_t* perm, int32_t* slot, void* stream) {
+  using namespace moe;
+  if (T < 0 || T > kNaMaxT || E < 1 || E > kNaMaxE || k < 1 || k > kNaMaxK || k > E)
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !idx || !w || !counts || !offsets || !perm || !slot) return MOE_ERR_INVALID_ARG;
+  unsigned char* s = nullptr;
+  if (na_scratch(&s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
+  int32_t* hist = reinterpret_cast<int32_t*>(s + kNaHist);
+  int32_t* base = reinterpret_cast<int32_t*>(s + kNaBase);
+  int4* tiles = reinterpret_cast<int4*>(s + kNaTilesOff);
+  int32_t* ntiles = reinterpret_cast<int32_t*>(s + kNaNtiles);
+  // every scratch word is written before it is read: nothing to clear
+  topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(
+      logits, 1, T, E, k, logit_bias, nullptr, 256, nullptr, 0,
+      reinterpret_cast<float*>(s + kNaLogits), idx, w, nullptr, nullptr, hist,
+      reinterpret_cast<int*>(s + kNaErr));
+  scan_tiles_kernel<<<1, 1024, 0, st>>>(hist, nblk, T, E, k, 0, base, counts, offsets, tiles,
+                                        ntiles);
+  scatter_kernel<<<nblk, 256, 0, st>>>(idx, w, nullptr, offsets, base, T, E, k, 0, perm, slot,
+                                       reinterpret_cast<int32_t*>(s + kNaDst),
+                                       reinterpret_cast<float*>(s + kNaWrow));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -26,8 +26,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
 # names of the functions include/moe.h declares (checked by the ABI test)
 EXPORTS = ["moe_create", "moe_destroy", "moe_route", "moe_route_from_logits", "moe_forward",
            "moe_forward_host", "moe_decode", "moe_decode_host", "moe_profile_enable",
-           "moe_profile_read", "moe_get_device_error", "moe_status_string", "moe_last_error",
-           "moe_version"]
+           "moe_profile_read", "moe_route_from_logits_noalloc", "moe_get_device_error",
+           "moe_status_string", "moe_last_error", "moe_version"]
 
 STAGES = ["router", "topk", "scan", "scatter", "gate_up", "down", "combine"]
 
@@ -79,6 +79,7 @@ def load_library() -> ctypes.CDLL:
         "moe_decode_host": [ctypes.POINTER(P), I, P, P, F, P, P],
         "moe_profile_enable": [P, I],
         "moe_profile_read": [P, ctypes.POINTER(F), I, ctypes.POINTER(I)],
+        "moe_route_from_logits_noalloc": [P, I, I, I, P, P, P, P, P, P, P, P],
         "moe_get_device_error": [P, ctypes.POINTER(I)],
         "moe_status_string": [I],
         "moe_last_error": [],
@@ -258,3 +259,22 @@ def decode_host(layers: list, x_host: torch.Tensor, y_host: torch.Tensor,
     _check(load_library().moe_decode_host(arr, L, _ptr(x_host), _ptr(bias_host), float(eps),
                                           _ptr(y_host), _stream(stream)))
     return y_host
+
+
+def route_from_logits_noalloc(logits: torch.Tensor, k: int, bias: torch.Tensor | None = None,
+                              out: dict | None = None, stream=None) -> dict:
+    """Routing from fp32 logits [T, E] through the entry point that allocates no
+    device memory (T <= 2048, E <= 256).  Output tensors may be passed in
+    ``out`` (keys idx, w, counts, offsets, perm, slot); otherwise they are made
+    here with torch before the call."""
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = dict(idx=torch.empty(T, k, **i32), w=torch.empty(T, k, dtype=torch.float32, device=dev),
+                   counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                   perm=torch.empty(T * k, **i32), slot=torch.empty(T, k, **i32))
+    _check(load_library().moe_route_from_logits_noalloc(
+        _ptr(logits), T, E, k, _ptr(bias), _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["counts"]),
+        _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["slot"]), _stream(stream)))
+    return out
