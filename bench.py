@@ -40,6 +40,27 @@ GATEUP_FLOP_PER_ROW = 2 * D * 2 * I
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def profiled_traffic(kernel: str):
+    """DRAM bytes of `kernel` from profiles/traffic.txt, if the kernel's source
+    still has the hash recorded there (else None: the counters are stale)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split())
+        if kv.get("kernel") != kernel:
+            continue
+        src = os.path.join(ROOT, kv["source"])
+        if not os.path.exists(src):
+            return None
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        return kv if h.startswith(kv["sha256"]) else None
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -148,10 +169,10 @@ def l2_flush_buffer(torch, device):
     return torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
 
 
-def build_decode(torch, M, sd, gen, device):
+def build_decode(torch, M, sd, gen, device, n_layers=DECODE_LAYERS):
     shape = gen.MoEShape(d=D, E=E, k=K, I=I)
     layers = []
-    for l in range(DECODE_LAYERS):
+    for l in range(n_layers):
         w = sd.make_layer(0, l, shape, device=device)
         layers.append(M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=1,
                                         layouts=M.MOE_LAYOUT_DECODE), w))
@@ -160,8 +181,18 @@ def build_decode(torch, M, sd, gen, device):
     return layers
 
 
+def decode_traffic(n_layers):
+    kv = profiled_traffic("decode_kernel")
+    return int(kv["bytes_per_layer"]) * n_layers if kv else None
+
+
+def gateup_traffic():
+    kv = profiled_traffic("grouped_mma_gateup")
+    return int(kv["bytes_per_launch"]) if kv else None
+
+
 def run_decode(args, torch, M, sd, gen, device, peaks):
-    layers = build_decode(torch, M, sd, gen, device)
+    layers = build_decode(torch, M, sd, gen, device, args.decode_layers)
     nx = max(args.steps + args.warmup, 8)
     xs = sd.make_x(1, nx, D, device=device)  # a different token every step
     y = torch.empty(D, dtype=torch.bfloat16, device=device)
@@ -190,7 +221,7 @@ def run_decode(args, torch, M, sd, gen, device, peaks):
     ms_step = t_all0.elapsed_time(t_all1) / args.steps
     ms_step = max_over_ranks(ms_step, device)
     kernel_ms = statistics.mean(per)
-    bytes_launch = LAYER_BYTES_DECODE * DECODE_LAYERS
+    bytes_launch = LAYER_BYTES_DECODE * args.decode_layers
     achieved = bytes_launch / (kernel_ms * 1e-3) / 1e9
     # end to end through the C ABI with host buffers
     xh = xs[:args.steps].cpu().pin_memory()
@@ -216,10 +247,10 @@ def run_decode(args, torch, M, sd, gen, device, peaks):
     err = layers[0].device_error()
     return dict(
         ms_per_step=ms_step, value=args.world * 1000.0 / ms_step, unit="tokens/s",
-        us_per_layer=ms_step * 1000.0 / DECODE_LAYERS, phase_us=phases,
+        us_per_layer=ms_step * 1000.0 / args.decode_layers, phase_us=phases,
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                   "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                  "traffic": None, "kernel": "decode_kernel",
+                  "traffic": decode_traffic(args.decode_layers), "kernel": "decode_kernel",
                   "algorithmic_bytes_per_launch": bytes_launch},
         e2e={"value": args.world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": D * 2,
              "d2h_bytes_per_step": D * 2},
@@ -284,7 +315,8 @@ def run_prefill(args, torch, M, sd, gen, device, peaks):
         us_per_layer=ms_step * 1000.0,
         stage_ms={k: round(v / max(calls, 1), 4) for k, v in stages.items()},
         roofline={"bound": "tensor", "achieved": round(gu_tflops, 1), "peak": peak,
-                  "unit": "TFLOP/s", "frac": round(gu_tflops / peak, 4), "traffic": None,
+                  "unit": "TFLOP/s", "frac": round(gu_tflops / peak, 4),
+                  "traffic": gateup_traffic(),
                   "kernel": "grouped_mma_kernel<gate/up>",
                   "algorithmic_flop_per_launch": rows * GATEUP_FLOP_PER_ROW},
         step_roofline_frac=round((total_flop / (peak * 1e12)) / (ms_step * 1e-3), 4),
@@ -391,6 +423,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
+    ap.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
+                    help="layers of the decode chain (profiling captures use fewer)")
     args = ap.parse_args()
     ws, rank, local = dist_info()
     args.world = ws
