@@ -1,7 +1,7 @@
 // Grouped tensor-core GEMM for sm_103a: tcgen05.mma with TMEM accumulators,
-// operands staged in shared memory by the tensor memory accelerator (bulk
-// copies for the weight codes, 2-D tensor tiles and 4-row gathers for the
-// token rows), 4-bit weights dequantised tile by tile inside the pipeline.
+// token-row operands staged in shared memory by the tensor memory accelerator
+// (2-D tensor tiles and 4-row gathers, multicast across a cluster), 4-bit
+// weights dequantised tile by tile inside the pipeline.
 //
 // One work unit computes two 128-row weight tiles (A0, A1) against one token
 // tile of up to 256 rows (B), over K in blocks of 64 (one quantisation group
@@ -27,14 +27,17 @@
 //   warp 0      B producer (lane 0 issues TMA; the warp stages row indices)
 //               and, for the router, the A bulk copies
 //   warp 1      lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
-//   warp 2      lane 0 issues the bulk copies of the weight codes
-//   warps 4..7  dequantise codes -> fp16 A tiles (128-byte swizzled, K-major)
+//   warps 4..7  load the weight codes from global memory (three K blocks
+//               ahead, in registers) and dequantise them into fp16 A tiles
+//               (128-byte swizzled, K-major)
 //   warps 8..15 epilogue: tcgen05.ld, activation / scaling, staging in shared
 //               memory, bulk stores of 64-byte row segments
-// Rings: A 2 stages, B 3 stages, codes 3 stages.  TMEM: two fp32 accumulators
-// of 256 columns (A0 at column 0, A1 at column 256).
+// Rings: A 2 stages, B 4 stages.  TMEM: two fp32 accumulators of 256 columns
+// (A0 at column 0, A1 at column 256).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <cstdlib>
 
 #include "moe_internal.h"
 #include "ptx.cuh"
@@ -43,23 +46,39 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kAStages = 2, kBStages = 3, kCStages = 3;
-constexpr int kAStage = 32768;  // two 128 x 64 x 16-bit tiles
-constexpr int kBStage = 32768;  // up to 256 x 64 x 16-bit
+constexpr int kAStages = 2;
+constexpr int kBStage = 32768;   // up to 256 x 64 x 16-bit
 constexpr int kEpiWarps = 8;
-constexpr int kStageBuf = 2048;  // per epilogue warp and buffer: 16 rows x 64 x 16-bit
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kAStages * kAStage;
-constexpr int kOffCodes = kOffB + kBStages * kBStage;
-constexpr int kOffStage = kOffCodes + kCStages * kCodeChunk;
-constexpr int kOffRows = kOffStage + kEpiWarps * 2 * kStageBuf;  // 256 gather row indices
-constexpr int kOffBar = kOffRows + 256 * 4;
-constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kCStages + 3;
-constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Per-mode shape of a work unit and of the pipeline:
+//   NA   128-row weight tiles per unit (gate/up: the gate and the up tile of
+//        the same features; router: 256 experts; down: 256 output rows).  One
+//        tile per unit is supported (units are then chunk halves), but on
+//        GB300 it measured slower for the down projection: twice the B reads
+//   NACC TMEM accumulator buffers: two fit when a unit needs only 256
+//        columns (one tile), letting an epilogue overlap the next unit's MMAs
+template <int MODE>
+struct Cfg {
+  static constexpr int NA = 2;
+  static constexpr int NACC = 1;
+  static constexpr int B_STAGES = 4;
+  static constexpr int A_STAGE = NA * 16384;
+  // epilogue: per chunk of 16 rows, NSEG 64-byte segments per row (down: one
+  // per weight tile; gate/up: one, the SwiGLU of the tile pair)
+  static constexpr int NSEG = (MODE == MMA_DOWN) ? NA : 1;
+  static constexpr int STAGE_BUF = 16 * 64 * NSEG;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + kAStages * A_STAGE;
+  static constexpr int OFF_STAGE = OFF_B + B_STAGES * kBStage;
+  static constexpr int OFF_ROWS = OFF_STAGE + kEpiWarps * 2 * STAGE_BUF;  // gather rows
+  static constexpr int OFF_BAR = OFF_ROWS + 256 * 4;
+  static constexpr int NUM_BARS = 2 * kAStages + 2 * B_STAGES + 2 * NACC + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
 
 struct Unit {
   int expert, row0, nrows, npad, m, ks;
@@ -87,26 +106,25 @@ __device__ __forceinline__ Unit get_unit(const MmaParams& p, int mode, int u) {
   return o;
 }
 
+template <int MODE>
 struct Smem {
+  using C = Cfg<MODE>;
   uint32_t base;
-  __device__ uint32_t a(int s) const { return base + kOffA + s * kAStage; }
-  __device__ uint32_t b(int s) const { return base + kOffB + s * kBStage; }
-  __device__ uint32_t codes(int s) const { return base + kOffCodes + s * kCodeChunk; }
+  __device__ uint32_t a(int s) const { return base + C::OFF_A + s * C::A_STAGE; }
+  __device__ uint32_t b(int s) const { return base + C::OFF_B + s * kBStage; }
   __device__ uint32_t stage(int w, int i) const {
-    return base + kOffStage + (w * 2 + i) * kStageBuf;
+    return base + C::OFF_STAGE + (w * 2 + i) * C::STAGE_BUF;
   }
-  __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
+  __device__ uint32_t bar(int i) const { return base + C::OFF_BAR + 8 * i; }
   __device__ uint32_t a_full(int s) const { return bar(s); }
   __device__ uint32_t a_empty(int s) const { return bar(kAStages + s); }
   __device__ uint32_t b_full(int s) const { return bar(2 * kAStages + s); }
-  __device__ uint32_t b_empty(int s) const { return bar(2 * kAStages + kBStages + s); }
-  __device__ uint32_t c_full(int s) const { return bar(2 * kAStages + 2 * kBStages + s); }
-  __device__ uint32_t c_empty(int s) const {
-    return bar(2 * kAStages + 2 * kBStages + kCStages + s);
+  __device__ uint32_t b_empty(int s) const { return bar(2 * kAStages + C::B_STAGES + s); }
+  __device__ uint32_t acc_full(int b) const { return bar(2 * kAStages + 2 * C::B_STAGES + b); }
+  __device__ uint32_t acc_empty(int b) const {
+    return bar(2 * kAStages + 2 * C::B_STAGES + C::NACC + b);
   }
-  __device__ uint32_t acc_full() const { return bar(kNumBars - 3); }
-  __device__ uint32_t acc_empty() const { return bar(kNumBars - 2); }
-  __device__ uint32_t drain() const { return bar(kNumBars - 1); }
+  __device__ uint32_t drain() const { return bar(C::NUM_BARS - 1); }
 };
 
 __device__ __forceinline__ void record_timeout(volatile int* abort_flag, int* err) {
@@ -168,44 +186,114 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t v, int j, uint32_t s2,
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// TMA loads of B: a 2-D tile (16 rows) or a 4-row gather.  With CL > 1 the
+// data is multicast to the same shared-memory offset of every CTA of the
+// cluster and each CTA's barrier at `bar` receives its bytes.
+template <int CL>
 __device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(bar)
-      : "memory");
+  if (CL == 1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+  } else {
+    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+  }
 }
 
+template <int CL>
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int4 rows,
                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar)
-      : "memory");
+  if (CL == 1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar)
+        : "memory");
+  } else {
+    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar), "h"(mask)
+        : "memory");
+  }
+}
+
+// tcgen05 commit that arrives on `bar` in every CTA of the cluster
+template <int CL>
+__device__ __forceinline__ void tc_commit_cluster(uint32_t bar) {
+  if (CL == 1) {
+    tc_commit(bar);
+  } else {
+    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-template <int MODE>
+// CL: CTAs per cluster.  The CL CTAs of a cluster work on the same token tile
+// (consecutive weight units m), each fetching every CL-th 16-row slab of B and
+// multicasting it to all of them; a B slot is reused only after every CTA's
+// MMAs have read it (each MMA commit arrives on the slot's barrier in all CTAs).
+template <int MODE, int CL>
 __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_constant__ MmaParams p) {
+  using C = Cfg<MODE>;
+  constexpr int kBStages = C::B_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Smem S{smem_u32(smem)};
+  const Smem<MODE> S{smem_u32(smem)};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   const int nunits =
       (MODE == MMA_ROUTER) ? p.nunits_host : (*p.ntiles_dev) * p.units_per_tile;
-  if ((int)blockIdx.x >= nunits) return;  // uniform over the CTA
+  // work: cluster units cu = cid, cid + ncl, ...; the CTA of rank r takes unit
+  // cu * CL + r (same tile for the whole cluster, weight unit m = consecutive)
+  const int ncu = nunits / CL;
+  const int cid = (CL == 1) ? (int)blockIdx.x : (int)cluster_id();
+  const int ncl = (CL == 1) ? (int)gridDim.x : (int)cluster_count();
+  const int crank = (CL == 1) ? 0 : (int)cluster_rank();
+  if (cid >= ncu) return;  // uniform over the cluster
 
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* rows_s = reinterpret_cast<int*>(smem + kOffRows);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* rows_s = reinterpret_cast<int*>(smem + C::OFF_ROWS);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -214,14 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     }
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(S.b_full(s), 1);
-      mbar_init(S.b_empty(s), 1);
+      mbar_init(S.b_empty(s), CL);
     }
-    for (int s = 0; s < kCStages; ++s) {
-      mbar_init(S.c_full(s), 1);
-      mbar_init(S.c_empty(s), 4);
+    for (int b = 0; b < C::NACC; ++b) {
+      mbar_init(S.acc_full(b), 1);
+      mbar_init(S.acc_empty(b), kEpiWarps);
     }
-    mbar_init(S.acc_full(), 1);
-    mbar_init(S.acc_empty(), kEpiWarps);
     mbar_init(S.drain(), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -232,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kbu = p.kb_per_unit;
@@ -240,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     // ------------------------------------------------------ B (+ router A)
     uint32_t gb = 0, ga = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const Unit t = get_unit(p, MODE, u);
+    for (int cu = cid; cu < ncu && ok; cu += ncl) {
+      const Unit t = get_unit(p, MODE, cu * CL + crank);
       if (MODE == MMA_GATEUP) {
         // row indices of the unit's tokens; padding rows repeat a valid row
         __syncwarp();
@@ -271,23 +358,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         }
         const uint32_t bs = S.b(s);
         const int x = (k0 + kb) * 64;
+        // the whole tile arrives in every CTA; this CTA fetches 16-row slabs
+        // crank, crank + CL, ... (4 gathers or one 2-D tile per slab)
+        if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
+        __syncwarp();
+        const int nslab = t.npad >> 4;
         if (MODE == MMA_GATEUP) {
-          // 4-row gathers, issued by 16 lanes (lane i: rows 4i, 4i + 64, ...)
-          if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
-          __syncwarp();
-          if (lane < 16) {
-            for (int n = 4 * lane; n < t.npad; n += 64) {
-              const int4 r4 = *reinterpret_cast<const int4*>(rows_s + n);
-              tma_gather4(bs + n * 128, &p.tmB, x, r4, S.b_full(s));
-            }
+          const int nops = ((nslab - crank + CL - 1) / CL) * 4;
+          for (int o = lane; o < nops; o += 32) {
+            const int n = 16 * (crank + CL * (o >> 2)) + 4 * (o & 3);
+            const int4 r4 = *reinterpret_cast<const int4*>(rows_s + n);
+            tma_gather4<CL>(bs + n * 128, &p.tmB, x, r4, S.b_full(s));
           }
-        } else if (lane == 0) {
-          {
-            const int nbox = (t.npad + 31) >> 5;
-            mbar_arrive_expect_tx(S.b_full(s), (uint32_t)nbox * 4096);
-            for (int i = 0; i < nbox; ++i)
-              tma_tile_2d(bs + i * 4096, &p.tmB, x, t.row0 + 32 * i, S.b_full(s));
-          }
+        } else {
+          for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
+            tma_tile_2d<CL>(bs + sl * 2048, &p.tmB, x, t.row0 + 16 * sl, S.b_full(s));
         }
         ++gb;
       }
@@ -296,9 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t ga = 0, gb = 0, i = 0;
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
-        const Unit t = get_unit(p, MODE, u);
-        if (!thread_wait(S.acc_empty(), (i & 1) ^ 1, abort_flag, p.err)) break;
+      for (int cu = cid; cu < ncu; cu += ncl, ++i) {
+        const Unit t = get_unit(p, MODE, cu * CL + crank);
+        const int ab = (C::NACC == 2) ? (int)(i & 1) : 0;
+        const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
+        if (!thread_wait(S.acc_empty(ab), aph ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
         bool ok = true;
@@ -312,76 +399,93 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a0 = sdesc_k_sw128(S.a(sa) + kk * 32);
-            const uint64_t a1 = sdesc_k_sw128(S.a(sa) + 16384 + kk * 32);
             const uint64_t bd = sdesc_k_sw128(S.b(sb) + kk * 32);
             const uint32_t acc = (kb | kk) ? 1u : 0u;
-            tc_mma_f16(tmem, a0, bd, idesc, acc);
-            tc_mma_f16(tmem + 256, a1, bd, idesc, acc);
+#pragma unroll
+            for (int j = 0; j < C::NA; ++j) {
+              const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384 + kk * 32);
+              // NA == 2: tile j -> columns 256 j; NACC == 2: buffer ab -> columns 256 ab
+              tc_mma_f16(tmem + 256 * (C::NA == 2 ? j : ab), ad, bd, idesc, acc);
+            }
           }
           tc_commit(S.a_empty(sa));
-          tc_commit(S.b_empty(sb));
+          tc_commit_cluster<CL>(S.b_empty(sb));
         }
         if (!ok) break;
-        tc_commit(S.acc_full());
+        tc_commit(S.acc_full(ab));
       }
       // every issued MMA has finished before TMEM is released
       tc_commit(S.drain());
       mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
     }
-  } else if (warp == 2) {
-    // ---------------------------------------------------------- codes
-    if (MODE != MMA_ROUTER && lane == 0) {
-      uint32_t gc = 0;
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-        const Unit t = get_unit(p, MODE, u);
-        const uint8_t* src = p.wA + (long long)t.expert * p.a_expert_stride +
-                             (long long)t.m * p.a_unit_stride;
-        for (int kb = 0; kb < kbu; ++kb, ++gc) {
-          const int s = gc % kCStages;
-          if (!thread_wait(S.c_empty(s), ((gc / kCStages) & 1) ^ 1, abort_flag, p.err)) goto c_done;
-          mbar_arrive_expect_tx(S.c_full(s), kCodeChunk);
-          bulk_g2s(S.codes(s), src + (long long)kb * p.a_chunk, kCodeChunk, S.c_full(s));
-        }
-      }
-    c_done:;
-    }
   } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------------------- dequantise
+    // ------------------------------------------------ dequantise (codes from
+    // global memory straight into registers, three K blocks ahead)
     if (MODE != MMA_ROUTER) {
-      const int dw = warp - 4;
-      uint32_t ga = 0, gc = 0;
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-        for (int kb = 0; kb < kbu; ++kb, ++ga, ++gc) {
-          const int sc = gc % kCStages, sa = ga % kAStages;
-          if (!warp_wait(S.c_full(sc), (gc / kCStages) & 1, abort_flag, p.err)) goto dq_done;
-          if (!warp_wait(S.a_empty(sa), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) goto dq_done;
-          const uint32_t codes = S.codes(sc);
-          const uint32_t a = S.a(sa);
-          const int c = lane & 7;
-#pragma unroll 4
-          for (int it = 0; it < 16; ++it) {
-            const int r = 4 * (dw + 4 * it) + (lane >> 3);
-            const uint32_t v = ld_shared_u32(codes + r * 32 + c * 4);
-            const uint32_t sb = ld_shared_u32(codes + 8192 + r * 4);
-            const uint32_t s2 = __byte_perm(sb, 0, 0x1010);
-            const uint32_t b2 = __byte_perm(sb, 0, 0x3232);
-            const uint32_t w0 = dequant_pair(v, 0, s2, b2);
-            const uint32_t w1 = dequant_pair(v, 1, s2, b2);
-            const uint32_t w2 = dequant_pair(v, 2, s2, b2);
-            const uint32_t w3 = dequant_pair(v, 3, s2, b2);
-            const uint32_t dst = a + (r >> 7) * 16384 + (r & 127) * 128 + ((c ^ (r & 7)) << 4);
-            st_shared_v4(dst, w0, w1, w2, w3);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(S.a_full(sa));
-            mbar_arrive(S.c_empty(sc));
+      const int t = threadIdx.x - 128;  // 0..127: rows t (A0) and t + 128 (A1)
+      const int nmy = (ncu - cid + ncl - 1) / ncl;  // this CTA's units
+      const int total = nmy * kbu;
+      // source chunk of the CTA's global K-block number g
+      // chunks hold 256 rows; a one-tile unit m is rows 128 (m % 2) .. +127 of
+      // chunk unit m / 2.  Thread t dequantises row t (and, with two tiles,
+      // row t + 128) of the unit.
+      struct Codes {
+        uint4 a0, a1, b0, b1;
+        uint32_t sa, sb;
+      };
+      auto load = [&](int g, Codes& c) {
+        if (g < total) {
+          const int j = g / kbu;
+          const Unit u = get_unit(p, MODE, (cid + j * ncl) * CL + crank);
+          const int cu = (C::NA == 2) ? u.m : (u.m >> 1);
+          const int r0 = (C::NA == 2) ? t : ((u.m & 1) * 128 + t);
+          const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
+                              (long long)cu * p.a_unit_stride +
+                              (long long)(g - j * kbu) * p.a_chunk;
+          const uint4* ra = reinterpret_cast<const uint4*>(ch + r0 * 32);
+          c.a0 = __ldg(ra);
+          c.a1 = __ldg(ra + 1);
+          c.sa = __ldg(reinterpret_cast<const uint32_t*>(ch + 8192) + r0);
+          if (C::NA == 2) {
+            const uint4* rb = reinterpret_cast<const uint4*>(ch + (t + 128) * 32);
+            c.b0 = __ldg(rb);
+            c.b1 = __ldg(rb + 1);
+            c.sb = __ldg(reinterpret_cast<const uint32_t*>(ch + 8192) + t + 128);
           }
         }
+      };
+      // one row: 8 words -> 8 swizzled 16-byte chunks of the A tile
+      auto emit_row = [&](uint32_t a, int r, const uint4& w0, const uint4& w1, uint32_t sbv) {
+        const uint32_t s2 = __byte_perm(sbv, 0, 0x1010);
+        const uint32_t b2 = __byte_perm(sbv, 0, 0x3232);
+        const uint32_t rowb = a + (r >> 7) * 16384 + (r & 127) * 128;
+        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          st_shared_v4(rowb + ((c ^ (r & 7)) << 4), dequant_pair(w[c], 0, s2, b2),
+                       dequant_pair(w[c], 1, s2, b2), dequant_pair(w[c], 2, s2, b2),
+                       dequant_pair(w[c], 3, s2, b2));
+        }
+      };
+      Codes c0, c1, c2;
+      load(0, c0);
+      load(1, c1);
+      load(2, c2);
+      uint32_t ga = 0;
+      for (int g = 0; g < total; ++g, ++ga) {
+        const Codes cur = c0;
+        c0 = c1;
+        c1 = c2;
+        load(g + 3, c2);
+        const int sa = ga % kAStages;
+        if (!warp_wait(S.a_empty(sa), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) break;
+        const uint32_t a = S.a(sa);
+        emit_row(a, t, cur.a0, cur.a1, cur.sa);
+        if (C::NA == 2) emit_row(a, t + 128, cur.b0, cur.b1, cur.sb);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(S.a_full(sa));
       }
-    dq_done:;
     }
   } else if (warp >= 8) {
     // ---------------------------------------------------------- epilogue
@@ -390,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     const int half = e >> 2;           // columns [128*half, 128*half + 128)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t i = 0, nst = 0;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
-      const Unit t = get_unit(p, MODE, u);
+    for (int cu = cid; cu < ncu; cu += ncl, ++i) {
+      const Unit t = get_unit(p, MODE, cu * CL + crank);
       const int c0 = half * 128;
       const int c1 = min(c0 + 128, t.npad);
       // row data of the warp's 128 columns, fetched while the MMAs run:
@@ -408,12 +512,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
           }
         }
       }
-      if (!warp_wait(S.acc_full(), i & 1, abort_flag, p.err)) break;
+      const int ab = (C::NACC == 2) ? (int)(i & 1) : 0;
+      const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
+      if (!warp_wait(S.acc_full(ab), aph, abort_flag, p.err)) break;
       tc_fence_after();
+      const uint32_t tacc = tmem + lane_base + 256 * ab;
       for (int n0 = c0; n0 < c1; n0 += 16) {
         uint32_t r0[16], r1[16];
-        tmem_ld16(tmem + lane_base + n0, r0);
-        tmem_ld16(tmem + lane_base + 256 + n0, r1);
+        tmem_ld16(tacc + n0, r0);
+        if (C::NA == 2) tmem_ld16(tacc + 256 + n0, r1);
         const int nvalid = min(16, t.nrows - n0);
         // this chunk's rows n0..n0+15 are held by lanes (n0 - c0) % 32 + j
         // in register slot (n0 - c0) / 32
@@ -443,49 +550,48 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
           }
           continue;
         }
-        // stage [16 rows][32 or 64 values] in shared memory, then 16-byte
+        // stage [16 rows][NSEG x 32 values] in shared memory, then 16-byte
         // vector stores of whole 64-byte row segments
+        constexpr int NSEG = C::NSEG;
         const uint32_t sbuf = S.stage(e, nst & 1);
         __syncwarp();  // the buffer's previous reads are done
         if (nvalid > 0) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float v0 = __uint_as_float(r0[j]);
-            const float v1 = __uint_as_float(r1[j]);
             if (MODE == MMA_GATEUP) {
-              const float h = v0 / (1.0f + __expf(-v0)) * v1;
+              const float v1 = __uint_as_float(r1[j]);
+              const float h = __fdividef(v0, 1.0f + __expf(-v0)) * v1;
               st_shared_u16(sbuf + j * 64 + lane * 2, __half_as_ushort(__float2half_rn(h)));
             } else {
               const float sc = __shfl_sync(0xffffffffu, rsc, j);
-              st_shared_u16(sbuf + j * 128 + lane * 2,
+              st_shared_u16(sbuf + j * 64 * NSEG + lane * 2,
                             __bfloat16_as_ushort(__float2bfloat16_rn(sc * v0)));
-              st_shared_u16(sbuf + j * 128 + 64 + lane * 2,
-                            __bfloat16_as_ushort(__float2bfloat16_rn(sc * v1)));
+              if (NSEG == 2)
+                st_shared_u16(sbuf + j * 128 + 64 + lane * 2,
+                              __bfloat16_as_ushort(__float2bfloat16_rn(sc * __uint_as_float(r1[j]))));
             }
           }
         }
         __syncwarp();
-        if (MODE == MMA_GATEUP) {
-          // 16 rows x 64 bytes: lane -> (row lane/4 + 8i, 16-byte piece lane%4)
+        // 16 rows x NSEG segments x four 16-byte pieces: piece pi = lane + 32 it
 #pragma unroll
-          for (int it = 0; it < 2; ++it) {
-            const int j = (lane >> 2) + 8 * it;
+        for (int it = 0; it < 2 * NSEG; ++it) {
+          const int pi = lane + 32 * it;
+          const int j = pi / (4 * NSEG);
+          const int seg = (pi >> 2) % NSEG;
+          const int part = pi & 3;
+          if (MODE == MMA_GATEUP) {
             if (j < nvalid) {
-              const uint4 v = ld_shared_v4(sbuf + j * 64 + (lane & 3) * 16);
+              const uint4 v = ld_shared_v4(sbuf + j * 64 + part * 16);
               const long long row = t.row0 + n0 + j;
-              *reinterpret_cast<uint4*>(p.H + row * p.ldh + t.m * 128 + q * 32 + (lane & 3) * 8) = v;
+              *reinterpret_cast<uint4*>(p.H + row * p.ldh + t.m * 128 + q * 32 + part * 8) = v;
             }
-          }
-        } else {
-          // 16 rows x 2 segments x 64 bytes: lane -> (row lane/8 + 4i, piece lane%8)
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int j = (lane >> 3) + 4 * it;
+          } else {
             const long long dj = __shfl_sync(0xffffffffu, rdst, j);
             if (j < nvalid) {
-              const int pc = lane & 7;  // pieces 0..3: first segment, 4..7: second
-              const uint4 v = ld_shared_v4(sbuf + j * 128 + pc * 16);
-              uint16_t* yr = p.Y + dj * p.ldy + t.m * 256 + q * 32 + (pc >> 2) * 128 + (pc & 3) * 8;
+              const uint4 v = ld_shared_v4(sbuf + j * 64 * NSEG + seg * 64 + part * 16);
+              uint16_t* yr = p.Y + dj * p.ldy + t.m * (128 * NSEG) + seg * 128 + q * 32 + part * 8;
               *reinterpret_cast<uint4*>(yr) = v;
             }
           }
@@ -494,29 +600,81 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(S.acc_empty());
+      if (lane == 0) mbar_arrive(S.acc_empty(ab));
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync_all();  // no CTA leaves while peers may still write to it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-template <int MODE>
+template <int MODE, int CL>
 cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_mma_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(grouped_mma_kernel<MODE, CL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MODE>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_mma_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+  // no more clusters than can be resident at once (persistent CTAs)
+  static int max_grid = -1;
+  if (max_grid < 0) {
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(CL);
+    q.blockDim = dim3(kThreads);
+    q.dynamicSmemBytes = Cfg<MODE>::SMEM;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = CL;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    q.attrs = a;
+    q.numAttrs = 1;
+    int ncl = 0;
+    if (cudaOccupancyMaxActiveClusters(&ncl, grouped_mma_kernel<MODE, CL>, &q) != cudaSuccess ||
+        ncl <= 0) {
+      cudaGetLastError();
+      ncl = 0;
+    }
+    max_grid = ncl * CL;
+  }
+  if (max_grid > 0 && grid > max_grid) grid = max_grid;
+  grid = grid / CL * CL;
+  if (grid < CL) grid = CL;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<MODE>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_mma_kernel<MODE, CL>, p);
+}
+
+// CTAs per cluster for a grouped launch: a power of two dividing the units
+// of one tile.  Defaults measured on GB300 (T=4096, Zipf): gate/up 4, down 2;
+// MOE_GEMM_CLUSTER (1, 2, 4) overrides both for tuning.
+int cluster_for(int mode, int units_per_tile) {
+  static int env = -1;
+  if (env < 0) {
+    const char* e = getenv("MOE_GEMM_CLUSTER");
+    env = e ? atoi(e) : 0;
+    if (env != 1 && env != 2 && env != 4) env = 0;
+  }
+  int cl = env ? env : (mode == MMA_GATEUP ? 4 : 2);
+  while (cl > 1 && units_per_tile % cl != 0) cl >>= 1;
+  return cl;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -557,11 +715,16 @@ cudaError_t make_tmap_16bit(CUtensorMap* map, const void* base, long long rows, 
 
 cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st) {
   if (grid <= 0) return cudaSuccess;
-  switch (mode) {
-    case MMA_ROUTER: return launch_mode<MMA_ROUTER>(p, grid, st);
-    case MMA_GATEUP: return launch_mode<MMA_GATEUP>(p, grid, st);
-    default: return launch_mode<MMA_DOWN>(p, grid, st);
+  if (mode == MMA_ROUTER) return launch_mode<MMA_ROUTER, 1>(p, grid, st);
+  const int cl = cluster_for(mode, p.units_per_tile);
+  if (mode == MMA_GATEUP) {
+    if (cl == 4) return launch_mode<MMA_GATEUP, 4>(p, grid, st);
+    if (cl == 2) return launch_mode<MMA_GATEUP, 2>(p, grid, st);
+    return launch_mode<MMA_GATEUP, 1>(p, grid, st);
   }
+  if (cl == 4) return launch_mode<MMA_DOWN, 4>(p, grid, st);
+  if (cl == 2) return launch_mode<MMA_DOWN, 2>(p, grid, st);
+  return launch_mode<MMA_DOWN, 1>(p, grid, st);
 }
 
 }  // namespace moe

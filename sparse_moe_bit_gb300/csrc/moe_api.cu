@@ -164,7 +164,7 @@ moe_status alloc_all(Handle* h) {
     CK(dalloc(&w.H, (size_t)T * k1 * c.I * 2), "alloc");
     CK(dalloc(&w.Y, (size_t)T * k1 * c.d * 2), "alloc");
     CK(make_tmap_16bit(&h->tm_x16, w.x16, T, c.d, 1, false), "tensor map (x16)");
-    CK(make_tmap_16bit(&h->tm_h, w.H, T * k1, c.I, 32, false), "tensor map (H)");
+    CK(make_tmap_16bit(&h->tm_h, w.H, T * k1, c.I, 16, false), "tensor map (H)");
   }
   CK(dalloc(&w.x_dev, (size_t)T * c.d * 2), "alloc");
   CK(dalloc(&w.y_dev, (size_t)T * c.d * 2), "alloc");
@@ -197,7 +197,7 @@ moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int
     p.a_expert_stride = 0;
     p.a_unit_stride = (long long)(c.d / 64) * kRouterChunk;
     p.a_chunk = kRouterChunk;
-    CK(make_tmap_16bit(&p.tmB, x, T, c.d, 32, true), "tensor map (x)");
+    CK(make_tmap_16bit(&p.tmB, x, T, c.d, 16, true), "tensor map (x)");
     p.b_rowmap = nullptr;
     p.out_f32 = h->ws.logit_part;
     p.E = c.E;
@@ -241,7 +241,7 @@ moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
   int grid = units < h->num_sms ? (int)units : h->num_sms;
   prof_mark(h, 4, st);
   CK(launch_grouped_mma(MMA_GATEUP, p, grid, st), "gate/up launch");
-  // down projection + routing weight
+  // down projection + routing weight: two 128-row weight tiles per unit
   p.kb_per_unit = c.I / 64;
   p.m_units = c.d / 256;
   p.units_per_tile = p.m_units;

@@ -64,7 +64,7 @@ struct Handle {
   uint16_t* w_sg = nullptr;      // bf16 [d]
   Workspace ws;
   CUtensorMap tm_x16;  // gate/up B: x16 [Tmax][d], 1-row box (4-row gathers)
-  CUtensorMap tm_h;    // down B: H [Tmax*(k+1)][I], 32-row box
+  CUtensorMap tm_h;    // down B: H [Tmax*(k+1)][I], 16-row box
   // per-stage timing (moe_profile_enable)
   static constexpr int kStagesTimed = 7;
   static constexpr int kProfCalls = 4096;
@@ -101,7 +101,7 @@ struct MmaParams {
   long long a_unit_stride;    // bytes per 256-row unit
   int a_chunk;                // bytes per K block
   // B operand rows: gathered through b_rowmap (gate/up: 4-row TMA gathers) or
-  // contiguous from row0 (router, down: 32-row TMA tiles)
+  // contiguous from row0 (router, down: 16-row TMA tiles)
   const int32_t* b_rowmap;    // grouped row -> source row, or null
   // epilogue
   float* out_f32;             // router partials [KS][T][E]
