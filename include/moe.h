@@ -177,8 +177,9 @@ typedef struct moe_decode_trace {
   void* out;       /* bf16 [L][d], output of every layer */
   int64_t* timestamps; /* int64 [L][4]: GPU clock (ns) in the first CTA at the
                           start of a layer, after its weight copies are issued,
-                          after the gate/up barrier, and at the end of the down
-                          projection (profiling aid) */
+                          once the gate/up results of every CTA have arrived,
+                          and at the end of the down projection (profiling
+                          aid) */
 } moe_decode_trace;
 
 /*

@@ -14,17 +14,19 @@
 // Two grid-wide barriers per layer.  CTA c owns output features
 // [c*d/G, (c+1)*d/G) and a contiguous range of the (slot j, feature f) units
 // of the k+1 active experts.
-//   A : every CTA rebuilds x_l = out_{l-1} / sqrt(mean(out_{l-1}^2) + eps)
-//       from the previous output, turns the router sums P_l into logits
-//       (times the same 1/rms), repeats the top-k selection, and issues the
-//       bulk copies of its gate/up rows and its down rows.
+//   A : every CTA reads the previous output out_{l-1} and the router sums P_l
+//       in one pass, folds 1/rms(out_{l-1}) into the logits (the rest of the
+//       layer works on the unnormalised vector and scales its dot products),
+//       repeats the top-k selection in one warp and issues the bulk copies of
+//       its gate/up rows and its down rows straight after it.
 //   GU: h_j[f] = silu(G_j[f] . x) * (U_j[f] . x) for the owned units -> global
 //       -> grid barrier
 //   D : out[f] = sum_j w_j (D_j[f] . h_j) + sigma (D_s[f] . h_s) for the owned
-//       features (fixed order), then the next layer's router partial sums over
-//       those features: P_{l+1}[e] += sum_f out[f] W_r'[e][f], accumulated as
-//       64-bit fixed-point integers (2^-32 units), so the sum is exact and does
-//       not depend on the order of arrival -> grid barrier
+//       features, then the next layer's router partial sums over those
+//       features: P_{l+1}[e] += sum_f out[f] W_r'[e][f], accumulated as 64-bit
+//       fixed-point integers (2^-32 units) into one of several copies of P (so
+//       that fewer CTAs meet on one address); integer addition makes the sum
+//       exact and independent of the order of arrival -> grid barrier
 // Dot products use the split s*q + beta per 64-group:
 //   sum_i (s q_i + beta) x_i = s (sum_i (128 + q_i) x_i - 128 X) + beta X,
 // X = sum_i x_i, with the code turned into the fp32 value 128 + q by one byte
@@ -45,15 +47,17 @@ constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxDecLayers = 64;
 constexpr int kMaxUnitsPerWarp = 4;
+constexpr int kPCopies = 8;  // copies of the router sums: CTA c adds into copy c % kPCopies
+constexpr int kPSlots = 3;   // layer l's sums live in slot l % kPSlots
+constexpr int kDC = 4;       // output features a warp takes per expert in the down step
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kFix = 4294967296.0f;  // 2^32
 
 struct DecLayer {
-  const uint8_t* gu_codes;  // [n_exp][2I][d/2]
-  const uint32_t* gu_sb;    // [n_exp][2I][d/64]
-  const uint8_t* dn_codes;  // [n_exp][d][I/2]
-  const uint32_t* dn_sb;    // [n_exp][d][sbp]
-  const uint16_t* w_rt;     // [d][Ep] router transposed + shared-gate column
+  const uint8_t* gu;     // [n_exp][I] units of d + d/8 bytes (gate, up codes; their s,b)
+  const uint8_t* dn;     // [n_exp][d] rows of I/2 + 4*sbp bytes (codes; s,b words)
+  const uint16_t* w_rt;  // [d][Ep] router transposed + shared-gate column
 };
 
 struct DecParams {
@@ -72,9 +76,9 @@ struct DecParams {
   float* tr_w;          // [L][k] or null
   uint16_t* tr_out;     // [L][d] or null
   int64_t* tr_ns;       // [L][4] or null
-  float* H;             // [k1][I]
-  uint16_t* out;        // [d]
-  unsigned long long* P;  // [L][E+1] fixed-point router sums, zero at launch
+  float* H;             // [k1*I] h of the active experts (unit j*I + f)
+  uint16_t* out;        // [2][d]: layer l writes row l % 2
+  unsigned long long* P;  // [kPSlots][kPCopies][E+1] fixed-point router sums, zero at launch
   unsigned* bar;        // grid barrier arrivals, zero at launch
   int* abort_flag;      // zero at launch
   int* err;
@@ -82,7 +86,8 @@ struct DecParams {
 
 // shared-memory carve-up (the host sizes the launch with the same function)
 struct DecSmem {
-  size_t xs2, xg, hs2, hw, gu, dn, rt, outs, lg, sel_e, sel_w, misc, red, bars, ok, total;
+  size_t xs2, xg, hs2, hw, gu, dn, rt, outs, part, lg, lb, sel_e, sel_w, misc, red, infl, bars,
+      ok, total;
 };
 __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align) {
   o = (o + align - 1) / align * align;
@@ -102,18 +107,21 @@ __host__ __device__ inline DecSmem dec_smem(int d, int I, int k1, int E, int Ep,
   s.dn = dec_take(o, (size_t)k1 * nf_max * (I / 2 + 4 * sbp), 128);
   s.rt = dec_take(o, (size_t)nf_max * Ep * 2, 128);
   s.outs = dec_take(o, (size_t)nf_max * 4, 16);
+  s.part = dec_take(o, (size_t)k1 * nf_max * 4, 16);
   s.lg = dec_take(o, (size_t)(E + 1) * 4, 16);
+  s.lb = dec_take(o, (size_t)E * 4, 16);
   s.sel_e = dec_take(o, kMaxK * 4, 16);
   s.sel_w = dec_take(o, kMaxK * 4, 16);
   s.misc = dec_take(o, 16, 16);
   s.red = dec_take(o, kDecWarps * 4, 16);
-  s.bars = dec_take(o, (kDecWarps + 2) * 8, 8);
+  s.infl = dec_take(o, (kDecWarps + 2) * 4, 16);
+  s.bars = dec_take(o, (kDecWarps + 3) * 8, 8);
   s.ok = dec_take(o, 16, 16);
   s.total = o;
   return s;
 }
 
-__device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+__device__ __forceinline__ float bf16f(uint32_t v) { return __uint_as_float(v << 16); }
 
 template <int B>
 __device__ __forceinline__ float code_plus128(uint32_t bytes) {
@@ -168,14 +176,71 @@ __device__ __forceinline__ double softmax_term(float v, double m) {
   return exp((double)v - m);
 }
 
+
+// Top-k of lg[0..E) in one warp, ranked by (value descending, index
+// ascending), NaN taken as -inf.  Lane l holds the experts l, l+32, ... as
+// 64-bit keys (order key << 32 | ~index), sorts them (bitonic network) and
+// then each round needs only the head of every lane: the warp maximum of the
+// high words, then of the low words among the lanes that hold it, names the
+// winner, whose lane drops its head.  sel_e[r] = the r-th choice (lane 0
+// writes it).
+template <int VPL>
+__device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int lane, int* sel_e,
+                                          bool* nan_seen) {
+  unsigned long long K[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    unsigned long long key = 0ull;  // empty; every real key is larger
+    if (e < E) {
+      float v = lg[e];
+      if (v != v) {
+        v = -INFINITY;
+        *nan_seen = true;
+      }
+      key = ((unsigned long long)ord_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+    }
+    K[j] = key;
+  }
+#pragma unroll
+  for (int size = 2; size <= VPL; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const unsigned long long a = K[i], b = K[j];
+          const bool sw = desc ? (a < b) : (a > b);
+          K[i] = sw ? b : a;
+          K[j] = sw ? a : b;
+        }
+      }
+    }
+  }
+  for (int r = 0; r < k; ++r) {
+    const uint32_t hi = (uint32_t)(K[0] >> 32), lo = (uint32_t)K[0];
+    const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+    if (hi == mh && lo == ml) {
+#pragma unroll
+      for (int j = 0; j + 1 < VPL; ++j) K[j] = K[j + 1];
+      K[VPL - 1] = 0ull;
+    }
+    if (lane == 0) sel_e[r] = (int)(0xFFFFFFFFu - ml);
+  }
+}
+
 // Grid-wide barrier number n (0-based): arrivals are counted monotonically, so
-// barrier n completes at (n + 1) * gridDim.x.  Bounded: on time-out (or when
-// another CTA gave up) every CTA leaves the kernel.
+// barrier n completes at (n + 1) * gridDim.x.  The arrival is a release and
+// the poll an acquire at GPU scope, which orders every CTA's writes before the
+// barrier (its threads meet at __syncthreads first) with every read after it.
+// Bounded: on time-out (or when another CTA gave up) every CTA leaves.
 __device__ bool grid_sync(const DecParams& p, unsigned n, int* s_ok) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    __threadfence();
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p.bar), "r"(1u) : "memory");
     const unsigned target = (n + 1) * gridDim.x;
     const uint64_t t0 = globaltimer_ns();
@@ -196,18 +261,26 @@ __device__ bool grid_sync(const DecParams& p, unsigned n, int* s_ok) {
         }
       }
     }
-    __threadfence();
     *s_ok = ok;
   }
   __syncthreads();
   return *s_ok != 0;
 }
 
+// Bounded wait on an mbarrier phase; the thread sleeps in hardware between
+// checks.  On time-out (or when another CTA gave up) records the error.
 __device__ __forceinline__ bool copy_wait(const DecParams& p, uint32_t bar, uint32_t parity) {
-  if (mbar_wait_bounded(bar, parity, p.abort_flag, kWaitNs)) return true;
-  atomicOr(p.err, MOE_DEVERR_WAIT_TIMEOUT);
-  atomicExch(p.abort_flag, 1);
-  return false;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*(volatile int*)p.abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(p.err, MOE_DEVERR_WAIT_TIMEOUT);
+      atomicExch(p.abort_flag, 1);
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ void stamp(const DecParams& p, int l, int i) {
@@ -232,15 +305,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   uint8_t* dn_buf = dsm + L.dn;
   const uint16_t* rt_buf = reinterpret_cast<const uint16_t*>(dsm + L.rt);
   float* outs = reinterpret_cast<float*>(dsm + L.outs);
-  float* lg = reinterpret_cast<float*>(dsm + L.lg);
+  float* part = reinterpret_cast<float*>(dsm + L.part);  // [k1][nf_max] D_j[f] . h_j
+  float* lg = reinterpret_cast<float*>(dsm + L.lg);  // raw sums, then logits; [E]: shared gate
+  float* lb = reinterpret_cast<float*>(dsm + L.lb);  // logit bias
   int* sel_e = reinterpret_cast<int*>(dsm + L.sel_e);
   float* sel_w = reinterpret_cast<float*>(dsm + L.sel_w);
   float* misc = reinterpret_cast<float*>(dsm + L.misc);  // [0] sigma, [1] 1/rms
   float* red = reinterpret_cast<float*>(dsm + L.red);
+  // parity of the copies in flight on each mbarrier (-1: none), for the
+  // bounded drain on the error path
+  volatile int* infl = reinterpret_cast<volatile int*>(dsm + L.infl);
   const uint32_t bar0 = smem_u32(dsm + L.bars);  // [warps] gate/up, then down, router
   int* s_ok = reinterpret_cast<int*>(dsm + L.ok);
-  const uint32_t dn_bar = bar0 + 8 * kDecWarps;
-  const uint32_t rt_bar = bar0 + 8 * (kDecWarps + 1);
+  const int kDnBar = kDecWarps, kRtBar = kDecWarps + 1;
+  const uint32_t dn_bar = bar0 + 8 * kDnBar;
+  const uint32_t rt_bar = bar0 + 8 * kRtBar;
+  const uint32_t route_bar = bar0 + 8 * (kDecWarps + 2);  // the top-k of the layer is known
+  const int wwarp = kDecWarps - 1;  // computes the routing weights (it has the fewest units)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, c = blockIdx.x;
@@ -252,20 +333,36 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int wu1 = min(wu0 + p.upw, u1);
   const int nu = wu1 - wu0;
   const int gu_unit = d + d / 8;
-  const int dn_stride = p.nf_max * (I / 2 + 4 * sbp);
+  const int dn_row = I / 2 + 4 * sbp;
+  const int dn_stride = p.nf_max * dn_row;
 
   if (tid == 0) {
-    for (int i = 0; i < kDecWarps + 2; ++i) mbar_init(bar0 + 8 * i, 1);
+    for (int i = 0; i < kDecWarps + 3; ++i) mbar_init(bar0 + 8 * i, 1);
     fence_mbar_init();
   }
+  if (tid < kDecWarps + 2) infl[tid] = -1;
   __syncthreads();
-  uint32_t ph_gu = 0, ph_dn = 0, ph_rt = 0;
+  uint32_t ph_gu = 0, ph_dn = 0, ph_rt = 0, ph_route = 0;
   unsigned nsync = 0;
+
+  // Error path: wait, with a bound, for this CTA's bulk copies still in
+  // flight, so that none lands in shared memory after the CTA has left.
+  auto drain = [&]() {
+    if (lane != 0) return;
+    for (int i = 0; i < kDecWarps + 2; ++i) {
+      const int pty = infl[i];
+      if (pty < 0) continue;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar0 + 8 * i, (uint32_t)pty)) {
+        if (globaltimer_ns() - t0 > kDrainNs) break;
+      }
+    }
+  };
 
   // x (bf16 [d]) -> shared memory in the lane-interleaved pair layout, with
   // optional RMS normalisation; also the owned features' values and the
-  // group sums.  Returns 1/rms (1 when not normalised).
-  auto load_x = [&](const uint16_t* src, bool norm, bool keep_own) -> float {
+  // group sums (used for the input of the first layer of a launch).
+  auto load_x = [&](const uint16_t* src, bool norm) {
     float r = 1.0f;
     if (norm) {
       float ss = 0.f;
@@ -289,7 +386,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const float v = bf16f(__ldcg(src + i)) * r;
       const int g = i >> 6, e = i & 63;
       xf[((e >> 1) * ng + g) * 2 + (e & 1)] = v;
-      if (keep_own && i >= f0 && i < f1) outs[i - f0] = v;
+      if (i >= f0 && i < f1) outs[i - f0] = v;
     }
     __syncthreads();
     for (int g = warp; g < ng; g += kDecWarps) {
@@ -298,94 +395,174 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (lane == 0) xg[g] = s;
     }
     __syncthreads();
-    return r;
   };
 
-  // P_dst[e] += sum_{f owned} outs[f] * W'[e][f]  (e = E: the shared gate)
-  auto router_partial = [&](unsigned long long* Pl) {
+  // P_slot[copy c % kPCopies][e] += sum_{f owned} outs[f] * W'[e][f]
+  // (e = E: the shared gate)
+  auto router_partial = [&](int slot) {
+    unsigned long long* Pq =
+        p.P + ((long long)slot * kPCopies + (c % kPCopies)) * (long long)(E + 1);
     for (int e = tid; e <= E; e += kDecThreads) {
       float acc = 0.f;
       for (int f = 0; f < nf; ++f) acc = fmaf(outs[f], bf16f(rt_buf[f * Ep + e]), acc);
-      const long long v = __float2ll_rn(acc * kFix);
-      atomicAdd(Pl + e, (unsigned long long)v);
+      atomicAdd(Pq + e, (unsigned long long)__float2ll_rn(acc * kFix));
     }
   };
 
   auto issue_router_copy = [&](int l) {
-    if (tid == kDecThreads - 32 && nf > 0) {  // lane 0 of the last warp
+    if (tid == 32 && nf > 0) {  // lane 0 of warp 1
       const uint32_t bytes = (uint32_t)nf * Ep * 2;
+      infl[kRtBar] = (int)ph_rt;
       mbar_arrive_expect_tx(rt_bar, bytes);
       bulk_g2s(smem_u32(dsm + L.rt), p.layer[l].w_rt + (long long)f0 * Ep, bytes, rt_bar);
     }
   };
 
-  // ---- prologue: x_0 and the router sums of layer 0
-  load_x(p.x, p.norm_first != 0, true);
+  // After the grid barrier that follows the gate/up step: h of all active
+  // experts -> shared memory (pair layout).
+  auto gather_h = [&]() {
+    float* hf = reinterpret_cast<float*>(hs2);
+    for (int i = tid; i < k1 * I; i += kDecThreads) {
+      const int j = i / I, e = i - j * I;
+      const int w = e >> 3, q = (e & 7) >> 1;
+      hf[(((j * 4 + q) * nwi) + w) * 2 + (e & 1)] = __ldcg(p.H + i);
+    }
+    __syncthreads();
+  };
+
+  // ---- prologue: x_0 and the router sums of layer 0 (slot 0)
   issue_router_copy(0);
+  load_x(p.x, p.norm_first != 0);
   if (nf > 0) {
-    if (!copy_wait(p, rt_bar, ph_rt)) return;
+    if (!copy_wait(p, rt_bar, ph_rt)) {
+      drain();
+      return;
+    }
+    if (tid == 0) infl[kRtBar] = -1;
   }
   ph_rt ^= 1;
-  if (nf > 0) router_partial(p.P);
-  if (!grid_sync(p, nsync++, s_ok)) return;
+  if (nf > 0) router_partial(0);
+  if (!grid_sync(p, nsync++, s_ok)) {
+    drain();
+    return;
+  }
 
   for (int l = 0; l < p.L; ++l) {
     const DecLayer& W = p.layer[l];
     stamp(p, l, 0);
-    // ---- A: x_l, logits, top-k, copies
-    const float r = (l == 0) ? 1.0f : load_x(p.out, true, false);
-    for (int e = tid; e <= E; e += kDecThreads) {
-      const long long s = (long long)__ldcg(p.P + (long long)l * (E + 1) + e);
-      float v = (float)((double)s * (1.0 / 4294967296.0)) * r;
-      if (e < E) {
-        if (p.bias) v += p.bias[(long long)l * E + e];
-        lg[e] = v;
-        if (c == 0) p.logits[(long long)l * E + e] = v;
-      } else {
-        const float sg = p.has_shared ? 1.0f / (1.0f + expf(-v)) : 0.0f;
-        misc[0] = sg;
-        if (c == 0) p.sigma[l] = sg;
+    // ---- A: out_{l-1} and P_l in one pass; routing in warp 0; copies
+    if (l + 1 < p.L) issue_router_copy(l + 1);
+    if (l > 0) {
+      const uint16_t* src = p.out + (long long)((l - 1) & 1) * d;
+      float ss = 0.f;
+      for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
+        const int i0 = ib + 4 * tid;
+        const bool act = i0 < d;
+        uint2 raw = make_uint2(0u, 0u);
+        if (act) raw = __ldcg(reinterpret_cast<const uint2*>(src + i0));
+        const float v0 = bf16f(raw.x & 0xFFFFu), v1 = bf16f(raw.x >> 16);
+        const float v2 = bf16f(raw.y & 0xFFFFu), v3 = bf16f(raw.y >> 16);
+        ss = fmaf(v0, v0, ss);
+        ss = fmaf(v1, v1, ss);
+        ss = fmaf(v2, v2, ss);
+        ss = fmaf(v3, v3, ss);
+        float s = (v0 + v1) + (v2 + v3);  // 16 lanes hold one 64-group
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        s += __shfl_xor_sync(0xffffffffu, s, 8);
+        if (act) {
+          const int g = i0 >> 6, e = i0 & 63;
+          xs2[(e >> 1) * ng + g] = make_float2(v0, v1);
+          xs2[((e >> 1) + 1) * ng + g] = make_float2(v2, v3);
+          if ((lane & 15) == 0) xg[g] = s;
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) red[warp] = ss;
+    }
+    {
+      const unsigned long long* Ps = p.P + (long long)(l % kPSlots) * kPCopies * (E + 1);
+      for (int e = tid; e <= E; e += kDecThreads) {
+        long long s = 0;
+#pragma unroll
+        for (int q = 0; q < kPCopies; ++q) s += (long long)__ldcg(Ps + q * (E + 1) + e);
+        lg[e] = (float)((double)s * (1.0 / 4294967296.0));
+        if (e < E) lb[e] = p.bias ? p.bias[(long long)l * E + e] : 0.0f;
+      }
+      if (c == 0) {  // the slot of layer l-1 is free (read before the last barrier)
+        unsigned long long* Pz =
+            p.P + (long long)((l + kPSlots - 1) % kPSlots) * kPCopies * (E + 1);
+        for (int i = tid; i < kPCopies * (E + 1); i += kDecThreads) Pz[i] = 0ull;
       }
     }
     __syncthreads();
+    float r = 1.0f;  // 1/rms of out_{l-1} (x_0 is normalised already)
+    if (l > 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) t += red[w];
+      r = rsqrtf(t / (float)d + p.eps);
+    }
     if (warp == 0) {
-      constexpr int VPL = kMaxE / 32;
-      uint32_t key[VPL];
-      bool nan_seen = false;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        float v = -INFINITY;
+      for (int e = lane; e <= E; e += 32) {
+        float v = lg[e] * r;
         if (e < E) {
-          v = lg[e];
-          if (v != v) {
-            v = -INFINITY;
-            nan_seen = true;
-          }
+          v += lb[e];
+          lg[e] = v;
+          if (c == 0) p.logits[(long long)l * E + e] = v;
+        } else {
+          const float sg = p.has_shared ? 1.0f / (1.0f + expf(-v)) : 0.0f;
+          misc[0] = sg;
+          if (c == 0) p.sigma[l] = sg;
         }
-        key[j] = (e < E) ? ord_key(v) : 0u;
-      }
-      if (__any_sync(0xffffffffu, nan_seen) && lane == 0 && c == 0)
-        atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
-      uint32_t taken = 0;
-      for (int rr = 0; rr < k; ++rr) {
-        uint32_t bk = 0;
-        int be = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          const int e = lane + 32 * j;
-          if (e < E && !((taken >> j) & 1u) && (key[j] > bk || be == INT_MAX)) {
-            bk = key[j];
-            be = e;
-          }
-        }
-        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t win = __reduce_min_sync(
-            0xffffffffu, (bk == m && be != INT_MAX) ? (uint32_t)be : 0xFFFFFFFFu);
-        if ((int)(win & 31) == lane) taken |= 1u << (win >> 5);
-        if (lane == 0) sel_e[rr] = (int)win;
       }
       __syncwarp();
+      bool nan_seen = false;
+      if (E <= 256) warp_topk<8>(lg, E, k, lane, sel_e, &nan_seen);
+      else warp_topk<kMaxE / 32>(lg, E, k, lane, sel_e, &nan_seen);
+      if (__any_sync(0xffffffffu, nan_seen) && lane == 0 && c == 0)
+        atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
+      __syncwarp();
+      // bulk copies: lane i < 16 those of warp i's gate/up units (one per
+      // expert the units fall in), lane 16 the CTA's down rows of the k+1
+      // experts (one per expert)
+      if (lane < kDecWarps) {
+        const int a0 = min(u0 + lane * p.upw, u1), a1 = min(a0 + p.upw, u1);
+        if (a1 > a0) {
+          const uint32_t bar = bar0 + 8 * lane;
+          infl[lane] = (int)ph_gu;
+          mbar_arrive_expect_tx(bar, (uint32_t)((a1 - a0) * gu_unit));
+          uint32_t dst = smem_u32(gu_buf + (size_t)lane * p.upw * gu_unit);
+          for (int u = a0; u < a1;) {
+            const int j = u / I, f = u - j * I;
+            const int n = min(a1 - u, I - f);
+            const long long ex = (j < k) ? sel_e[j] : E;
+            bulk_g2s(dst, W.gu + (ex * I + f) * gu_unit, (uint32_t)(n * gu_unit), bar);
+            dst += (uint32_t)(n * gu_unit);
+            u += n;
+          }
+        }
+      } else if (lane == kDecWarps && nf > 0) {
+        infl[kDnBar] = (int)ph_dn;
+        mbar_arrive_expect_tx(dn_bar, (uint32_t)(k1 * nf * dn_row));
+        for (int j = 0; j < k1; ++j) {
+          const long long ex = (j < k) ? sel_e[j] : E;
+          bulk_g2s(smem_u32(dn_buf + (size_t)j * dn_stride), W.dn + (ex * d + f0) * dn_row,
+                   (uint32_t)(nf * dn_row), dn_bar);
+        }
+      } else if (lane == kDecWarps + 1) {
+        mbar_arrive(route_bar);  // sel_e and the logits are in shared memory
+      }
+      stamp(p, l, 1);
+    }
+    if (warp == wwarp) {
+      // routing weights (fp64 softmax over the k chosen logits), off the
+      // path of the copies and of the other warps' gate/up work
+      if (!copy_wait(p, route_bar, ph_route)) {
+        drain();
+        return;
+      }
       const int my_e = (lane < k) ? sel_e[lane] : 0;
       float my_v = (lane < k) ? lg[my_e] : -INFINITY;
       if (my_v != my_v) my_v = -INFINITY;
@@ -405,157 +582,161 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
     }
-    __syncthreads();
-    // bulk copies: the warp's gate/up units, the CTA's down rows, the next router
-    if (lane == 0 && nu > 0) {
-      const uint32_t bar = bar0 + 8 * warp;
-      mbar_arrive_expect_tx(bar, (uint32_t)(nu * gu_unit));
-      for (int t = 0; t < nu; ++t) {
-        const int u = wu0 + t;
-        const int j = u / I, f = u - (u / I) * I;
-        const long long ex = (j < k) ? sel_e[j] : E;
-        const long long rg = ex * 2 * I + f, ru = rg + I;
-        const uint32_t dst = smem_u32(gu_buf + (size_t)(warp * p.upw + t) * gu_unit);
-        bulk_g2s(dst, W.gu_codes + rg * (d / 2), d / 2, bar);
-        bulk_g2s(dst + d / 2, W.gu_codes + ru * (d / 2), d / 2, bar);
-        bulk_g2s(dst + d, W.gu_sb + rg * ng, d / 16, bar);
-        bulk_g2s(dst + d + d / 16, W.gu_sb + ru * ng, d / 16, bar);
-      }
-    }
-    if (tid == 32 && nf > 0) {  // lane 0 of warp 1: the down rows of the k+1 experts
-      mbar_arrive_expect_tx(dn_bar, (uint32_t)(k1 * nf * (I / 2 + 4 * sbp)));
-      for (int j = 0; j < k1; ++j) {
-        const long long ex = (j < k) ? sel_e[j] : E;
-        const uint32_t dst = smem_u32(dn_buf + (size_t)j * dn_stride);
-        bulk_g2s(dst, W.dn_codes + (ex * d + f0) * (I / 2), (uint32_t)nf * (I / 2), dn_bar);
-        bulk_g2s(dst + p.nf_max * (I / 2), W.dn_sb + (ex * d + f0) * sbp, (uint32_t)nf * 4 * sbp,
-                 dn_bar);
-      }
-    }
-    if (l + 1 < p.L) issue_router_copy(l + 1);
-    stamp(p, l, 1);
+    ph_route ^= 1;
 
-    // ---- GU: h = silu(gate . x) * (up . x) for the warp's units
+    // ---- GU: h = silu(gate . x) * (up . x) for the warp's units, tagged
     if (nu > 0) {
-      if (!copy_wait(p, bar0 + 8 * warp, ph_gu)) return;
+      if (!copy_wait(p, bar0 + 8 * warp, ph_gu)) {
+        drain();
+        return;
+      }
+      if (lane == 0) infl[warp] = -1;
       float ag[kMaxUnitsPerWarp], au[kMaxUnitsPerWarp];
 #pragma unroll
       for (int t = 0; t < kMaxUnitsPerWarp; ++t) ag[t] = au[t] = 0.f;
       for (int g = lane; g < ng; g += 32) {
-        float2 xv[32];
+        float2 pg[kMaxUnitsPerWarp], pu[kMaxUnitsPerWarp];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] = xs2[i * ng + g];
+        for (int t = 0; t < kMaxUnitsPerWarp; ++t) pg[t] = pu[t] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // K indices 32*hf .. 32*hf+31 of the group
+          float2 xv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xv[i] = xs2[(16 * hf + i) * ng + g];
+#pragma unroll
+          for (int t = 0; t < kMaxUnitsPerWarp; ++t) {
+            if (t < nu) {
+              const uint8_t* ub = gu_buf + (size_t)(warp * p.upw + t) * gu_unit + g * 32 + hf * 16;
+              const uint4 cg = *reinterpret_cast<const uint4*>(ub);
+              const uint4 cu = *reinterpret_cast<const uint4*>(ub + d / 2);
+              pg[t] = dot8(cg.x, xv[0], xv[1], xv[2], xv[3], pg[t]);
+              pu[t] = dot8(cu.x, xv[0], xv[1], xv[2], xv[3], pu[t]);
+              pg[t] = dot8(cg.y, xv[4], xv[5], xv[6], xv[7], pg[t]);
+              pu[t] = dot8(cu.y, xv[4], xv[5], xv[6], xv[7], pu[t]);
+              pg[t] = dot8(cg.z, xv[8], xv[9], xv[10], xv[11], pg[t]);
+              pu[t] = dot8(cu.z, xv[8], xv[9], xv[10], xv[11], pu[t]);
+              pg[t] = dot8(cg.w, xv[12], xv[13], xv[14], xv[15], pg[t]);
+              pu[t] = dot8(cu.w, xv[12], xv[13], xv[14], xv[15], pu[t]);
+            }
+          }
+        }
         const float X = xg[g];
 #pragma unroll
         for (int t = 0; t < kMaxUnitsPerWarp; ++t) {
           if (t < nu) {
             const uint8_t* ub = gu_buf + (size_t)(warp * p.upw + t) * gu_unit;
-            const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
-            const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
-            const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
-            const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
             const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
             const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
-            float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
-            pg = dot8(cg0.x, xv[0], xv[1], xv[2], xv[3], pg);
-            pu = dot8(cu0.x, xv[0], xv[1], xv[2], xv[3], pu);
-            pg = dot8(cg0.y, xv[4], xv[5], xv[6], xv[7], pg);
-            pu = dot8(cu0.y, xv[4], xv[5], xv[6], xv[7], pu);
-            pg = dot8(cg0.z, xv[8], xv[9], xv[10], xv[11], pg);
-            pu = dot8(cu0.z, xv[8], xv[9], xv[10], xv[11], pu);
-            pg = dot8(cg0.w, xv[12], xv[13], xv[14], xv[15], pg);
-            pu = dot8(cu0.w, xv[12], xv[13], xv[14], xv[15], pu);
-            pg = dot8(cg1.x, xv[16], xv[17], xv[18], xv[19], pg);
-            pu = dot8(cu1.x, xv[16], xv[17], xv[18], xv[19], pu);
-            pg = dot8(cg1.y, xv[20], xv[21], xv[22], xv[23], pg);
-            pu = dot8(cu1.y, xv[20], xv[21], xv[22], xv[23], pu);
-            pg = dot8(cg1.z, xv[24], xv[25], xv[26], xv[27], pg);
-            pu = dot8(cu1.z, xv[24], xv[25], xv[26], xv[27], pu);
-            pg = dot8(cg1.w, xv[28], xv[29], xv[30], xv[31], pg);
-            pu = dot8(cu1.w, xv[28], xv[29], xv[30], xv[31], pu);
-            ag[t] += s_of(sbg) * ((pg.x + pg.y) - 128.0f * X) + b_of(sbg) * X;
-            au[t] += s_of(sbu) * ((pu.x + pu.y) - 128.0f * X) + b_of(sbu) * X;
+            ag[t] += s_of(sbg) * ((pg[t].x + pg[t].y) - 128.0f * X) + b_of(sbg) * X;
+            au[t] += s_of(sbu) * ((pu[t].x + pu[t].y) - 128.0f * X) + b_of(sbu) * X;
           }
         }
       }
 #pragma unroll
       for (int t = 0; t < kMaxUnitsPerWarp; ++t) {
         if (t < nu) {
-          const float g = warp_sum(ag[t]);
-          const float u = warp_sum(au[t]);
-          if (lane == 0) p.H[wu0 + t] = g / (1.0f + expf(-g)) * u;  // unit = j*I + f
+          const float g = warp_sum(ag[t]) * r;
+          const float u = warp_sum(au[t]) * r;
+          const float h = g / (1.0f + expf(-g)) * u;
+          if (lane == 0) p.H[wu0 + t] = h;  // unit j*I + f
         }
       }
     }
     ph_gu ^= 1;
-    if (!grid_sync(p, nsync++, s_ok)) return;
-    stamp(p, l, 2);
 
     // ---- D: h of every active expert -> shared memory (pair layout + word sums)
-    {
-      float* hf = reinterpret_cast<float*>(hs2);
-      for (int i = tid; i < k1 * I; i += kDecThreads) {
-        const int j = i / I, e = i - j * I;
-        const int w = e >> 3, q = (e & 7) >> 1;
-        hf[(((j * 4 + q) * nwi) + w) * 2 + (e & 1)] = __ldcg(p.H + i);
-      }
-      __syncthreads();
-      for (int i = tid; i < k1 * nwi; i += kDecThreads) {
-        const int j = i / nwi, w = i - j * nwi;
-        float s = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 v = hs2[(j * 4 + q) * nwi + w];
-          s += v.x + v.y;
-        }
-        hw[i] = s;
-      }
-      __syncthreads();
+    if (!grid_sync(p, nsync++, s_ok)) {
+      drain();
+      return;
     }
+    gather_h();
+    stamp(p, l, 2);
+    for (int i = tid; i < k1 * nwi; i += kDecThreads) {
+      const int j = i / nwi, w = i - j * nwi;
+      float s = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 v = hs2[(j * 4 + q) * nwi + w];
+        s += v.x + v.y;
+      }
+      hw[i] = s;
+    }
+    __syncthreads();
     if (nf > 0) {
-      if (!copy_wait(p, dn_bar, ph_dn)) return;
+      if (!copy_wait(p, dn_bar, ph_dn)) {
+        drain();
+        return;
+      }
+      if (tid == 0) infl[kDnBar] = -1;
     }
     ph_dn ^= 1;
+    // warp per (expert j, run of kDC owned features): h_j is read from shared
+    // memory once per run; lane: words w2, w2+1 of a row (one scale group)
     {
-      const float sigma = misc[0];
-      for (int fl = warp; fl < nf; fl += kDecWarps) {
-        float outv = 0.f;
-        for (int j = 0; j < k1; ++j) {
-          const uint8_t* rowc = dn_buf + (size_t)j * dn_stride + (size_t)fl * (I / 2);
-          const uint32_t* rows = reinterpret_cast<const uint32_t*>(
-              dn_buf + (size_t)j * dn_stride + (size_t)p.nf_max * (I / 2) + (size_t)fl * 4 * sbp);
-          float a = 0.f;
-          for (int w = lane; w < nwi; w += 32) {
-            const uint32_t cw = reinterpret_cast<const uint32_t*>(rowc)[w];
-            const float2* hp = hs2 + (size_t)j * 4 * nwi + w;
-            const float2 acc =
-                dot8(cw, hp[0], hp[nwi], hp[2 * nwi], hp[3 * nwi], make_float2(0.f, 0.f));
-            const float Hs = hw[j * nwi + w];
-            const uint32_t sb = rows[w >> 3];
-            a += s_of(sb) * ((acc.x + acc.y) - 128.0f * Hs) + b_of(sb) * Hs;
+      const int nch = (nf + kDC - 1) / kDC;
+      const int qs = nwi / 2;  // float4 stride between the pair rows of hs2
+      for (int item = warp; item < k1 * nch; item += kDecWarps) {
+        const int j = item / nch, fa = (item - j * nch) * kDC;
+        float acc[kDC];
+#pragma unroll
+        for (int q = 0; q < kDC; ++q) acc[q] = 0.f;
+        for (int w2 = 2 * lane; w2 < nwi; w2 += 64) {
+          const float4* hp = reinterpret_cast<const float4*>(hs2 + (size_t)j * 4 * nwi + w2);
+          const float4 h0 = hp[0], h1 = hp[qs], h2 = hp[2 * qs], h3 = hp[3 * qs];
+          const float2 hs = *reinterpret_cast<const float2*>(hw + j * nwi + w2);
+          const float Hs = hs.x + hs.y;
+#pragma unroll
+          for (int q = 0; q < kDC; ++q) {
+            if (fa + q < nf) {
+              const uint8_t* rowc = dn_buf + (size_t)j * dn_stride + (size_t)(fa + q) * dn_row;
+              const uint2 cw = *reinterpret_cast<const uint2*>(rowc + w2 * 4);
+              const uint32_t sb = reinterpret_cast<const uint32_t*>(rowc + I / 2)[w2 >> 3];
+              float2 ac = dot8(cw.x, make_float2(h0.x, h0.y), make_float2(h1.x, h1.y),
+                               make_float2(h2.x, h2.y), make_float2(h3.x, h3.y),
+                               make_float2(0.f, 0.f));
+              ac = dot8(cw.y, make_float2(h0.z, h0.w), make_float2(h1.z, h1.w),
+                        make_float2(h2.z, h2.w), make_float2(h3.z, h3.w), ac);
+              acc[q] += s_of(sb) * ((ac.x + ac.y) - 128.0f * Hs) + b_of(sb) * Hs;
+            }
           }
-          a = warp_sum(a);
-          outv += ((j < k) ? sel_w[j] : sigma) * a;
         }
-        if (lane == 0) {
-          const uint16_t o = __bfloat16_as_ushort(__float2bfloat16_rn(outv));
-          const int f = f0 + fl;
-          outs[fl] = bf16f(o);
-          p.out[f] = o;
-          if (p.tr_out) p.tr_out[(long long)l * d + f] = o;
-          if (l == p.L - 1) p.y[f] = o;
+#pragma unroll
+        for (int q = 0; q < kDC; ++q) {
+          const float v = warp_sum(acc[q]);
+          if (lane == 0 && fa + q < nf) part[j * p.nf_max + fa + q] = v;
         }
+      }
+      __syncthreads();
+      // out[f] = sum_j w_j part[j][f] (fixed order), rounded to bf16
+      const float sigma = misc[0];
+      uint16_t* outl = p.out + (long long)(l & 1) * d;
+      for (int fl = tid; fl < nf; fl += kDecThreads) {
+        float o = 0.f;
+        for (int j = 0; j < k1; ++j) o = fmaf((j < k) ? sel_w[j] : sigma, part[j * p.nf_max + fl], o);
+        const uint16_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        const int f = f0 + fl;
+        outs[fl] = bf16f(ob);
+        outl[f] = ob;
+        if (p.tr_out) p.tr_out[(long long)l * d + f] = ob;
+        if (l == p.L - 1) p.y[f] = ob;
       }
     }
     __syncthreads();
     stamp(p, l, 3);
     if (l + 1 < p.L) {
       if (nf > 0) {
-        if (!copy_wait(p, rt_bar, ph_rt)) return;
+        if (!copy_wait(p, rt_bar, ph_rt)) {
+          drain();
+          return;
+        }
+        if (tid == 0) infl[kRtBar] = -1;
       }
       ph_rt ^= 1;
-      if (nf > 0) router_partial(p.P + (long long)(l + 1) * (E + 1));
-      if (!grid_sync(p, nsync++, s_ok)) return;
+      if (nf > 0) router_partial((l + 1) % kPSlots);
+      if (!grid_sync(p, nsync++, s_ok)) {
+        drain();
+        return;
+      }
     }
   }
 }
@@ -564,8 +745,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 size_t decode_scratch_bytes(const Handle* h, int L) {
   const moe_config& c = h->cfg;
-  return 256 + (size_t)L * c.E * 4 + (size_t)L * 4 + (size_t)(c.k + 1) * c.I * 4 + (size_t)c.d * 2 +
-         (size_t)L * (c.E + 1) * 8 + 2048;
+  const int k1 = c.k + (c.has_shared ? 1 : 0);
+  return 256 + (size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 256 + 256 +
+         (size_t)k1 * c.I * 4 + 256 +
+         (size_t)L * c.E * 4 + (size_t)L * 4 + 256 + (size_t)2 * c.d * 2 + 2048;
 }
 
 cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const float* bias,
@@ -592,17 +775,28 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  // scratch: [barrier, abort | P] (zeroed before every launch) | H | logits | sigma | out
+  uint8_t* q = scr;
+  unsigned* bar = reinterpret_cast<unsigned*>(q);
+  int* abort_flag = reinterpret_cast<int*>(q + 4);
+  q += 256;
+  unsigned long long* P = reinterpret_cast<unsigned long long*>(q);
+  q += ((size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 255) / 256 * 256;
+  const size_t zero_bytes = (size_t)(q - scr);
+  float* H = reinterpret_cast<float*>(q);
+  q += ((size_t)k1 * c.I * 4 + 255) / 256 * 256;
+  float* logits_s = reinterpret_cast<float*>(q);
+  q += (size_t)kMaxDecLayers * c.E * 4;
+  float* sigma_s = reinterpret_cast<float*>(q);
+  q += (size_t)kMaxDecLayers * 4 + 256;
+  uint16_t* out = reinterpret_cast<uint16_t*>(q);
   for (int l0 = 0; l0 < L; l0 += kMaxDecLayers) {
     const int nl = (L - l0) < kMaxDecLayers ? (L - l0) : kMaxDecLayers;
     DecParams p;
     for (int i = 0; i < nl; ++i) {
       const Handle* h = layers[l0 + i];
-      const long long gu_codes = (long long)h->n_exp * 2 * c.I * (c.d / 2);
-      const long long dn_codes = (long long)h->n_exp * c.d * (c.I / 2);
-      p.layer[i].gu_codes = h->dc_gu;
-      p.layer[i].gu_sb = reinterpret_cast<const uint32_t*>(h->dc_gu + gu_codes);
-      p.layer[i].dn_codes = h->dc_dn;
-      p.layer[i].dn_sb = reinterpret_cast<const uint32_t*>(h->dc_dn + dn_codes);
+      p.layer[i].gu = h->dc_gu;
+      p.layer[i].dn = h->dc_dn;
       p.layer[i].w_rt = h->dc_router_t;
     }
     p.L = nl;
@@ -620,21 +814,13 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     p.bias = bias ? bias + (long long)l0 * c.E : nullptr;
     p.eps = eps;
     p.y = y;
-    uint8_t* q = scr;
-    p.bar = reinterpret_cast<unsigned*>(q);
-    p.abort_flag = reinterpret_cast<int*>(q + 4);
-    q += 256;
-    p.P = reinterpret_cast<unsigned long long*>(q);
-    const size_t pbytes = (size_t)nl * (c.E + 1) * 8;
-    q += (pbytes + 255) / 256 * 256;
-    p.logits = (trace && trace->logits) ? trace->logits + (long long)l0 * c.E
-                                        : reinterpret_cast<float*>(q);
-    q += (size_t)kMaxDecLayers * c.E * 4;
-    p.sigma = (trace && trace->sigma) ? trace->sigma + l0 : reinterpret_cast<float*>(q);
-    q += (size_t)kMaxDecLayers * 4 + 256;
-    p.H = reinterpret_cast<float*>(q);
-    q += (size_t)k1 * c.I * 4 + 256;
-    p.out = reinterpret_cast<uint16_t*>(q);
+    p.bar = bar;
+    p.abort_flag = abort_flag;
+    p.P = P;
+    p.H = H;
+    p.out = out;
+    p.logits = (trace && trace->logits) ? trace->logits + (long long)l0 * c.E : logits_s;
+    p.sigma = (trace && trace->sigma) ? trace->sigma + l0 : sigma_s;
     p.tr_idx = (trace && trace->idx) ? trace->idx + (long long)l0 * c.k : nullptr;
     p.tr_w = (trace && trace->w) ? trace->w + (long long)l0 * c.k : nullptr;
     p.tr_out = (trace && trace->out)
@@ -642,8 +828,8 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
                    : nullptr;
     p.tr_ns = (trace && trace->timestamps) ? trace->timestamps + (long long)l0 * 4 : nullptr;
     p.err = h0->dev_err;
-    // the barrier counter, the abort flag and the fixed-point sums start at zero
-    cudaError_t e = cudaMemsetAsync(scr, 0, 256 + pbytes, st);
+    // the barrier counter, the abort flag and the router sums start at zero
+    cudaError_t e = cudaMemsetAsync(scr, 0, zero_bytes, st);
     if (e != cudaSuccess) return e;
     void* args[] = {&p};
     e = cudaLaunchCooperativeKernel((const void*)decode_kernel, dim3(G), dim3(kDecThreads), args,

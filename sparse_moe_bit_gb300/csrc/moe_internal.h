@@ -57,8 +57,8 @@ struct Handle {
   uint8_t* pf_dn = nullptr;      // [n_exp][d/256][I/64][kCodeChunk]
   uint8_t* pf_router = nullptr;  // [ceil(E/256)][d/64][kRouterChunk]
   // decode layouts (bandwidth path)
-  uint8_t* dc_gu = nullptr;      // [n_exp][I][2 rows][d/2 codes + d/64*4 s,b]
-  uint8_t* dc_dn = nullptr;      // [n_exp][d][I/2 codes + I/64*4 s,b]
+  uint8_t* dc_gu = nullptr;      // [n_exp][I][gate codes | up codes | gate s,b | up s,b]
+  uint8_t* dc_dn = nullptr;      // [n_exp][d][I/2 codes | s,b words padded to 4]
   uint16_t* dc_router_t = nullptr;  // bf16 [d][Ep]: router transposed + w_sg column
   uint16_t* w_router = nullptr;  // bf16 [E][d]
   uint16_t* w_sg = nullptr;      // bf16 [d]

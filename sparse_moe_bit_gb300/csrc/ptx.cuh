@@ -43,6 +43,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_try_wait, but the thread may be suspended in hardware (up to
+// about a millisecond) until the phase completes, so that waiting warps take
+// no issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with parity `parity` of `bar` to complete.  Gives up
 // (returns false) when *abort becomes non-zero or after `limit_ns`; the
 // caller then records the error and leaves its loop.  No wait is unbounded.

@@ -16,9 +16,14 @@
 // block kb: two 128 x 64 bf16 tiles in the 128-byte swizzled K-major order of
 // the tensor-core operand (16-byte chunk c of row r stored at chunk c ^ (r%8)).
 //
-// Decode layout: codes as given (canonical), one array over all experts
-// (shared expert last), and scale/bias merged into one 32-bit word per group
-// (down rows padded to a multiple of four words).
+// Decode layout: one array over all experts (shared expert last) in which
+// everything a CTA reads for a run of features is contiguous, so that one
+// bulk copy brings it in.  Gate/up: per expert, per feature f, one unit of
+// d + d/8 bytes = gate codes of row f (d/2) | up codes of row I+f (d/2) |
+// gate scale/bias (d/64 words) | up scale/bias (d/64 words), a word being
+// fp16 scale | fp16 bias << 16.  Down: per expert, per output row f, I/2 bytes
+// of codes then the row's scale/bias words, padded with zero words to a
+// multiple of four.  Codes keep their canonical nibble order.
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
@@ -112,38 +117,66 @@ __global__ void repack_router_prefill_kernel(const uint16_t* __restrict__ wr, in
   }
 }
 
-// decode layout: codes copied as they are, scale/bias merged per group
-__global__ void repack_decode_kernel(ExpertSrc s, int nexp, int sb_pitch,
-                                     uint8_t* __restrict__ codes_out,
-                                     uint32_t* __restrict__ sb_out) {
-  const long long per_codes = (long long)s.R * (s.K / 2) / 16;  // uint4 per expert
-  const long long per_sb = (long long)s.R * sb_pitch;
-  const long long total = (long long)nexp * (per_codes + per_sb);
-  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
+__device__ __forceinline__ uint32_t sb_word(const uint16_t* sc, const uint16_t* bi, long long gi) {
+  return (uint32_t)sc[gi] | ((uint32_t)bi[gi] << 16);
+}
+
+// decode gate/up units: thread per 16-byte piece of a unit
+__global__ void repack_decode_gu_kernel(ExpertSrc s, int nexp, int I, uint8_t* __restrict__ out) {
+  const int d = s.K, ng = d / 64;
+  const int ub = d + d / 8;
+  const long long pieces = (long long)nexp * I * (ub / 16);
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < pieces;
        it += (long long)gridDim.x * blockDim.x) {
-    if (it < nexp * per_codes) {
-      const int x = (int)(it / per_codes);
-      const long long i = it - x * per_codes;
-      const uint8_t* c;
-      const uint16_t *sc, *bi;
-      expert_ptrs(s, x, c, sc, bi);
-      reinterpret_cast<uint4*>(codes_out)[it] = reinterpret_cast<const uint4*>(c)[i];
+    const long long unit = it / (ub / 16);
+    const int o = (int)(it - unit * (ub / 16)) * 16;
+    const int x = (int)(unit / I), f = (int)(unit - (long long)x * I);
+    const uint8_t* c;
+    const uint16_t *sc, *bi;
+    expert_ptrs(s, x, c, sc, bi);
+    uint4 v;
+    if (o < d) {
+      const int row = (o < d / 2) ? f : I + f;
+      const int off = (o < d / 2) ? o : o - d / 2;
+      v = *reinterpret_cast<const uint4*>(c + (long long)row * (d / 2) + off);
     } else {
-      const long long j = it - nexp * per_codes;
-      const int x = (int)(j / per_sb);
-      const long long i = j - x * per_sb;
-      const long long row = i / sb_pitch;
-      const int g = (int)(i - row * sb_pitch);
-      const uint8_t* c;
-      const uint16_t *sc, *bi;
-      expert_ptrs(s, x, c, sc, bi);
-      if (g < s.K / 64) {
-        const long long gi = row * (s.K / 64) + g;
-        sb_out[j] = (uint32_t)sc[gi] | ((uint32_t)bi[gi] << 16);
-      } else {
-        sb_out[j] = 0u;
-      }
+      const int w = (o - d) / 4;  // first of four words
+      const int row = (w < ng) ? f : I + f;
+      const int g = (w < ng) ? w : w - ng;
+      const long long gi = (long long)row * ng + g;
+      v = make_uint4(sb_word(sc, bi, gi), sb_word(sc, bi, gi + 1), sb_word(sc, bi, gi + 2),
+                     sb_word(sc, bi, gi + 3));
     }
+    *reinterpret_cast<uint4*>(out + unit * ub + o) = v;
+  }
+}
+
+// decode down rows: thread per 16-byte piece of a row
+__global__ void repack_decode_dn_kernel(ExpertSrc s, int nexp, int sb_pitch,
+                                        uint8_t* __restrict__ out) {
+  const int d = s.R, I = s.K, ng = I / 64;
+  const int rb = I / 2 + 4 * sb_pitch;
+  const long long pieces = (long long)nexp * d * (rb / 16);
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < pieces;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long row_all = it / (rb / 16);
+    const int o = (int)(it - row_all * (rb / 16)) * 16;
+    const int x = (int)(row_all / d), f = (int)(row_all - (long long)x * d);
+    const uint8_t* c;
+    const uint16_t *sc, *bi;
+    expert_ptrs(s, x, c, sc, bi);
+    uint4 v;
+    if (o < I / 2) {
+      v = *reinterpret_cast<const uint4*>(c + (long long)f * (I / 2) + o);
+    } else {
+      const int w = (o - I / 2) / 4;
+      uint32_t t[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        t[q] = (w + q < ng) ? sb_word(sc, bi, (long long)f * ng + w + q) : 0u;
+      v = make_uint4(t[0], t[1], t[2], t[3]);
+    }
+    *reinterpret_cast<uint4*>(out + row_all * rb + o) = v;
   }
 }
 
@@ -204,12 +237,8 @@ cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st) {
                                                        (c.E + 255) / 256, h->pf_router);
   }
   if (h->layouts & MOE_LAYOUT_DECODE) {
-    const long long gu_codes = (long long)h->n_exp * 2 * c.I * (c.d / 2);
-    const long long dn_codes = (long long)h->n_exp * c.d * (c.I / 2);
-    repack_decode_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.d / 64, h->dc_gu,
-                                               reinterpret_cast<uint32_t*>(h->dc_gu + gu_codes));
-    repack_decode_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, decode_dn_sb_pitch(c.I), h->dc_dn,
-                                               reinterpret_cast<uint32_t*>(h->dc_dn + dn_codes));
+    repack_decode_gu_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.I, h->dc_gu);
+    repack_decode_dn_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, decode_dn_sb_pitch(c.I), h->dc_dn);
     repack_router_decode_kernel<<<grid, 256, 0, st>>>(
         (const uint16_t*)w->w_router, c.has_shared ? (const uint16_t*)w->w_shared_gate : nullptr,
         c.E, c.d, decode_router_pitch(c.E), h->dc_router_t);
