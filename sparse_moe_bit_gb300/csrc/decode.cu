@@ -28,9 +28,10 @@
 //       that fewer CTAs meet on one address); integer addition makes the sum
 //       exact and independent of the order of arrival -> grid barrier
 // Dot products use the split s*q + beta per 64-group:
-//   sum_i (s q_i + beta) x_i = s (sum_i (128 + q_i) x_i - 128 X) + beta X,
-// X = sum_i x_i, with the code turned into the fp32 value 128 + q by one byte
-// permute (exponent byte 0x43, code in the top mantissa byte).
+//   sum_i (s q_i + beta) x_i = s sum_i q_i x_i + beta X,   X = sum_i x_i,
+// with sum_i q_i x_i an exact integer dot product (dp2a: two 16-bit inputs
+// times two 4-bit codes per instruction) of the codes and the inputs held as
+// 16-bit integers with one power-of-two scale per group of 64.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,11 +46,11 @@ namespace {
 
 constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
+static_assert(kDecWarps == 16, "the down step splits the warps into 8 feature pairs x 2 halves");
 constexpr int kMaxDecLayers = 64;
-constexpr int kMaxUnitsPerWarp = 4;
+constexpr int kMaxUnitsPerWarp = 4;  // units per warp the launch accepts
 constexpr int kPCopies = 8;  // copies of the router sums: CTA c adds into copy c % kPCopies
 constexpr int kPSlots = 3;   // layer l's sums live in slot l % kPSlots
-constexpr int kDC = 4;       // output features a warp takes per expert in the down step
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kFix = 4294967296.0f;  // 2^32
@@ -86,8 +87,8 @@ struct DecParams {
 
 // shared-memory carve-up (the host sizes the launch with the same function)
 struct DecSmem {
-  size_t xs2, xg, hs2, hw, gu, dn, rt, outs, part, lg, lb, sel_e, sel_w, misc, red, infl, bars,
-      ok, total;
+  size_t xq, xsc, xg, hf, hq, hsc, hps, gu, dn, rt, outs, part, lg, lb, sel_e, sel_w, misc, red,
+      infl, bars, ok, total;
 };
 __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align) {
   o = (o + align - 1) / align * align;
@@ -99,15 +100,18 @@ __host__ __device__ inline DecSmem dec_smem(int d, int I, int k1, int E, int Ep,
                                             int upw, int sbp) {
   DecSmem s;
   size_t o = 0;
-  s.xs2 = dec_take(o, (size_t)d * 4, 16);
+  s.xq = dec_take(o, (size_t)d * 2, 16);
+  s.xsc = dec_take(o, (size_t)(d / 64) * 4, 16);
   s.xg = dec_take(o, (size_t)(d / 64) * 4, 16);
-  s.hs2 = dec_take(o, (size_t)k1 * I * 4, 16);
-  s.hw = dec_take(o, (size_t)k1 * (I / 8) * 4, 16);
+  s.hf = dec_take(o, (size_t)k1 * I * 4, 16);
+  s.hq = dec_take(o, (size_t)k1 * I * 2, 16);
+  s.hsc = dec_take(o, (size_t)k1 * (I / 64) * 4, 16);
+  s.hps = dec_take(o, (size_t)k1 * (I / 16) * 4, 16);
   s.gu = dec_take(o, (size_t)kDecWarps * upw * (d + d / 8), 128);
   s.dn = dec_take(o, (size_t)k1 * nf_max * (I / 2 + 4 * sbp), 128);
   s.rt = dec_take(o, (size_t)nf_max * Ep * 2, 128);
   s.outs = dec_take(o, (size_t)nf_max * 4, 16);
-  s.part = dec_take(o, (size_t)k1 * nf_max * 4, 16);
+  s.part = dec_take(o, (size_t)2 * nf_max * 4, 16);
   s.lg = dec_take(o, (size_t)(E + 1) * 4, 16);
   s.lb = dec_take(o, (size_t)E * 4, 16);
   s.sel_e = dec_take(o, kMaxK * 4, 16);
@@ -122,33 +126,6 @@ __host__ __device__ inline DecSmem dec_smem(int d, int I, int k1, int E, int Ep,
 }
 
 __device__ __forceinline__ float bf16f(uint32_t v) { return __uint_as_float(v << 16); }
-
-template <int B>
-__device__ __forceinline__ float code_plus128(uint32_t bytes) {
-  return __uint_as_float(__byte_perm(bytes, 0x43000000u, 0x7044 | (B << 8)));
-}
-
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  const unsigned long long ua = *reinterpret_cast<unsigned long long*>(&a);
-  const unsigned long long ub = *reinterpret_cast<unsigned long long*>(&b);
-  const unsigned long long uc = *reinterpret_cast<unsigned long long*>(&c);
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(ua), "l"(ub), "l"(uc));
-  return *reinterpret_cast<float2*>(&d);
-}
-
-// acc += sum over the 8 codes of w (K indices 8m..8m+7) of (128 + q) * x,
-// x given as the pairs (x[8m+2b], x[8m+2b+1]), b = 0..3
-__device__ __forceinline__ float2 dot8(uint32_t w, float2 x0, float2 x1, float2 x2, float2 x3,
-                                       float2 acc) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
-  acc = ffma2(make_float2(code_plus128<0>(lo), code_plus128<0>(hi)), x0, acc);
-  acc = ffma2(make_float2(code_plus128<1>(lo), code_plus128<1>(hi)), x1, acc);
-  acc = ffma2(make_float2(code_plus128<2>(lo), code_plus128<2>(hi)), x2, acc);
-  acc = ffma2(make_float2(code_plus128<3>(lo), code_plus128<3>(hi)), x3, acc);
-  return acc;
-}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -168,6 +145,56 @@ __device__ __forceinline__ uint32_t ord_key(float v) {
   if (v == 0.0f) v = 0.0f;
   const uint32_t u = __float_as_uint(v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (.lo) or bytes 2, 3 (.hi);
+// a signed 16-bit pairs, b unsigned bytes
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Activations enter the dot products as 16-bit integers with one power-of-two
+// scale 2^e per group of 64, e = floor(log2 amax) - 13 so that every value of
+// the group is below 2^14 units: a bf16 value within 2^6 of its group's
+// maximum is represented exactly, any other value to within 2^-15 of the
+// group maximum.  (e >= -127 keeps 2^-e a normal float; smaller groups are
+// below 2^-114 everywhere.)
+__device__ __forceinline__ int group_exponent(float amax) {
+  const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;  // floor(log2 amax)
+  return max(ex - 13, -127);
+}
+// 2^-e for a group exponent e
+__device__ __forceinline__ float inv_pow2(int e) { return __int_as_float((127 - e) << 23); }
+// 2^e, exact also where it is subnormal (two power-of-two factors)
+__device__ __forceinline__ float pow2(int e) {
+  const int a = e >> 1, b = e - a;
+  return __int_as_float((a + 127) << 23) * __int_as_float((b + 127) << 23);
+}
+// fp32 bits whose low 16 bits are round(v * 2^-e) as a 16-bit integer:
+// adding 1.5 * 2^23 leaves the rounded integer in the low mantissa bits
+__device__ __forceinline__ uint32_t quant_bits(float v, float inv) {
+  return __float_as_uint(fmaf(v, inv, 12582912.0f));
+}
+// the low 16 bits of lo and of hi as one signed 16-bit pair
+__device__ __forceinline__ uint32_t pack_lo16(uint32_t lo, uint32_t hi) {
+  return __byte_perm(lo, hi, 0x5410);
+}
+// sum over the 8 codes of word w (K indices 8m..8m+7, two per byte, low
+// nibble first) of q * v, with v packed as (v0,v2), (v4,v6), (v1,v3), (v5,v7)
+__device__ __forceinline__ int dot8i(uint32_t w, uint4 v, int acc) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;         // q0 q2 q4 q6
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // q1 q3 q5 q7
+  acc = dp2a_lo(v.x, lo, acc);
+  acc = dp2a_hi(v.y, lo, acc);
+  acc = dp2a_lo(v.z, hi, acc);
+  return dp2a_hi(v.w, hi, acc);
 }
 
 __device__ __forceinline__ double softmax_term(float v, double m) {
@@ -297,15 +324,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int nwi = I / 8;  // words per down row
   const int sbp = p.sbp;
   const DecSmem L = dec_smem(d, I, k1, E, Ep, p.nf_max, p.upw, sbp);
-  float2* xs2 = reinterpret_cast<float2*>(dsm + L.xs2);  // [32 pairs][ng]
-  float* xg = reinterpret_cast<float*>(dsm + L.xg);      // [ng]
-  float2* hs2 = reinterpret_cast<float2*>(dsm + L.hs2);  // [k1][4 pairs][I/8]
-  float* hw = reinterpret_cast<float*>(dsm + L.hw);      // [k1][I/8]
+  uint4* xq = reinterpret_cast<uint4*>(dsm + L.xq);   // [8 words][ng] packed int16 x
+  float* xsc = reinterpret_cast<float*>(dsm + L.xsc);  // [ng] scale of a group of x
+  float* xg = reinterpret_cast<float*>(dsm + L.xg);    // [ng] sum of a group of x
+  float* hf = reinterpret_cast<float*>(dsm + L.hf);    // [k1][I] h as gathered
+  uint4* hq = reinterpret_cast<uint4*>(dsm + L.hq);    // [k1][I/8 words] packed int16 h
+  float* hsc = reinterpret_cast<float*>(dsm + L.hsc);  // [k1][I/64] scale of a group of h
+  float* hps = reinterpret_cast<float*>(dsm + L.hps);  // [k1][I/16] sum of h over a word pair
   uint8_t* gu_buf = dsm + L.gu;
   uint8_t* dn_buf = dsm + L.dn;
   const uint16_t* rt_buf = reinterpret_cast<const uint16_t*>(dsm + L.rt);
   float* outs = reinterpret_cast<float*>(dsm + L.outs);
-  float* part = reinterpret_cast<float*>(dsm + L.part);  // [k1][nf_max] D_j[f] . h_j
+  float* part = reinterpret_cast<float*>(dsm + L.part);  // [2][nf_max] halves of out[f]
   float* lg = reinterpret_cast<float*>(dsm + L.lg);  // raw sums, then logits; [E]: shared gate
   float* lb = reinterpret_cast<float*>(dsm + L.lb);  // logit bias
   int* sel_e = reinterpret_cast<int*>(dsm + L.sel_e);
@@ -359,9 +389,40 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   };
 
-  // x (bf16 [d]) -> shared memory in the lane-interleaved pair layout, with
-  // optional RMS normalisation; also the owned features' values and the
-  // group sums (used for the input of the first layer of a launch).
+  // Four consecutive activations v0..v3 at index i0 (a multiple of 4; the 16
+  // lanes of a half-warp hold one group of 64) -> 16-bit integers with the
+  // group's power-of-two scale, stored as the packed pairs the integer dot
+  // products take: word m of group g holds (x0,x2), (x4,x6), (x1,x3),
+  // (x5,x7) of K indices 8m..8m+7.  Also the group's scale and sum.  Every
+  // lane of the warp takes part (shuffles); act = false contributes nothing.
+  auto quant_x4 = [&](float v0, float v1, float v2, float v3, int i0, bool act) {
+    float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+    float sum = (v0 + v1) + (v2 + v3);
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    }
+    const int e = group_exponent(am);
+    const float inv = inv_pow2(e);
+    const uint32_t b0 = quant_bits(v0, inv), b1 = quant_bits(v1, inv);
+    const uint32_t b2 = quant_bits(v2, inv), b3 = quant_bits(v3, inv);
+    if (act) {
+      const int g = i0 >> 6, kk = i0 & 63;
+      uint32_t* wp = reinterpret_cast<uint32_t*>(xq + (kk >> 3) * ng + g);
+      const int h4 = (kk & 4) ? 1 : 0;  // second half of the word: x4..x7
+      wp[h4] = pack_lo16(b0, b2);
+      wp[2 + h4] = pack_lo16(b1, b3);
+      if ((lane & 15) == 0) {
+        xsc[g] = pow2(e);
+        xg[g] = sum;
+      }
+    }
+  };
+
+  // x (bf16 [d]) -> quantised activations in shared memory, with optional
+  // RMS normalisation; also the owned features' values (used for the input
+  // of the first layer of a launch).
   auto load_x = [&](const uint16_t* src, bool norm) {
     float r = 1.0f;
     if (norm) {
@@ -381,18 +442,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       __syncthreads();
       r = misc[1];
     }
-    float* xf = reinterpret_cast<float*>(xs2);
-    for (int i = tid; i < d; i += kDecThreads) {
-      const float v = bf16f(__ldcg(src + i)) * r;
-      const int g = i >> 6, e = i & 63;
-      xf[((e >> 1) * ng + g) * 2 + (e & 1)] = v;
-      if (i >= f0 && i < f1) outs[i - f0] = v;
-    }
-    __syncthreads();
-    for (int g = warp; g < ng; g += kDecWarps) {
-      const float2 v = xs2[lane * ng + g];
-      const float s = warp_sum(v.x + v.y);
-      if (lane == 0) xg[g] = s;
+    for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
+      const int i0 = ib + 4 * tid;
+      const bool act = i0 < d;
+      uint2 raw = make_uint2(0u, 0u);
+      if (act) raw = __ldcg(reinterpret_cast<const uint2*>(src + i0));
+      const float v[4] = {bf16f(raw.x & 0xFFFFu) * r, bf16f(raw.x >> 16) * r,
+                          bf16f(raw.y & 0xFFFFu) * r, bf16f(raw.y >> 16) * r};
+      quant_x4(v[0], v[1], v[2], v[3], i0, act);
+      if (act) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (i0 + q >= f0 && i0 + q < f1) outs[i0 + q - f0] = v[q];
+      }
     }
     __syncthreads();
   };
@@ -419,13 +481,41 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   };
 
   // After the grid barrier that follows the gate/up step: h of all active
-  // experts -> shared memory (pair layout).
+  // experts -> shared memory, then to 16-bit integers with one power-of-two
+  // scale per group of 64 (thread per word of 8 values; 8 threads per
+  // group), packed like the activations, with the sum of h over each word
+  // pair.
   auto gather_h = [&]() {
-    float* hf = reinterpret_cast<float*>(hs2);
-    for (int i = tid; i < k1 * I; i += kDecThreads) {
-      const int j = i / I, e = i - j * I;
-      const int w = e >> 3, q = (e & 7) >> 1;
-      hf[(((j * 4 + q) * nwi) + w) * 2 + (e & 1)] = __ldcg(p.H + i);
+    const int total = k1 * I;
+    for (int i = tid; i < total; i += kDecThreads) hf[i] = __ldcg(p.H + i);
+    __syncthreads();
+    const int nitems = k1 * nwi;
+    for (int base = 0; base < nitems; base += kDecThreads) {
+      const int it = base + tid;
+      const bool act = it < nitems;
+      float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
+      if (act) {
+        va = reinterpret_cast<const float4*>(hf)[2 * it];
+        vb = reinterpret_cast<const float4*>(hf)[2 * it + 1];
+      }
+      float am = fmaxf(fmaxf(fmaxf(fabsf(va.x), fabsf(va.y)), fmaxf(fabsf(va.z), fabsf(va.w))),
+                       fmaxf(fmaxf(fabsf(vb.x), fabsf(vb.y)), fmaxf(fabsf(vb.z), fabsf(vb.w))));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const int e = group_exponent(am);
+      const float inv = inv_pow2(e);
+      const uint32_t q0 = quant_bits(va.x, inv), q1 = quant_bits(va.y, inv);
+      const uint32_t q2 = quant_bits(va.z, inv), q3 = quant_bits(va.w, inv);
+      const uint32_t q4 = quant_bits(vb.x, inv), q5 = quant_bits(vb.y, inv);
+      const uint32_t q6 = quant_bits(vb.z, inv), q7 = quant_bits(vb.w, inv);
+      float ws = ((va.x + va.y) + (va.z + va.w)) + ((vb.x + vb.y) + (vb.z + vb.w));
+      ws += __shfl_xor_sync(0xffffffffu, ws, 1);  // the word pair (2m, 2m+1)
+      if (act) {
+        hq[it] = make_uint4(pack_lo16(q0, q2), pack_lo16(q4, q6), pack_lo16(q1, q3),
+                            pack_lo16(q5, q7));
+        if ((it & 7) == 0) hsc[it >> 3] = pow2(e);
+        if ((it & 1) == 0) hps[it >> 1] = ws;
+      }
     }
     __syncthreads();
   };
@@ -452,6 +542,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     stamp(p, l, 0);
     // ---- A: out_{l-1} and P_l in one pass; routing in warp 0; copies
     if (l + 1 < p.L) issue_router_copy(l + 1);
+    // every load of this step is issued before any of them is used: the
+    // router sums (expert e = tid), its bias, then the previous output
+    const unsigned long long* Ps = p.P + (long long)(l % kPSlots) * kPCopies * (E + 1);
+    unsigned long long pv[kPCopies];
+    float be = 0.0f;
+    if (tid <= E) {
+#pragma unroll
+      for (int q = 0; q < kPCopies; ++q) pv[q] = __ldcg(Ps + q * (E + 1) + tid);
+      if (tid < E && p.bias) be = __ldg(p.bias + (long long)l * E + tid);
+    }
     if (l > 0) {
       const uint16_t* src = p.out + (long long)((l - 1) & 1) * d;
       float ss = 0.f;
@@ -466,28 +566,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         ss = fmaf(v1, v1, ss);
         ss = fmaf(v2, v2, ss);
         ss = fmaf(v3, v3, ss);
-        float s = (v0 + v1) + (v2 + v3);  // 16 lanes hold one 64-group
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 4);
-        s += __shfl_xor_sync(0xffffffffu, s, 8);
-        if (act) {
-          const int g = i0 >> 6, e = i0 & 63;
-          xs2[(e >> 1) * ng + g] = make_float2(v0, v1);
-          xs2[((e >> 1) + 1) * ng + g] = make_float2(v2, v3);
-          if ((lane & 15) == 0) xg[g] = s;
-        }
+        quant_x4(v0, v1, v2, v3, i0, act);
       }
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
     }
     {
-      const unsigned long long* Ps = p.P + (long long)(l % kPSlots) * kPCopies * (E + 1);
-      for (int e = tid; e <= E; e += kDecThreads) {
-        long long s = 0;
+      if (tid <= E) {
+        long long sum = 0;
 #pragma unroll
-        for (int q = 0; q < kPCopies; ++q) s += (long long)__ldcg(Ps + q * (E + 1) + e);
-        lg[e] = (float)((double)s * (1.0 / 4294967296.0));
+        for (int q = 0; q < kPCopies; ++q) sum += (long long)pv[q];
+        lg[tid] = (float)((double)sum * (1.0 / 4294967296.0));
+        if (tid < E) lb[tid] = be;
+      }
+      for (int e = tid + kDecThreads; e <= E; e += kDecThreads) {  // E = 512 only
+        long long sum = 0;
+#pragma unroll
+        for (int q = 0; q < kPCopies; ++q) sum += (long long)__ldcg(Ps + q * (E + 1) + e);
+        lg[e] = (float)((double)sum * (1.0 / 4294967296.0));
         if (e < E) lb[e] = p.bias ? p.bias[(long long)l * E + e] : 0.0f;
       }
       if (c == 0) {  // the slot of layer l-1 is free (read before the last barrier)
@@ -591,77 +687,71 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         return;
       }
       if (lane == 0) infl[warp] = -1;
-      float ag[kMaxUnitsPerWarp], au[kMaxUnitsPerWarp];
+      // two units at a time; lane: one group of 64 inputs at a time, its
+      // activations in registers for both units
+      for (int t0 = 0; t0 < nu; t0 += 2) {
+        const bool two = t0 + 1 < nu;
+        const uint8_t* ub0 = gu_buf + (size_t)(warp * p.upw + t0) * gu_unit;
+        const uint8_t* ub1 = ub0 + gu_unit;
+        float ag0 = 0.f, au0 = 0.f, ag1 = 0.f, au1 = 0.f;
+        for (int g = lane; g < ng; g += 32) {
+          uint4 xw[8];
 #pragma unroll
-      for (int t = 0; t < kMaxUnitsPerWarp; ++t) ag[t] = au[t] = 0.f;
-      for (int g = lane; g < ng; g += 32) {
-        float2 pg[kMaxUnitsPerWarp], pu[kMaxUnitsPerWarp];
+          for (int m = 0; m < 8; ++m) xw[m] = xq[m * ng + g];
+          const float sc = xsc[g], X = xg[g];
 #pragma unroll
-        for (int t = 0; t < kMaxUnitsPerWarp; ++t) pg[t] = pu[t] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {  // K indices 32*hf .. 32*hf+31 of the group
-          float2 xv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xv[i] = xs2[(16 * hf + i) * ng + g];
-#pragma unroll
-          for (int t = 0; t < kMaxUnitsPerWarp; ++t) {
-            if (t < nu) {
-              const uint8_t* ub = gu_buf + (size_t)(warp * p.upw + t) * gu_unit + g * 32 + hf * 16;
-              const uint4 cg = *reinterpret_cast<const uint4*>(ub);
-              const uint4 cu = *reinterpret_cast<const uint4*>(ub + d / 2);
-              pg[t] = dot8(cg.x, xv[0], xv[1], xv[2], xv[3], pg[t]);
-              pu[t] = dot8(cu.x, xv[0], xv[1], xv[2], xv[3], pu[t]);
-              pg[t] = dot8(cg.y, xv[4], xv[5], xv[6], xv[7], pg[t]);
-              pu[t] = dot8(cu.y, xv[4], xv[5], xv[6], xv[7], pu[t]);
-              pg[t] = dot8(cg.z, xv[8], xv[9], xv[10], xv[11], pg[t]);
-              pu[t] = dot8(cu.z, xv[8], xv[9], xv[10], xv[11], pu[t]);
-              pg[t] = dot8(cg.w, xv[12], xv[13], xv[14], xv[15], pg[t]);
-              pu[t] = dot8(cu.w, xv[12], xv[13], xv[14], xv[15], pu[t]);
+          for (int t = 0; t < 2; ++t) {
+            if (t == 0 || two) {
+              const uint8_t* ub = t ? ub1 : ub0;
+              const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
+              const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
+              const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
+              const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
+              int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
+              int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
+              pg0 = dot8i(cg0.z, xw[2], pg0);
+              pg1 = dot8i(cg0.w, xw[3], pg1);
+              pu0 = dot8i(cu0.z, xw[2], pu0);
+              pu1 = dot8i(cu0.w, xw[3], pu1);
+              pg0 = dot8i(cg1.x, xw[4], pg0);
+              pg1 = dot8i(cg1.y, xw[5], pg1);
+              pu0 = dot8i(cu1.x, xw[4], pu0);
+              pu1 = dot8i(cu1.y, xw[5], pu1);
+              pg0 = dot8i(cg1.z, xw[6], pg0);
+              pg1 = dot8i(cg1.w, xw[7], pg1);
+              pu0 = dot8i(cu1.z, xw[6], pu0);
+              pu1 = dot8i(cu1.w, xw[7], pu1);
+              const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
+              const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
+              const float vg = s_of(sbg) * (sc * (float)(pg0 + pg1)) + b_of(sbg) * X;
+              const float vu = s_of(sbu) * (sc * (float)(pu0 + pu1)) + b_of(sbu) * X;
+              if (t == 0) {
+                ag0 += vg;
+                au0 += vu;
+              } else {
+                ag1 += vg;
+                au1 += vu;
+              }
             }
           }
         }
-        const float X = xg[g];
-#pragma unroll
-        for (int t = 0; t < kMaxUnitsPerWarp; ++t) {
-          if (t < nu) {
-            const uint8_t* ub = gu_buf + (size_t)(warp * p.upw + t) * gu_unit;
-            const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
-            const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
-            ag[t] += s_of(sbg) * ((pg[t].x + pg[t].y) - 128.0f * X) + b_of(sbg) * X;
-            au[t] += s_of(sbu) * ((pu[t].x + pu[t].y) - 128.0f * X) + b_of(sbu) * X;
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kMaxUnitsPerWarp; ++t) {
-        if (t < nu) {
-          const float g = warp_sum(ag[t]) * r;
-          const float u = warp_sum(au[t]) * r;
-          const float h = g / (1.0f + expf(-g)) * u;
-          if (lane == 0) p.H[wu0 + t] = h;  // unit j*I + f
+        const float g0 = warp_sum(ag0) * r, u0 = warp_sum(au0) * r;
+        const float g1 = warp_sum(ag1) * r, u1v = warp_sum(au1) * r;
+        if (lane == 0) {
+          p.H[wu0 + t0] = g0 / (1.0f + expf(-g0)) * u0;  // unit j*I + f
+          if (two) p.H[wu0 + t0 + 1] = g1 / (1.0f + expf(-g1)) * u1v;
         }
       }
     }
     ph_gu ^= 1;
 
-    // ---- D: h of every active expert -> shared memory (pair layout + word sums)
+    // ---- D: h of every active expert -> shared memory (quantised, packed)
     if (!grid_sync(p, nsync++, s_ok)) {
       drain();
       return;
     }
     gather_h();
     stamp(p, l, 2);
-    for (int i = tid; i < k1 * nwi; i += kDecThreads) {
-      const int j = i / nwi, w = i - j * nwi;
-      float s = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 v = hs2[(j * 4 + q) * nwi + w];
-        s += v.x + v.y;
-      }
-      hw[i] = s;
-    }
-    __syncthreads();
     if (nf > 0) {
       if (!copy_wait(p, dn_bar, ph_dn)) {
         drain();
@@ -670,49 +760,51 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (tid == 0) infl[kDnBar] = -1;
     }
     ph_dn ^= 1;
-    // warp per (expert j, run of kDC owned features): h_j is read from shared
-    // memory once per run; lane: words w2, w2+1 of a row (one scale group)
+    // warp w: owned features 2*(w % 8) and 2*(w % 8) + 1 (then + 16, ...)
+    // over one half of the experts (w / 8); lane: words w2, w2+1 of a row
+    // (one scale group).  A lane sums its share over the half's experts, so a
+    // warp needs one reduction per feature; part[half][f] takes the result.
     {
-      const int nch = (nf + kDC - 1) / kDC;
-      const int qs = nwi / 2;  // float4 stride between the pair rows of hs2
-      for (int item = warp; item < k1 * nch; item += kDecWarps) {
-        const int j = item / nch, fa = (item - j * nch) * kDC;
-        float acc[kDC];
-#pragma unroll
-        for (int q = 0; q < kDC; ++q) acc[q] = 0.f;
+      const int jh = (k1 + 1) / 2;
+      const int ja = (warp >= 8) ? jh : 0, jb = (warp >= 8) ? k1 : jh;
+      const float sigma = misc[0];
+      for (int fp = 2 * (warp & 7); fp < nf; fp += 16) {
+        const bool two = fp + 1 < nf;
+        float a0 = 0.f, a1 = 0.f;
         for (int w2 = 2 * lane; w2 < nwi; w2 += 64) {
-          const float4* hp = reinterpret_cast<const float4*>(hs2 + (size_t)j * 4 * nwi + w2);
-          const float4 h0 = hp[0], h1 = hp[qs], h2 = hp[2 * qs], h3 = hp[3 * qs];
-          const float2 hs = *reinterpret_cast<const float2*>(hw + j * nwi + w2);
-          const float Hs = hs.x + hs.y;
-#pragma unroll
-          for (int q = 0; q < kDC; ++q) {
-            if (fa + q < nf) {
-              const uint8_t* rowc = dn_buf + (size_t)j * dn_stride + (size_t)(fa + q) * dn_row;
-              const uint2 cw = *reinterpret_cast<const uint2*>(rowc + w2 * 4);
-              const uint32_t sb = reinterpret_cast<const uint32_t*>(rowc + I / 2)[w2 >> 3];
-              float2 ac = dot8(cw.x, make_float2(h0.x, h0.y), make_float2(h1.x, h1.y),
-                               make_float2(h2.x, h2.y), make_float2(h3.x, h3.y),
-                               make_float2(0.f, 0.f));
-              ac = dot8(cw.y, make_float2(h0.z, h0.w), make_float2(h1.z, h1.w),
-                        make_float2(h2.z, h2.w), make_float2(h3.z, h3.w), ac);
-              acc[q] += s_of(sb) * ((ac.x + ac.y) - 128.0f * Hs) + b_of(sb) * Hs;
+          for (int j = ja; j < jb; ++j) {
+            const int hw0 = j * nwi + w2;
+            const uint4 h0 = hq[hw0], h1 = hq[hw0 + 1];
+            const float sc = hsc[hw0 >> 3], Hs = hps[hw0 >> 1];
+            const float wj = (j < k) ? sel_w[j] : sigma;
+            const uint8_t* row0 = dn_buf + (size_t)j * dn_stride + (size_t)fp * dn_row;
+            {
+              const uint2 cw = *reinterpret_cast<const uint2*>(row0 + w2 * 4);
+              const uint32_t sb = reinterpret_cast<const uint32_t*>(row0 + I / 2)[w2 >> 3];
+              const int iv = dot8i(cw.y, h1, dot8i(cw.x, h0, 0));
+              a0 = fmaf(wj, s_of(sb) * (sc * (float)iv) + b_of(sb) * Hs, a0);
+            }
+            if (two) {
+              const uint8_t* row1 = row0 + dn_row;
+              const uint2 cw = *reinterpret_cast<const uint2*>(row1 + w2 * 4);
+              const uint32_t sb = reinterpret_cast<const uint32_t*>(row1 + I / 2)[w2 >> 3];
+              const int iv = dot8i(cw.y, h1, dot8i(cw.x, h0, 0));
+              a1 = fmaf(wj, s_of(sb) * (sc * (float)iv) + b_of(sb) * Hs, a1);
             }
           }
         }
-#pragma unroll
-        for (int q = 0; q < kDC; ++q) {
-          const float v = warp_sum(acc[q]);
-          if (lane == 0 && fa + q < nf) part[j * p.nf_max + fa + q] = v;
+        a0 = warp_sum(a0);
+        a1 = warp_sum(a1);
+        if (lane == 0) {
+          part[(warp >> 3) * p.nf_max + fp] = a0;
+          if (two) part[(warp >> 3) * p.nf_max + fp + 1] = a1;
         }
       }
       __syncthreads();
-      // out[f] = sum_j w_j part[j][f] (fixed order), rounded to bf16
-      const float sigma = misc[0];
+      // out[f] = the two halves' sums (fixed order), rounded to bf16
       uint16_t* outl = p.out + (long long)(l & 1) * d;
       for (int fl = tid; fl < nf; fl += kDecThreads) {
-        float o = 0.f;
-        for (int j = 0; j < k1; ++j) o = fmaf((j < k) ? sel_w[j] : sigma, part[j * p.nf_max + fl], o);
+        const float o = part[fl] + part[p.nf_max + fl];
         const uint16_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(o));
         const int f = f0 + fl;
         outs[fl] = bf16f(ob);
