@@ -240,8 +240,8 @@ def run_decode(args, torch, M, sd, gen, device, peaks):
     ts = tr["timestamps"].cpu().numpy().astype("float64") / 1000.0
     phases = {
         "route_and_issue_copies": float((ts[:, 1] - ts[:, 0]).mean()),
-        "gate_up_and_h_exchange": float((ts[:, 2] - ts[:, 1]).mean()),
-        "down": float((ts[:, 3] - ts[:, 2]).mean()),
+        "gate_up_down_partials_and_barrier": float((ts[:, 2] - ts[:, 1]).mean()),
+        "sum_partials": float((ts[:, 3] - ts[:, 2]).mean()),
         "router_partials_and_barrier": float((ts[1:, 0] - ts[:-1, 3]).mean()),
     }
     err = layers[0].device_error()

@@ -177,8 +177,9 @@ typedef struct moe_decode_trace {
   void* out;       /* bf16 [L][d], output of every layer */
   int64_t* timestamps; /* int64 [L][4]: GPU clock (ns) in the first CTA at the
                           start of a layer, after its weight copies are issued,
-                          once the gate/up results of every CTA have arrived,
-                          and at the end of the down projection (profiling
+                          once every CTA's gate/up and partial down projection
+                          is done (after the grid barrier), and once the layer
+                          output of the CTA's features is summed (profiling
                           aid) */
 } moe_decode_trace;
 

@@ -1,8 +1,8 @@
 // Batch-1 decode path: one persistent cooperative kernel runs every layer of
 // the chain on CUDA cores.  The work is bound by weight reads (4.5 bits per
-// weight): each CTA streams only its share of the selected experts' rows into
-// shared memory with bulk (TMA) copies issued as soon as the routing is known,
-// and computes while they land.
+// weight): each CTA streams only its share of the selected experts' weights
+// into shared memory with bulk (TMA) copies issued as soon as the routing is
+// known, and computes while they land.
 // Source: Perplexity, "Optimizing on-device inference for Apple Silicon",
 // §"Optimizing the one-row weight path" (a row-parallel GEMV: a SIMD group
 // cooperates on one output while reading different parts of the weight
@@ -11,27 +11,33 @@
 // routing score and the shared expert's result) and §"Keep each decode step
 // on the GPU" (no host synchronisation between steps).
 //
-// Two grid-wide barriers per layer.  CTA c owns output features
-// [c*d/G, (c+1)*d/G) and a contiguous range of the (slot j, feature f) units
-// of the k+1 active experts.
+// The k+1 active experts' intermediate features are cut into blocks of 32
+// (one expert each); CTA c takes blocks c, c+G, ... and, for a block, computes
+// its 32 gated features h = silu(G x) * (U x) and at once their share of the
+// output projection, w_j * D_j[:, block] h_block, over all d output features
+// (the "partial" of the block).  So h never leaves the CTA; only the partials
+// are exchanged.  CTA c also owns the output features [c*d/G, (c+1)*d/G).
+// Two grid-wide barriers per layer:
 //   A : every CTA reads the previous output out_{l-1} and the router sums P_l
 //       in one pass, folds 1/rms(out_{l-1}) into the logits (the rest of the
 //       layer works on the unnormalised vector and scales its dot products),
 //       repeats the top-k selection in one warp and issues the bulk copies of
-//       its gate/up rows and its down rows straight after it.
-//   GU: h_j[f] = silu(G_j[f] . x) * (U_j[f] . x) for the owned units -> global
+//       its block's gate/up rows and down columns straight after it.
+//   B : gate/up of the block (two features per warp), h of the block to
+//       16-bit integers, the block's partial over all d outputs -> global
 //       -> grid barrier
-//   D : out[f] = sum_j w_j (D_j[f] . h_j) + sigma (D_s[f] . h_s) for the owned
-//       features, then the next layer's router partial sums over those
-//       features: P_{l+1}[e] += sum_f out[f] W_r'[e][f], accumulated as 64-bit
-//       fixed-point integers (2^-32 units) into one of several copies of P (so
-//       that fewer CTAs meet on one address); integer addition makes the sum
-//       exact and independent of the order of arrival -> grid barrier
+//   R : out[f] = sum over blocks of the partials (fixed order) for the owned
+//       features, rounded to bf16; then the next layer's router partial sums
+//       over those features: P_{l+1}[e] += sum_f out[f] W_r'[e][f],
+//       accumulated as 64-bit fixed-point integers (2^-32 units) into one of
+//       several copies of P (so that fewer CTAs meet on one address); integer
+//       addition makes the sum exact and independent of the order of
+//       arrival -> grid barrier
 // Dot products use the split s*q + beta per 64-group:
 //   sum_i (s q_i + beta) x_i = s sum_i q_i x_i + beta X,   X = sum_i x_i,
 // with sum_i q_i x_i an exact integer dot product (dp2a: two 16-bit inputs
 // times two 4-bit codes per instruction) of the codes and the inputs held as
-// 16-bit integers with one power-of-two scale per group of 64.
+// 16-bit integers with one power-of-two scale per group of inputs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -46,26 +52,29 @@ namespace {
 
 constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
-static_assert(kDecWarps == 16, "the down step splits the warps into 8 feature pairs x 2 halves");
+constexpr int kBlk = 32;                        // intermediate features per block
+constexpr int kUnitsPerWarp = kBlk / kDecWarps;  // gate/up features a warp computes
+static_assert(kUnitsPerWarp == 2, "gate/up takes two features per warp");
 constexpr int kMaxDecLayers = 64;
-constexpr int kMaxUnitsPerWarp = 4;  // units per warp the launch accepts
 constexpr int kPCopies = 8;  // copies of the router sums: CTA c adds into copy c % kPCopies
 constexpr int kPSlots = 3;   // layer l's sums live in slot l % kPSlots
+constexpr int kRedChunks = 32;  // partial sums per owned feature in the reduction
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 constexpr float kFix = 4294967296.0f;  // 2^32
 
 struct DecLayer {
   const uint8_t* gu;     // [n_exp][I] units of d + d/8 bytes (gate, up codes; their s,b)
-  const uint8_t* dn;     // [n_exp][d] rows of I/2 + 4*sbp bytes (codes; s,b words)
+  const uint8_t* dnc;    // [n_exp][I/32][d] 16 bytes: the 32 codes of a block in row f
+  const uint32_t* dnsb;  // [n_exp][I/64][d] scale/bias word of row f, input group g
   const uint16_t* w_rt;  // [d][Ep] router transposed + shared-gate column
 };
 
 struct DecParams {
   DecLayer layer[kMaxDecLayers];
   int L, d, E, k, I, has_shared, Ep;
-  int nf_max, upw;  // output features per CTA (max), units per warp (max)
-  int sbp;          // 32-bit scale/bias words per down row (padded)
+  int nf_max;  // output features per CTA (max)
+  int NB;      // blocks per layer: (k+1 or k) * I / 32
   const uint16_t* x;
   int norm_first;  // 1: x is an earlier layer's output (normalise it first)
   const float* bias;  // [L][E] or null
@@ -77,7 +86,7 @@ struct DecParams {
   float* tr_w;          // [L][k] or null
   uint16_t* tr_out;     // [L][d] or null
   int64_t* tr_ns;       // [L][4] or null
-  float* H;             // [k1*I] h of the active experts (unit j*I + f)
+  float* part;          // [NB][d] the blocks' weighted partial outputs
   uint16_t* out;        // [2][d]: layer l writes row l % 2
   unsigned long long* P;  // [kPSlots][kPCopies][E+1] fixed-point router sums, zero at launch
   unsigned* bar;        // grid barrier arrivals, zero at launch
@@ -87,7 +96,7 @@ struct DecParams {
 
 // shared-memory carve-up (the host sizes the launch with the same function)
 struct DecSmem {
-  size_t xq, xsc, xg, hf, hq, hsc, hps, gu, dn, rt, outs, part, lg, lb, sel_e, sel_w, misc, red,
+  size_t xq, xsc, xg, gu, dnc, dnsb, hb, hpk, rt, outs, red2, lg, lb, sel_e, sel_w, misc, red,
       infl, bars, ok, total;
 };
 __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align) {
@@ -96,22 +105,20 @@ __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align
   o += bytes;
   return r;
 }
-__host__ __device__ inline DecSmem dec_smem(int d, int I, int k1, int E, int Ep, int nf_max,
-                                            int upw, int sbp) {
+__host__ __device__ inline DecSmem dec_smem(int d, int E, int Ep, int nf_max) {
   DecSmem s;
   size_t o = 0;
   s.xq = dec_take(o, (size_t)d * 2, 16);
   s.xsc = dec_take(o, (size_t)(d / 64) * 4, 16);
   s.xg = dec_take(o, (size_t)(d / 64) * 4, 16);
-  s.hf = dec_take(o, (size_t)k1 * I * 4, 16);
-  s.hq = dec_take(o, (size_t)k1 * I * 2, 16);
-  s.hsc = dec_take(o, (size_t)k1 * (I / 64) * 4, 16);
-  s.hps = dec_take(o, (size_t)k1 * (I / 16) * 4, 16);
-  s.gu = dec_take(o, (size_t)kDecWarps * upw * (d + d / 8), 128);
-  s.dn = dec_take(o, (size_t)k1 * nf_max * (I / 2 + 4 * sbp), 128);
+  s.gu = dec_take(o, (size_t)kBlk * (d + d / 8), 128);
+  s.dnc = dec_take(o, (size_t)d * 16, 128);
+  s.dnsb = dec_take(o, (size_t)d * 4, 128);
+  s.hb = dec_take(o, (size_t)kBlk * 4, 16);
+  s.hpk = dec_take(o, (size_t)(kBlk / 8) * 16, 16);
   s.rt = dec_take(o, (size_t)nf_max * Ep * 2, 128);
   s.outs = dec_take(o, (size_t)nf_max * 4, 16);
-  s.part = dec_take(o, (size_t)2 * nf_max * 4, 16);
+  s.red2 = dec_take(o, (size_t)kRedChunks * 16 * 4, 16);
   s.lg = dec_take(o, (size_t)(E + 1) * 4, 16);
   s.lb = dec_take(o, (size_t)E * 4, 16);
   s.sel_e = dec_take(o, kMaxK * 4, 16);
@@ -319,28 +326,26 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ DecParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   const int d = p.d, E = p.E, k = p.k, I = p.I, Ep = p.Ep;
-  const int k1 = k + (p.has_shared ? 1 : 0);
   const int ng = d / 64;
-  const int nwi = I / 8;  // words per down row
-  const int sbp = p.sbp;
-  const DecSmem L = dec_smem(d, I, k1, E, Ep, p.nf_max, p.upw, sbp);
+  const int NB = p.NB;
+  const int bpe = I / kBlk;  // blocks per expert
+  const DecSmem L = dec_smem(d, E, Ep, p.nf_max);
   uint4* xq = reinterpret_cast<uint4*>(dsm + L.xq);   // [8 words][ng] packed int16 x
   float* xsc = reinterpret_cast<float*>(dsm + L.xsc);  // [ng] scale of a group of x
   float* xg = reinterpret_cast<float*>(dsm + L.xg);    // [ng] sum of a group of x
-  float* hf = reinterpret_cast<float*>(dsm + L.hf);    // [k1][I] h as gathered
-  uint4* hq = reinterpret_cast<uint4*>(dsm + L.hq);    // [k1][I/8 words] packed int16 h
-  float* hsc = reinterpret_cast<float*>(dsm + L.hsc);  // [k1][I/64] scale of a group of h
-  float* hps = reinterpret_cast<float*>(dsm + L.hps);  // [k1][I/16] sum of h over a word pair
-  uint8_t* gu_buf = dsm + L.gu;
-  uint8_t* dn_buf = dsm + L.dn;
+  uint8_t* gu_buf = dsm + L.gu;                        // [32 units] of d + d/8 bytes
+  const uint4* dnc = reinterpret_cast<const uint4*>(dsm + L.dnc);        // [d] block codes
+  const uint32_t* dnsb = reinterpret_cast<const uint32_t*>(dsm + L.dnsb);  // [d] s,b words
+  float* hb = reinterpret_cast<float*>(dsm + L.hb);    // [32] h of the block
+  uint4* hpk = reinterpret_cast<uint4*>(dsm + L.hpk);  // [4 words] packed int16 h
   const uint16_t* rt_buf = reinterpret_cast<const uint16_t*>(dsm + L.rt);
   float* outs = reinterpret_cast<float*>(dsm + L.outs);
-  float* part = reinterpret_cast<float*>(dsm + L.part);  // [2][nf_max] halves of out[f]
+  float* red2 = reinterpret_cast<float*>(dsm + L.red2);  // [chunks][16] reduction partials
   float* lg = reinterpret_cast<float*>(dsm + L.lg);  // raw sums, then logits; [E]: shared gate
   float* lb = reinterpret_cast<float*>(dsm + L.lb);  // logit bias
   int* sel_e = reinterpret_cast<int*>(dsm + L.sel_e);
   float* sel_w = reinterpret_cast<float*>(dsm + L.sel_w);
-  float* misc = reinterpret_cast<float*>(dsm + L.misc);  // [0] sigma, [1] 1/rms
+  float* misc = reinterpret_cast<float*>(dsm + L.misc);  // [0] sigma [1] 1/rms [2] h scale [3] h sum
   float* red = reinterpret_cast<float*>(dsm + L.red);
   // parity of the copies in flight on each mbarrier (-1: none), for the
   // bounded drain on the error path
@@ -351,20 +356,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t dn_bar = bar0 + 8 * kDnBar;
   const uint32_t rt_bar = bar0 + 8 * kRtBar;
   const uint32_t route_bar = bar0 + 8 * (kDecWarps + 2);  // the top-k of the layer is known
-  const int wwarp = kDecWarps - 1;  // computes the routing weights (it has the fewest units)
+  const int wwarp = kDecWarps - 1;  // computes the routing weights
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, c = blockIdx.x;
   const int f0 = (int)((long long)c * d / G), f1 = (int)((long long)(c + 1) * d / G);
   const int nf = f1 - f0;
-  const int U = k1 * I;
-  const int u0 = (int)((long long)c * U / G), u1 = (int)((long long)(c + 1) * U / G);
-  const int wu0 = min(u0 + warp * p.upw, u1);
-  const int wu1 = min(wu0 + p.upw, u1);
-  const int nu = wu1 - wu0;
   const int gu_unit = d + d / 8;
-  const int dn_row = I / 2 + 4 * sbp;
-  const int dn_stride = p.nf_max * dn_row;
 
   if (tid == 0) {
     for (int i = 0; i < kDecWarps + 3; ++i) mbar_init(bar0 + 8 * i, 1);
@@ -386,6 +384,31 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       while (!mbar_try_wait(bar0 + 8 * i, (uint32_t)pty)) {
         if (globaltimer_ns() - t0 > kDrainNs) break;
       }
+    }
+  };
+
+  // Block b: expert slot j = b / bpe (slot k: the shared expert), features
+  // (b % bpe) * 32 .. + 31.  Issue its bulk copies: lane i < 16 the gate/up
+  // rows of warp i's two features, lane 16 the block's down columns (codes
+  // of every output row, then the rows' scale/bias words of its input
+  // group).  Called by every lane of one warp.
+  auto issue_block = [&](int b, const DecLayer& W) {
+    const int j = b / bpe, i0 = (b - j * bpe) * kBlk;
+    const long long ex = (j < k) ? sel_e[j] : E;
+    if (lane < kDecWarps) {
+      const uint32_t bar = bar0 + 8 * lane;
+      const uint32_t bytes = (uint32_t)(kUnitsPerWarp * gu_unit);
+      infl[lane] = (int)ph_gu;
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(smem_u32(gu_buf + (size_t)lane * kUnitsPerWarp * gu_unit),
+               W.gu + (ex * I + i0 + lane * kUnitsPerWarp) * gu_unit, bytes, bar);
+    } else if (lane == kDecWarps) {
+      infl[kDnBar] = (int)ph_dn;
+      mbar_arrive_expect_tx(dn_bar, (uint32_t)(d * 20));
+      bulk_g2s(smem_u32(dsm + L.dnc), W.dnc + (ex * bpe + i0 / kBlk) * (long long)d * 16,
+               (uint32_t)(d * 16), dn_bar);
+      bulk_g2s(smem_u32(dsm + L.dnsb), W.dnsb + (ex * (I / 64) + i0 / 64) * (long long)d,
+               (uint32_t)(d * 4), dn_bar);
     }
   };
 
@@ -478,46 +501,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_arrive_expect_tx(rt_bar, bytes);
       bulk_g2s(smem_u32(dsm + L.rt), p.layer[l].w_rt + (long long)f0 * Ep, bytes, rt_bar);
     }
-  };
-
-  // After the grid barrier that follows the gate/up step: h of all active
-  // experts -> shared memory, then to 16-bit integers with one power-of-two
-  // scale per group of 64 (thread per word of 8 values; 8 threads per
-  // group), packed like the activations, with the sum of h over each word
-  // pair.
-  auto gather_h = [&]() {
-    const int total = k1 * I;
-    for (int i = tid; i < total; i += kDecThreads) hf[i] = __ldcg(p.H + i);
-    __syncthreads();
-    const int nitems = k1 * nwi;
-    for (int base = 0; base < nitems; base += kDecThreads) {
-      const int it = base + tid;
-      const bool act = it < nitems;
-      float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-      if (act) {
-        va = reinterpret_cast<const float4*>(hf)[2 * it];
-        vb = reinterpret_cast<const float4*>(hf)[2 * it + 1];
-      }
-      float am = fmaxf(fmaxf(fmaxf(fabsf(va.x), fabsf(va.y)), fmaxf(fabsf(va.z), fabsf(va.w))),
-                       fmaxf(fmaxf(fabsf(vb.x), fabsf(vb.y)), fmaxf(fabsf(vb.z), fabsf(vb.w))));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      const int e = group_exponent(am);
-      const float inv = inv_pow2(e);
-      const uint32_t q0 = quant_bits(va.x, inv), q1 = quant_bits(va.y, inv);
-      const uint32_t q2 = quant_bits(va.z, inv), q3 = quant_bits(va.w, inv);
-      const uint32_t q4 = quant_bits(vb.x, inv), q5 = quant_bits(vb.y, inv);
-      const uint32_t q6 = quant_bits(vb.z, inv), q7 = quant_bits(vb.w, inv);
-      float ws = ((va.x + va.y) + (va.z + va.w)) + ((vb.x + vb.y) + (vb.z + vb.w));
-      ws += __shfl_xor_sync(0xffffffffu, ws, 1);  // the word pair (2m, 2m+1)
-      if (act) {
-        hq[it] = make_uint4(pack_lo16(q0, q2), pack_lo16(q4, q6), pack_lo16(q1, q3),
-                            pack_lo16(q5, q7));
-        if ((it & 7) == 0) hsc[it >> 3] = pow2(e);
-        if ((it & 1) == 0) hps[it >> 1] = ws;
-      }
-    }
-    __syncthreads();
   };
 
   // ---- prologue: x_0 and the router sums of layer 0 (slot 0)
@@ -620,36 +603,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (__any_sync(0xffffffffu, nan_seen) && lane == 0 && c == 0)
         atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
       __syncwarp();
-      // bulk copies: lane i < 16 those of warp i's gate/up units (one per
-      // expert the units fall in), lane 16 the CTA's down rows of the k+1
-      // experts (one per expert)
-      if (lane < kDecWarps) {
-        const int a0 = min(u0 + lane * p.upw, u1), a1 = min(a0 + p.upw, u1);
-        if (a1 > a0) {
-          const uint32_t bar = bar0 + 8 * lane;
-          infl[lane] = (int)ph_gu;
-          mbar_arrive_expect_tx(bar, (uint32_t)((a1 - a0) * gu_unit));
-          uint32_t dst = smem_u32(gu_buf + (size_t)lane * p.upw * gu_unit);
-          for (int u = a0; u < a1;) {
-            const int j = u / I, f = u - j * I;
-            const int n = min(a1 - u, I - f);
-            const long long ex = (j < k) ? sel_e[j] : E;
-            bulk_g2s(dst, W.gu + (ex * I + f) * gu_unit, (uint32_t)(n * gu_unit), bar);
-            dst += (uint32_t)(n * gu_unit);
-            u += n;
-          }
-        }
-      } else if (lane == kDecWarps && nf > 0) {
-        infl[kDnBar] = (int)ph_dn;
-        mbar_arrive_expect_tx(dn_bar, (uint32_t)(k1 * nf * dn_row));
-        for (int j = 0; j < k1; ++j) {
-          const long long ex = (j < k) ? sel_e[j] : E;
-          bulk_g2s(smem_u32(dn_buf + (size_t)j * dn_stride), W.dn + (ex * d + f0) * dn_row,
-                   (uint32_t)(nf * dn_row), dn_bar);
-        }
-      } else if (lane == kDecWarps + 1) {
-        mbar_arrive(route_bar);  // sel_e and the logits are in shared memory
-      }
+      if (c < NB) issue_block(c, W);
+      if (lane == kDecWarps + 1) mbar_arrive(route_bar);  // sel_e and the logits are ready
       stamp(p, l, 1);
     }
     if (warp == wwarp) {
@@ -680,20 +635,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     ph_route ^= 1;
 
-    // ---- GU: h = silu(gate . x) * (up . x) for the warp's units, tagged
-    if (nu > 0) {
+    // ---- B: the CTA's blocks: gate/up, h, and the block's partial output
+    for (int b = c, nb = 0; b < NB; b += G, ++nb) {
+      const int j = b / bpe;
+      if (nb > 0) {
+        __syncthreads();  // the previous block's buffers are no longer read
+        if (warp == 0) issue_block(b, W);
+      }
+      // gate/up: warp -> features 2*warp, 2*warp + 1 of the block; lane: one
+      // group of 64 inputs at a time, its activations in registers for both
       if (!copy_wait(p, bar0 + 8 * warp, ph_gu)) {
         drain();
         return;
       }
       if (lane == 0) infl[warp] = -1;
-      // two units at a time; lane: one group of 64 inputs at a time, its
-      // activations in registers for both units
-      for (int t0 = 0; t0 < nu; t0 += 2) {
-        const bool two = t0 + 1 < nu;
-        const uint8_t* ub0 = gu_buf + (size_t)(warp * p.upw + t0) * gu_unit;
-        const uint8_t* ub1 = ub0 + gu_unit;
-        float ag0 = 0.f, au0 = 0.f, ag1 = 0.f, au1 = 0.f;
+      ph_gu ^= 1;
+      {
+        const uint8_t* ub0 = gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit;
+        float ag[2] = {0.f, 0.f}, au[2] = {0.f, 0.f};
         for (int g = lane; g < ng; g += 32) {
           uint4 xw[8];
 #pragma unroll
@@ -701,119 +660,117 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const float sc = xsc[g], X = xg[g];
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (t == 0 || two) {
-              const uint8_t* ub = t ? ub1 : ub0;
-              const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
-              const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
-              const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
-              const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
-              int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
-              int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
-              pg0 = dot8i(cg0.z, xw[2], pg0);
-              pg1 = dot8i(cg0.w, xw[3], pg1);
-              pu0 = dot8i(cu0.z, xw[2], pu0);
-              pu1 = dot8i(cu0.w, xw[3], pu1);
-              pg0 = dot8i(cg1.x, xw[4], pg0);
-              pg1 = dot8i(cg1.y, xw[5], pg1);
-              pu0 = dot8i(cu1.x, xw[4], pu0);
-              pu1 = dot8i(cu1.y, xw[5], pu1);
-              pg0 = dot8i(cg1.z, xw[6], pg0);
-              pg1 = dot8i(cg1.w, xw[7], pg1);
-              pu0 = dot8i(cu1.z, xw[6], pu0);
-              pu1 = dot8i(cu1.w, xw[7], pu1);
-              const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
-              const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
-              const float vg = s_of(sbg) * (sc * (float)(pg0 + pg1)) + b_of(sbg) * X;
-              const float vu = s_of(sbu) * (sc * (float)(pu0 + pu1)) + b_of(sbu) * X;
-              if (t == 0) {
-                ag0 += vg;
-                au0 += vu;
-              } else {
-                ag1 += vg;
-                au1 += vu;
-              }
-            }
+            const uint8_t* ub = ub0 + t * gu_unit;
+            const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
+            const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
+            const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
+            const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
+            int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
+            int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
+            pg0 = dot8i(cg0.z, xw[2], pg0);
+            pg1 = dot8i(cg0.w, xw[3], pg1);
+            pu0 = dot8i(cu0.z, xw[2], pu0);
+            pu1 = dot8i(cu0.w, xw[3], pu1);
+            pg0 = dot8i(cg1.x, xw[4], pg0);
+            pg1 = dot8i(cg1.y, xw[5], pg1);
+            pu0 = dot8i(cu1.x, xw[4], pu0);
+            pu1 = dot8i(cu1.y, xw[5], pu1);
+            pg0 = dot8i(cg1.z, xw[6], pg0);
+            pg1 = dot8i(cg1.w, xw[7], pg1);
+            pu0 = dot8i(cu1.z, xw[6], pu0);
+            pu1 = dot8i(cu1.w, xw[7], pu1);
+            const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
+            const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
+            ag[t] += s_of(sbg) * (sc * (float)(pg0 + pg1)) + b_of(sbg) * X;
+            au[t] += s_of(sbu) * (sc * (float)(pu0 + pu1)) + b_of(sbu) * X;
           }
         }
-        const float g0 = warp_sum(ag0) * r, u0 = warp_sum(au0) * r;
-        const float g1 = warp_sum(ag1) * r, u1v = warp_sum(au1) * r;
-        if (lane == 0) {
-          p.H[wu0 + t0] = g0 / (1.0f + expf(-g0)) * u0;  // unit j*I + f
-          if (two) p.H[wu0 + t0 + 1] = g1 / (1.0f + expf(-g1)) * u1v;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const float gv = warp_sum(ag[t]) * r, uv = warp_sum(au[t]) * r;
+          if (lane == 0) hb[warp * kUnitsPerWarp + t] = gv / (1.0f + expf(-gv)) * uv;
         }
       }
-    }
-    ph_gu ^= 1;
-
-    // ---- D: h of every active expert -> shared memory (quantised, packed)
-    if (!grid_sync(p, nsync++, s_ok)) {
-      drain();
-      return;
-    }
-    gather_h();
-    stamp(p, l, 2);
-    if (nf > 0) {
+      __syncthreads();
+      // h of the block -> 16-bit integers with one power-of-two scale, packed
+      // as the integer dot products take them (word m: features 8m..8m+7)
+      if (warp == 0) {
+        const float v = hb[lane];
+        float am = fabsf(v), hs = v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+          hs += __shfl_xor_sync(0xffffffffu, hs, o);
+        }
+        const int e = group_exponent(am);
+        uint32_t* qt = reinterpret_cast<uint32_t*>(red2);
+        qt[lane] = quant_bits(v, inv_pow2(e));
+        __syncwarp();
+        if (lane < kBlk / 8) {
+          const uint32_t* q8 = qt + lane * 8;
+          hpk[lane] = make_uint4(pack_lo16(q8[0], q8[2]), pack_lo16(q8[4], q8[6]),
+                                 pack_lo16(q8[1], q8[3]), pack_lo16(q8[5], q8[7]));
+        }
+        if (lane == 0) {
+          misc[2] = pow2(e);
+          misc[3] = hs;
+        }
+      }
       if (!copy_wait(p, dn_bar, ph_dn)) {
         drain();
         return;
       }
       if (tid == 0) infl[kDnBar] = -1;
-    }
-    ph_dn ^= 1;
-    // warp w: owned features 2*(w % 8) and 2*(w % 8) + 1 (then + 16, ...)
-    // over one half of the experts (w / 8); lane: words w2, w2+1 of a row
-    // (one scale group).  A lane sums its share over the half's experts, so a
-    // warp needs one reduction per feature; part[half][f] takes the result.
-    {
-      const int jh = (k1 + 1) / 2;
-      const int ja = (warp >= 8) ? jh : 0, jb = (warp >= 8) ? k1 : jh;
-      const float sigma = misc[0];
-      for (int fp = 2 * (warp & 7); fp < nf; fp += 16) {
-        const bool two = fp + 1 < nf;
-        float a0 = 0.f, a1 = 0.f;
-        for (int w2 = 2 * lane; w2 < nwi; w2 += 64) {
-          for (int j = ja; j < jb; ++j) {
-            const int hw0 = j * nwi + w2;
-            const uint4 h0 = hq[hw0], h1 = hq[hw0 + 1];
-            const float sc = hsc[hw0 >> 3], Hs = hps[hw0 >> 1];
-            const float wj = (j < k) ? sel_w[j] : sigma;
-            const uint8_t* row0 = dn_buf + (size_t)j * dn_stride + (size_t)fp * dn_row;
-            {
-              const uint2 cw = *reinterpret_cast<const uint2*>(row0 + w2 * 4);
-              const uint32_t sb = reinterpret_cast<const uint32_t*>(row0 + I / 2)[w2 >> 3];
-              const int iv = dot8i(cw.y, h1, dot8i(cw.x, h0, 0));
-              a0 = fmaf(wj, s_of(sb) * (sc * (float)iv) + b_of(sb) * Hs, a0);
-            }
-            if (two) {
-              const uint8_t* row1 = row0 + dn_row;
-              const uint2 cw = *reinterpret_cast<const uint2*>(row1 + w2 * 4);
-              const uint32_t sb = reinterpret_cast<const uint32_t*>(row1 + I / 2)[w2 >> 3];
-              const int iv = dot8i(cw.y, h1, dot8i(cw.x, h0, 0));
-              a1 = fmaf(wj, s_of(sb) * (sc * (float)iv) + b_of(sb) * Hs, a1);
-            }
-          }
-        }
-        a0 = warp_sum(a0);
-        a1 = warp_sum(a1);
-        if (lane == 0) {
-          part[(warp >> 3) * p.nf_max + fp] = a0;
-          if (two) part[(warp >> 3) * p.nf_max + fp + 1] = a1;
-        }
-      }
+      ph_dn ^= 1;
       __syncthreads();
-      // out[f] = the two halves' sums (fixed order), rounded to bf16
-      uint16_t* outl = p.out + (long long)(l & 1) * d;
-      for (int fl = tid; fl < nf; fl += kDecThreads) {
-        const float o = part[fl] + part[p.nf_max + fl];
-        const uint16_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-        const int f = f0 + fl;
-        outs[fl] = bf16f(ob);
-        outl[f] = ob;
-        if (p.tr_out) p.tr_out[(long long)l * d + f] = ob;
-        if (l == p.L - 1) p.y[f] = ob;
+      // the block's partial output: part[b][f] = w_j (s sum_i q_i h_i + beta H)
+      {
+        const uint4 h0 = hpk[0], h1 = hpk[1], h2 = hpk[2], h3 = hpk[3];
+        const float hsc = misc[2], Hs = misc[3];
+        const float wj = (j < k) ? sel_w[j] : misc[0];
+        float* pb = p.part + (long long)b * d;
+        for (int f = tid; f < d; f += kDecThreads) {
+          const uint4 cw = dnc[f];
+          const uint32_t sb = dnsb[f];
+          const int a = (dot8i(cw.x, h0, 0) + dot8i(cw.y, h1, 0)) +
+                        (dot8i(cw.z, h2, 0) + dot8i(cw.w, h3, 0));
+          pb[f] = wj * (s_of(sb) * (hsc * (float)a) + b_of(sb) * Hs);
+        }
       }
     }
-    __syncthreads();
+
+    // ---- every block's partial is in global memory
+    if (!grid_sync(p, nsync++, s_ok)) {
+      drain();
+      return;
+    }
+    stamp(p, l, 2);
+    // ---- R: out[f] = sum over blocks of part[b][f] (fixed order), bf16
+    {
+      uint16_t* outl = p.out + (long long)(l & 1) * d;
+      for (int fl0 = 0; fl0 < nf; fl0 += 16) {
+        const int fl = fl0 + (tid & 15), ch = tid >> 4;  // 32 chunks of blocks
+        float s = 0.f;
+        if (fl < nf) {
+          const float* pf = p.part + f0 + fl;
+#pragma unroll 4
+          for (int b = ch; b < NB; b += kRedChunks) s += __ldcg(pf + (long long)b * d);
+        }
+        red2[ch * 16 + (tid & 15)] = s;
+        __syncthreads();
+        if (tid < 16 && fl0 + tid < nf) {
+          float o = 0.f;
+          for (int q = 0; q < kRedChunks; ++q) o += red2[q * 16 + tid];
+          const uint16_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          const int f = f0 + fl0 + tid;
+          outs[fl0 + tid] = bf16f(ob);
+          outl[f] = ob;
+          if (p.tr_out) p.tr_out[(long long)l * d + f] = ob;
+          if (l == p.L - 1) p.y[f] = ob;
+        }
+        __syncthreads();
+      }
+    }
     stamp(p, l, 3);
     if (l + 1 < p.L) {
       if (nf > 0) {
@@ -838,8 +795,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 size_t decode_scratch_bytes(const Handle* h, int L) {
   const moe_config& c = h->cfg;
   const int k1 = c.k + (c.has_shared ? 1 : 0);
-  return 256 + (size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 256 + 256 +
-         (size_t)k1 * c.I * 4 + 256 +
+  const size_t NB = (size_t)k1 * c.I / kBlk;
+  return 256 + (size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 256 + NB * c.d * 4 + 256 +
          (size_t)L * c.E * 4 + (size_t)L * 4 + 256 + (size_t)2 * c.d * 2 + 2048;
 }
 
@@ -851,12 +808,9 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
   const int k1 = c.k + (c.has_shared ? 1 : 0);
   const int G = h0->num_sms;
   const int nf_max = (c.d + G - 1) / G;
-  const int units_cta = (k1 * c.I + G - 1) / G;
-  const int upw = (units_cta + kDecWarps - 1) / kDecWarps;
-  if (upw > kMaxUnitsPerWarp) return cudaErrorInvalidConfiguration;
+  const int NB = k1 * c.I / kBlk;
   const int Ep = decode_router_pitch(c.E);
-  const int sbp = decode_dn_sb_pitch(c.I);
-  const DecSmem sm = dec_smem(c.d, c.I, k1, c.E, Ep, nf_max, upw, sbp);
+  const DecSmem sm = dec_smem(c.d, c.E, Ep, nf_max);
   if (sm.total > 227 * 1024) return cudaErrorInvalidConfiguration;
   static_assert(sizeof(DecParams) < 32000, "kernel parameter size");
   uint8_t* scr = reinterpret_cast<uint8_t*>(h0->ws.logit_part);
@@ -867,7 +821,7 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  // scratch: [barrier, abort | P] (zeroed before every launch) | H | logits | sigma | out
+  // scratch: [barrier, abort | P] (zeroed before every launch) | partials | logits | sigma | out
   uint8_t* q = scr;
   unsigned* bar = reinterpret_cast<unsigned*>(q);
   int* abort_flag = reinterpret_cast<int*>(q + 4);
@@ -875,8 +829,8 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
   unsigned long long* P = reinterpret_cast<unsigned long long*>(q);
   q += ((size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 255) / 256 * 256;
   const size_t zero_bytes = (size_t)(q - scr);
-  float* H = reinterpret_cast<float*>(q);
-  q += ((size_t)k1 * c.I * 4 + 255) / 256 * 256;
+  float* part = reinterpret_cast<float*>(q);
+  q += ((size_t)NB * c.d * 4 + 255) / 256 * 256;
   float* logits_s = reinterpret_cast<float*>(q);
   q += (size_t)kMaxDecLayers * c.E * 4;
   float* sigma_s = reinterpret_cast<float*>(q);
@@ -888,7 +842,9 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     for (int i = 0; i < nl; ++i) {
       const Handle* h = layers[l0 + i];
       p.layer[i].gu = h->dc_gu;
-      p.layer[i].dn = h->dc_dn;
+      p.layer[i].dnc = h->dc_dn;
+      p.layer[i].dnsb =
+          reinterpret_cast<const uint32_t*>(h->dc_dn + (size_t)h->n_exp * c.I / 2 * c.d);
       p.layer[i].w_rt = h->dc_router_t;
     }
     p.L = nl;
@@ -899,8 +855,7 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     p.has_shared = c.has_shared;
     p.Ep = Ep;
     p.nf_max = nf_max;
-    p.upw = upw;
-    p.sbp = sbp;
+    p.NB = NB;
     p.x = (l0 == 0) ? x : y;
     p.norm_first = (l0 == 0) ? 0 : 1;
     p.bias = bias ? bias + (long long)l0 * c.E : nullptr;
@@ -909,7 +864,7 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     p.bar = bar;
     p.abort_flag = abort_flag;
     p.P = P;
-    p.H = H;
+    p.part = part;
     p.out = out;
     p.logits = (trace && trace->logits) ? trace->logits + (long long)l0 * c.E : logits_s;
     p.sigma = (trace && trace->sigma) ? trace->sigma + l0 : sigma_s;

@@ -127,8 +127,7 @@ moe_status alloc_all(Handle* h) {
   }
   if (h->layouts & MOE_LAYOUT_DECODE) {
     CK(dalloc(&h->dc_gu, (size_t)h->n_exp * 2 * c.I * (c.d / 2 + c.d / 16)), "alloc");
-    CK(dalloc(&h->dc_dn, (size_t)h->n_exp * c.d * (c.I / 2 + 4 * decode_dn_sb_pitch(c.I))),
-       "alloc");
+    CK(dalloc(&h->dc_dn, (size_t)h->n_exp * c.d * (c.I / 2 + c.I / 16)), "alloc");
     CK(dalloc(&h->dc_router_t, (size_t)c.d * decode_router_pitch(c.E) * 2), "alloc");
   }
   CK(dalloc(&h->w_router, (size_t)c.E * c.d * 2), "alloc");

@@ -58,7 +58,7 @@ struct Handle {
   uint8_t* pf_router = nullptr;  // [ceil(E/256)][d/64][kRouterChunk]
   // decode layouts (bandwidth path)
   uint8_t* dc_gu = nullptr;      // [n_exp][I][gate codes | up codes | gate s,b | up s,b]
-  uint8_t* dc_dn = nullptr;      // [n_exp][d][I/2 codes | s,b words padded to 4]
+  uint8_t* dc_dn = nullptr;      // codes [n_exp][I/32][d][16 B], then s,b [n_exp][I/64][d]
   uint16_t* dc_router_t = nullptr;  // bf16 [d][Ep]: router transposed + w_sg column
   uint16_t* w_router = nullptr;  // bf16 [E][d]
   uint16_t* w_sg = nullptr;      // bf16 [d]
@@ -80,7 +80,6 @@ struct Handle {
 inline int decode_router_pitch(int E) { return ((E + 1) + 7) & ~7; }
 // 32-bit scale/bias words per row of the decode down layout: I/64 groups,
 // padded to a multiple of 4 (16-byte rows for bulk copies)
-inline int decode_dn_sb_pitch(int I) { return ((I / 64) + 3) & ~3; }
 
 // ---- grouped tensor-core GEMM (grouped_mma.cu)
 enum MmaMode { MMA_ROUTER = 0, MMA_GATEUP = 1, MMA_DOWN = 2 };

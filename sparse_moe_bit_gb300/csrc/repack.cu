@@ -21,9 +21,10 @@
 // bulk copy brings it in.  Gate/up: per expert, per feature f, one unit of
 // d + d/8 bytes = gate codes of row f (d/2) | up codes of row I+f (d/2) |
 // gate scale/bias (d/64 words) | up scale/bias (d/64 words), a word being
-// fp16 scale | fp16 bias << 16.  Down: per expert, per output row f, I/2 bytes
-// of codes then the row's scale/bias words, padded with zero words to a
-// multiple of four.  Codes keep their canonical nibble order.
+// fp16 scale | fp16 bias << 16.  Down: by blocks of 32 input features, for
+// each output row the block's 16 bytes of codes (all rows of a block
+// contiguous), then the rows' scale/bias words per input group of 64.  Codes
+// keep their canonical nibble order.
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
@@ -151,32 +152,34 @@ __global__ void repack_decode_gu_kernel(ExpertSrc s, int nexp, int I, uint8_t* _
   }
 }
 
-// decode down rows: thread per 16-byte piece of a row
-__global__ void repack_decode_dn_kernel(ExpertSrc s, int nexp, int sb_pitch,
-                                        uint8_t* __restrict__ out) {
-  const int d = s.R, I = s.K, ng = I / 64;
-  const int rb = I / 2 + 4 * sb_pitch;
-  const long long pieces = (long long)nexp * d * (rb / 16);
-  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < pieces;
+// decode down weights, by blocks of 32 input features: codes
+// [x][blk][f] (16 bytes: the block's 32 codes of output row f, canonical
+// nibble order), then scale/bias words [x][g][f] (row f, input group g); one
+// thread per 16-byte piece of codes or per word
+__global__ void repack_decode_dn_kernel(ExpertSrc s, int nexp, uint8_t* __restrict__ out) {
+  const int d = s.R, I = s.K, ng = I / 64, nblk = I / 32;
+  const long long pieces = (long long)nexp * nblk * d;
+  const long long words = (long long)nexp * ng * d;
+  uint32_t* sb_out = reinterpret_cast<uint32_t*>(out + pieces * 16);
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < pieces + words;
        it += (long long)gridDim.x * blockDim.x) {
-    const long long row_all = it / (rb / 16);
-    const int o = (int)(it - row_all * (rb / 16)) * 16;
-    const int x = (int)(row_all / d), f = (int)(row_all - (long long)x * d);
     const uint8_t* c;
     const uint16_t *sc, *bi;
-    expert_ptrs(s, x, c, sc, bi);
-    uint4 v;
-    if (o < I / 2) {
-      v = *reinterpret_cast<const uint4*>(c + (long long)f * (I / 2) + o);
+    if (it < pieces) {
+      const int f = (int)(it % d);
+      const long long xb = it / d;
+      const int blk = (int)(xb % nblk), x = (int)(xb / nblk);
+      expert_ptrs(s, x, c, sc, bi);
+      reinterpret_cast<uint4*>(out)[it] =
+          *reinterpret_cast<const uint4*>(c + (long long)f * (I / 2) + blk * 16);
     } else {
-      const int w = (o - I / 2) / 4;
-      uint32_t t[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        t[q] = (w + q < ng) ? sb_word(sc, bi, (long long)f * ng + w + q) : 0u;
-      v = make_uint4(t[0], t[1], t[2], t[3]);
+      const long long w = it - pieces;
+      const int f = (int)(w % d);
+      const long long xg = w / d;
+      const int g = (int)(xg % ng), x = (int)(xg / ng);
+      expert_ptrs(s, x, c, sc, bi);
+      sb_out[w] = sb_word(sc, bi, (long long)f * ng + g);
     }
-    *reinterpret_cast<uint4*>(out + row_all * rb + o) = v;
   }
 }
 
@@ -238,7 +241,7 @@ cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st) {
   }
   if (h->layouts & MOE_LAYOUT_DECODE) {
     repack_decode_gu_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.I, h->dc_gu);
-    repack_decode_dn_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, decode_dn_sb_pitch(c.I), h->dc_dn);
+    repack_decode_dn_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, h->dc_dn);
     repack_router_decode_kernel<<<grid, 256, 0, st>>>(
         (const uint16_t*)w->w_router, c.has_shared ? (const uint16_t*)w->w_shared_gate : nullptr,
         c.E, c.d, decode_router_pitch(c.E), h->dc_router_t);
