@@ -56,12 +56,18 @@ int router_ksplit(int d) {
   return ks;
 }
 
+// Token tiles of 128 rows, or of 64 when 128-row tiles leave SMs idle (each
+// unit streams its share of the router weights from L2 whatever its width,
+// so halving the tile pays only while the units do not exceed the SMs).
 RouterPlan plan_router(const Handle* h, int T) {
   RouterPlan r;
-  r.n = T >= 128 ? 128 : ((T + 15) & ~15);
-  r.tiles = ceil_div(T, r.n);
   r.m_units = ceil_div(h->cfg.E, 256);
   r.ks = router_ksplit(h->cfg.d);
+  r.n = T >= 128 ? 128 : ((T + 15) & ~15);
+  if (r.n == 128 && ceil_div(T, 128) * r.m_units * r.ks < h->num_sms &&
+      ceil_div(T, 64) * r.m_units * r.ks <= h->num_sms)
+    r.n = 64;
+  r.tiles = ceil_div(T, r.n);
   r.units = r.tiles * r.m_units * r.ks;
   return r;
 }

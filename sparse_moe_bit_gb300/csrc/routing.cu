@@ -18,25 +18,33 @@
 namespace moe {
 namespace {
 
-// (value, index) order of the selection: larger value first, then lower index.
-__device__ __forceinline__ bool beats(float va, int ea, float vb, int eb) {
-  return va > vb || (va == vb && ea < eb);
-}
-
 __device__ __forceinline__ double softmax_term(float v, double m) {
   if (m == INFINITY) return v == INFINITY ? 1.0 : 0.0;
   if (m == -INFINITY) return 1.0;
   return exp((double)v - m);
 }
 
-// One warp per token.  Sums the router's K-split partial logits (fixed
-// order), adds the bias, keeps the top k by (logit desc, index asc) and
-// computes the renormalised softmax weights in fp64.  When x is given it
-// also writes the fp16 copy of the token's activations and the shared
-// expert's gate sigma = sigmoid(w_sg . x).  Each block counts its assignments
-// per expert (hist[block][e]).
-constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
+// order-preserving key of a float (larger value, larger key); -0 taken as +0
+__device__ __forceinline__ uint32_t ord_key(float v) {
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp per token, 32 tokens per block (one block = one row of the
+// histogram).  Sums the router's K-split partial logits (fixed order), adds
+// the bias, keeps the top k by (logit desc, index asc) and computes the
+// renormalised softmax weights in fp64.  When x is given it also writes the
+// fp16 copy of the token's activations and the shared expert's gate
+// sigma = sigmoid(w_sg . x).  Each block counts its assignments per expert
+// (hist[block][e]).
+// Selection: lane l holds the order keys of experts l, l+32, ...; each round
+// every lane finds its best key not yet taken (first slot among equal keys,
+// i.e. the lowest index), the warp maximum of those and then the smallest
+// expert index among the lanes holding it name the winner (two warp
+// reductions per round).
+constexpr int kTopkThreads = 32 * kTokPerBlock;
+static_assert(kTopkThreads <= 1024, "one warp per token of a block");
 
 template <int VPL>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
@@ -46,80 +54,67 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     float* __restrict__ sigma, uint16_t* __restrict__ x16, int32_t* __restrict__ hist,
     int* __restrict__ err) {
   __shared__ int cnt[kMaxE];
+  __shared__ float s_v[kTokPerBlock][kMaxK];  // the kept logits of each token, in order
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
 
-  for (int tt = 0; tt < kTokPerBlock / kTopkWarps; ++tt) {
-    const int t = blockIdx.x * kTokPerBlock + warp * (kTokPerBlock / kTopkWarps) + tt;
-    if (t >= T) break;
+  const int t = blockIdx.x * kTokPerBlock + warp;
+  if (t < T) {
     float v[VPL];
+    uint32_t key[VPL];
     bool nan_seen = false;
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int e = lane + 32 * j;
       float s = -INFINITY;
+      uint32_t kk = 0u;  // empty; every real key is larger
       if (e < E) {
         s = 0.0f;
-        for (int p = 0; p < KS; ++p) s += part[((long long)p * T + t) * E + e];
+        for (int q = 0; q < KS; ++q) s += part[((long long)q * T + t) * E + e];
         if (bias) s += bias[e];
         logits[(long long)t * E + e] = s;
         if (s != s) {
           nan_seen = true;
           s = -INFINITY;
         }
+        kk = ord_key(s);
       }
       v[j] = s;
+      key[j] = kk;
     }
     if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, MOE_DEVERR_NAN_LOGIT);
 
-    uint32_t taken = 0;
-    float sel_v[kMaxK];
-    int sel_e[kMaxK];
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && beats(v[j], e, bv, be)) {
-          bv = v[j];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (beats(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel_v[r] = bv;
-      sel_e[r] = be;
-    }
-    // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0); with infinite
-    // logits the limit: +inf experts share equally, all -inf share equally
-    // lane r owns slot r: one fp64 exp per kept expert, the sum by a fixed
-    // butterfly (the same order on every run)
-    const double m = (double)sel_v[0];
+    // lane r keeps the r-th choice
     float my_v = -INFINITY;
     int my_e = 0;
     for (int r = 0; r < k; ++r) {
+      uint32_t bk = 0u;
+      int bj = 0;
+      float bv = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const bool better = key[j] > bk;
+        bk = better ? key[j] : bk;
+        bv = better ? v[j] : bv;
+        bj = better ? j : bj;
+      }
+      const uint32_t M = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t win =
+          __reduce_min_sync(0xffffffffu, bk == M ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+      const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31u));
+      if ((int)(win & 31u) == lane) {
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) key[j] = (j == (int)(win >> 5)) ? 0u : key[j];
+      }
       if (lane == r) {
-        my_v = sel_v[r];
-        my_e = sel_e[r];
+        my_v = wv;
+        my_e = (int)win;
       }
     }
-    const double ex = (lane < k) ? softmax_term(my_v, m) : 0.0;
-    double den = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
     if (lane < k) {
       idx_out[(long long)t * k + lane] = my_e;
-      w_out[(long long)t * k + lane] = (float)(ex / den);
+      s_v[warp][lane] = my_v;
       atomicAdd(&cnt[my_e], 1);
     }
 
@@ -127,7 +122,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
       const uint16_t* xr = x + (long long)t * d;
       uint16_t* xo = x16 + (long long)t * d;
       float dot = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
       for (int c = lane * 8; c < d; c += 256) {
         const uint4 raw = *reinterpret_cast<const uint4*>(xr + c);
         const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -154,6 +149,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     }
   }
   __syncthreads();
+  // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0); with infinite
+  // logits the limit: +inf experts share equally, all -inf share equally.
+  // fp64 runs at a small fraction of fp32 here, so a warp takes 32 / kp
+  // tokens at once (lane: token, slot), kp = 8 or 16 >= k; the sum over a
+  // token's slots is a fixed butterfly (the same order on every run).
+  {
+    const int kp = (k <= 8) ? 8 : 16;
+    const int tpw = 32 / kp;  // tokens per warp
+    const int tl = warp * tpw + lane / kp, r = lane % kp;
+    if (warp * tpw < kTokPerBlock) {
+      const int tt = blockIdx.x * kTokPerBlock + tl;
+      const bool on = tl < kTokPerBlock && tt < T && r < k;
+      const double m = on ? (double)s_v[tl][0] : 0.0;
+      const double ex = on ? softmax_term(s_v[tl][r], m) : 0.0;
+      double den = ex;
+      for (int off = kp >> 1; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      if (on) w_out[(long long)tt * k + r] = (float)(ex / den);
+    }
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     hist[(long long)blockIdx.x * E + e] = cnt[e];
 }
