@@ -46,6 +46,7 @@
 
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "softmax_df.cuh"
 
 namespace moe {
 namespace {
@@ -202,12 +203,6 @@ __device__ __forceinline__ int dot8i(uint32_t w, uint4 v, int acc) {
   acc = dp2a_hi(v.y, lo, acc);
   acc = dp2a_lo(v.z, hi, acc);
   return dp2a_hi(v.w, hi, acc);
-}
-
-__device__ __forceinline__ double softmax_term(float v, double m) {
-  if (m == INFINITY) return v == INFINITY ? 1.0 : 0.0;
-  if (m == -INFINITY) return 1.0;
-  return exp((double)v - m);
 }
 
 
@@ -559,14 +554,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         long long sum = 0;
 #pragma unroll
         for (int q = 0; q < kPCopies; ++q) sum += (long long)pv[q];
-        lg[tid] = (float)((double)sum * (1.0 / 4294967296.0));
+        lg[tid] = __ll2float_rn(sum) * (1.0f / 4294967296.0f);
         if (tid < E) lb[tid] = be;
       }
       for (int e = tid + kDecThreads; e <= E; e += kDecThreads) {  // E = 512 only
         long long sum = 0;
 #pragma unroll
         for (int q = 0; q < kPCopies; ++q) sum += (long long)__ldcg(Ps + q * (E + 1) + e);
-        lg[e] = (float)((double)sum * (1.0 / 4294967296.0));
+        lg[e] = __ll2float_rn(sum) * (1.0f / 4294967296.0f);
         if (e < E) lb[e] = p.bias ? p.bias[(long long)l * E + e] : 0.0f;
       }
       if (c == 0) {  // the slot of layer l-1 is free (read before the last barrier)
@@ -608,8 +603,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       stamp(p, l, 1);
     }
     if (warp == wwarp) {
-      // routing weights (fp64 softmax over the k chosen logits), off the
-      // path of the copies and of the other warps' gate/up work
+      // routing weights (softmax over the k chosen logits in double-float
+      // arithmetic, within one ulp of fp64), off the path of the copies and
+      // of the other warps' gate/up work
       if (!copy_wait(p, route_bar, ph_route)) {
         drain();
         return;
@@ -619,13 +615,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (my_v != my_v) my_v = -INFINITY;
       float top = lg[sel_e[0]];
       if (top != top) top = -INFINITY;
-      const double m = (double)top;
-      const double ex = (lane < k) ? softmax_term(my_v, m) : 0.0;
-      double den = ex;
+      const dflt ex = (lane < k) ? df_softmax_term(my_v, top) : dflt{0.0f, 0.0f};
+      dflt den = ex;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      for (int o = 16; o > 0; o >>= 1) {
+        const dflt ot = {__shfl_xor_sync(0xffffffffu, den.hi, o),
+                         __shfl_xor_sync(0xffffffffu, den.lo, o)};
+        den = df_add(den, ot);
+      }
       if (lane < k) {
-        const float wv = (float)(ex / den);
+        const float wv = df_div(ex, den).hi;
         sel_w[lane] = wv;
         if (c == 0) {
           if (p.tr_idx) p.tr_idx[(long long)l * k + lane] = my_e;

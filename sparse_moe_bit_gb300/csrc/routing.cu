@@ -14,15 +14,10 @@
 #include <mutex>
 
 #include "moe_internal.h"
+#include "softmax_df.cuh"
 
 namespace moe {
 namespace {
-
-__device__ __forceinline__ double softmax_term(float v, double m) {
-  if (m == INFINITY) return v == INFINITY ? 1.0 : 0.0;
-  if (m == -INFINITY) return 1.0;
-  return exp((double)v - m);
-}
 
 // order-preserving key of a float (larger value, larger key); -0 taken as +0
 __device__ __forceinline__ uint32_t ord_key(float v) {
@@ -64,15 +59,33 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     float v[VPL];
     uint32_t key[VPL];
     bool nan_seen = false;
+    // all of the lane's loads first (one round trip), then the sums in the
+    // fixed order 0 + part_0 + part_1 + ... + bias
+    float pa[VPL], ba[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      pa[j] = (e < E) ? __ldg(part + (long long)t * E + e) : 0.0f;
+      ba[j] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
+    }
+    for (int q = 1; q < KS; ++q) {
+      float pq[VPL];
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int e = lane + 32 * j;
+        pq[j] = (e < E) ? __ldg(part + ((long long)q * T + t) * E + e) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) pa[j] += pq[j];
+    }
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int e = lane + 32 * j;
       float s = -INFINITY;
       uint32_t kk = 0u;  // empty; every real key is larger
       if (e < E) {
-        s = 0.0f;
-        for (int q = 0; q < KS; ++q) s += part[((long long)q * T + t) * E + e];
-        if (bias) s += bias[e];
+        s = 0.0f + pa[j];
+        if (bias) s += ba[j];
         logits[(long long)t * E + e] = s;
         if (s != s) {
           nan_seen = true;
@@ -149,11 +162,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     }
   }
   __syncthreads();
-  // weights, fp64: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0); with infinite
-  // logits the limit: +inf experts share equally, all -inf share equally.
-  // fp64 runs at a small fraction of fp32 here, so a warp takes 32 / kp
-  // tokens at once (lane: token, slot), kp = 8 or 16 >= k; the sum over a
-  // token's slots is a fixed butterfly (the same order on every run).
+  // weights: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0) in double-float
+  // arithmetic (within one ulp of the fp64 value; see softmax_df.cuh); with
+  // infinite logits the limit: +inf experts share equally, all -inf share
+  // equally.  A warp takes 32 / kp tokens at once (lane: token, slot),
+  // kp = 8 or 16 >= k; the sum over a token's slots is a fixed butterfly
+  // (the same order on every run).
   {
     const int kp = (k <= 8) ? 8 : 16;
     const int tpw = 32 / kp;  // tokens per warp
@@ -161,15 +175,71 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     if (warp * tpw < kTokPerBlock) {
       const int tt = blockIdx.x * kTokPerBlock + tl;
       const bool on = tl < kTokPerBlock && tt < T && r < k;
-      const double m = on ? (double)s_v[tl][0] : 0.0;
-      const double ex = on ? softmax_term(s_v[tl][r], m) : 0.0;
-      double den = ex;
-      for (int off = kp >> 1; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-      if (on) w_out[(long long)tt * k + r] = (float)(ex / den);
+      const dflt ex = on ? df_softmax_term(s_v[tl][r], s_v[tl][0]) : dflt{0.0f, 0.0f};
+      dflt den = ex;
+      for (int off = kp >> 1; off > 0; off >>= 1) {
+        const dflt o = {__shfl_xor_sync(0xffffffffu, den.hi, off),
+                        __shfl_xor_sync(0xffffffffu, den.lo, off)};
+        den = df_add(den, o);
+      }
+      if (on) w_out[(long long)tt * k + r] = df_div(ex, den).hi;
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     hist[(long long)blockIdx.x * E + e] = cnt[e];
+}
+
+// The fp16 copy of the activations (the gate/up GEMM's operand) and the
+// shared expert's gate sigma = sigmoid(w_sg . x): one warp per token, 8
+// tokens per block, w_sg staged in shared memory, each lane's loads of a
+// row issued together.
+constexpr int kCvtThreads = 256;
+constexpr int kCvtTokens = kCvtThreads / 32;
+
+__global__ void __launch_bounds__(kCvtThreads) x16_sigma_kernel(
+    const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_sg,
+    int has_shared, float* __restrict__ sigma, uint16_t* __restrict__ x16) {
+  extern __shared__ uint4 s_wsg[];  // d / 8
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
+    s_wsg[i] = has_shared ? reinterpret_cast<const uint4*>(w_sg)[i] : make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kCvtTokens + warp;
+  if (t >= T) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * d);
+  uint4* xo = reinterpret_cast<uint4*>(x16 + (long long)t * d);
+  float dot = 0.0f;
+  for (int c0 = lane; c0 < d / 8; c0 += 32 * 8) {
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < d / 8) raw[i] = __ldcs(xr + c0 + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + 32 * i;
+      if (c < d / 8) {
+        const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        const uint4 sg = s_wsg[c];
+        const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(wv[q] << 16);
+          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
+          dot = fmaf(lo, __uint_as_float(sv[q] << 16), dot);
+          dot = fmaf(hi, __uint_as_float(sv[q] & 0xFFFF0000u), dot);
+        }
+        xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+    }
+  }
+  if (has_shared) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) sigma[t] = 1.0f / (1.0f + expf(-dot));
+  }
 }
 
 // Exclusive scan of one value per thread over the whole block (<= 1024
@@ -367,6 +437,11 @@ cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const
                         const uint16_t* x, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
+  if (x) {  // fp16 activations and the shared gate, in a kernel of their own
+    x16_sigma_kernel<<<(T + kCvtTokens - 1) / kCvtTokens, kCvtThreads, (size_t)c.d * 2, st>>>(
+        x, T, c.d, h->w_sg, c.has_shared, ws.sigma, ws.x16);
+    x = nullptr;
+  }
   const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
   if (c.E <= 256)
     topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
