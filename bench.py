@@ -239,10 +239,10 @@ def run_decode(args, torch, M, sd, gen, device, peaks):
     torch.cuda.synchronize(device)
     ts = tr["timestamps"].cpu().numpy().astype("float64") / 1000.0
     phases = {
-        "route_and_issue_copies": float((ts[:, 1] - ts[:, 0]).mean()),
-        "gate_up_down_partials_and_barrier": float((ts[:, 2] - ts[:, 1]).mean()),
-        "sum_partials": float((ts[:, 3] - ts[:, 2]).mean()),
-        "router_partials_and_barrier": float((ts[1:, 0] - ts[:-1, 3]).mean()),
+        "logits_topk_issue": float((ts[:, 1] - ts[:, 0]).mean()),
+        "stream_gate_up_down_partials": float((ts[:, 2] - ts[:, 1]).mean()),
+        "exchange_and_sum_partials": float((ts[:, 3] - ts[:, 2]).mean()),
+        "router_sums_and_next_inputs": float((ts[1:, 0] - ts[:-1, 3]).mean()),
     }
     err = layers[0].device_error()
     return dict(

@@ -77,7 +77,9 @@ enum { MOE_LAYOUT_PREFILL = 1, MOE_LAYOUT_DECODE = 2 };
 enum {
   MOE_DEVERR_WAIT_TIMEOUT = 1,   /* a pipeline wait passed its time limit    */
   MOE_DEVERR_NAN_LOGIT = 2,      /* a router logit was NaN (treated as -inf) */
-  MOE_DEVERR_GRID_TIMEOUT = 4    /* a grid-wide barrier passed its limit     */
+  MOE_DEVERR_GRID_TIMEOUT = 4,   /* a wait on another CTA passed its limit   */
+  MOE_DEVERR_RANGE = 8           /* a decode router partial sum was outside
+                                    +-2^20 (clamped; fixed-point range)     */
 };
 
 typedef struct moe_config {
@@ -175,11 +177,11 @@ typedef struct moe_decode_trace {
   float* w;        /* fp32 [L][k] */
   float* sigma;    /* fp32 [L], shared-expert gate */
   void* out;       /* bf16 [L][d], output of every layer */
-  int64_t* timestamps; /* int64 [L][4]: GPU clock (ns) in the first CTA at the
-                          start of a layer, after its weight copies are issued,
-                          once every CTA's gate/up and partial down projection
-                          is done (after the grid barrier), and once the layer
-                          output of the CTA's features is summed (profiling
+  int64_t* timestamps; /* int64 [L][4]: GPU clock (ns) in the first CTA once
+                          the layer's router sums and input are complete,
+                          after its weight copies are issued, once its
+                          partial down projections are written, and once the
+                          layer output of its features is summed (profiling
                           aid) */
 } moe_decode_trace;
 

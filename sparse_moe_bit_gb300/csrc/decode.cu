@@ -17,22 +17,33 @@
 // output projection, w_j * D_j[:, block] h_block, over all d output features
 // (the "partial" of the block).  So h never leaves the CTA; only the partials
 // are exchanged.  CTA c also owns the output features [c*d/G, (c+1)*d/G).
-// Two grid-wide barriers per layer:
-//   A : every CTA reads the previous output out_{l-1} and the router sums P_l
-//       in one pass, folds 1/rms(out_{l-1}) into the logits (the rest of the
-//       layer works on the unnormalised vector and scales its dot products),
-//       repeats the top-k selection in one warp and issues the bulk copies of
-//       its block's gate/up rows and down columns straight after it.
+//
+// There is no grid-wide barrier: every value one CTA hands to another carries
+// the proof of its own completeness in the same machine word, and the reader
+// polls the data itself (one L2 round trip after the last writer, where a
+// barrier followed by a read costs two):
+//   * a partial is a 64-bit word (fp32 value, 32-bit tag of launch and
+//     layer), stored and loaded as one single-copy-atomic access;
+//   * an output feature is a 32-bit word (bf16 value, 16-bit layer tag);
+//   * the router sums are 64-bit fixed-point integers (2^-32 units) added
+//     with atomics into one of several copies, each addend also adding 1 to
+//     an arrival count in the top 6 bits; a copy is complete when its count
+//     equals the number of CTAs that add into it.  Integer addition makes the
+//     sum exact and independent of the order of arrival.
+// One layer:
+//   A : poll the router sums P_l and the previous output out_{l-1}; fold
+//       1/rms(out_{l-1}) into the logits (the rest of the layer works on the
+//       unnormalised vector and scales its dot products); top-k over the
+//       whole CTA (rank within 32-expert chunks, then among the chunks'
+//       candidates); bulk copies of the block's gate/up rows (one per warp)
+//       and down columns.
 //   B : gate/up of the block (two features per warp), h of the block to
-//       16-bit integers, the block's partial over all d outputs -> global
-//       -> grid barrier
-//   R : out[f] = sum over blocks of the partials (fixed order) for the owned
-//       features, rounded to bf16; then the next layer's router partial sums
-//       over those features: P_{l+1}[e] += sum_f out[f] W_r'[e][f],
-//       accumulated as 64-bit fixed-point integers (2^-32 units) into one of
-//       several copies of P (so that fewer CTAs meet on one address); integer
-//       addition makes the sum exact and independent of the order of
-//       arrival -> grid barrier
+//       16-bit integers, the block's tagged partial over all d outputs.
+//   C : poll the partials of the owned features, out[f] = their sum in a
+//       fixed order, rounded to bf16 and published; the next layer's router
+//       sums over the owned features, P_{l+1}[e] += sum_f out[f] W_r'[e][f].
+// A CTA whose block belongs to the shared expert (known without routing)
+// issues the next layer's copies as soon as its buffers are free.
 // Dot products use the split s*q + beta per 64-group:
 //   sum_i (s q_i + beta) x_i = s sum_i q_i x_i + beta X,   X = sum_i x_i,
 // with sum_i q_i x_i an exact integer dot product (dp2a: two 16-bit inputs
@@ -58,11 +69,14 @@ constexpr int kUnitsPerWarp = kBlk / kDecWarps;  // gate/up features a warp comp
 static_assert(kUnitsPerWarp == 2, "gate/up takes two features per warp");
 constexpr int kMaxDecLayers = 64;
 constexpr int kPCopies = 8;  // copies of the router sums: CTA c adds into copy c % kPCopies
-constexpr int kPSlots = 3;   // layer l's sums live in slot l % kPSlots
+constexpr int kCountShift = 58;                      // arrival count: bits 58..63
+constexpr long long kPOffset = 1ll << 52;            // added to every addend (keeps it >= 0)
+constexpr long long kPMaxAbs = (1ll << 52) - 1;      // |addend| limit (2^20 in value)
+constexpr int kMaxPerCopy = 31;                      // 31 * 2^53 < 2^58: no carry into the count
 constexpr int kRedChunks = 32;  // partial sums per owned feature in the reduction
+constexpr int kPollMax = 8;     // partials in flight per thread in one polling pass
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
-constexpr float kFix = 4294967296.0f;  // 2^32
 
 struct DecLayer {
   const uint8_t* gu;     // [n_exp][I] units of d + d/8 bytes (gate, up codes; their s,b)
@@ -76,6 +90,7 @@ struct DecParams {
   int L, d, E, k, I, has_shared, Ep;
   int nf_max;  // output features per CTA (max)
   int NB;      // blocks per layer: (k+1 or k) * I / 32
+  unsigned epoch;  // launch number: part of the partials' tags
   const uint16_t* x;
   int norm_first;  // 1: x is an earlier layer's output (normalise it first)
   const float* bias;  // [L][E] or null
@@ -87,18 +102,17 @@ struct DecParams {
   float* tr_w;          // [L][k] or null
   uint16_t* tr_out;     // [L][d] or null
   int64_t* tr_ns;       // [L][4] or null
-  float* part;          // [NB][d] the blocks' weighted partial outputs
-  uint16_t* out;        // [2][d]: layer l writes row l % 2
-  unsigned long long* P;  // [kPSlots][kPCopies][E+1] fixed-point router sums, zero at launch
-  unsigned* bar;        // grid barrier arrivals, zero at launch
+  unsigned long long* part;  // [NB][d] tagged partial outputs of the blocks
+  uint32_t* out;        // [2][d] tagged outputs: layer l writes row l % 2; zero at launch
+  unsigned long long* P;  // [L][kPCopies][E+1] counted fixed-point router sums, zero at launch
   int* abort_flag;      // zero at launch
   int* err;
 };
 
 // shared-memory carve-up (the host sizes the launch with the same function)
 struct DecSmem {
-  size_t xq, xsc, xg, gu, dnc, dnsb, hb, hpk, rt, outs, red2, lg, lb, sel_e, sel_w, misc, red,
-      infl, bars, ok, total;
+  size_t xq, xsc, xg, gu, dnc, dnsb, hb, hpk, rt, outs, red2, lg, lb, keys, cand, sel_e, sel_w,
+      misc, red, infl, bars, total;
 };
 __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align) {
   o = (o + align - 1) / align * align;
@@ -109,6 +123,7 @@ __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align
 __host__ __device__ inline DecSmem dec_smem(int d, int E, int Ep, int nf_max) {
   DecSmem s;
   size_t o = 0;
+  const int nch = (E + 31) / 32;
   s.xq = dec_take(o, (size_t)d * 2, 16);
   s.xsc = dec_take(o, (size_t)(d / 64) * 4, 16);
   s.xg = dec_take(o, (size_t)(d / 64) * 4, 16);
@@ -122,13 +137,14 @@ __host__ __device__ inline DecSmem dec_smem(int d, int E, int Ep, int nf_max) {
   s.red2 = dec_take(o, (size_t)kRedChunks * 16 * 4, 16);
   s.lg = dec_take(o, (size_t)(E + 1) * 4, 16);
   s.lb = dec_take(o, (size_t)E * 4, 16);
+  s.keys = dec_take(o, (size_t)nch * 32 * 8, 16);
+  s.cand = dec_take(o, (size_t)nch * kMaxK * 8, 16);
   s.sel_e = dec_take(o, kMaxK * 4, 16);
   s.sel_w = dec_take(o, kMaxK * 4, 16);
   s.misc = dec_take(o, 16, 16);
   s.red = dec_take(o, kDecWarps * 4, 16);
   s.infl = dec_take(o, (kDecWarps + 2) * 4, 16);
-  s.bars = dec_take(o, (kDecWarps + 3) * 8, 8);
-  s.ok = dec_take(o, 16, 16);
+  s.bars = dec_take(o, (kDecWarps + 2) * 8, 8);
   s.total = o;
   return s;
 }
@@ -206,94 +222,105 @@ __device__ __forceinline__ int dot8i(uint32_t w, uint4 v, int acc) {
 }
 
 
-// Top-k of lg[0..E) in one warp, ranked by (value descending, index
-// ascending), NaN taken as -inf.  Lane l holds the experts l, l+32, ... as
-// 64-bit keys (order key << 32 | ~index), sorts them (bitonic network) and
-// then each round needs only the head of every lane: the warp maximum of the
-// high words, then of the low words among the lanes that hold it, names the
-// winner, whose lane drops its head.  sel_e[r] = the r-th choice (lane 0
-// writes it).
-template <int VPL>
-__device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int lane, int* sel_e,
-                                          bool* nan_seen) {
-  unsigned long long K[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    unsigned long long key = 0ull;  // empty; every real key is larger
-    if (e < E) {
-      float v = lg[e];
-      if (v != v) {
-        v = -INFINITY;
-        *nan_seen = true;
-      }
-      key = ((unsigned long long)ord_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
-    }
-    K[j] = key;
-  }
-#pragma unroll
-  for (int size = 2; size <= VPL; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const unsigned long long a = K[i], b = K[j];
-          const bool sw = desc ? (a < b) : (a > b);
-          K[i] = sw ? b : a;
-          K[j] = sw ? a : b;
-        }
-      }
-    }
-  }
-  for (int r = 0; r < k; ++r) {
-    const uint32_t hi = (uint32_t)(K[0] >> 32), lo = (uint32_t)K[0];
-    const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
-    const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
-    if (hi == mh && lo == ml) {
-#pragma unroll
-      for (int j = 0; j + 1 < VPL; ++j) K[j] = K[j + 1];
-      K[VPL - 1] = 0ull;
-    }
-    if (lane == 0) sel_e[r] = (int)(0xFFFFFFFFu - ml);
-  }
+// Single-copy-atomic accesses of another CTA's data at GPU scope (the L1
+// cache is not used, so a poll sees the latest value in L2).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a));
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+// four 32-bit words, each read atomically on its own
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t* a) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(a));
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* a, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_u64(unsigned long long* a, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
 }
 
-// Grid-wide barrier number n (0-based): arrivals are counted monotonically, so
-// barrier n completes at (n + 1) * gridDim.x.  The arrival is a release and
-// the poll an acquire at GPU scope, which orders every CTA's writes before the
-// barrier (its threads meet at __syncthreads first) with every read after it.
-// Bounded: on time-out (or when another CTA gave up) every CTA leaves.
-__device__ bool grid_sync(const DecParams& p, unsigned n, int* s_ok) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p.bar), "r"(1u) : "memory");
-    const unsigned target = (n + 1) * gridDim.x;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 0;; ++i) {
-      unsigned v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.bar) : "memory");
-      if (v >= target) break;
-      if ((i & 15u) == 15u) {
-        if (*(volatile int*)p.abort_flag) {
-          ok = 0;
-          break;
-        }
-        if (globaltimer_ns() - t0 > kWaitNs) {
-          atomicOr(p.err, MOE_DEVERR_GRID_TIMEOUT);
-          atomicExch(p.abort_flag, 1);
-          ok = 0;
-          break;
-        }
-      }
+// Pacing of a poll on another CTA's data: a short sleep per round; gives up
+// (true) when another CTA gave up or, recording the error, after kWaitNs.
+__device__ __forceinline__ bool poll_give_up(const DecParams& p, uint64_t& t0, uint32_t& n) {
+  ++n;
+  if ((n & 15u) == 1u) {
+    if (*(volatile int*)p.abort_flag) return true;
+    const uint64_t t = globaltimer_ns();
+    if (n == 1u) {
+      t0 = t;
+    } else if (t - t0 > kWaitNs) {
+      atomicOr(p.err, MOE_DEVERR_GRID_TIMEOUT);
+      atomicExch(p.abort_flag, 1);
+      return true;
     }
-    *s_ok = ok;
+  }
+  __nanosleep(20);
+  return false;
+}
+
+// Top-k over the whole CTA, ranked by (value descending, index ascending).
+// keys[e] (e < 32 * chunks) = order key of expert e's logit << 32 | ~e, 0
+// past E: distinct, larger is better; cand[] zero; both written by the
+// caller before a barrier.  An expert's rank within its chunk of 32 makes
+// the chunk's k best candidates (an expert of the overall top k has fewer
+// than k better experts anywhere, so also in its chunk); a candidate's rank
+// among all candidates is then its overall rank: sel_e[rank] for rank < k.
+// Two threads count for a key (16 comparisons each), and 512 / (candidates)
+// threads, a power of two, for a candidate.
+__device__ __forceinline__ void cta_topk(const unsigned long long* keys, unsigned long long* cand,
+                                         int E, int k, int* sel_e, int tid) {
+  const int nch = (E + 31) >> 5, nc = nch * k;
+  // whole warps in every pass (the shuffles); keys past E are 0
+  for (int t = tid; t < 64 * nch; t += kDecThreads) {
+    const int e = t >> 1, h = t & 1;
+    const unsigned long long my = keys[e];
+    const unsigned long long* kc = keys + (e & ~31) + 16 * h;
+    int rank = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) rank += (kc[i] > my) ? 1 : 0;
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    if (h == 0 && e < E && rank < k) cand[(e >> 5) * k + rank] = my;
   }
   __syncthreads();
-  return *s_ok != 0;
+  int tpc = 32;  // threads per candidate
+  while (tpc > 1 && tpc * nc > kDecThreads) tpc >>= 1;
+  const int tot = (nc * tpc + 31) & ~31;
+  for (int t = tid; t < tot; t += kDecThreads) {
+    const int ci = t / tpc, part = t % tpc;
+    const unsigned long long my = (ci < nc) ? cand[ci] : 0ull;
+    int rank = 0;
+    if (ci < nc)
+      for (int j = part; j < nc; j += tpc) rank += (cand[j] > my) ? 1 : 0;
+    for (int o = 1; o < tpc; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (part == 0 && my != 0ull && rank < k) sel_e[rank] = (int)(0xFFFFFFFFu - (uint32_t)my);
+  }
+  __syncthreads();
+}
+
+// round(v * 2^32) as a 64-bit integer for |v| < 2^20, from 32-bit
+// conversions (the 64-bit ones are slow): x = v 2^32 is exact; its high part
+// floor(x / 2^24) and the remainder x - hi 2^24 (in [0, 2^24), exact) convert
+// exactly, the remainder rounded to nearest even.
+__device__ __forceinline__ long long fix32(float v) {
+  const float x = v * 4294967296.0f;
+  const float hi = floorf(x * 5.9604644775390625e-8f);  // 2^-24
+  const float rem = fmaf(-hi, 16777216.0f, x);
+  return (long long)__float2int_rn(hi) * 16777216ll + (long long)__float2int_rn(rem);
+}
+// a 64-bit integer s (|s| < 2^62) times 2^-32 in fp32: the sum of its two
+// 32-bit halves, each converted exactly or within half an ulp
+__device__ __forceinline__ float unfix32(long long s) {
+  const int hi = (int)(s >> 32);
+  const unsigned lo = (unsigned)(s & 0xFFFFFFFFll);
+  return fmaf((float)lo, 2.3283064365386963e-10f, (float)hi);  // lo 2^-32 + hi
 }
 
 // Bounded wait on an mbarrier phase; the thread sleeps in hardware between
@@ -324,6 +351,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int ng = d / 64;
   const int NB = p.NB;
   const int bpe = I / kBlk;  // blocks per expert
+  const int nch = (E + 31) >> 5;
   const DecSmem L = dec_smem(d, E, Ep, p.nf_max);
   uint4* xq = reinterpret_cast<uint4*>(dsm + L.xq);   // [8 words][ng] packed int16 x
   float* xsc = reinterpret_cast<float*>(dsm + L.xsc);  // [ng] scale of a group of x
@@ -336,8 +364,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint16_t* rt_buf = reinterpret_cast<const uint16_t*>(dsm + L.rt);
   float* outs = reinterpret_cast<float*>(dsm + L.outs);
   float* red2 = reinterpret_cast<float*>(dsm + L.red2);  // [chunks][16] reduction partials
-  float* lg = reinterpret_cast<float*>(dsm + L.lg);  // raw sums, then logits; [E]: shared gate
-  float* lb = reinterpret_cast<float*>(dsm + L.lb);  // logit bias
+  float* lg = reinterpret_cast<float*>(dsm + L.lg);      // logits
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(dsm + L.keys);
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(dsm + L.cand);
   int* sel_e = reinterpret_cast<int*>(dsm + L.sel_e);
   float* sel_w = reinterpret_cast<float*>(dsm + L.sel_w);
   float* misc = reinterpret_cast<float*>(dsm + L.misc);  // [0] sigma [1] 1/rms [2] h scale [3] h sum
@@ -346,11 +375,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // bounded drain on the error path
   volatile int* infl = reinterpret_cast<volatile int*>(dsm + L.infl);
   const uint32_t bar0 = smem_u32(dsm + L.bars);  // [warps] gate/up, then down, router
-  int* s_ok = reinterpret_cast<int*>(dsm + L.ok);
   const int kDnBar = kDecWarps, kRtBar = kDecWarps + 1;
   const uint32_t dn_bar = bar0 + 8 * kDnBar;
   const uint32_t rt_bar = bar0 + 8 * kRtBar;
-  const uint32_t route_bar = bar0 + 8 * (kDecWarps + 2);  // the top-k of the layer is known
   const int wwarp = kDecWarps - 1;  // computes the routing weights
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -360,13 +387,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int gu_unit = d + d / 8;
 
   if (tid == 0) {
-    for (int i = 0; i < kDecWarps + 3; ++i) mbar_init(bar0 + 8 * i, 1);
+    for (int i = 0; i < kDecWarps + 2; ++i) mbar_init(bar0 + 8 * i, 1);
     fence_mbar_init();
   }
   if (tid < kDecWarps + 2) infl[tid] = -1;
   __syncthreads();
-  uint32_t ph_gu = 0, ph_dn = 0, ph_rt = 0, ph_route = 0;
-  unsigned nsync = 0;
+  uint32_t ph_gu = 0, ph_dn = 0, ph_rt = 0;
+  bool pre = false;  // the CTA's first block of this layer was issued during the last one
 
   // Error path: wait, with a bound, for this CTA's bulk copies still in
   // flight, so that none lands in shared memory after the CTA has left.
@@ -383,28 +410,29 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   };
 
   // Block b: expert slot j = b / bpe (slot k: the shared expert), features
-  // (b % bpe) * 32 .. + 31.  Issue its bulk copies: lane i < 16 the gate/up
-  // rows of warp i's two features, lane 16 the block's down columns (codes
-  // of every output row, then the rows' scale/bias words of its input
-  // group).  Called by every lane of one warp.
-  auto issue_block = [&](int b, const DecLayer& W) {
+  // (b % bpe) * 32 .. + 31.  issue_gu (lane 0 of each warp): the gate/up rows
+  // of the warp's two features; issue_dn (one thread): the block's down
+  // columns (codes of every output row, then the rows' scale/bias words of
+  // its input group).
+  auto issue_gu = [&](int b, const DecLayer& W) {
     const int j = b / bpe, i0 = (b - j * bpe) * kBlk;
     const long long ex = (j < k) ? sel_e[j] : E;
-    if (lane < kDecWarps) {
-      const uint32_t bar = bar0 + 8 * lane;
-      const uint32_t bytes = (uint32_t)(kUnitsPerWarp * gu_unit);
-      infl[lane] = (int)ph_gu;
-      mbar_arrive_expect_tx(bar, bytes);
-      bulk_g2s(smem_u32(gu_buf + (size_t)lane * kUnitsPerWarp * gu_unit),
-               W.gu + (ex * I + i0 + lane * kUnitsPerWarp) * gu_unit, bytes, bar);
-    } else if (lane == kDecWarps) {
-      infl[kDnBar] = (int)ph_dn;
-      mbar_arrive_expect_tx(dn_bar, (uint32_t)(d * 20));
-      bulk_g2s(smem_u32(dsm + L.dnc), W.dnc + (ex * bpe + i0 / kBlk) * (long long)d * 16,
-               (uint32_t)(d * 16), dn_bar);
-      bulk_g2s(smem_u32(dsm + L.dnsb), W.dnsb + (ex * (I / 64) + i0 / 64) * (long long)d,
-               (uint32_t)(d * 4), dn_bar);
-    }
+    const uint32_t bar = bar0 + 8 * warp;
+    const uint32_t bytes = (uint32_t)(kUnitsPerWarp * gu_unit);
+    infl[warp] = (int)ph_gu;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_u32(gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit),
+             W.gu + (ex * I + i0 + warp * kUnitsPerWarp) * gu_unit, bytes, bar);
+  };
+  auto issue_dn = [&](int b, const DecLayer& W) {
+    const int j = b / bpe, i0 = (b - j * bpe) * kBlk;
+    const long long ex = (j < k) ? sel_e[j] : E;
+    infl[kDnBar] = (int)ph_dn;
+    mbar_arrive_expect_tx(dn_bar, (uint32_t)(d * 20));
+    bulk_g2s(smem_u32(dsm + L.dnc), W.dnc + (ex * bpe + i0 / kBlk) * (long long)d * 16,
+             (uint32_t)(d * 16), dn_bar);
+    bulk_g2s(smem_u32(dsm + L.dnsb), W.dnsb + (ex * (I / 64) + i0 / 64) * (long long)d,
+             (uint32_t)(d * 4), dn_bar);
   };
 
   // Four consecutive activations v0..v3 at index i0 (a multiple of 4; the 16
@@ -446,7 +474,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (norm) {
       float ss = 0.f;
       for (int i = tid; i < d; i += kDecThreads) {
-        const float v = bf16f(__ldcg(src + i));
+        const float v = bf16f(__ldg(src + i));
         ss += v * v;
       }
       ss = warp_sum(ss);
@@ -464,7 +492,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int i0 = ib + 4 * tid;
       const bool act = i0 < d;
       uint2 raw = make_uint2(0u, 0u);
-      if (act) raw = __ldcg(reinterpret_cast<const uint2*>(src + i0));
+      if (act) raw = __ldg(reinterpret_cast<const uint2*>(src + i0));
       const float v[4] = {bf16f(raw.x & 0xFFFFu) * r, bf16f(raw.x >> 16) * r,
                           bf16f(raw.y & 0xFFFFu) * r, bf16f(raw.y >> 16) * r};
       quant_x4(v[0], v[1], v[2], v[3], i0, act);
@@ -477,20 +505,61 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
   };
 
-  // P_slot[copy c % kPCopies][e] += sum_{f owned} outs[f] * W'[e][f]
-  // (e = E: the shared gate)
-  auto router_partial = [&](int slot) {
+  // Router sums of layer ln over the owned features, added into copy
+  // c % kPCopies of P_ln with one arrival each: P[e] += 2^58 + 2^52 +
+  // round(2^32 sum_{f owned} outs[f] W'[e][f]) (e = E: the shared gate).
+  // Every CTA adds to every entry (zero without owned features), so that the
+  // counts reach their known totals.
+  auto router_partial = [&](int ln) {
     unsigned long long* Pq =
-        p.P + ((long long)slot * kPCopies + (c % kPCopies)) * (long long)(E + 1);
+        p.P + ((long long)ln * kPCopies + (c % kPCopies)) * (long long)(E + 1);
+    bool range_err = false;
     for (int e = tid; e <= E; e += kDecThreads) {
       float acc = 0.f;
       for (int f = 0; f < nf; ++f) acc = fmaf(outs[f], bf16f(rt_buf[f * Ep + e]), acc);
-      atomicAdd(Pq + e, (unsigned long long)__float2ll_rn(acc * kFix));
+      long long v;
+      if (fabsf(acc) < 1048575.0f) {
+        v = fix32(acc);
+      } else {  // outside the fixed-point range (or NaN): clamped, error bit
+        v = (acc > 0.0f) ? kPMaxAbs : -kPMaxAbs;
+        range_err = true;
+      }
+      red_add_u64(Pq + e, (1ull << kCountShift) + (unsigned long long)(v + kPOffset));
     }
+    if (range_err) atomicOr(p.err, MOE_DEVERR_RANGE);
+  };
+
+  // The router sum of entry e of P_ln, once every copy's count is complete.
+  auto poll_P = [&](const unsigned long long* Ps, int e, long long& sum) -> bool {
+    unsigned long long w[kPCopies];
+#pragma unroll
+    for (int q = 0; q < kPCopies; ++q) w[q] = ld_relaxed_u64(Ps + q * (E + 1) + e);
+    uint64_t t0 = 0;
+    uint32_t n = 0;
+    for (;;) {
+      unsigned pend = 0;
+#pragma unroll
+      for (int q = 0; q < kPCopies; ++q) {
+        const unsigned want = (G > q) ? (unsigned)((G - q + kPCopies - 1) / kPCopies) : 0u;
+        if ((unsigned)(w[q] >> kCountShift) != want) pend |= 1u << q;
+      }
+      if (!pend) break;
+      if (poll_give_up(p, t0, n)) return false;
+#pragma unroll
+      for (int q = 0; q < kPCopies; ++q)
+        if ((pend >> q) & 1u) w[q] = ld_relaxed_u64(Ps + q * (E + 1) + e);
+    }
+    sum = 0;
+#pragma unroll
+    for (int q = 0; q < kPCopies; ++q) {
+      const long long cnt = (long long)(w[q] >> kCountShift);
+      sum += (long long)(w[q] & ((1ull << kCountShift) - 1ull)) - cnt * kPOffset;
+    }
+    return true;
   };
 
   auto issue_router_copy = [&](int l) {
-    if (tid == 32 && nf > 0) {  // lane 0 of warp 1
+    if (tid == 2 && nf > 0) {
       const uint32_t bytes = (uint32_t)nf * Ep * 2;
       infl[kRtBar] = (int)ph_rt;
       mbar_arrive_expect_tx(rt_bar, bytes);
@@ -498,7 +567,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   };
 
-  // ---- prologue: x_0 and the router sums of layer 0 (slot 0)
+  // ---- prologue: x_0 and the router sums of layer 0
   issue_router_copy(0);
   load_x(p.x, p.norm_first != 0);
   if (nf > 0) {
@@ -506,40 +575,44 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       drain();
       return;
     }
-    if (tid == 0) infl[kRtBar] = -1;
+    if (tid == 2) infl[kRtBar] = -1;
   }
   ph_rt ^= 1;
-  if (nf > 0) router_partial(0);
-  if (!grid_sync(p, nsync++, s_ok)) {
-    drain();
-    return;
-  }
+  router_partial(0);
 
   for (int l = 0; l < p.L; ++l) {
     const DecLayer& W = p.layer[l];
-    stamp(p, l, 0);
-    // ---- A: out_{l-1} and P_l in one pass; routing in warp 0; copies
-    if (l + 1 < p.L) issue_router_copy(l + 1);
-    // every load of this step is issued before any of them is used: the
-    // router sums (expert e = tid), its bias, then the previous output
-    const unsigned long long* Ps = p.P + (long long)(l % kPSlots) * kPCopies * (E + 1);
-    unsigned long long pv[kPCopies];
-    float be = 0.0f;
-    if (tid <= E) {
-#pragma unroll
-      for (int q = 0; q < kPCopies; ++q) pv[q] = __ldcg(Ps + q * (E + 1) + tid);
-      if (tid < E && p.bias) be = __ldg(p.bias + (long long)l * E + tid);
-    }
+    const uint32_t ptag = ((p.epoch << 6) | (uint32_t)l) | 0x80000000u;  // partials of layer l
+    // ---- A: the router sums P_l (entry e = tid, and E when E = kDecThreads)
+    //      and the previous output, polled in one pass
+    bool bad = false;
+    const unsigned long long* Ps = p.P + (long long)l * kPCopies * (E + 1);
+    long long ps0 = 0, ps1 = 0;
+    if (tid <= E && !poll_P(Ps, tid, ps0)) bad = true;
+    if (tid + kDecThreads <= E && !poll_P(Ps, tid + kDecThreads, ps1)) bad = true;
     if (l > 0) {
-      const uint16_t* src = p.out + (long long)((l - 1) & 1) * d;
+      const uint32_t* src = p.out + (long long)((l - 1) & 1) * d;
+      const uint32_t want = (uint32_t)l;  // tag of layer l-1
       float ss = 0.f;
       for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
         const int i0 = ib + 4 * tid;
         const bool act = i0 < d;
-        uint2 raw = make_uint2(0u, 0u);
-        if (act) raw = __ldcg(reinterpret_cast<const uint2*>(src + i0));
-        const float v0 = bf16f(raw.x & 0xFFFFu), v1 = bf16f(raw.x >> 16);
-        const float v2 = bf16f(raw.y & 0xFFFFu), v3 = bf16f(raw.y >> 16);
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (act && !bad) {
+          raw = ld_relaxed_v4(src + i0);
+          uint64_t t0 = 0;
+          uint32_t n = 0;
+          while ((raw.x >> 16) != want || (raw.y >> 16) != want || (raw.z >> 16) != want ||
+                 (raw.w >> 16) != want) {
+            if (poll_give_up(p, t0, n)) {
+              bad = true;
+              break;
+            }
+            raw = ld_relaxed_v4(src + i0);
+          }
+        }
+        const float v0 = bf16f(raw.x & 0xFFFFu), v1 = bf16f(raw.y & 0xFFFFu);
+        const float v2 = bf16f(raw.z & 0xFFFFu), v3 = bf16f(raw.w & 0xFFFFu);
         ss = fmaf(v0, v0, ss);
         ss = fmaf(v1, v1, ss);
         ss = fmaf(v2, v2, ss);
@@ -549,28 +622,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
     }
-    {
-      if (tid <= E) {
-        long long sum = 0;
-#pragma unroll
-        for (int q = 0; q < kPCopies; ++q) sum += (long long)pv[q];
-        lg[tid] = __ll2float_rn(sum) * (1.0f / 4294967296.0f);
-        if (tid < E) lb[tid] = be;
-      }
-      for (int e = tid + kDecThreads; e <= E; e += kDecThreads) {  // E = 512 only
-        long long sum = 0;
-#pragma unroll
-        for (int q = 0; q < kPCopies; ++q) sum += (long long)__ldcg(Ps + q * (E + 1) + e);
-        lg[e] = __ll2float_rn(sum) * (1.0f / 4294967296.0f);
-        if (e < E) lb[e] = p.bias ? p.bias[(long long)l * E + e] : 0.0f;
-      }
-      if (c == 0) {  // the slot of layer l-1 is free (read before the last barrier)
-        unsigned long long* Pz =
-            p.P + (long long)((l + kPSlots - 1) % kPSlots) * kPCopies * (E + 1);
-        for (int i = tid; i < kPCopies * (E + 1); i += kDecThreads) Pz[i] = 0ull;
-      }
+    if (__syncthreads_or(bad)) {
+      drain();
+      return;
     }
-    __syncthreads();
+    if (l + 1 < p.L) issue_router_copy(l + 1);  // the router buffer is no longer read
+    stamp(p, l, 0);
     float r = 1.0f;  // 1/rms of out_{l-1} (x_0 is normalised already)
     if (l > 0) {
       float t = 0.f;
@@ -578,38 +635,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       for (int w = 0; w < kDecWarps; ++w) t += red[w];
       r = rsqrtf(t / (float)d + p.eps);
     }
-    if (warp == 0) {
-      for (int e = lane; e <= E; e += 32) {
-        float v = lg[e] * r;
-        if (e < E) {
-          v += lb[e];
-          lg[e] = v;
-          if (c == 0) p.logits[(long long)l * E + e] = v;
-        } else {
-          const float sg = p.has_shared ? 1.0f / (1.0f + expf(-v)) : 0.0f;
-          misc[0] = sg;
-          if (c == 0) p.sigma[l] = sg;
+    // logits, the shared gate, and the top-k keys
+    bool nan_seen = false;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = tid + i * kDecThreads;
+      if (e > E) continue;
+      float v = unfix32(i == 0 ? ps0 : ps1) * r;
+      if (e < E) {
+        if (p.bias) v += __ldg(p.bias + (long long)l * E + e);
+        lg[e] = v;
+        if (c == 0) p.logits[(long long)l * E + e] = v;
+        if (v != v) {
+          v = -INFINITY;
+          nan_seen = true;
         }
+        keys[e] = ((unsigned long long)ord_key(v) << 32) |
+                  (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+      } else {
+        const float sg = p.has_shared ? 1.0f / (1.0f + expf(-v)) : 0.0f;
+        misc[0] = sg;
+        if (c == 0) p.sigma[l] = sg;
       }
-      __syncwarp();
-      bool nan_seen = false;
-      if (E <= 256) warp_topk<8>(lg, E, k, lane, sel_e, &nan_seen);
-      else warp_topk<kMaxE / 32>(lg, E, k, lane, sel_e, &nan_seen);
-      if (__any_sync(0xffffffffu, nan_seen) && lane == 0 && c == 0)
-        atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
-      __syncwarp();
-      if (c < NB) issue_block(c, W);
-      if (lane == kDecWarps + 1) mbar_arrive(route_bar);  // sel_e and the logits are ready
-      stamp(p, l, 1);
     }
+    for (int e = E + tid; e < nch * 32; e += kDecThreads) keys[e] = 0ull;
+    for (int i = tid; i < nch * k; i += kDecThreads) cand[i] = 0ull;
+    if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
+    cta_topk(keys, cand, E, k, sel_e, tid);
+    if (c < NB && !pre) {
+      if (lane == 0) issue_gu(c, W);
+      if (tid == 1) issue_dn(c, W);
+    }
+    pre = false;
+    stamp(p, l, 1);
     if (warp == wwarp) {
       // routing weights (softmax over the k chosen logits in double-float
       // arithmetic, within one ulp of fp64), off the path of the copies and
       // of the other warps' gate/up work
-      if (!copy_wait(p, route_bar, ph_route)) {
-        drain();
-        return;
-      }
       const int my_e = (lane < k) ? sel_e[lane] : 0;
       float my_v = (lane < k) ? lg[my_e] : -INFINITY;
       if (my_v != my_v) my_v = -INFINITY;
@@ -632,14 +694,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
     }
-    ph_route ^= 1;
 
-    // ---- B: the CTA's blocks: gate/up, h, and the block's partial output
+    // ---- B: the CTA's blocks: gate/up, h, and the block's tagged partial
     for (int b = c, nb = 0; b < NB; b += G, ++nb) {
       const int j = b / bpe;
       if (nb > 0) {
         __syncthreads();  // the previous block's buffers are no longer read
-        if (warp == 0) issue_block(b, W);
+        if (lane == 0) issue_gu(b, W);
+        if (tid == 1) issue_dn(b, W);
       }
       // gate/up: warp -> features 2*warp, 2*warp + 1 of the block; lane: one
       // group of 64 inputs at a time, its activations in registers for both
@@ -719,51 +781,88 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         drain();
         return;
       }
-      if (tid == 0) infl[kDnBar] = -1;
+      if (tid == 1) infl[kDnBar] = -1;
       ph_dn ^= 1;
       __syncthreads();
-      // the block's partial output: part[b][f] = w_j (s sum_i q_i h_i + beta H)
+      // the block's partial output: part[b][f] = w_j (s sum_i q_i h_i + beta H),
+      // published with the layer's tag
       {
         const uint4 h0 = hpk[0], h1 = hpk[1], h2 = hpk[2], h3 = hpk[3];
         const float hsc = misc[2], Hs = misc[3];
         const float wj = (j < k) ? sel_w[j] : misc[0];
-        float* pb = p.part + (long long)b * d;
+        unsigned long long* pb = p.part + (long long)b * d;
+        const unsigned long long tg = (unsigned long long)ptag << 32;
         for (int f = tid; f < d; f += kDecThreads) {
           const uint4 cw = dnc[f];
           const uint32_t sb = dnsb[f];
           const int a = (dot8i(cw.x, h0, 0) + dot8i(cw.y, h1, 0)) +
                         (dot8i(cw.z, h2, 0) + dot8i(cw.w, h3, 0));
-          pb[f] = wj * (s_of(sb) * (hsc * (float)a) + b_of(sb) * Hs);
+          const float v = wj * (s_of(sb) * (hsc * (float)a) + b_of(sb) * Hs);
+          st_relaxed_u64(pb + f, tg | __float_as_uint(v));
         }
       }
     }
-
-    // ---- every block's partial is in global memory
-    if (!grid_sync(p, nsync++, s_ok)) {
-      drain();
-      return;
+    // The next layer's first block of this CTA belongs to the shared expert:
+    // its weights do not depend on the routing, so they load now.
+    if (l + 1 < p.L && p.has_shared && c < NB && c / bpe == k) {
+      __syncthreads();  // this layer's buffers are no longer read
+      if (lane == 0) issue_gu(c, p.layer[l + 1]);
+      if (tid == 1) issue_dn(c, p.layer[l + 1]);
+      pre = true;
     }
     stamp(p, l, 2);
-    // ---- R: out[f] = sum over blocks of part[b][f] (fixed order), bf16
+
+    // ---- C: out[f] = sum over blocks of part[b][f] (fixed order), bf16,
+    //      published with the layer's tag
     {
-      uint16_t* outl = p.out + (long long)(l & 1) * d;
+      uint32_t* outl = p.out + (long long)(l & 1) * d;
+      const uint32_t otag = (uint32_t)(l + 1) << 16;
       for (int fl0 = 0; fl0 < nf; fl0 += 16) {
         const int fl = fl0 + (tid & 15), ch = tid >> 4;  // 32 chunks of blocks
         float s = 0.f;
         if (fl < nf) {
-          const float* pf = p.part + f0 + fl;
-#pragma unroll 4
-          for (int b = ch; b < NB; b += kRedChunks) s += __ldcg(pf + (long long)b * d);
+          const unsigned long long* pf = p.part + f0 + fl;
+          for (int bp = ch; bp < NB && !bad; bp += kRedChunks * kPollMax) {
+            unsigned long long v[kPollMax];
+#pragma unroll
+            for (int i = 0; i < kPollMax; ++i) {
+              const int b = bp + i * kRedChunks;
+              v[i] = (b < NB) ? ld_relaxed_u64(pf + (long long)b * d)
+                              : ((unsigned long long)ptag << 32);
+            }
+            uint64_t t0 = 0;
+            uint32_t n = 0;
+            for (;;) {
+              unsigned pend = 0;
+#pragma unroll
+              for (int i = 0; i < kPollMax; ++i)
+                if ((uint32_t)(v[i] >> 32) != ptag) pend |= 1u << i;
+              if (!pend) break;
+              if (poll_give_up(p, t0, n)) {
+                bad = true;
+                break;
+              }
+#pragma unroll
+              for (int i = 0; i < kPollMax; ++i)
+                if ((pend >> i) & 1u) v[i] = ld_relaxed_u64(pf + (long long)(bp + i * kRedChunks) * d);
+            }
+#pragma unroll
+            for (int i = 0; i < kPollMax; ++i)
+              if (bp + i * kRedChunks < NB) s += __uint_as_float((uint32_t)v[i]);
+          }
         }
         red2[ch * 16 + (tid & 15)] = s;
-        __syncthreads();
+        if (__syncthreads_or(bad)) {
+          drain();
+          return;
+        }
         if (tid < 16 && fl0 + tid < nf) {
           float o = 0.f;
           for (int q = 0; q < kRedChunks; ++q) o += red2[q * 16 + tid];
           const uint16_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(o));
           const int f = f0 + fl0 + tid;
           outs[fl0 + tid] = bf16f(ob);
-          outl[f] = ob;
+          st_relaxed_u32(outl + f, otag | ob);
           if (p.tr_out) p.tr_out[(long long)l * d + f] = ob;
           if (l == p.L - 1) p.y[f] = ob;
         }
@@ -777,14 +876,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           drain();
           return;
         }
-        if (tid == 0) infl[kRtBar] = -1;
+        if (tid == 2) infl[kRtBar] = -1;
       }
       ph_rt ^= 1;
-      if (nf > 0) router_partial((l + 1) % kPSlots);
-      if (!grid_sync(p, nsync++, s_ok)) {
-        drain();
-        return;
-      }
+      router_partial(l + 1);
     }
   }
 }
@@ -795,17 +890,19 @@ size_t decode_scratch_bytes(const Handle* h, int L) {
   const moe_config& c = h->cfg;
   const int k1 = c.k + (c.has_shared ? 1 : 0);
   const size_t NB = (size_t)k1 * c.I / kBlk;
-  return 256 + (size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 256 + NB * c.d * 4 + 256 +
-         (size_t)L * c.E * 4 + (size_t)L * 4 + 256 + (size_t)2 * c.d * 2 + 2048;
+  auto r256 = [](size_t b) { return (b + 255) / 256 * 256; };
+  return 256 + r256((size_t)2 * c.d * 4) + r256((size_t)L * kPCopies * (c.E + 1) * 8) +
+         r256(NB * c.d * 8) + r256((size_t)L * c.E * 4) + r256((size_t)L * 4) + 256;
 }
 
 cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const float* bias,
                           float eps, uint16_t* y, const moe_decode_trace* trace,
                           cudaStream_t st) {
-  const Handle* h0 = layers[0];
+  Handle* h0 = layers[0];
   const moe_config& c = h0->cfg;
   const int k1 = c.k + (c.has_shared ? 1 : 0);
   const int G = h0->num_sms;
+  if ((G + kPCopies - 1) / kPCopies > kMaxPerCopy) return cudaErrorInvalidConfiguration;
   const int nf_max = (c.d + G - 1) / G;
   const int NB = k1 * c.I / kBlk;
   const int Ep = decode_router_pitch(c.E);
@@ -820,23 +917,23 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  // scratch: [barrier, abort | P] (zeroed before every launch) | partials | logits | sigma | out
-  uint8_t* q = scr;
-  unsigned* bar = reinterpret_cast<unsigned*>(q);
-  int* abort_flag = reinterpret_cast<int*>(q + 4);
-  q += 256;
-  unsigned long long* P = reinterpret_cast<unsigned long long*>(q);
-  q += ((size_t)kPSlots * kPCopies * (c.E + 1) * 8 + 255) / 256 * 256;
-  const size_t zero_bytes = (size_t)(q - scr);
-  float* part = reinterpret_cast<float*>(q);
-  q += ((size_t)NB * c.d * 4 + 255) / 256 * 256;
-  float* logits_s = reinterpret_cast<float*>(q);
-  q += (size_t)kMaxDecLayers * c.E * 4;
-  float* sigma_s = reinterpret_cast<float*>(q);
-  q += (size_t)kMaxDecLayers * 4 + 256;
-  uint16_t* out = reinterpret_cast<uint16_t*>(q);
+  auto r256 = [](size_t b) { return (b + 255) / 256 * 256; };
+  // scratch: [abort | out | P] (zeroed before every launch) | partials | logits | sigma
   for (int l0 = 0; l0 < L; l0 += kMaxDecLayers) {
     const int nl = (L - l0) < kMaxDecLayers ? (L - l0) : kMaxDecLayers;
+    uint8_t* q = scr;
+    int* abort_flag = reinterpret_cast<int*>(q);
+    q += 256;
+    uint32_t* out = reinterpret_cast<uint32_t*>(q);
+    q += r256((size_t)2 * c.d * 4);
+    unsigned long long* P = reinterpret_cast<unsigned long long*>(q);
+    const size_t zero_bytes = (size_t)(q - scr) + (size_t)nl * kPCopies * (c.E + 1) * 8;
+    q += r256((size_t)kMaxDecLayers * kPCopies * (c.E + 1) * 8);
+    unsigned long long* part = reinterpret_cast<unsigned long long*>(q);
+    q += r256((size_t)NB * c.d * 8);
+    float* logits_s = reinterpret_cast<float*>(q);
+    q += r256((size_t)kMaxDecLayers * c.E * 4);
+    float* sigma_s = reinterpret_cast<float*>(q);
     DecParams p;
     for (int i = 0; i < nl; ++i) {
       const Handle* h = layers[l0 + i];
@@ -855,12 +952,12 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     p.Ep = Ep;
     p.nf_max = nf_max;
     p.NB = NB;
+    p.epoch = ++h0->dec_epoch;
     p.x = (l0 == 0) ? x : y;
     p.norm_first = (l0 == 0) ? 0 : 1;
     p.bias = bias ? bias + (long long)l0 * c.E : nullptr;
     p.eps = eps;
     p.y = y;
-    p.bar = bar;
     p.abort_flag = abort_flag;
     p.P = P;
     p.part = part;
@@ -874,7 +971,7 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
                    : nullptr;
     p.tr_ns = (trace && trace->timestamps) ? trace->timestamps + (long long)l0 * 4 : nullptr;
     p.err = h0->dev_err;
-    // the barrier counter, the abort flag and the router sums start at zero
+    // the abort flag, the tagged outputs and the router sums start at zero
     cudaError_t e = cudaMemsetAsync(scr, 0, zero_bytes, st);
     if (e != cudaSuccess) return e;
     void* args[] = {&p};

@@ -72,6 +72,7 @@ struct Handle {
   int prof_calls = 0;
   cudaEvent_t* prof_ev = nullptr;  // [kProfCalls][kStagesTimed + 1]
   int* dev_err = nullptr;
+  unsigned dec_epoch = 0;  // decode launches so far (tags the exchanged partials)
   cudaStream_t last_stream = nullptr;
 };
 
