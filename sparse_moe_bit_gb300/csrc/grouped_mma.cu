@@ -12,8 +12,8 @@
 //            (dequantised to fp16), B = the expert's grouped token rows of x
 //            (fp16, gathered through the permutation); epilogue
 //            H = silu(A0 x) * (A1 x) -> fp16.
-//   down   : A0, A1 = down rows f..f+255 (dequantised), B = the expert's rows
-//            of H; epilogue Y[dst] = w_row * (A x) -> bf16, written to the
+//   down   : A = down rows f..f+127 (dequantised), B = the expert's rows of
+//            H; epilogue Y[dst] = w_row * (A x) -> bf16, written to the
 //            token's contribution row (deterministic combine later).
 // Source: Perplexity, "Optimizing on-device inference for Apple Silicon",
 // §"Dequantize weights during matrix multiplication" (one small weight tile
@@ -23,17 +23,20 @@
 // expert's row count: the token dimension N of each tile is the expert's
 // remaining row count rounded up to 16, at most 256).
 //
-// Warp roles (512 threads, one CTA per SM, persistent over the unit list):
-//   warp 0      B producer (lane 0 issues TMA; the warp stages row indices)
-//               and, for the router, the A bulk copies
-//   warp 1      lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
-//   warps 4..7  load the weight codes from global memory (three K blocks
-//               ahead, in registers) and dequantise them into fp16 A tiles
-//               (128-byte swizzled, K-major)
-//   warps 8..15 epilogue: tcgen05.ld, activation / scaling, staging in shared
-//               memory, bulk stores of 64-byte row segments
-// Rings: A 2 stages, B 4 stages.  TMEM: two fp32 accumulators of 256 columns
-// (A0 at column 0, A1 at column 256).
+// Warp roles (640 threads, one CTA per SM, persistent over the unit list):
+//   warp 0       B producer (lane 0 issues TMA; the warp stages row indices)
+//                and, for the router, the A bulk copies
+//   warp 1       lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
+//   warp 2       down: lane 0 issues the bulk copies of the code ring
+//   warps 4..11  dequantise the weight codes into fp16 A tiles (128-byte
+//                swizzled, K-major): gate/up one row per thread (codes loaded
+//                from global memory three K blocks ahead, in registers);
+//                down half a row per thread (codes from the ring)
+//   warps 12..19 epilogue: tcgen05.ld, activation / scaling, staging in
+//                shared memory, 16-byte stores of 64-byte row segments
+// Rings: A 2 stages, B 4 stages (down: 3, and 8 stages of codes).  TMEM: two
+// fp32 accumulators of 256 columns (gate/up and router: tiles A0 and A1 of
+// one unit; down: two units in turn).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,7 +48,10 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
+constexpr int kDeqWarps = 8;   // warps 4 .. 11
+constexpr int kEpiWarp0 = 12;  // warps 12 .. 19
+constexpr int kHalfChunk = 4608;  // 128 rows x (32 B codes + 4 B scale/bias)
 constexpr int kAStages = 2;
 constexpr int kBStage = 32768;   // up to 256 x 64 x 16-bit
 constexpr int kEpiWarps = 8;
@@ -54,16 +60,22 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Per-mode shape of a work unit and of the pipeline:
 //   NA   128-row weight tiles per unit (gate/up: the gate and the up tile of
-//        the same features; router: 256 experts; down: 256 output rows).  One
-//        tile per unit is supported (units are then chunk halves), but on
-//        GB300 it measured slower for the down projection: twice the B reads
+//        the same features; router: 256 experts; down: 128 output rows, one
+//        half of a 256-row code chunk)
 //   NACC TMEM accumulator buffers: two fit when a unit needs only 256
-//        columns (one tile), letting an epilogue overlap the next unit's MMAs
+//        columns (one tile), so that the down projection's epilogue (the
+//        contribution rows, the largest write of the block) overlaps the
+//        next unit's MMAs
+//   CST  stages of the down projection's code ring: the codes and scale/bias
+//        words of a unit's half chunk arrive by bulk copy (4.5 KB per K
+//        block), far enough ahead to hide the memory latency that limited
+//        dequantisation from registers loaded three K blocks ahead
 template <int MODE>
 struct Cfg {
-  static constexpr int NA = 2;
-  static constexpr int NACC = 1;
-  static constexpr int B_STAGES = 4;
+  static constexpr int NA = (MODE == MMA_DOWN) ? 1 : 2;
+  static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
+  static constexpr int CST = (MODE == MMA_DOWN) ? 8 : 0;
+  static constexpr int B_STAGES = (MODE == MMA_DOWN) ? 3 : 4;
   static constexpr int A_STAGE = NA * 16384;
   // epilogue: per chunk of 16 rows, NSEG 64-byte segments per row (down: one
   // per weight tile; gate/up: one, the SwiGLU of the tile pair)
@@ -71,10 +83,11 @@ struct Cfg {
   static constexpr int STAGE_BUF = 16 * 64 * NSEG;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + kAStages * A_STAGE;
-  static constexpr int OFF_STAGE = OFF_B + B_STAGES * kBStage;
+  static constexpr int OFF_CODE = OFF_B + B_STAGES * kBStage;
+  static constexpr int OFF_STAGE = OFF_CODE + CST * kHalfChunk;
   static constexpr int OFF_ROWS = OFF_STAGE + kEpiWarps * 2 * STAGE_BUF;  // gather rows
   static constexpr int OFF_BAR = OFF_ROWS + 256 * 4;
-  static constexpr int NUM_BARS = 2 * kAStages + 2 * B_STAGES + 2 * NACC + 1;
+  static constexpr int NUM_BARS = 2 * kAStages + 2 * B_STAGES + 2 * NACC + 2 * CST + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -123,6 +136,13 @@ struct Smem {
   __device__ uint32_t acc_full(int b) const { return bar(2 * kAStages + 2 * C::B_STAGES + b); }
   __device__ uint32_t acc_empty(int b) const {
     return bar(2 * kAStages + 2 * C::B_STAGES + C::NACC + b);
+  }
+  __device__ uint32_t code(int s) const { return base + C::OFF_CODE + s * kHalfChunk; }
+  __device__ uint32_t c_full(int s) const {
+    return bar(2 * kAStages + 2 * C::B_STAGES + 2 * C::NACC + s);
+  }
+  __device__ uint32_t c_empty(int s) const {
+    return bar(2 * kAStages + 2 * C::B_STAGES + 2 * C::NACC + C::CST + s);
   }
   __device__ uint32_t drain() const { return bar(C::NUM_BARS - 1); }
 };
@@ -297,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(S.a_full(s), MODE == MMA_ROUTER ? 1 : 4);
+      mbar_init(S.a_full(s), MODE == MMA_ROUTER ? 1 : kDeqWarps);
       mbar_init(S.a_empty(s), 1);
     }
     for (int s = 0; s < kBStages; ++s) {
@@ -307,6 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     for (int b = 0; b < C::NACC; ++b) {
       mbar_init(S.acc_full(b), 1);
       mbar_init(S.acc_empty(b), kEpiWarps);
+    }
+    for (int s = 0; s < C::CST; ++s) {
+      mbar_init(S.c_full(s), 1);
+      mbar_init(S.c_empty(s), kDeqWarps);
     }
     mbar_init(S.drain(), 1);
     *abort_flag = 0;
@@ -327,8 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     // ------------------------------------------------------ B (+ router A)
     uint32_t gb = 0, ga = 0;
     bool ok = true;
+    Unit tn = get_unit(p, MODE, cid * CL + crank);
     for (int cu = cid; cu < ncu && ok; cu += ncl) {
-      const Unit t = get_unit(p, MODE, cu * CL + crank);
+      const Unit t = tn;
+      if (cu + ncl < ncu) tn = get_unit(p, MODE, (cu + ncl) * CL + crank);
       if (MODE == MMA_GATEUP) {
         // row indices of the unit's tokens; padding rows repeat a valid row
         __syncwarp();
@@ -381,8 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t ga = 0, gb = 0, i = 0;
+      Unit tn = get_unit(p, MODE, cid * CL + crank);
       for (int cu = cid; cu < ncu; cu += ncl, ++i) {
-        const Unit t = get_unit(p, MODE, cu * CL + crank);
+        const Unit t = tn;  // the next unit's descriptor loads during this one
+        if (cu + ncl < ncu) tn = get_unit(p, MODE, (cu + ncl) * CL + crank);
         const int ab = (C::NACC == 2) ? (int)(i & 1) : 0;
         const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
         if (!thread_wait(S.acc_empty(ab), aph ^ 1, abort_flag, p.err)) break;
@@ -418,84 +446,120 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       tc_commit(S.drain());
       mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------ dequantise (codes from
-    // global memory straight into registers, three K blocks ahead)
+  } else if (warp == 2 && MODE == MMA_DOWN) {
+    // ------------------------------------------------ code ring (down)
+    if (lane == 0) {
+      const int nmy = (ncu - cid + ncl - 1) / ncl;
+      const int total = nmy * kbu;
+      for (int g = 0; g < total; ++g) {
+        const int s = g % C::CST;
+        if (!thread_wait(S.c_empty(s), ((g / C::CST) & 1) ^ 1, abort_flag, p.err)) break;
+        const int j = g / kbu;
+        const Unit u = get_unit(p, MODE, (cid + j * ncl) * CL + crank);
+        // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, then s,b words
+        const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
+                            (long long)(u.m >> 1) * p.a_unit_stride +
+                            (long long)(g - j * kbu) * p.a_chunk;
+        const int h = u.m & 1;
+        mbar_arrive_expect_tx(S.c_full(s), kHalfChunk);
+        bulk_g2s(S.code(s), ch + h * 4096, 4096, S.c_full(s));
+        bulk_g2s(S.code(s) + 4096, ch + 8192 + h * 512, 512, S.c_full(s));
+      }
+    }
+  } else if (warp >= 4 && warp < 4 + kDeqWarps) {
+    // ------------------------------------------------ dequantise
     if (MODE != MMA_ROUTER) {
-      const int t = threadIdx.x - 128;  // 0..127: rows t (A0) and t + 128 (A1)
+      const int t = threadIdx.x - 128;  // 0..255
+      // two tiles: row t of the unit (tile t >> 7); one tile: row t & 127,
+      // K half t >> 7 (32 values)
+      const int row = (C::NA == 2) ? t : (t & 127);
+      const int kh = (C::NA == 2) ? 0 : (t >> 7);
       const int nmy = (ncu - cid + ncl - 1) / ncl;  // this CTA's units
       const int total = nmy * kbu;
-      // source chunk of the CTA's global K-block number g
-      // chunks hold 256 rows; a one-tile unit m is rows 128 (m % 2) .. +127 of
-      // chunk unit m / 2.  Thread t dequantises row t (and, with two tiles,
-      // row t + 128) of the unit.
       struct Codes {
-        uint4 a0, a1, b0, b1;
-        uint32_t sa, sb;
+        uint4 a0, a1;
+        uint32_t sa;
       };
+      // gate/up: source chunk of the CTA's global K-block number g, loaded
+      // straight into registers (chunks hold 256 rows, one unit)
       auto load = [&](int g, Codes& c) {
         if (g < total) {
           const int j = g / kbu;
           const Unit u = get_unit(p, MODE, (cid + j * ncl) * CL + crank);
-          const int cu = (C::NA == 2) ? u.m : (u.m >> 1);
-          const int r0 = (C::NA == 2) ? t : ((u.m & 1) * 128 + t);
           const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
-                              (long long)cu * p.a_unit_stride +
+                              (long long)u.m * p.a_unit_stride +
                               (long long)(g - j * kbu) * p.a_chunk;
-          const uint4* ra = reinterpret_cast<const uint4*>(ch + r0 * 32);
+          const uint4* ra = reinterpret_cast<const uint4*>(ch + row * 32);
           c.a0 = __ldg(ra);
           c.a1 = __ldg(ra + 1);
-          c.sa = __ldg(reinterpret_cast<const uint32_t*>(ch + 8192) + r0);
-          if (C::NA == 2) {
-            const uint4* rb = reinterpret_cast<const uint4*>(ch + (t + 128) * 32);
-            c.b0 = __ldg(rb);
-            c.b1 = __ldg(rb + 1);
-            c.sb = __ldg(reinterpret_cast<const uint32_t*>(ch + 8192) + t + 128);
+          c.sa = __ldg(reinterpret_cast<const uint32_t*>(ch + 8192) + row);
+        }
+      };
+      // words w[i] (K 8 (4 kh + i) .. +7) of row r -> swizzled 16-byte chunks
+      auto emit = [&](uint32_t a, int r, const Codes& cc) {
+        const uint32_t s2 = __byte_perm(cc.sa, 0, 0x1010);
+        const uint32_t b2 = __byte_perm(cc.sa, 0, 0x3232);
+        const uint32_t rowb = a + (r >> 7) * 16384 + (r & 127) * 128;
+        const uint32_t w[8] = {cc.a0.x, cc.a0.y, cc.a0.z, cc.a0.w,
+                               cc.a1.x, cc.a1.y, cc.a1.z, cc.a1.w};
+        constexpr int NW = (C::NA == 2) ? 8 : 4;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+          const int c = 4 * kh + i;
+          st_shared_v4(rowb + ((c ^ (r & 7)) << 4), dequant_pair(w[i], 0, s2, b2),
+                       dequant_pair(w[i], 1, s2, b2), dequant_pair(w[i], 2, s2, b2),
+                       dequant_pair(w[i], 3, s2, b2));
+        }
+      };
+      if (C::CST == 0) {
+        Codes c0, c1, c2;
+        load(0, c0);
+        load(1, c1);
+        load(2, c2);
+        uint32_t ga = 0;
+        for (int g = 0; g < total; ++g, ++ga) {
+          const Codes cur = c0;
+          c0 = c1;
+          c1 = c2;
+          load(g + 3, c2);
+          const int sa = ga % kAStages;
+          if (!warp_wait(S.a_empty(sa), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) break;
+          emit(S.a(sa), row, cur);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(S.a_full(sa));
+        }
+      } else {
+        for (int g = 0; g < total; ++g) {
+          const int sc = g % (C::CST > 0 ? C::CST : 1), sa = g % kAStages;
+          if (!warp_wait(S.c_full(sc), (g / (C::CST > 0 ? C::CST : 1)) & 1, abort_flag, p.err) ||
+              !warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err))
+            break;
+          Codes cur;
+          cur.a0 = ld_shared_v4(S.code(sc) + row * 32 + kh * 16);
+          cur.a1 = cur.a0;
+          cur.sa = ld_shared_u32(S.code(sc) + 4096 + row * 4);
+          emit(S.a(sa), row, cur);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(S.c_empty(sc));
+            mbar_arrive(S.a_full(sa));
           }
         }
-      };
-      // one row: 8 words -> 8 swizzled 16-byte chunks of the A tile
-      auto emit_row = [&](uint32_t a, int r, const uint4& w0, const uint4& w1, uint32_t sbv) {
-        const uint32_t s2 = __byte_perm(sbv, 0, 0x1010);
-        const uint32_t b2 = __byte_perm(sbv, 0, 0x3232);
-        const uint32_t rowb = a + (r >> 7) * 16384 + (r & 127) * 128;
-        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          st_shared_v4(rowb + ((c ^ (r & 7)) << 4), dequant_pair(w[c], 0, s2, b2),
-                       dequant_pair(w[c], 1, s2, b2), dequant_pair(w[c], 2, s2, b2),
-                       dequant_pair(w[c], 3, s2, b2));
-        }
-      };
-      Codes c0, c1, c2;
-      load(0, c0);
-      load(1, c1);
-      load(2, c2);
-      uint32_t ga = 0;
-      for (int g = 0; g < total; ++g, ++ga) {
-        const Codes cur = c0;
-        c0 = c1;
-        c1 = c2;
-        load(g + 3, c2);
-        const int sa = ga % kAStages;
-        if (!warp_wait(S.a_empty(sa), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) break;
-        const uint32_t a = S.a(sa);
-        emit_row(a, t, cur.a0, cur.a1, cur.sa);
-        if (C::NA == 2) emit_row(a, t + 128, cur.b0, cur.b1, cur.sb);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(S.a_full(sa));
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------- epilogue
-    const int e = warp - 8;            // 0..7
+    const int e = warp - kEpiWarp0;    // 0..7
     const int q = warp & 3;            // TMEM lane quarter
     const int half = e >> 2;           // columns [128*half, 128*half + 128)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t i = 0, nst = 0;
+    Unit tn = get_unit(p, MODE, cid * CL + crank);
     for (int cu = cid; cu < ncu; cu += ncl, ++i) {
-      const Unit t = get_unit(p, MODE, cu * CL + crank);
+      const Unit t = tn;
+      if (cu + ncl < ncu) tn = get_unit(p, MODE, (cu + ncl) * CL + crank);
       const int c0 = half * 128;
       const int c1 = min(c0 + 128, t.npad);
       // row data of the warp's 128 columns, fetched while the MMAs run:

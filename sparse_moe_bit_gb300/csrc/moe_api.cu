@@ -246,9 +246,9 @@ moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
   int grid = units < h->num_sms ? (int)units : h->num_sms;
   prof_mark(h, 4, st);
   CK(launch_grouped_mma(MMA_GATEUP, p, grid, st), "gate/up launch");
-  // down projection + routing weight: two 128-row weight tiles per unit
+  // down projection + routing weight: one 128-row weight tile per unit
   p.kb_per_unit = c.I / 64;
-  p.m_units = c.d / 256;
+  p.m_units = c.d / 128;
   p.units_per_tile = p.m_units;
   p.wA = h->pf_dn;
   p.a_unit_stride = (long long)(c.I / 64) * kCodeChunk;
