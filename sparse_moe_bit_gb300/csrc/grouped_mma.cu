@@ -303,13 +303,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 
   const int nunits =
       (MODE == MMA_ROUTER) ? p.nunits_host : (*p.ntiles_dev) * p.units_per_tile;
-  // work: cluster units cu = cid, cid + ncl, ...; the CTA of rank r takes unit
-  // cu * CL + r (same tile for the whole cluster, weight unit m = consecutive)
+  // work: the i-th cluster unit of cluster cid is cunit(i), snake order over
+  // the tile list (sorted by size: full tiles first, then remainders largest
+  // first), so that every cluster gets a similar mix; the CTA of rank r takes
+  // unit cu * CL + r (same tile for the whole cluster, weight unit m =
+  // consecutive)
   const int ncu = nunits / CL;
   const int cid = (CL == 1) ? (int)blockIdx.x : (int)cluster_id();
   const int ncl = (CL == 1) ? (int)gridDim.x : (int)cluster_count();
   const int crank = (CL == 1) ? 0 : (int)cluster_rank();
   if (cid >= ncu) return;  // uniform over the cluster
+  auto cunit = [&](int i) {
+    const int base = i * ncl;
+    return (i & 1) ? base + (ncl - 1 - cid) : base + cid;
+  };
+  const int nmy = ncu / ncl + ((cunit(ncu / ncl) < ncu) ? 1 : 0);  // this cluster's units
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -351,10 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     // ------------------------------------------------------ B (+ router A)
     uint32_t gb = 0, ga = 0;
     bool ok = true;
-    Unit tn = get_unit(p, MODE, cid * CL + crank);
-    for (int cu = cid; cu < ncu && ok; cu += ncl) {
+    Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
+    for (int i = 0; i < nmy && ok; ++i) {
       const Unit t = tn;
-      if (cu + ncl < ncu) tn = get_unit(p, MODE, (cu + ncl) * CL + crank);
+      if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
       if (MODE == MMA_GATEUP) {
         // row indices of the unit's tokens; padding rows repeat a valid row
         __syncwarp();
@@ -406,11 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t ga = 0, gb = 0, i = 0;
-      Unit tn = get_unit(p, MODE, cid * CL + crank);
-      for (int cu = cid; cu < ncu; cu += ncl, ++i) {
+      uint32_t ga = 0, gb = 0;
+      Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
+      for (int i = 0; i < nmy; ++i) {
         const Unit t = tn;  // the next unit's descriptor loads during this one
-        if (cu + ncl < ncu) tn = get_unit(p, MODE, (cu + ncl) * CL + crank);
+        if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
         const int ab = (C::NACC == 2) ? (int)(i & 1) : 0;
         const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
         if (!thread_wait(S.acc_empty(ab), aph ^ 1, abort_flag, p.err)) break;
@@ -449,13 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   } else if (warp == 2 && MODE == MMA_DOWN) {
     // ------------------------------------------------ code ring (down)
     if (lane == 0) {
-      const int nmy = (ncu - cid + ncl - 1) / ncl;
       const int total = nmy * kbu;
       for (int g = 0; g < total; ++g) {
         const int s = g % C::CST;
         if (!thread_wait(S.c_empty(s), ((g / C::CST) & 1) ^ 1, abort_flag, p.err)) break;
         const int j = g / kbu;
-        const Unit u = get_unit(p, MODE, (cid + j * ncl) * CL + crank);
+        const Unit u = get_unit(p, MODE, cunit(j) * CL + crank);
         // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, then s,b words
         const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
                             (long long)(u.m >> 1) * p.a_unit_stride +
@@ -474,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       // K half t >> 7 (32 values)
       const int row = (C::NA == 2) ? t : (t & 127);
       const int kh = (C::NA == 2) ? 0 : (t >> 7);
-      const int nmy = (ncu - cid + ncl - 1) / ncl;  // this CTA's units
       const int total = nmy * kbu;
       struct Codes {
         uint4 a0, a1;
@@ -485,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       auto load = [&](int g, Codes& c) {
         if (g < total) {
           const int j = g / kbu;
-          const Unit u = get_unit(p, MODE, (cid + j * ncl) * CL + crank);
+          const Unit u = get_unit(p, MODE, cunit(j) * CL + crank);
           const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
                               (long long)u.m * p.a_unit_stride +
                               (long long)(g - j * kbu) * p.a_chunk;
@@ -555,11 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     const int q = warp & 3;            // TMEM lane quarter
     const int half = e >> 2;           // columns [128*half, 128*half + 128)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t i = 0, nst = 0;
-    Unit tn = get_unit(p, MODE, cid * CL + crank);
-    for (int cu = cid; cu < ncu; cu += ncl, ++i) {
+    uint32_t nst = 0;
+    Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
+    for (int i = 0; i < nmy; ++i) {
       const Unit t = tn;
-      if (cu + ncl < ncu) tn = get_unit(p, MODE, (cu + ncl) * CL + crank);
+      if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
       const int c0 = half * 128;
       const int c1 = min(c0 + 128, t.npad);
       // row data of the warp's 128 columns, fetched while the MMAs run:

@@ -278,39 +278,67 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
 // each expert's remainder tile, larger remainders first (ties in expert
 // order).  The shared expert (index E, all T tokens, rows T*k..T*k+T-1)
 // takes part like any expert.
+// The scan over blocks: P = 1024 / E threads per expert (thread p*E + e),
+// each over a contiguous range of blocks, 16 loads in flight at a time; the
+// ranges' sums are exchanged in shared memory, then each thread writes its
+// range's bases from its range prefix.
+constexpr int kScanBatch = 16;
 __global__ void __launch_bounds__(1024) scan_tiles_kernel(
     const int32_t* __restrict__ hist, int nblk, int T, int E, int k, int has_shared,
     int32_t* __restrict__ base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int4* __restrict__ tiles, int32_t* __restrict__ ntiles) {
   __shared__ int warp_tot[32];
   __shared__ int s_total;
-  __shared__ int s_cls[kMaxE + 1];
   __shared__ int s_clsb[17];
+  __shared__ int s_part[1024];
+  __shared__ int s_wcls[32][16];  // per warp: experts of each remainder class
   const int tid = threadIdx.x;
   const int nexp = E + (has_shared ? 1 : 0);
 
+  const int P = blockDim.x / E;  // >= 2 (E <= 512)
+  const int pe = tid % E, pp = tid / E;
+  const int nbp = (nblk + P - 1) / P;
+  const int b0 = pp * nbp, b1 = min(nblk, b0 + nbp);
+  int part = 0;
+  if (pp < P) {
+    for (int b = b0; b < b1; b += kScanBatch) {
+      int c[kScanBatch];
+#pragma unroll
+      for (int q = 0; q < kScanBatch; ++q)
+        c[q] = (b + q < b1) ? hist[(long long)(b + q) * E + pe] : 0;
+#pragma unroll
+      for (int q = 0; q < kScanBatch; ++q) part += c[q];
+    }
+    s_part[tid] = part;
+  }
+  __syncthreads();
   int cnt = 0;
-  if (tid < E) {
-    int b = 0;
-    for (; b + 8 <= nblk; b += 8) {
-      int c[8];
+  if (pp < P) {
+    int pre = 0, tot = 0;
+    for (int q = 0; q < P; ++q) {
+      const int v = s_part[q * E + pe];
+      pre += (q < pp) ? v : 0;
+      tot += v;
+    }
+    int run = pre;
+    for (int b = b0; b < b1; b += kScanBatch) {
+      int c[kScanBatch];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) c[q] = hist[(long long)(b + q) * E + tid];
+      for (int q = 0; q < kScanBatch; ++q)
+        c[q] = (b + q < b1) ? hist[(long long)(b + q) * E + pe] : 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        base[(long long)(b + q) * E + tid] = cnt;
-        cnt += c[q];
+      for (int q = 0; q < kScanBatch; ++q) {
+        if (b + q < b1) base[(long long)(b + q) * E + pe] = run;
+        run += c[q];
       }
     }
-    for (; b < nblk; ++b) {
-      const int c = hist[(long long)b * E + tid];
-      base[(long long)b * E + tid] = cnt;
-      cnt += c;
+    if (pp == 0) {
+      counts[pe] = tot;
+      cnt = tot;  // thread e (< E) continues with its expert's count
     }
-    counts[tid] = cnt;
-  } else if (tid == E && has_shared) {
-    cnt = T;
   }
+  if (tid == E && has_shared) cnt = T;
+  __syncthreads();
   // offsets over the routed experts
   const int off = block_exclusive_scan(tid < E ? cnt : 0, warp_tot, &s_total);
   if (tid <= E) offsets[tid] = (tid < E) ? off : s_total;
@@ -321,10 +349,16 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(
   // remainder tiles: class c = npad/16 - 1 (0..15), larger classes first
   const int tail = (tid < nexp) ? cnt % kTileRows : 0;
   const int cls = tail ? ((tail + 15) >> 4) - 1 : -1;
-  if (tid < nexp) s_cls[tid] = cls;
   if (tid < 17) s_clsb[tid] = 0;
+  if (tid < 32 * 16) (&s_wcls[0][0])[tid] = 0;
   __syncthreads();
   if (cls >= 0) atomicAdd(&s_clsb[cls], 1);
+  // rank of the expert among the lower-indexed experts of its class: within
+  // the warp by matching lanes, then the counts of the earlier warps
+  const int lane = tid & 31, wid = tid >> 5;
+  const unsigned same = __match_any_sync(0xffffffffu, cls);
+  const int wrank = __popc(same & ((1u << lane) - 1u));
+  if (cls >= 0 && wrank == 0) s_wcls[wid][cls] = __popc(same);
   __syncthreads();
   if (tid == 0) {
     int run = total_full;
@@ -342,8 +376,8 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(
     for (int i = 0; i < nf; ++i)
       tiles[full_off + i] = make_int4(e, row_base + i * kTileRows, kTileRows, kTileRows);
     if (cls >= 0) {
-      int rank = 0;
-      for (int f = 0; f < e; ++f) rank += (s_cls[f] == cls);
+      int rank = wrank;
+      for (int w = 0; w < wid; ++w) rank += s_wcls[w][cls];
       tiles[s_clsb[cls] + rank] = make_int4(e, row_base + nf * kTileRows, tail, (tail + 15) & ~15);
     }
   }
@@ -406,14 +440,21 @@ __global__ void __launch_bounds__(256) scatter_kernel(
 
 // out[t][f] = sum_{j=0}^{k1-1} Y[t*k1 + j][f], fp32 in slot order (the
 // shared expert's term last), rounded once to bf16.  The routing weights were
-// applied when the rows of Y were written.
+// applied when the rows of Y were written.  A thread's loads of all k1 rows
+// are issued before the sum (k1 <= kMaxK + 1).
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y, int k1,
                                                      int d, uint16_t* __restrict__ out) {
   const int t = blockIdx.x;
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < k1; ++j) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(Y + ((long long)t * k1 + j) * d + c);
+    uint4 rv[kMaxK + 1];
+#pragma unroll
+    for (int j = 0; j < kMaxK + 1; ++j)
+      if (j < k1) rv[j] = __ldcs(reinterpret_cast<const uint4*>(Y + ((long long)t * k1 + j) * d + c));
+#pragma unroll
+    for (int j = 0; j < kMaxK + 1; ++j) {
+      if (j >= k1) break;
+      const uint4 raw = rv[j];
       const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
