@@ -75,6 +75,7 @@ constexpr long long kPMaxAbs = (1ll << 52) - 1;      // |addend| limit (2^20 in 
 constexpr int kMaxPerCopy = 31;                      // 31 * 2^53 < 2^58: no carry into the count
 constexpr int kRedChunks = 32;  // partial sums per owned feature in the reduction
 constexpr int kPollMax = 8;     // partials in flight per thread in one polling pass
+constexpr int kMaxOwned = 16;   // owned output features summed per pass (router sums)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
@@ -379,6 +380,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t dn_bar = bar0 + 8 * kDnBar;
   const uint32_t rt_bar = bar0 + 8 * kRtBar;
   const int wwarp = kDecWarps - 1;  // computes the routing weights
+  // bulk copies other than a warp's own gate/up rows (the issuing thread
+  // waits for each): down columns by warp 14, router rows by warp 15
+  constexpr int kDnTid = (kDecWarps - 2) * 32 + 1, kRtTid = (kDecWarps - 1) * 32 + 31;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, c = blockIdx.x;
@@ -515,8 +519,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         p.P + ((long long)ln * kPCopies + (c % kPCopies)) * (long long)(E + 1);
     bool range_err = false;
     for (int e = tid; e <= E; e += kDecThreads) {
+      // every load of the entry first (nf <= kMaxOwned), then the sum
       float acc = 0.f;
-      for (int f = 0; f < nf; ++f) acc = fmaf(outs[f], bf16f(rt_buf[f * Ep + e]), acc);
+      for (int f0 = 0; f0 < nf; f0 += kMaxOwned) {
+        uint16_t wv[kMaxOwned];
+        float ov[kMaxOwned];
+#pragma unroll
+        for (int i = 0; i < kMaxOwned; ++i) {
+          wv[i] = (f0 + i < nf) ? rt_buf[(f0 + i) * Ep + e] : (uint16_t)0;
+          ov[i] = (f0 + i < nf) ? outs[f0 + i] : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxOwned; ++i) acc = fmaf(ov[i], bf16f(wv[i]), acc);
+      }
       long long v;
       if (fabsf(acc) < 1048575.0f) {
         v = fix32(acc);
@@ -559,7 +574,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   };
 
   auto issue_router_copy = [&](int l) {
-    if (tid == 2 && nf > 0) {
+    if (tid == kRtTid && nf > 0) {
       const uint32_t bytes = (uint32_t)nf * Ep * 2;
       infl[kRtBar] = (int)ph_rt;
       mbar_arrive_expect_tx(rt_bar, bytes);
@@ -575,7 +590,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       drain();
       return;
     }
-    if (tid == 2) infl[kRtBar] = -1;
+    if (tid == kRtTid) infl[kRtBar] = -1;
   }
   ph_rt ^= 1;
   router_partial(0);
@@ -626,7 +641,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       drain();
       return;
     }
-    if (l + 1 < p.L) issue_router_copy(l + 1);  // the router buffer is no longer read
     stamp(p, l, 0);
     float r = 1.0f;  // 1/rms of out_{l-1} (x_0 is normalised already)
     if (l > 0) {
@@ -664,7 +678,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     cta_topk(keys, cand, E, k, sel_e, tid);
     if (c < NB && !pre) {
       if (lane == 0) issue_gu(c, W);
-      if (tid == 1) issue_dn(c, W);
+      if (tid == kDnTid) issue_dn(c, W);
     }
     pre = false;
     stamp(p, l, 1);
@@ -693,6 +707,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (p.tr_w) p.tr_w[(long long)l * k + lane] = wv;
         }
       }
+      // the next layer's router rows (read at the end of this layer; the
+      // buffer's last reads were before this layer's first barrier)
+      if (l + 1 < p.L) issue_router_copy(l + 1);
     }
 
     // ---- B: the CTA's blocks: gate/up, h, and the block's tagged partial
@@ -701,7 +718,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (nb > 0) {
         __syncthreads();  // the previous block's buffers are no longer read
         if (lane == 0) issue_gu(b, W);
-        if (tid == 1) issue_dn(b, W);
+        if (tid == kDnTid) issue_dn(b, W);
       }
       // gate/up: warp -> features 2*warp, 2*warp + 1 of the block; lane: one
       // group of 64 inputs at a time, its activations in registers for both
@@ -781,7 +798,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         drain();
         return;
       }
-      if (tid == 1) infl[kDnBar] = -1;
+      if (tid == kDnTid) infl[kDnBar] = -1;
       ph_dn ^= 1;
       __syncthreads();
       // the block's partial output: part[b][f] = w_j (s sum_i q_i h_i + beta H),
@@ -807,7 +824,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (l + 1 < p.L && p.has_shared && c < NB && c / bpe == k) {
       __syncthreads();  // this layer's buffers are no longer read
       if (lane == 0) issue_gu(c, p.layer[l + 1]);
-      if (tid == 1) issue_dn(c, p.layer[l + 1]);
+      if (tid == kDnTid) issue_dn(c, p.layer[l + 1]);
       pre = true;
     }
     stamp(p, l, 2);
@@ -876,7 +893,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           drain();
           return;
         }
-        if (tid == 2) infl[kRtBar] = -1;
+        if (tid == kRtTid) infl[kRtBar] = -1;
       }
       ph_rt ^= 1;
       router_partial(l + 1);
