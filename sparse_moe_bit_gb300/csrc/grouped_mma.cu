@@ -1,7 +1,7 @@
 // Grouped tensor-core GEMM for sm_103a: tcgen05.mma with TMEM accumulators,
 // token-row operands staged in shared memory by the tensor memory accelerator
-// (2-D tensor tiles and 4-row gathers, multicast across a cluster), 4-bit
-// weights dequantised tile by tile inside the pipeline.
+// (2-D tensor tiles multicast across a cluster), 4-bit weights dequantised
+// tile by tile inside the pipeline.
 //
 // One work unit computes two 128-row weight tiles (A0, A1) against one token
 // tile of up to 256 rows (B), over K in blocks of 64 (one quantisation group
@@ -10,7 +10,7 @@
 //            out = fp32 partial logits of one K split.
 //   gate/up: A0 = gate rows f..f+127, A1 = up rows f..f+127 of one expert
 //            (dequantised to fp16), B = the expert's grouped token rows of x
-//            (fp16, gathered through the permutation); epilogue
+//            (fp16, already permuted into grouped-row order); epilogue
 //            H = silu(A0 x) * (A1 x) -> fp16.
 //   down   : A = down rows f..f+127 (dequantised), B = the expert's rows of
 //            H; epilogue Y[dst] = w_row * (A x) -> bf16, written to the
@@ -24,7 +24,7 @@
 // remaining row count rounded up to 16, at most 256).
 //
 // Warp roles (640 threads, one CTA per SM, persistent over the unit list):
-//   warp 0       B producer (lane 0 issues TMA; the warp stages row indices)
+//   warp 0       B producer (the warp's lanes issue the 16-row TMA tiles)
 //                and, for the router, the A bulk copies
 //   warp 1       lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
 //   warp 2       down: lane 0 issues the bulk copies of the code ring
@@ -85,8 +85,7 @@ struct Cfg {
   static constexpr int OFF_B = OFF_A + kAStages * A_STAGE;
   static constexpr int OFF_CODE = OFF_B + B_STAGES * kBStage;
   static constexpr int OFF_STAGE = OFF_CODE + CST * kHalfChunk;
-  static constexpr int OFF_ROWS = OFF_STAGE + kEpiWarps * 2 * STAGE_BUF;  // gather rows
-  static constexpr int OFF_BAR = OFF_ROWS + 256 * 4;
+  static constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * 2 * STAGE_BUF;
   static constexpr int NUM_BARS = 2 * kAStages + 2 * B_STAGES + 2 * NACC + 2 * CST + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
@@ -206,9 +205,9 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t v, int j, uint32_t s2,
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// TMA loads of B: a 2-D tile (16 rows) or a 4-row gather.  With CL > 1 the
-// data is multicast to the same shared-memory offset of every CTA of the
-// cluster and each CTA's barrier at `bar` receives its bytes.
+// TMA load of B: a 2-D tile (16 rows).  With CL > 1 the data is multicast to
+// the same shared-memory offset of every CTA of the cluster and each CTA's
+// barrier at `bar` receives its bytes.
 template <int CL>
 __device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             uint32_t bar) {
@@ -224,25 +223,6 @@ __device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-  }
-}
-
-template <int CL>
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int4 rows,
-                                            uint32_t bar) {
-  if (CL == 1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(tm), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar)
-        : "memory");
-  } else {
-    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-        "l"(tm), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar), "h"(mask)
         : "memory");
   }
 }
@@ -321,7 +301,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  int* rows_s = reinterpret_cast<int*>(smem + C::OFF_ROWS);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -363,13 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     for (int i = 0; i < nmy && ok; ++i) {
       const Unit t = tn;
       if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
-      if (MODE == MMA_GATEUP) {
-        // row indices of the unit's tokens; padding rows repeat a valid row
-        __syncwarp();
-        for (int i = lane; i < t.npad; i += 32)
-          rows_s[i] = p.b_rowmap[t.row0 + (i < t.nrows ? i : 0)];
-        __syncwarp();
-      }
       const int k0 = t.ks * kbu;
       const uint8_t* asrc = p.wA + (long long)t.m * p.a_unit_stride + (long long)k0 * p.a_chunk;
       for (int kb = 0; kb < kbu; ++kb) {
@@ -393,21 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         const uint32_t bs = S.b(s);
         const int x = (k0 + kb) * 64;
         // the whole tile arrives in every CTA; this CTA fetches 16-row slabs
-        // crank, crank + CL, ... (4 gathers or one 2-D tile per slab)
+        // crank, crank + CL, ... (one 2-D tile per slab)
         if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
         __syncwarp();
         const int nslab = t.npad >> 4;
-        if (MODE == MMA_GATEUP) {
-          const int nops = ((nslab - crank + CL - 1) / CL) * 4;
-          for (int o = lane; o < nops; o += 32) {
-            const int n = 16 * (crank + CL * (o >> 2)) + 4 * (o & 3);
-            const int4 r4 = *reinterpret_cast<const int4*>(rows_s + n);
-            tma_gather4<CL>(bs + n * 128, &p.tmB, x, r4, S.b_full(s));
-          }
-        } else {
-          for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
-            tma_tile_2d<CL>(bs + sl * 2048, &p.tmB, x, t.row0 + 16 * sl, S.b_full(s));
-        }
+        for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
+          tma_tile_2d<CL>(bs + sl * 2048, &p.tmB, x, t.row0 + 16 * sl, S.b_full(s));
         ++gb;
       }
     }
@@ -459,8 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     if (lane == 0) {
       const int total = nmy * kbu;
       for (int g = 0; g < total; ++g) {
-        const int s = g % C::CST;
-        if (!thread_wait(S.c_empty(s), ((g / C::CST) & 1) ^ 1, abort_flag, p.err)) break;
+        constexpr int kCst = C::CST > 0 ? C::CST : 1;
+        const int s = g % kCst;
+        if (!thread_wait(S.c_empty(s), ((g / kCst) & 1) ^ 1, abort_flag, p.err)) break;
         const int j = g / kbu;
         const Unit u = get_unit(p, MODE, cunit(j) * CL + crank);
         // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, then s,b words

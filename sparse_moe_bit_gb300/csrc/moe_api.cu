@@ -81,7 +81,7 @@ void free_handle(Handle* h) {
   if (!h) return;
   void* ptrs[] = {h->pf_gu, h->pf_dn, h->pf_router, h->dc_gu, h->dc_dn, h->dc_router_t,
                   h->w_router, h->w_sg, h->dev_err, h->ws.logit_part, h->ws.logits,
-                  h->ws.idx, h->ws.w, h->ws.sigma, h->ws.x16, h->ws.hist, h->ws.base,
+                  h->ws.idx, h->ws.w, h->ws.sigma, h->ws.xp, h->ws.hist, h->ws.base,
                   h->ws.counts, h->ws.offsets, h->ws.perm, h->ws.slot, h->ws.dst, h->ws.wrow,
                   h->ws.tiles, h->ws.ntiles, h->ws.H, h->ws.Y, h->ws.x_dev, h->ws.y_dev,
                   h->ws.bias_dev};
@@ -165,10 +165,10 @@ moe_status alloc_all(Handle* h) {
   CK(dalloc(&w.tiles, (size_t)w.max_tiles * sizeof(int4)), "alloc");
   CK(dalloc(&w.ntiles, 16), "alloc");
   if (h->layouts & MOE_LAYOUT_PREFILL) {
-    CK(dalloc(&w.x16, (size_t)T * c.d * 2), "alloc");
+    CK(dalloc(&w.xp, (size_t)T * k1 * c.d * 2), "alloc");
     CK(dalloc(&w.H, (size_t)T * k1 * c.I * 2), "alloc");
     CK(dalloc(&w.Y, (size_t)T * k1 * c.d * 2), "alloc");
-    CK(make_tmap_16bit(&h->tm_x16, w.x16, T, c.d, 1, false), "tensor map (x16)");
+    CK(make_tmap_16bit(&h->tm_xp, w.xp, T * k1, c.d, 16, false), "tensor map (xp)");
     CK(make_tmap_16bit(&h->tm_h, w.H, T * k1, c.I, 16, false), "tensor map (H)");
   }
   CK(dalloc(&w.x_dev, (size_t)T * c.d * 2), "alloc");
@@ -203,7 +203,6 @@ moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int
     p.a_unit_stride = (long long)(c.d / 64) * kRouterChunk;
     p.a_chunk = kRouterChunk;
     CK(make_tmap_16bit(&p.tmB, x, T, c.d, 16, true), "tensor map (x)");
-    p.b_rowmap = nullptr;
     p.out_f32 = h->ws.logit_part;
     p.E = c.E;
     p.err = h->dev_err;
@@ -214,7 +213,7 @@ moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int
     ks = rp.ks;
   }
   prof_mark(h, 1, st);
-  CK(launch_topk(h, part, ks, T, bias, x, st), "top-k launch");
+  CK(launch_topk(h, part, ks, T, bias, st), "top-k launch");
   prof_mark(h, 2, st);
   CK(launch_scan_tiles(h, T, st), "scan launch");
   prof_mark(h, 3, st);
@@ -222,7 +221,7 @@ moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int
   return MOE_OK;
 }
 
-moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
+moe_status run_experts(Handle* h, const uint16_t* x, int T, uint16_t* y, cudaStream_t st) {
   const moe_config& c = h->cfg;
   Workspace& w = h->ws;
   const int mt = max_tiles_for(h, T);
@@ -238,13 +237,14 @@ moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
   p.wA = h->pf_gu;
   p.a_unit_stride = (long long)(c.d / 64) * kCodeChunk;
   p.a_expert_stride = p.a_unit_stride * (c.I / 128);
-  p.tmB = h->tm_x16;
-  p.b_rowmap = w.perm;
+  p.tmB = h->tm_xp;
   p.H = w.H;
   p.ldh = c.I;
   long long units = (long long)mt * p.m_units;
   int grid = units < h->num_sms ? (int)units : h->num_sms;
   prof_mark(h, 4, st);
+  CK(launch_permute(h, x, T, st), "permute launch");
+  prof_mark(h, 5, st);
   CK(launch_grouped_mma(MMA_GATEUP, p, grid, st), "gate/up launch");
   // down projection + routing weight: one 128-row weight tile per unit
   p.kb_per_unit = c.I / 64;
@@ -254,18 +254,17 @@ moe_status run_experts(Handle* h, int T, uint16_t* y, cudaStream_t st) {
   p.a_unit_stride = (long long)(c.I / 64) * kCodeChunk;
   p.a_expert_stride = p.a_unit_stride * (c.d / 256);
   p.tmB = h->tm_h;
-  p.b_rowmap = nullptr;
   p.Y = w.Y;
   p.ldy = c.d;
   p.dst_row = w.dst;
   p.row_scale = w.wrow;
   units = (long long)mt * p.m_units;
   grid = units < h->num_sms ? (int)units : h->num_sms;
-  prof_mark(h, 5, st);
-  CK(launch_grouped_mma(MMA_DOWN, p, grid, st), "down launch");
   prof_mark(h, 6, st);
-  CK(launch_combine(h, T, y, st), "combine launch");
+  CK(launch_grouped_mma(MMA_DOWN, p, grid, st), "down launch");
   prof_mark(h, 7, st);
+  CK(launch_combine(h, T, y, st), "combine launch");
+  prof_mark(h, 8, st);
   if (h->prof && h->prof_calls < Handle::kProfCalls) ++h->prof_calls;
   return MOE_OK;
 }
@@ -437,7 +436,7 @@ moe_status moe_forward(moe_handle* h, const void* x, int T, const float* logit_b
     uint16_t* yc = static_cast<uint16_t*>(y) + (size_t)t0 * c.d;
     s = run_routing(h, xc, nullptr, tc, logit_bias, st);
     if (s != MOE_OK) return s;
-    s = run_experts(h, tc, yc, st);
+    s = run_experts(h, xc, tc, yc, st);
     if (s != MOE_OK) return s;
   }
   return MOE_OK;

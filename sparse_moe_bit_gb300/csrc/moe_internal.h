@@ -26,7 +26,7 @@ struct Workspace {
   int32_t* idx = nullptr;       // [Tmax][k]
   float* w = nullptr;           // [Tmax][k]
   float* sigma = nullptr;       // [Tmax]
-  uint16_t* x16 = nullptr;      // [Tmax][d] fp16 copy of the activations
+  uint16_t* xp = nullptr;       // [Tmax*(k+1)][d] fp16 activations in grouped-row order
   int32_t* hist = nullptr;      // [nblk][E]
   int32_t* base = nullptr;      // [nblk][E]
   int32_t* counts = nullptr;    // [E]
@@ -63,10 +63,10 @@ struct Handle {
   uint16_t* w_router = nullptr;  // bf16 [E][d]
   uint16_t* w_sg = nullptr;      // bf16 [d]
   Workspace ws;
-  CUtensorMap tm_x16;  // gate/up B: x16 [Tmax][d], 1-row box (4-row gathers)
+  CUtensorMap tm_xp;   // gate/up B: xp [Tmax*(k+1)][d], 16-row box
   CUtensorMap tm_h;    // down B: H [Tmax*(k+1)][I], 16-row box
   // per-stage timing (moe_profile_enable)
-  static constexpr int kStagesTimed = 7;
+  static constexpr int kStagesTimed = 8;
   static constexpr int kProfCalls = 4096;
   bool prof = false;
   int prof_calls = 0;
@@ -100,9 +100,8 @@ struct MmaParams {
   long long a_expert_stride;  // bytes per expert
   long long a_unit_stride;    // bytes per 256-row unit
   int a_chunk;                // bytes per K block
-  // B operand rows: gathered through b_rowmap (gate/up: 4-row TMA gathers) or
-  // contiguous from row0 (router, down: 16-row TMA tiles)
-  const int32_t* b_rowmap;    // grouped row -> source row, or null
+  // B operand rows: contiguous from row0 (16-row TMA tiles; gate/up reads the
+  // activations already permuted into grouped-row order)
   // epilogue
   float* out_f32;             // router partials [KS][T][E]
   int E;
@@ -122,7 +121,8 @@ cudaError_t make_tmap_16bit(CUtensorMap* map, const void* base, long long rows, 
 
 // ---- routing (routing.cu)
 cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
-                        const uint16_t* x, cudaStream_t st);
+                        cudaStream_t st);
+cudaError_t launch_permute(const Handle* h, const uint16_t* x, int T, cudaStream_t st);
 cudaError_t launch_scan_tiles(const Handle* h, int T, cudaStream_t st);
 cudaError_t launch_scatter(const Handle* h, int T, cudaStream_t st);
 cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st);

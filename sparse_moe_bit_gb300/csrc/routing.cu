@@ -29,9 +29,7 @@ __device__ __forceinline__ uint32_t ord_key(float v) {
 // One warp per token, 32 tokens per block (one block = one row of the
 // histogram).  Sums the router's K-split partial logits (fixed order), adds
 // the bias, keeps the top k by (logit desc, index asc) and computes the
-// renormalised softmax weights in fp64.  When x is given it also writes the
-// fp16 copy of the token's activations and the shared expert's gate
-// sigma = sigmoid(w_sg . x).  Each block counts its assignments per expert
+// renormalised softmax weights.  Each block counts its assignments per expert
 // (hist[block][e]).
 // Selection: lane l holds the order keys of experts l, l+32, ...; each round
 // every lane finds its best key not yet taken (first slot among equal keys,
@@ -44,10 +42,8 @@ static_assert(kTopkThreads <= 1024, "one warp per token of a block");
 template <int VPL>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float* __restrict__ part, int KS, int T, int E, int k, const float* __restrict__ bias,
-    const uint16_t* __restrict__ x, int d, const uint16_t* __restrict__ w_sg, int has_shared,
     float* __restrict__ logits, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
-    float* __restrict__ sigma, uint16_t* __restrict__ x16, int32_t* __restrict__ hist,
-    int* __restrict__ err) {
+    int32_t* __restrict__ hist, int* __restrict__ err) {
   __shared__ int cnt[kMaxE];
   __shared__ float s_v[kTokPerBlock][kMaxK];  // the kept logits of each token, in order
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,35 +127,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
       atomicAdd(&cnt[my_e], 1);
     }
 
-    if (x) {
-      const uint16_t* xr = x + (long long)t * d;
-      uint16_t* xo = x16 + (long long)t * d;
-      float dot = 0.0f;
-#pragma unroll 8
-      for (int c = lane * 8; c < d; c += 256) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(xr + c);
-        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t hv[4];
-        uint4 sg = make_uint4(0, 0, 0, 0);
-        if (has_shared) sg = *reinterpret_cast<const uint4*>(w_sg + c);
-        const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(wv[q] << 16);
-          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
-          const __half2 h2 = __floats2half2_rn(lo, hi);
-          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
-          dot = fmaf(lo, __uint_as_float(sv[q] << 16), dot);
-          dot = fmaf(hi, __uint_as_float(sv[q] & 0xFFFF0000u), dot);
-        }
-        *reinterpret_cast<uint4*>(xo + c) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-      }
-      if (has_shared) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        if (lane == 0) sigma[t] = 1.0f / (1.0f + expf(-dot));
-      }
-    }
   }
   __syncthreads();
   // weights: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0) in double-float
@@ -189,38 +156,41 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     hist[(long long)blockIdx.x * E + e] = cnt[e];
 }
 
-// The fp16 copy of the activations (the gate/up GEMM's operand) and the
-// shared expert's gate sigma = sigmoid(w_sg . x): one warp per token, 8
-// tokens per block, w_sg staged in shared memory, each lane's loads of a
-// row issued together.
-constexpr int kCvtThreads = 256;
-constexpr int kCvtTokens = kCvtThreads / 32;
+// The gate/up GEMM's B operand in grouped order: xp[r] = fp16(x[perm[r]])
+// for every grouped row r, so that the GEMM loads whole 16-row tiles by TMA
+// (a gather of 4 rows per operation measured as that kernel's limit).  One
+// warp per row, the row's loads issued together; the warp of a shared-expert
+// row (r = T k + t) also computes that token's gate sigma = sigmoid(w_sg . x)
+// and the row's weight.
+constexpr int kPermThreads = 256;
+constexpr int kPermRows = kPermThreads / 32;
 
-__global__ void __launch_bounds__(kCvtThreads) x16_sigma_kernel(
-    const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_sg,
-    int has_shared, float* __restrict__ sigma, uint16_t* __restrict__ x16) {
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int R, int Tk, int d,
+    const uint16_t* __restrict__ w_sg, int has_shared, float* __restrict__ sigma,
+    float* __restrict__ wrow, uint16_t* __restrict__ xp) {
   extern __shared__ uint4 s_wsg[];  // d / 8
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
     s_wsg[i] = has_shared ? reinterpret_cast<const uint4*>(w_sg)[i] : make_uint4(0, 0, 0, 0);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kCvtTokens + warp;
-  if (t >= T) return;
+  const int r = blockIdx.x * kPermRows + warp;
+  if (r >= R) return;
+  const int t = perm[r];
+  const bool gate = has_shared && r >= Tk;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * d);
-  uint4* xo = reinterpret_cast<uint4*>(x16 + (long long)t * d);
+  uint4* xo = reinterpret_cast<uint4*>(xp + (long long)r * d);
   float dot = 0.0f;
   for (int c0 = lane; c0 < d / 8; c0 += 32 * 8) {
     uint4 raw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (c0 + 32 * i < d / 8) raw[i] = __ldcs(xr + c0 + 32 * i);
+      if (c0 + 32 * i < d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int c = c0 + 32 * i;
       if (c < d / 8) {
         const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        const uint4 sg = s_wsg[c];
-        const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
         uint32_t hv[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -228,17 +198,29 @@ __global__ void __launch_bounds__(kCvtThreads) x16_sigma_kernel(
           const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
           const __half2 h2 = __floats2half2_rn(lo, hi);
           hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
-          dot = fmaf(lo, __uint_as_float(sv[q] << 16), dot);
-          dot = fmaf(hi, __uint_as_float(sv[q] & 0xFFFF0000u), dot);
         }
         xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        if (gate) {
+          const uint4 sg = s_wsg[c];
+          const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), dot);
+            dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
+                       dot);
+          }
+        }
       }
     }
   }
-  if (has_shared) {
+  if (gate) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (lane == 0) sigma[t] = 1.0f / (1.0f + expf(-dot));
+    if (lane == 0) {
+      const float sg = 1.0f / (1.0f + expf(-dot));
+      sigma[t] = sg;
+      wrow[r] = sg;
+    }
   }
 }
 
@@ -387,9 +369,10 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(
 // (t, j) with expert e = offsets[e] + base[block][e] + (number of tokens
 // of this block before t that chose e).  Also fills, per grouped row, the
 // routing weight and the contribution row t*(k+has_shared)+j, and the rows of
-// the shared expert (T*k + t).
+// the shared expert (T*k + t; their weight, the gate, comes with the
+// permuted activations).
 __global__ void __launch_bounds__(256) scatter_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ w, const float* __restrict__ sigma,
+    const int32_t* __restrict__ idx, const float* __restrict__ w,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ base, int T, int E, int k,
     int has_shared, int32_t* __restrict__ perm, int32_t* __restrict__ slot,
     int32_t* __restrict__ dst, float* __restrict__ wrow) {
@@ -431,7 +414,6 @@ __global__ void __launch_bounds__(256) scatter_kernel(
       if (t < T) {
         const int row = T * k + t;
         perm[row] = t;
-        wrow[row] = sigma[t];
         dst[row] = t * k1 + k;
       }
     }
@@ -475,23 +457,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 }  // namespace
 
 cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
-                        const uint16_t* x, cudaStream_t st) {
+                        cudaStream_t st) {
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
-  if (x) {  // fp16 activations and the shared gate, in a kernel of their own
-    x16_sigma_kernel<<<(T + kCvtTokens - 1) / kCvtTokens, kCvtThreads, (size_t)c.d * 2, st>>>(
-        x, T, c.d, h->w_sg, c.has_shared, ws.sigma, ws.x16);
-    x = nullptr;
-  }
   const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
   if (c.E <= 256)
-    topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
-                                          c.has_shared, ws.logits, ws.idx, ws.w, ws.sigma,
-                                          ws.x16, ws.hist, h->dev_err);
+    topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, ws.logits, ws.idx,
+                                                  ws.w, ws.hist, h->dev_err);
   else
-    topk_kernel<16><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, x, c.d, h->w_sg,
-                                           c.has_shared, ws.logits, ws.idx, ws.w, ws.sigma,
-                                           ws.x16, ws.hist, h->dev_err);
+    topk_kernel<16><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, ws.logits, ws.idx,
+                                                   ws.w, ws.hist, h->dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const Handle* h, const uint16_t* x, int T, cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const Workspace& ws = h->ws;
+  const int R = T * (c.k + (c.has_shared ? 1 : 0));
+  permute_kernel<<<(R + kPermRows - 1) / kPermRows, kPermThreads, (size_t)c.d * 2, st>>>(
+      x, ws.perm, R, T * c.k, c.d, h->w_sg, c.has_shared, ws.sigma, ws.wrow, ws.xp);
   return cudaGetLastError();
 }
 
@@ -508,7 +492,7 @@ cudaError_t launch_scatter(const Handle* h, int T, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
   const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
-  scatter_kernel<<<nblk, 256, 0, st>>>(ws.idx, ws.w, ws.sigma, ws.offsets, ws.base, T, c.E, c.k,
+  scatter_kernel<<<nblk, 256, 0, st>>>(ws.idx, ws.w, ws.offsets, ws.base, T, c.E, c.k,
                                        c.has_shared, ws.perm, ws.slot, ws.dst, ws.wrow);
   return cudaGetLastError();
 }
@@ -596,12 +580,11 @@ extern "C" moe_status moe_route_from_logits_noalloc(const float* logits, int T, 
   int32_t* ntiles = reinterpret_cast<int32_t*>(s + kNaNtiles);
   // every scratch word is written before it is read: nothing to clear
   topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(
-      logits, 1, T, E, k, logit_bias, nullptr, 256, nullptr, 0,
-      reinterpret_cast<float*>(s + kNaLogits), idx, w, nullptr, nullptr, hist,
+      logits, 1, T, E, k, logit_bias, reinterpret_cast<float*>(s + kNaLogits), idx, w, hist,
       reinterpret_cast<int*>(s + kNaErr));
   scan_tiles_kernel<<<1, 1024, 0, st>>>(hist, nblk, T, E, k, 0, base, counts, offsets, tiles,
                                         ntiles);
-  scatter_kernel<<<nblk, 256, 0, st>>>(idx, w, nullptr, offsets, base, T, E, k, 0, perm, slot,
+  scatter_kernel<<<nblk, 256, 0, st>>>(idx, w, offsets, base, T, E, k, 0, perm, slot,
                                        reinterpret_cast<int32_t*>(s + kNaDst),
                                        reinterpret_cast<float*>(s + kNaWrow));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
