@@ -344,6 +344,108 @@ def run_prefill(args, torch, M, sd, gen, device, peaks):
         gpu_launches=7 * args.steps, clocks=clocks, device_error=err)
 
 
+SWEEP_T = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072]
+SWEEP_CHUNK = 8192
+
+
+def point_roofline(T, experts_touched, chunks, peaks):
+    """max(FLOP at peak, bytes at HBM bandwidth) for one call: the touched
+    experts' 4.5-bit weights (counted per chunk), the router per chunk, x in
+    and y out (bf16)."""
+    flop = FLOP_PER_TOKEN * T
+    nbytes = experts_touched * EXPERT_BYTES + chunks * ROUTER_BYTES + 4 * D * T
+    t_flop = flop / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = nbytes / (peaks["hbm_gbs"] * 1e9)
+    return max(t_flop, t_bytes), ("tensor" if t_flop >= t_bytes else "hbm")
+
+
+def time_call(torch, fn, flush, reps, stream):
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts) * 1000.0  # us
+
+
+def run_sweep(args, torch, M, sd, gen, device, peaks):
+    """The prefill length sweep (uniform and Zipf routing, chunks of 8192
+    tokens above that) and the T=32768 extreme-imbalance case (one
+    unchunked call).  Per point: us per call, tokens/s and the fraction of
+    that call's roofline."""
+    shape = gen.MoEShape(d=D, E=E, k=K, I=I)
+    w = sd.make_layer(0, 0, shape, device=device)
+    layer = M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=SWEEP_CHUNK,
+                              layouts=M.MOE_LAYOUT_PREFILL), w)
+    stress = M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=32768,
+                               layouts=M.MOE_LAYOUT_PREFILL), w)
+    del w
+    torch.cuda.empty_cache()
+    x = sd.make_x(0, max(SWEEP_T), D, device=device)
+    out = torch.empty_like(x)
+    flush = l2_flush_buffer(torch, device)
+    stream = torch.cuda.current_stream(device)
+    zipf = torch.from_numpy(gen.zipf_bias(0, E)).to(device)
+
+    def touched(lay, xs, bias, chunk):
+        n = 0
+        for t0 in range(0, xs.shape[0], chunk):
+            r = lay.route(xs[t0:t0 + chunk], bias)
+            n += int((r["counts"] > 0).sum().item()) + 1  # + the shared expert
+        return n
+
+    points = []
+    for routing, bias in (("uniform", None), ("zipf", zipf)):
+        for T in SWEEP_T:
+            xs, ys = x[:T], out[:T]
+            for _ in range(2):
+                layer.forward(xs, bias, out=ys)
+            us = time_call(torch, lambda: layer.forward(xs, bias, out=ys), flush,
+                           3 if T >= 32768 else 5, stream)
+            chunks = (T + SWEEP_CHUNK - 1) // SWEEP_CHUNK
+            t_roof, bound = point_roofline(T, touched(layer, xs, bias, SWEEP_CHUNK), chunks, peaks)
+            points.append({"routing": routing, "T": T, "us": round(us, 1),
+                           "tokens_per_s": round(T / (us * 1e-6), 1), "bound": bound,
+                           "roofline_frac": round(t_roof / (us * 1e-6), 4)})
+    # extreme imbalance: the 8 top-ranked experts share one bias, set by
+    # bisection on this layer's own logits of a 2048-token sample so that they
+    # take half of the assignments; the 64 bottom-ranked experts get -1e4
+    T = 32768
+    rank = torch.from_numpy(gen.expert_ranking(0, E)).to(device)
+    hot, cold = rank <= 8, rank > E - 64
+    lg = layer.route(x[:2048])["logits"]
+    lo, hi = -10.0, 20.0
+    for _ in range(40):
+        mid = 0.5 * (lo + hi)
+        b = torch.where(hot, torch.tensor(mid, device=device),
+                        torch.where(cold, torch.tensor(-1e4, device=device),
+                                    torch.tensor(0.0, device=device)))
+        share = hot[torch.topk(lg + b, K, dim=1).indices].float().mean().item()
+        lo, hi = (mid, hi) if share < 0.5 else (lo, mid)
+    bias = torch.where(hot, torch.tensor(0.5 * (lo + hi), device=device),
+                       torch.where(cold, torch.tensor(-1e4, device=device),
+                                   torch.tensor(0.0, device=device))).float()
+    xs, ys = x[:T], out[:T]
+    for _ in range(2):
+        stress.forward(xs, bias, out=ys)
+    us = time_call(torch, lambda: stress.forward(xs, bias, out=ys), flush, 3, stream)
+    counts = stress.route(xs, bias)["counts"]
+    t_roof, bound = point_roofline(T, int((counts > 0).sum().item()) + 1, 1, peaks)
+    hot_share = float(counts[hot].sum().item()) / (T * K)
+    stress_pt = {"T": T, "us": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
+                 "bound": bound, "roofline_frac": round(t_roof / (us * 1e-6), 4),
+                 "hot_share": round(hot_share, 3),
+                 "empty_experts": int((counts == 0).sum().item())}
+    layer.close()
+    stress.close()
+    return points, stress_pt
+
+
 # ------------------------------------------------------------------ oracle arm
 def cpu_threads():
     try:
@@ -443,6 +545,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
     ap.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
                     help="layers of the decode chain (profiling captures use fewer)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the prefill length sweep and the imbalance case")
     args = ap.parse_args()
     ws, rank, local = dist_info()
     args.world = ws
@@ -480,6 +584,7 @@ def main():
     runner = {"decode": run_decode, "prefill": run_prefill}
     res = runner[primary](args, torch, M, sd, gen, device, peaks)
     sec = runner[secondary](args, torch, M, sd, gen, device, peaks) if secondary else None
+    sweep = None if args.no_sweep else run_sweep(args, torch, M, sd, gen, device, peaks)
 
     if rank != 0:
         return 0
@@ -507,6 +612,15 @@ def main():
                     "max_expert_rows"):
             if key in sec:
                 line[secondary][key] = sec[key]
+    if sweep is not None:
+        line["prefill_sweep"] = {
+            "config": "same layer as the prefill line; T in 256..128K, uniform and Zipf "
+                      "routing, chunks of 8192 tokens above that; one call per point, "
+                      "L2 flushed between calls, median of 3-5",
+            "points": sweep[0]}
+        line["imbalance_T32768"] = dict(
+            sweep[1], config="8 hot experts take half of the assignments, 64 experts get "
+                             "none; one unchunked call")
     if ws == 1:
         try:
             line["cpu_baseline"] = cpu_baseline(primary)
