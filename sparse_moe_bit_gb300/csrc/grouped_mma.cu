@@ -27,14 +27,13 @@
 //   warp 0       B producer (the warp's lanes issue the 16-row TMA tiles)
 //                and, for the router, the A bulk copies
 //   warp 1       lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
-//   warp 2       down: lane 0 issues the bulk copies of the code ring
-//   warps 4..11  dequantise the weight codes into fp16 A tiles (128-byte
-//                swizzled, K-major): gate/up one row per thread (codes loaded
-//                from global memory three K blocks ahead, in registers);
-//                down half a row per thread (codes from the ring)
+//   warp 2       lane 0 issues the bulk copies of the code ring
+//   warps 4..11  dequantise the weight codes from the ring into fp16 A tiles
+//                (128-byte swizzled, K-major): gate/up one row per thread,
+//                down half a row per thread
 //   warps 12..19 epilogue: tcgen05.ld, activation / scaling, staging in
 //                shared memory, 16-byte stores of 64-byte row segments
-// Rings: A 2 stages, B 4 stages (down: 3, and 8 stages of codes).  TMEM: two
+// Rings: A 2 stages, B 3 stages, codes 4 (gate/up) or 8 (down).  TMEM: two
 // fp32 accumulators of 256 columns (gate/up and router: tiles A0 and A1 of
 // one unit; down: two units in turn).
 #include <cuda_bf16.h>
@@ -66,16 +65,18 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 //        columns (one tile), so that the down projection's epilogue (the
 //        contribution rows, the largest write of the block) overlaps the
 //        next unit's MMAs
-//   CST  stages of the down projection's code ring: the codes and scale/bias
-//        words of a unit's half chunk arrive by bulk copy (4.5 KB per K
-//        block), far enough ahead to hide the memory latency that limited
-//        dequantisation from registers loaded three K blocks ahead
+//   CST  stages of the code ring: the codes and scale/bias words of a unit's
+//        chunk (gate/up: 256 rows, 9 KB per K block) or half chunk (down:
+//        4.5 KB) arrive by bulk copy, far enough ahead to hide the memory
+//        latency that limited dequantisation from registers loaded three K
+//        blocks ahead (cold experts at small T come from HBM)
 template <int MODE>
 struct Cfg {
   static constexpr int NA = (MODE == MMA_DOWN) ? 1 : 2;
   static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
-  static constexpr int CST = (MODE == MMA_DOWN) ? 8 : 0;
-  static constexpr int B_STAGES = (MODE == MMA_DOWN) ? 3 : 4;
+  static constexpr int CST = (MODE == MMA_DOWN) ? 8 : (MODE == MMA_GATEUP ? 4 : 0);
+  static constexpr int CODE_STAGE = NA * kHalfChunk;
+  static constexpr int B_STAGES = 3;
   static constexpr int A_STAGE = NA * 16384;
   // epilogue: per chunk of 16 rows, NSEG 64-byte segments per row (down: one
   // per weight tile; gate/up: one, the SwiGLU of the tile pair)
@@ -84,7 +85,7 @@ struct Cfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + kAStages * A_STAGE;
   static constexpr int OFF_CODE = OFF_B + B_STAGES * kBStage;
-  static constexpr int OFF_STAGE = OFF_CODE + CST * kHalfChunk;
+  static constexpr int OFF_STAGE = OFF_CODE + CST * CODE_STAGE;
   static constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * 2 * STAGE_BUF;
   static constexpr int NUM_BARS = 2 * kAStages + 2 * B_STAGES + 2 * NACC + 2 * CST + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
@@ -136,7 +137,7 @@ struct Smem {
   __device__ uint32_t acc_empty(int b) const {
     return bar(2 * kAStages + 2 * C::B_STAGES + C::NACC + b);
   }
-  __device__ uint32_t code(int s) const { return base + C::OFF_CODE + s * kHalfChunk; }
+  __device__ uint32_t code(int s) const { return base + C::OFF_CODE + s * C::CODE_STAGE; }
   __device__ uint32_t c_full(int s) const {
     return bar(2 * kAStages + 2 * C::B_STAGES + 2 * C::NACC + s);
   }
@@ -417,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       tc_commit(S.drain());
       mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
     }
-  } else if (warp == 2 && MODE == MMA_DOWN) {
-    // ------------------------------------------------ code ring (down)
+  } else if (warp == 2 && MODE != MMA_ROUTER) {
+    // ------------------------------------------------ code ring
     if (lane == 0) {
       const int total = nmy * kbu;
       for (int g = 0; g < total; ++g) {
@@ -427,14 +428,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         if (!thread_wait(S.c_empty(s), ((g / kCst) & 1) ^ 1, abort_flag, p.err)) break;
         const int j = g / kbu;
         const Unit u = get_unit(p, MODE, cunit(j) * CL + crank);
-        // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, then s,b words
-        const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
-                            (long long)(u.m >> 1) * p.a_unit_stride +
-                            (long long)(g - j * kbu) * p.a_chunk;
-        const int h = u.m & 1;
-        mbar_arrive_expect_tx(S.c_full(s), kHalfChunk);
-        bulk_g2s(S.code(s), ch + h * 4096, 4096, S.c_full(s));
-        bulk_g2s(S.code(s) + 4096, ch + 8192 + h * 512, 512, S.c_full(s));
+        if (C::NA == 2) {  // the whole chunk of unit m
+          const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
+                              (long long)u.m * p.a_unit_stride +
+                              (long long)(g - j * kbu) * p.a_chunk;
+          mbar_arrive_expect_tx(S.c_full(s), kCodeChunk);
+          bulk_g2s(S.code(s), ch, kCodeChunk, S.c_full(s));
+        } else {  // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, s,b words
+          const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
+                              (long long)(u.m >> 1) * p.a_unit_stride +
+                              (long long)(g - j * kbu) * p.a_chunk;
+          const int h = u.m & 1;
+          mbar_arrive_expect_tx(S.c_full(s), kHalfChunk);
+          bulk_g2s(S.code(s), ch + h * 4096, 4096, S.c_full(s));
+          bulk_g2s(S.code(s) + 4096, ch + 8192 + h * 512, 512, S.c_full(s));
+        }
       }
     }
   } else if (warp >= 4 && warp < 4 + kDeqWarps) {
@@ -449,21 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       struct Codes {
         uint4 a0, a1;
         uint32_t sa;
-      };
-      // gate/up: source chunk of the CTA's global K-block number g, loaded
-      // straight into registers (chunks hold 256 rows, one unit)
-      auto load = [&](int g, Codes& c) {
-        if (g < total) {
-          const int j = g / kbu;
-          const Unit u = get_unit(p, MODE, cunit(j) * CL + crank);
-          const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
-                              (long long)u.m * p.a_unit_stride +
-                              (long long)(g - j * kbu) * p.a_chunk;
-          const uint4* ra = reinterpret_cast<const uint4*>(ch + row * 32);
-          c.a0 = __ldg(ra);
-          c.a1 = __ldg(ra + 1);
-          c.sa = __ldg(reinterpret_cast<const uint32_t*>(ch + 8192) + row);
-        }
       };
       // words w[i] (K 8 (4 kh + i) .. +7) of row r -> swizzled 16-byte chunks
       auto emit = [&](uint32_t a, int r, const Codes& cc) {
@@ -481,41 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
                        dequant_pair(w[i], 3, s2, b2));
         }
       };
-      if (C::CST == 0) {
-        Codes c0, c1, c2;
-        load(0, c0);
-        load(1, c1);
-        load(2, c2);
-        uint32_t ga = 0;
-        for (int g = 0; g < total; ++g, ++ga) {
-          const Codes cur = c0;
-          c0 = c1;
-          c1 = c2;
-          load(g + 3, c2);
-          const int sa = ga % kAStages;
-          if (!warp_wait(S.a_empty(sa), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) break;
-          emit(S.a(sa), row, cur);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(S.a_full(sa));
-        }
-      } else {
-        for (int g = 0; g < total; ++g) {
-          const int sc = g % (C::CST > 0 ? C::CST : 1), sa = g % kAStages;
-          if (!warp_wait(S.c_full(sc), (g / (C::CST > 0 ? C::CST : 1)) & 1, abort_flag, p.err) ||
-              !warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err))
-            break;
-          Codes cur;
-          cur.a0 = ld_shared_v4(S.code(sc) + row * 32 + kh * 16);
-          cur.a1 = cur.a0;
-          cur.sa = ld_shared_u32(S.code(sc) + 4096 + row * 4);
-          emit(S.a(sa), row, cur);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(S.c_empty(sc));
-            mbar_arrive(S.a_full(sa));
-          }
+      constexpr int kCst = C::CST > 0 ? C::CST : 1;
+      for (int g = 0; g < total; ++g) {
+        const int sc = g % kCst, sa = g % kAStages;
+        if (!warp_wait(S.c_full(sc), (g / kCst) & 1, abort_flag, p.err) ||
+            !warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err))
+          break;
+        Codes cur;  // row `row` of the ring stage: codes, then the s,b word
+        cur.a0 = ld_shared_v4(S.code(sc) + row * 32 + kh * 16);
+        cur.a1 = (C::NA == 2) ? ld_shared_v4(S.code(sc) + row * 32 + 16) : cur.a0;
+        cur.sa = ld_shared_u32(S.code(sc) + 32 * 128 * C::NA + row * 4);
+        emit(S.a(sa), row, cur);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(S.c_empty(sc));
+          mbar_arrive(S.a_full(sa));
         }
       }
     }
