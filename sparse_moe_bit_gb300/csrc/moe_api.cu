@@ -83,7 +83,7 @@ void free_handle(Handle* h) {
                   h->w_router, h->w_sg, h->dev_err, h->ws.logit_part, h->ws.logits,
                   h->ws.idx, h->ws.w, h->ws.sigma, h->ws.xp, h->ws.hist, h->ws.base,
                   h->ws.counts, h->ws.offsets, h->ws.perm, h->ws.slot, h->ws.dst, h->ws.wrow,
-                  h->ws.tiles, h->ws.ntiles, h->ws.H, h->ws.Y, h->ws.x_dev, h->ws.y_dev,
+                  h->ws.tiles, h->ws.ntiles, h->ws.ticket, h->ws.H, h->ws.Y, h->ws.x_dev, h->ws.y_dev,
                   h->ws.bias_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -164,6 +164,8 @@ moe_status alloc_all(Handle* h) {
   CK(dalloc(&w.wrow, (size_t)T * k1 * 4), "alloc");
   CK(dalloc(&w.tiles, (size_t)w.max_tiles * sizeof(int4)), "alloc");
   CK(dalloc(&w.ntiles, 16), "alloc");
+  CK(dalloc(&w.ticket, 16), "alloc");
+  CK(cudaMemset(w.ticket, 0, 16), "memset");
   if (h->layouts & MOE_LAYOUT_PREFILL) {
     CK(dalloc(&w.xp, (size_t)T * k1 * c.d * 2), "alloc");
     CK(dalloc(&w.H, (size_t)T * k1 * c.I * 2), "alloc");

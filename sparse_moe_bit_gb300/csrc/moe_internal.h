@@ -37,6 +37,7 @@ struct Workspace {
   float* wrow = nullptr;        // [Tmax*(k+1)] grouped row -> routing weight
   int4* tiles = nullptr;        // [max_tiles] {expert, row0, nrows, npad}
   int32_t* ntiles = nullptr;    // [1]
+  unsigned* ticket = nullptr;   // [1] blocks of the scan done (zero between calls)
   uint16_t* H = nullptr;        // [Tmax*(k+1)][I] fp16 SwiGLU activations
   uint16_t* Y = nullptr;        // [Tmax*(k+1)][d] bf16 weighted contributions
   int max_tiles = 0;

@@ -260,45 +260,52 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
 // each expert's remainder tile, larger remainders first (ties in expert
 // order).  The shared expert (index E, all T tokens, rows T*k..T*k+T-1)
 // takes part like any expert.
-// The scan over blocks: P = 1024 / E threads per expert (thread p*E + e),
-// each over a contiguous range of blocks, 16 loads in flight at a time; the
-// ranges' sums are exchanged in shared memory, then each thread writes its
-// range's bases from its range prefix.
+// The scan over blocks is split by experts over the grid: block g takes
+// experts [g*EB, (g+1)*EB) with P = 1024 / EB threads per expert (thread
+// p*EB + e), each over a contiguous range of blocks, 16 loads in flight at a
+// time; the ranges' sums are exchanged in shared memory, then each thread
+// writes its range's bases from its range prefix.  The last block to finish
+// (a ticket counter, reset by that block for the next call) computes the
+// offsets and the tile map from every expert's count.
 constexpr int kScanBatch = 16;
 __global__ void __launch_bounds__(1024) scan_tiles_kernel(
     const int32_t* __restrict__ hist, int nblk, int T, int E, int k, int has_shared,
     int32_t* __restrict__ base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int4* __restrict__ tiles, int32_t* __restrict__ ntiles) {
+    int4* __restrict__ tiles, int32_t* __restrict__ ntiles, unsigned* __restrict__ ticket) {
   __shared__ int warp_tot[32];
   __shared__ int s_total;
   __shared__ int s_clsb[17];
   __shared__ int s_part[1024];
   __shared__ int s_wcls[32][16];  // per warp: experts of each remainder class
+  __shared__ int s_last;
   const int tid = threadIdx.x;
   const int nexp = E + (has_shared ? 1 : 0);
 
-  const int P = blockDim.x / E;  // >= 2 (E <= 512)
-  const int pe = tid % E, pp = tid / E;
+  const int EB = (E + gridDim.x - 1) / gridDim.x;  // experts of this block
+  const int e0 = blockIdx.x * EB, ne = min(E, e0 + EB) - e0;
+  const int P = blockDim.x / EB;  // >= 2 (EB <= 512)
+  const int pe = tid % EB, pp = tid / EB;
+  const int ex = e0 + pe;
   const int nbp = (nblk + P - 1) / P;
   const int b0 = pp * nbp, b1 = min(nblk, b0 + nbp);
+  const bool mine = pp < P && pe < ne;
   int part = 0;
-  if (pp < P) {
+  if (mine) {
     for (int b = b0; b < b1; b += kScanBatch) {
       int c[kScanBatch];
 #pragma unroll
       for (int q = 0; q < kScanBatch; ++q)
-        c[q] = (b + q < b1) ? hist[(long long)(b + q) * E + pe] : 0;
+        c[q] = (b + q < b1) ? hist[(long long)(b + q) * E + ex] : 0;
 #pragma unroll
       for (int q = 0; q < kScanBatch; ++q) part += c[q];
     }
-    s_part[tid] = part;
   }
+  if (tid < P * EB) s_part[tid] = part;
   __syncthreads();
-  int cnt = 0;
-  if (pp < P) {
+  if (mine) {
     int pre = 0, tot = 0;
     for (int q = 0; q < P; ++q) {
-      const int v = s_part[q * E + pe];
+      const int v = s_part[q * EB + pe];
       pre += (q < pp) ? v : 0;
       tot += v;
     }
@@ -307,19 +314,30 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(
       int c[kScanBatch];
 #pragma unroll
       for (int q = 0; q < kScanBatch; ++q)
-        c[q] = (b + q < b1) ? hist[(long long)(b + q) * E + pe] : 0;
+        c[q] = (b + q < b1) ? hist[(long long)(b + q) * E + ex] : 0;
 #pragma unroll
       for (int q = 0; q < kScanBatch; ++q) {
-        if (b + q < b1) base[(long long)(b + q) * E + pe] = run;
+        if (b + q < b1) base[(long long)(b + q) * E + ex] = run;
         run += c[q];
       }
     }
-    if (pp == 0) {
-      counts[pe] = tot;
-      cnt = tot;  // thread e (< E) continues with its expert's count
-    }
+    if (pp == 0) counts[ex] = tot;
   }
+  // the last block continues with every expert's count
+  if (gridDim.x > 1) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  } else {
+    __syncthreads();
+  }
+  int cnt = 0;
+  if (tid < E) cnt = __ldcg(counts + tid);
   if (tid == E && has_shared) cnt = T;
+  if (tid == 0 && gridDim.x > 1) *ticket = 0u;  // for the next call
   __syncthreads();
   // offsets over the routed experts
   const int off = block_exclusive_scan(tid < E ? cnt : 0, warp_tot, &s_total);
@@ -483,8 +501,9 @@ cudaError_t launch_scan_tiles(const Handle* h, int T, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
   const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
-  scan_tiles_kernel<<<1, 1024, 0, st>>>(ws.hist, nblk, T, c.E, c.k, c.has_shared, ws.base,
-                                        ws.counts, ws.offsets, ws.tiles, ws.ntiles);
+  const int nb = c.E >= 64 ? (c.E / 32 < 8 ? c.E / 32 : 8) : 1;  // experts split over blocks
+  scan_tiles_kernel<<<nb, 1024, 0, st>>>(ws.hist, nblk, T, c.E, c.k, c.has_shared, ws.base,
+                                         ws.counts, ws.offsets, ws.tiles, ws.ntiles, ws.ticket);
   return cudaGetLastError();
 }
 
@@ -583,7 +602,7 @@ extern "C" moe_status moe_route_from_logits_noalloc(const float* logits, int T, 
       logits, 1, T, E, k, logit_bias, reinterpret_cast<float*>(s + kNaLogits), idx, w, hist,
       reinterpret_cast<int*>(s + kNaErr));
   scan_tiles_kernel<<<1, 1024, 0, st>>>(hist, nblk, T, E, k, 0, base, counts, offsets, tiles,
-                                        ntiles);
+                                        ntiles, nullptr);
   scatter_kernel<<<nblk, 256, 0, st>>>(idx, w, offsets, base, T, E, k, 0, perm, slot,
                                        reinterpret_cast<int32_t*>(s + kNaDst),
                                        reinterpret_cast<float*>(s + kNaWrow));
