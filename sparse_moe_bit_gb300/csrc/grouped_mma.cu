@@ -74,6 +74,7 @@ template <int MODE>
 struct Cfg {
   static constexpr int NA = (MODE == MMA_DOWN) ? 1 : 2;
   static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
+  static constexpr int NISS = NA;  // MMA-issuing threads (one per weight tile)
   static constexpr int CST = (MODE == MMA_DOWN) ? 8 : (MODE == MMA_GATEUP ? 4 : 0);
   static constexpr int CODE_STAGE = NA * kHalfChunk;
   static constexpr int B_STAGES = 3;
@@ -306,21 +307,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(S.a_full(s), MODE == MMA_ROUTER ? 1 : kDeqWarps);
-      mbar_init(S.a_empty(s), 1);
+      mbar_init(S.a_empty(s), C::NISS);
     }
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(S.b_full(s), 1);
-      mbar_init(S.b_empty(s), CL);
+      mbar_init(S.b_empty(s), CL * C::NISS);
     }
     for (int b = 0; b < C::NACC; ++b) {
-      mbar_init(S.acc_full(b), 1);
+      mbar_init(S.acc_full(b), C::NISS);
       mbar_init(S.acc_empty(b), kEpiWarps);
     }
     for (int s = 0; s < C::CST; ++s) {
       mbar_init(S.c_full(s), 1);
       mbar_init(S.c_empty(s), kDeqWarps);
     }
-    mbar_init(S.drain(), 1);
+    mbar_init(S.drain(), C::NISS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -375,10 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         ++gb;
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (warp == 3 && C::NISS == 2)) {
     // ---------------------------------------------------------- MMA issuer
+    // With two weight tiles per unit, lane 0 of warp 1 issues tile 0's MMAs
+    // and lane 0 of warp 3 tile 1's: a single thread issues a tcgen05.mma
+    // no faster than one per ~56 cycles (measured), which bounded the small
+    // tiles; two issuers on separate accumulators overlap.
     if (lane == 0) {
-      uint32_t ga = 0, gb = 0;
+      const int q = (warp == 1) ? 0 : 1;  // this issuer's tile (two-tile units)
+      uint32_t sa = 0, pa = 0, sb = 0, pb = 0;  // ring slots and phase parities
       Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
       for (int i = 0; i < nmy; ++i) {
         const Unit t = tn;  // the next unit's descriptor loads during this one
@@ -389,27 +395,30 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         tc_fence_after();
         const uint32_t idesc = idesc_f16(128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
         bool ok = true;
-        for (int kb = 0; kb < kbu; ++kb, ++ga, ++gb) {
-          const int sa = ga % kAStages, sb = gb % kBStages;
-          if (!thread_wait(S.a_full(sa), (ga / kAStages) & 1, abort_flag, p.err) ||
-              !thread_wait(S.b_full(sb), (gb / kBStages) & 1, abort_flag, p.err)) {
+        for (int kb = 0; kb < kbu; ++kb) {
+          if (!thread_wait(S.a_full(sa), pa, abort_flag, p.err) ||
+              !thread_wait(S.b_full(sb), pb, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          // K step kk: both operands advance by 32 bytes (2 in the
+          // descriptor's address field, which holds the address / 16)
+          const uint64_t bd = sdesc_k_sw128(S.b(sb));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_k_sw128(S.b(sb) + kk * 32);
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
+          for (int j = 0; j < C::NA; ++j) {
+            if (C::NISS == 2 && j != q) continue;
+            const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384);
+            // NA == 2: tile j -> columns 256 j; NACC == 2: buffer ab -> columns 256 ab
+            const uint32_t dcol = tmem + 256 * (C::NA == 2 ? j : ab);
 #pragma unroll
-            for (int j = 0; j < C::NA; ++j) {
-              const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384 + kk * 32);
-              // NA == 2: tile j -> columns 256 j; NACC == 2: buffer ab -> columns 256 ab
-              tc_mma_f16(tmem + 256 * (C::NA == 2 ? j : ab), ad, bd, idesc, acc);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f16(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           }
           tc_commit(S.a_empty(sa));
           tc_commit_cluster<CL>(S.b_empty(sb));
+          if (++sa == kAStages) { sa = 0; pa ^= 1; }
+          if (++sb == (uint32_t)kBStages) { sb = 0; pb ^= 1; }
         }
         if (!ok) break;
         tc_commit(S.acc_full(ab));
