@@ -197,14 +197,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// fp16 pair (q_lo, q_hi) * s + beta from the nibbles at bit 4j and 16+4j
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t v, int j, uint32_t s2, uint32_t b2) {
-  const uint32_t t = ((v >> (4 * j)) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-  __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&t),
-                      __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  __half2 r = __hfma2(q, *reinterpret_cast<const __half2*>(&s2),
-                      *reinterpret_cast<const __half2*>(&b2));
-  return *reinterpret_cast<uint32_t*>(&r);
+// The four fp16 pairs s*q + beta of the 8 codes of word v (pair j = K
+// indices 2j, 2j+1 in the nibbles at bits 4j and 16+4j).  A nibble ORed
+// into the low mantissa bits of 1024.0 (ulp 1) gives 1024 + q; the nibble
+// at bits 4..7 ORed into 64.0 (ulp 1/16) gives 64 + q: so pairs 0 and 1
+// need no shift and pairs 2 and 3 one 8-bit shift of the word.  One
+// subtraction makes q exact, one fused multiply-add rounds s*q + beta once.
+__device__ __forceinline__ uint4 dequant_word(uint32_t v, uint32_t s2, uint32_t b2) {
+  const uint32_t v8 = v >> 8;
+  const uint32_t t[4] = {(v & 0x000F000Fu) | 0x64006400u, (v & 0x00F000F0u) | 0x54005400u,
+                         (v8 & 0x000F000Fu) | 0x64006400u, (v8 & 0x00F000F0u) | 0x54005400u};
+  const __half2 m1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const __half2 m64 = __halves2half2(__ushort_as_half(0x5400), __ushort_as_half(0x5400));
+  uint32_t r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&t[j]), (j & 1) ? m64 : m1024);
+    const __half2 h = __hfma2(q, *reinterpret_cast<const __half2*>(&s2),
+                              *reinterpret_cast<const __half2*>(&b2));
+    r[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 // TMA load of B: a 2-D tile (16 rows).  With CL > 1 the data is multicast to
@@ -478,9 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
           const int c = 4 * kh + i;
-          st_shared_v4(rowb + ((c ^ (r & 7)) << 4), dequant_pair(w[i], 0, s2, b2),
-                       dequant_pair(w[i], 1, s2, b2), dequant_pair(w[i], 2, s2, b2),
-                       dequant_pair(w[i], 3, s2, b2));
+          const uint4 d4 = dequant_word(w[i], s2, b2);
+          st_shared_v4(rowb + ((c ^ (r & 7)) << 4), d4.x, d4.y, d4.z, d4.w);
         }
       };
       constexpr int kCst = C::CST > 0 ? C::CST : 1;
