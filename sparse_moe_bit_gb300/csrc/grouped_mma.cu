@@ -51,44 +51,66 @@ constexpr int kThreads = 640;
 constexpr int kDeqWarps = 8;   // warps 4 .. 11
 constexpr int kEpiWarp0 = 12;  // warps 12 .. 19
 constexpr int kHalfChunk = 4608;  // 128 rows x (32 B codes + 4 B scale/bias)
-constexpr int kAStages = 2;
-constexpr int kBStage = 32768;   // up to 256 x 64 x 16-bit
 constexpr int kEpiWarps = 8;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Per-mode shape of a work unit and of the pipeline:
-//   NA   128-row weight tiles per unit (gate/up: the gate and the up tile of
-//        the same features; router: 256 experts; down: 128 output rows, one
-//        half of a 256-row code chunk)
-//   NACC TMEM accumulator buffers: two fit when a unit needs only 256
-//        columns (one tile), so that the down projection's epilogue (the
-//        contribution rows, the largest write of the block) overlaps the
-//        next unit's MMAs
-//   CST  stages of the code ring: the codes and scale/bias words of a unit's
-//        chunk (gate/up: 256 rows, 9 KB per K block) or half chunk (down:
-//        4.5 KB) arrive by bulk copy, far enough ahead to hide the memory
-//        latency that limited dequantisation from registers loaded three K
-//        blocks ahead (cold experts at small T come from HBM)
-template <int MODE>
+//   NA     128-row weight tiles per unit (gate/up: the gate and the up tile
+//          of the same features; router: 256 experts; down: 128 output
+//          rows, one half of a 256-row code chunk)
+//   NACC   TMEM accumulator buffers: two when a unit needs one tile, so that
+//          the down projection's epilogue (the contribution rows, the
+//          largest write of the block) overlaps the next unit's MMAs
+//   NMAX   TMEM columns of one accumulator (the widest token tile)
+//   TMEM_A the dequantised weight tile (the MMA's A operand) is written by
+//          the dequantising threads straight into tensor memory (128 lanes x
+//          32 columns per tile and K block, two fp16 per column), so that it
+//          neither passes through shared memory nor is read from it by the
+//          tensor core: shared-memory bandwidth, not the MMA rate, bounded
+//          both grouped GEMMs with the A tiles in shared memory.  The TMEM
+//          budget (512 columns) then holds the accumulators for token tiles
+//          of up to 192 rows plus A_STAGES A stages.  The router's bf16 A
+//          arrives pre-swizzled by bulk copy and stays in shared memory.
+//   CST    stages of the code ring: the codes and scale/bias words of a
+//          unit's chunk (gate/up: 256 rows, 9 KB per K block) or half chunk
+//          (down: 4.5 KB) arrive by bulk copy, far enough ahead to hide the
+//          memory latency (cold experts at small T come from HBM)
+template <int MODE, bool PAIR>
 struct Cfg {
+  static constexpr bool TMEM_A = MODE != MMA_ROUTER;
   static constexpr int NA = (MODE == MMA_DOWN) ? 1 : 2;
   static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
   static constexpr int NISS = NA;  // MMA-issuing threads (one per weight tile)
-  static constexpr int CST = (MODE == MMA_DOWN) ? 8 : (MODE == MMA_GATEUP ? 4 : 0);
+  static constexpr int NMAX = TMEM_A ? kTileRows : 256;
+  static constexpr int A_COLS = NA * 32;  // TMEM columns of one A stage
+  static constexpr int A_COL0 = NMAX * (NA == 2 ? 2 : NACC);
+  // as many A stages as the rest of TMEM holds (at most 8): the ring's depth
+  // bounds the pipeline, whose round trip (dequantise, signal, MMA, commit)
+  // is longer than one K block's MMAs
+  static constexpr int A_STAGES =
+      TMEM_A ? ((512 - A_COL0) / A_COLS < 8 ? (512 - A_COL0) / A_COLS : 8) : 2;
+  static_assert(!TMEM_A || A_COL0 + A_STAGES * A_COLS <= 512, "TMEM budget");
+  static_assert(TMEM_A || NA * NMAX <= 512, "TMEM budget");
+  static constexpr int CST = (MODE == MMA_DOWN) ? 8 : (MODE == MMA_GATEUP ? 6 : 0);
   static constexpr int CODE_STAGE = NA * kHalfChunk;
-  static constexpr int B_STAGES = 3;
-  static constexpr int A_STAGE = NA * 16384;
+  // B ring: up to NMAX token rows (a pair's CTA holds half of them) x 64 K
+  static constexpr int B_STAGES = PAIR ? 8 : (TMEM_A ? 4 : 3);
+  static constexpr int B_STAGE = (PAIR ? NMAX / 2 : NMAX) * 128;
+  static constexpr int A_STAGE = TMEM_A ? 0 : NA * 16384;  // shared-memory A (router)
   // epilogue: per chunk of 16 rows, NSEG 64-byte segments per row (down: one
   // per weight tile; gate/up: one, the SwiGLU of the tile pair)
   static constexpr int NSEG = (MODE == MMA_DOWN) ? NA : 1;
   static constexpr int STAGE_BUF = 16 * 64 * NSEG;
+  // columns of the accumulator taken by each of the two epilogue halves
+  static constexpr int EPI_COLS = TMEM_A ? NMAX / 2 : 128;
+  static_assert(EPI_COLS % 16 == 0 && EPI_COLS <= 128, "epilogue column split");
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + kAStages * A_STAGE;
-  static constexpr int OFF_CODE = OFF_B + B_STAGES * kBStage;
+  static constexpr int OFF_B = OFF_A + A_STAGES * A_STAGE;
+  static constexpr int OFF_CODE = OFF_B + B_STAGES * B_STAGE;
   static constexpr int OFF_STAGE = OFF_CODE + CST * CODE_STAGE;
   static constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * 2 * STAGE_BUF;
-  static constexpr int NUM_BARS = 2 * kAStages + 2 * B_STAGES + 2 * NACC + 2 * CST + 1;
+  static constexpr int NUM_BARS = 2 * A_STAGES + 2 * B_STAGES + 2 * NACC + 2 * CST + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -98,7 +120,9 @@ struct Unit {
   int expert, row0, nrows, npad, m, ks;
 };
 
-__device__ __forceinline__ Unit get_unit(const MmaParams& p, int mode, int u) {
+// pad: token rows per MMA column step of the tile (16; 32 for CTA pairs, whose
+// two halves of B must each be whole 16-row slabs)
+__device__ __forceinline__ Unit get_unit(const MmaParams& p, int mode, int u, int pad) {
   Unit o;
   const int tile = u / p.units_per_tile;
   const int r = u - tile * p.units_per_tile;
@@ -116,34 +140,36 @@ __device__ __forceinline__ Unit get_unit(const MmaParams& p, int mode, int u) {
     o.ks = 0;
     o.m = r;
   }
-  o.npad = (o.nrows + 15) & ~15;
+  o.npad = (o.nrows + pad - 1) & ~(pad - 1);
   return o;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 struct Smem {
-  using C = Cfg<MODE>;
+  using C = Cfg<MODE, PAIR>;
   uint32_t base;
   __device__ uint32_t a(int s) const { return base + C::OFF_A + s * C::A_STAGE; }
-  __device__ uint32_t b(int s) const { return base + C::OFF_B + s * kBStage; }
+  __device__ uint32_t b(int s) const { return base + C::OFF_B + s * C::B_STAGE; }
   __device__ uint32_t stage(int w, int i) const {
     return base + C::OFF_STAGE + (w * 2 + i) * C::STAGE_BUF;
   }
   __device__ uint32_t bar(int i) const { return base + C::OFF_BAR + 8 * i; }
   __device__ uint32_t a_full(int s) const { return bar(s); }
-  __device__ uint32_t a_empty(int s) const { return bar(kAStages + s); }
-  __device__ uint32_t b_full(int s) const { return bar(2 * kAStages + s); }
-  __device__ uint32_t b_empty(int s) const { return bar(2 * kAStages + C::B_STAGES + s); }
-  __device__ uint32_t acc_full(int b) const { return bar(2 * kAStages + 2 * C::B_STAGES + b); }
+  __device__ uint32_t a_empty(int s) const { return bar(C::A_STAGES + s); }
+  __device__ uint32_t b_full(int s) const { return bar(2 * C::A_STAGES + s); }
+  __device__ uint32_t b_empty(int s) const { return bar(2 * C::A_STAGES + C::B_STAGES + s); }
+  __device__ uint32_t acc_full(int b) const {
+    return bar(2 * C::A_STAGES + 2 * C::B_STAGES + b);
+  }
   __device__ uint32_t acc_empty(int b) const {
-    return bar(2 * kAStages + 2 * C::B_STAGES + C::NACC + b);
+    return bar(2 * C::A_STAGES + 2 * C::B_STAGES + C::NACC + b);
   }
   __device__ uint32_t code(int s) const { return base + C::OFF_CODE + s * C::CODE_STAGE; }
   __device__ uint32_t c_full(int s) const {
-    return bar(2 * kAStages + 2 * C::B_STAGES + 2 * C::NACC + s);
+    return bar(2 * C::A_STAGES + 2 * C::B_STAGES + 2 * C::NACC + s);
   }
   __device__ uint32_t c_empty(int s) const {
-    return bar(2 * kAStages + 2 * C::B_STAGES + 2 * C::NACC + C::CST + s);
+    return bar(2 * C::A_STAGES + 2 * C::B_STAGES + 2 * C::NACC + C::CST + s);
   }
   __device__ uint32_t drain() const { return bar(C::NUM_BARS - 1); }
 };
@@ -220,6 +246,18 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t v, uint32_t s2, uint32_t 
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// silu(z) = z sigmoid(z) = z/2 (1 + tanh(z/2)): one special-function
+// instruction per value (the hardware tanh approximation, relative error
+// about 2^-11, the rounding of the fp16 result) instead of an exponential
+// and a reciprocal -- the gate/up epilogue, which the MMAs wait for, was
+// bound by that unit.
+__device__ __forceinline__ float silu_tanh(float z) {
+  const float hz = 0.5f * z;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hz));
+  return fmaf(hz, t, hz);
+}
+
 // TMA load of B: a 2-D tile (16 rows).  With CL > 1 the data is multicast to
 // the same shared-memory offset of every CTA of the cluster and each CTA's
 // barrier at `bar` receives its bytes.
@@ -240,6 +278,18 @@ __device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm,
         "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
         : "memory");
   }
+}
+
+// TMA load of this CTA's half of a pair's B tile (a 16-row slab into its own
+// shared memory); the bytes are counted on the barrier at `bar_cluster`, a
+// shared::cluster address in either CTA of the pair (the MMA-issuing one).
+__device__ __forceinline__ void tma_tile_2d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
 }
 
 // tcgen05 commit that arrives on `bar` in every CTA of the cluster
@@ -285,14 +335,29 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
 // (consecutive weight units m), each fetching every CL-th 16-row slab of B and
 // multicasting it to all of them; a B slot is reused only after every CTA's
 // MMAs have read it (each MMA commit arrives on the slot's barrier in all CTAs).
-template <int MODE, int CL>
+// PAIR (CL = 2, grouped modes): the two CTAs form a tcgen05 pair.  The even
+// CTA issues MMAs of M = 256 over both CTAs' A tiles (its own weight unit m
+// and the odd CTA's m + 1, each dequantised into its own TMEM); each CTA
+// loads half of the token tile into its own shared memory, so that every
+// B byte is written to and read from one SM's shared memory only once for
+// 256 weight rows.  The odd CTA's dequantising and epilogue warps arrive on
+// the even CTA's barriers; the even CTA's commits arrive on both CTAs'.
+template <int MODE, int CL, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_constant__ MmaParams p) {
-  using C = Cfg<MODE>;
+  static_assert(!PAIR || (CL == 2 && MODE != MMA_ROUTER), "pairs: two CTAs, grouped modes");
+  using C = Cfg<MODE, PAIR>;
+  constexpr int kPad = PAIR ? 32 : 16;
+  // gate/up: the epilogue warps, idle while a unit's MMAs run (its single
+  // accumulator pair is drained only at the unit's end), dequantise every
+  // other K block, halving the dequantisation latency the MMAs see
+  constexpr bool kDeqSplit = (MODE == MMA_GATEUP);
+  static_assert(!kDeqSplit || Cfg<MODE, PAIR>::A_STAGES >= 2, "two dequantising groups");
   constexpr int kBStages = C::B_STAGES;
+  constexpr int kAStages = C::A_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Smem<MODE> S{smem_u32(smem)};
+  const Smem<MODE, PAIR> S{smem_u32(smem)};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -313,22 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     return (i & 1) ? base + (ncl - 1 - cid) : base + cid;
   };
   const int nmy = ncu / ncl + ((cunit(ncu / ncl) < ncu) ? 1 : 0);  // this cluster's units
+  const bool leader = !PAIR || crank == 0;  // issues the MMAs
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(S.a_full(s), MODE == MMA_ROUTER ? 1 : kDeqWarps);
+      mbar_init(S.a_full(s), MODE == MMA_ROUTER ? 1 : (PAIR ? 2 : 1) * kDeqWarps);
       mbar_init(S.a_empty(s), C::NISS);
     }
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(S.b_full(s), 1);
-      mbar_init(S.b_empty(s), CL * C::NISS);
+      mbar_init(S.b_empty(s), (PAIR ? 1 : CL) * C::NISS);
     }
     for (int b = 0; b < C::NACC; ++b) {
       mbar_init(S.acc_full(b), C::NISS);
-      mbar_init(S.acc_empty(b), kEpiWarps);
+      mbar_init(S.acc_empty(b), (PAIR ? 2 : 1) * kEpiWarps);
     }
     for (int s = 0; s < C::CST; ++s) {
       mbar_init(S.c_full(s), 1);
@@ -339,8 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -349,14 +420,78 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const int kbu = p.kb_per_unit;
 
+  // Dequantise K block g (the g-th of this CTA's sequence) into its A stage in
+  // TMEM: thread t (0..255 of a group of 8 warps) takes row t of the unit
+  // (two tiles: tile t >> 7) or row t & 127, K half t >> 7 (one tile).  The
+  // warp's TMEM lane quarter (lanes 32 (warp % 4) ..) holds rows (t & 127).
+  // Returns false on a timeout.
+  auto dequant_kb = [&](int g, int t) -> bool {
+    const int row = (C::NA == 2) ? t : (t & 127);
+    const int kh = (C::NA == 2) ? 0 : (t >> 7);
+    const uint32_t a_lane = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t a_off = (C::NA == 2) ? (uint32_t)((t >> 7) * 32) : (uint32_t)(kh * 16);
+    constexpr int kCst = C::CST > 0 ? C::CST : 1;
+    constexpr int NW = (C::NA == 2) ? 8 : 4;  // code words of the row (8 values each)
+    const int sc = g % kCst, sa = g % kAStages;
+    // A stage sa is free once the MMAs of K block g - A_STAGES have completed.
+    // Pairs: those MMAs' commit arrives only on the B slot's barrier; the B
+    // ring is deeper than the A ring and K block g + B_STAGES - A_STAGES
+    // cannot complete before this one is dequantised, so the slot's phase
+    // for g - A_STAGES is still the one the parity names.
+    bool free_ok;
+    if constexpr (PAIR) {
+      static_assert(C::B_STAGES > C::A_STAGES, "B ring deeper than the A ring");
+      const int gp = g - kAStages;
+      free_ok = gp < 0 || warp_wait(S.b_empty(gp % C::B_STAGES), (gp / C::B_STAGES) & 1,
+                                    abort_flag, p.err);
+    } else {
+      free_ok = warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err);
+    }
+    if (!warp_wait(S.c_full(sc), (g / kCst) & 1, abort_flag, p.err) || !free_ok) return false;
+    // row `row` of the ring stage: codes, then the s,b word
+    const uint4 a0 = ld_shared_v4(S.code(sc) + row * 32 + kh * 16);
+    const uint4 a1 = (C::NA == 2) ? ld_shared_v4(S.code(sc) + row * 32 + 16) : a0;
+    const uint32_t sb = ld_shared_u32(S.code(sc) + 32 * 128 * C::NA + row * 4);
+    const uint32_t s2 = __byte_perm(sb, 0, 0x1010);
+    const uint32_t b2 = __byte_perm(sb, 0, 0x3232);
+    const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    uint32_t v[4 * NW];  // column 4 i + j = K pair (8 i + 2 j, 8 i + 2 j + 1)
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const uint4 d4 = dequant_word(w[i], s2, b2);
+      v[4 * i] = d4.x;
+      v[4 * i + 1] = d4.y;
+      v[4 * i + 2] = d4.z;
+      v[4 * i + 3] = d4.w;
+    }
+    // the MMAs that read this A stage before have completed (a_empty)
+    tc_fence_after();
+    const uint32_t ta = tmem + a_lane + C::A_COL0 + sa * C::A_COLS + a_off;
+    if constexpr (NW == 8)
+      tmem_st32(ta, v);
+    else
+      tmem_st16(ta, v);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(S.c_empty(sc));
+      if (leader)
+        mbar_arrive(S.a_full(sa));
+      else
+        mbar_arrive_cluster(mapa_shared(S.a_full(sa), 0));
+    }
+    return true;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------ B (+ router A)
     uint32_t gb = 0, ga = 0;
     bool ok = true;
-    Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
+    Unit tn = get_unit(p, MODE, cunit(0) * CL + crank, kPad);
     for (int i = 0; i < nmy && ok; ++i) {
       const Unit t = tn;
-      if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
+      if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank, kPad);
       const int k0 = t.ks * kbu;
       const uint8_t* asrc = p.wA + (long long)t.m * p.a_unit_stride + (long long)k0 * p.a_chunk;
       for (int kb = 0; kb < kbu; ++kb) {
@@ -379,13 +514,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         }
         const uint32_t bs = S.b(s);
         const int x = (k0 + kb) * 64;
-        // the whole tile arrives in every CTA; this CTA fetches 16-row slabs
-        // crank, crank + CL, ... (one 2-D tile per slab)
-        if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
-        __syncwarp();
-        const int nslab = t.npad >> 4;
-        for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
-          tma_tile_2d<CL>(bs + sl * 2048, &p.tmB, x, t.row0 + 16 * sl, S.b_full(s));
+        if constexpr (PAIR) {
+          // this CTA's half of the tile (rows crank * npad / 2 ..), counted on
+          // the even CTA's barrier, which expects the bytes of both halves
+          if (lane == 0 && leader) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
+          __syncwarp();
+          const int half = t.npad >> 1;
+          const uint32_t fb = mapa_shared(S.b_full(s), 0);
+          for (int sl = lane; sl < (half >> 4); sl += 32)
+            tma_tile_2d_pair(bs + sl * 2048, &p.tmB, x, t.row0 + crank * half + 16 * sl, fb);
+        } else {
+          // the whole tile arrives in every CTA; this CTA fetches 16-row slabs
+          // crank, crank + CL, ... (one 2-D tile per slab)
+          if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
+          __syncwarp();
+          const int nslab = t.npad >> 4;
+          for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
+            tma_tile_2d<CL>(bs + sl * 2048, &p.tmB, x, t.row0 + 16 * sl, S.b_full(s));
+        }
         ++gb;
       }
     }
@@ -395,22 +541,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     // and lane 0 of warp 3 tile 1's: a single thread issues a tcgen05.mma
     // no faster than one per ~56 cycles (measured), which bounded the small
     // tiles; two issuers on separate accumulators overlap.
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       const int q = (warp == 1) ? 0 : 1;  // this issuer's tile (two-tile units)
       uint32_t sa = 0, pa = 0, sb = 0, pb = 0;  // ring slots and phase parities
-      Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
+      Unit tn = get_unit(p, MODE, cunit(0) * CL + crank, kPad);
       for (int i = 0; i < nmy; ++i) {
         const Unit t = tn;  // the next unit's descriptor loads during this one
-        if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
+        if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank, kPad);
         const int ab = (C::NACC == 2) ? (int)(i & 1) : 0;
         const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
         if (!thread_wait(S.acc_empty(ab), aph ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t idesc = idesc_f16(128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
+        const uint32_t idesc = idesc_f16(PAIR ? 256 : 128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
         bool ok = true;
         for (int kb = 0; kb < kbu; ++kb) {
-          if (!thread_wait(S.a_full(sa), pa, abort_flag, p.err) ||
-              !thread_wait(S.b_full(sb), pb, abort_flag, p.err)) {
+          // both operands' barriers tested at once (the two tests' latencies
+          // overlap; a test costs ~130 cycles even on a completed phase, and
+          // the issuing thread is the pipeline's bottleneck at small N)
+          const bool ra = mbar_try_wait(S.a_full(sa), pa);
+          const bool rb = mbar_try_wait(S.b_full(sb), pb);
+          if (!(ra && rb) && (!thread_wait(S.a_full(sa), pa, abort_flag, p.err) ||
+                              !thread_wait(S.b_full(sb), pb, abort_flag, p.err))) {
             ok = false;
             break;
           }
@@ -421,25 +572,50 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 #pragma unroll
           for (int j = 0; j < C::NA; ++j) {
             if (C::NISS == 2 && j != q) continue;
-            const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384);
-            // NA == 2: tile j -> columns 256 j; NACC == 2: buffer ab -> columns 256 ab
-            const uint32_t dcol = tmem + 256 * (C::NA == 2 ? j : ab);
+            // NA == 2: tile j -> columns NMAX j; NACC == 2: buffer ab -> columns NMAX ab
+            const uint32_t dcol = tmem + C::NMAX * (C::NA == 2 ? j : ab);
+            if constexpr (C::TMEM_A) {
+              // A: 8 TMEM columns per K step of 16
+              const uint32_t at = tmem + C::A_COL0 + sa * C::A_COLS + j * 32;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_f16(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                if constexpr (PAIR)
+                  tc_mma_f16_ts_pair(dcol, at + 8 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+                else
+                  tc_mma_f16_ts(dcol, at + 8 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+              }
+            } else {
+              const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+            }
           }
-          tc_commit(S.a_empty(sa));
-          tc_commit_cluster<CL>(S.b_empty(sb));
+          if constexpr (PAIR) {
+            // one commit frees both stages: the dequantising warps wait on
+            // the B slot's barrier (see dequant_kb)
+            tc_commit_pair_mc(S.b_empty(sb), 3);
+          } else {
+            tc_commit(S.a_empty(sa));
+            tc_commit_cluster<CL>(S.b_empty(sb));
+          }
           if (++sa == kAStages) { sa = 0; pa ^= 1; }
           if (++sb == (uint32_t)kBStages) { sb = 0; pb ^= 1; }
         }
         if (!ok) break;
-        tc_commit(S.acc_full(ab));
+        if constexpr (PAIR)
+          tc_commit_pair_mc(S.acc_full(ab), 3);
+        else
+          tc_commit(S.acc_full(ab));
       }
-      // every issued MMA has finished before TMEM is released
-      tc_commit(S.drain());
-      mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
+      // every issued MMA has finished before TMEM is released (in both CTAs
+      // of a pair)
+      if constexpr (PAIR)
+        tc_commit_pair_mc(S.drain(), 3);
+      else
+        tc_commit(S.drain());
     }
+    if (lane == 0) mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
   } else if (warp == 2 && MODE != MMA_ROUTER) {
     // ------------------------------------------------ code ring
     if (lane == 0) {
@@ -449,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         const int s = g % kCst;
         if (!thread_wait(S.c_empty(s), ((g / kCst) & 1) ^ 1, abort_flag, p.err)) break;
         const int j = g / kbu;
-        const Unit u = get_unit(p, MODE, cunit(j) * CL + crank);
+        const Unit u = get_unit(p, MODE, cunit(j) * CL + crank, kPad);
         if (C::NA == 2) {  // the whole chunk of unit m
           const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
                               (long long)u.m * p.a_unit_stride +
@@ -469,50 +645,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     }
   } else if (warp >= 4 && warp < 4 + kDeqWarps) {
     // ------------------------------------------------ dequantise
-    if (MODE != MMA_ROUTER) {
-      const int t = threadIdx.x - 128;  // 0..255
-      // two tiles: row t of the unit (tile t >> 7); one tile: row t & 127,
-      // K half t >> 7 (32 values)
-      const int row = (C::NA == 2) ? t : (t & 127);
-      const int kh = (C::NA == 2) ? 0 : (t >> 7);
+    if constexpr (MODE != MMA_ROUTER) {
       const int total = nmy * kbu;
-      struct Codes {
-        uint4 a0, a1;
-        uint32_t sa;
-      };
-      // words w[i] (K 8 (4 kh + i) .. +7) of row r -> swizzled 16-byte chunks
-      auto emit = [&](uint32_t a, int r, const Codes& cc) {
-        const uint32_t s2 = __byte_perm(cc.sa, 0, 0x1010);
-        const uint32_t b2 = __byte_perm(cc.sa, 0, 0x3232);
-        const uint32_t rowb = a + (r >> 7) * 16384 + (r & 127) * 128;
-        const uint32_t w[8] = {cc.a0.x, cc.a0.y, cc.a0.z, cc.a0.w,
-                               cc.a1.x, cc.a1.y, cc.a1.z, cc.a1.w};
-        constexpr int NW = (C::NA == 2) ? 8 : 4;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-          const int c = 4 * kh + i;
-          const uint4 d4 = dequant_word(w[i], s2, b2);
-          st_shared_v4(rowb + ((c ^ (r & 7)) << 4), d4.x, d4.y, d4.z, d4.w);
-        }
-      };
-      constexpr int kCst = C::CST > 0 ? C::CST : 1;
-      for (int g = 0; g < total; ++g) {
-        const int sc = g % kCst, sa = g % kAStages;
-        if (!warp_wait(S.c_full(sc), (g / kCst) & 1, abort_flag, p.err) ||
-            !warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err))
-          break;
-        Codes cur;  // row `row` of the ring stage: codes, then the s,b word
-        cur.a0 = ld_shared_v4(S.code(sc) + row * 32 + kh * 16);
-        cur.a1 = (C::NA == 2) ? ld_shared_v4(S.code(sc) + row * 32 + 16) : cur.a0;
-        cur.sa = ld_shared_u32(S.code(sc) + 32 * 128 * C::NA + row * 4);
-        emit(S.a(sa), row, cur);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(S.c_empty(sc));
-          mbar_arrive(S.a_full(sa));
-        }
-      }
+      // gate/up: these warps take the even K blocks, the epilogue warps the
+      // odd ones (kbu is even, so the parity of g is that of the K block)
+      for (int g = 0; g < total; g += kDeqSplit ? 2 : 1)
+        if (!dequant_kb(g, threadIdx.x - 32 * 4)) break;
     }
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------- epilogue
@@ -521,12 +659,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     const int half = e >> 2;           // columns [128*half, 128*half + 128)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t nst = 0;
-    Unit tn = get_unit(p, MODE, cunit(0) * CL + crank);
+    Unit tn = get_unit(p, MODE, cunit(0) * CL + crank, kPad);
     for (int i = 0; i < nmy; ++i) {
       const Unit t = tn;
-      if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank);
-      const int c0 = half * 128;
-      const int c1 = min(c0 + 128, t.npad);
+      if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank, kPad);
+      if constexpr (kDeqSplit) {
+        // the odd K blocks of this unit (the MMAs of the next unit cannot
+        // start before this unit's epilogue has drained its accumulators)
+        bool ok = true;
+        for (int kb = 1; kb < kbu && ok; kb += 2)
+          ok = dequant_kb(i * kbu + kb, threadIdx.x - 32 * kEpiWarp0);
+        if (!ok) break;
+      }
+      const int c0 = half * C::EPI_COLS;
+      const int c1 = min(c0 + C::EPI_COLS, t.npad);
       // row data of the warp's 128 columns, fetched while the MMAs run:
       // lane l holds rows c0 + l + 32 v, v = 0..3
       float rsc4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -545,11 +691,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
       if (!warp_wait(S.acc_full(ab), aph, abort_flag, p.err)) break;
       tc_fence_after();
-      const uint32_t tacc = tmem + lane_base + 256 * ab;
+      const uint32_t tacc = tmem + lane_base + C::NMAX * ab;
       for (int n0 = c0; n0 < c1; n0 += 16) {
         uint32_t r0[16], r1[16];
         tmem_ld16(tacc + n0, r0);
-        if (C::NA == 2) tmem_ld16(tacc + 256 + n0, r1);
+        if (C::NA == 2) tmem_ld16(tacc + C::NMAX + n0, r1);
         const int nvalid = min(16, t.nrows - n0);
         // this chunk's rows n0..n0+15 are held by lanes (n0 - c0) % 32 + j
         // in register slot (n0 - c0) / 32
@@ -590,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
             const float v0 = __uint_as_float(r0[j]);
             if (MODE == MMA_GATEUP) {
               const float v1 = __uint_as_float(r1[j]);
-              const float h = __fdividef(v0, 1.0f + __expf(-v0)) * v1;
+              const float h = silu_tanh(v0) * v1;
               st_shared_u16(sbuf + j * 64 + lane * 2, __half_as_ushort(__float2half_rn(h)));
             } else {
               const float sc = __shfl_sync(0xffffffffu, rsc, j);
@@ -629,7 +775,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(S.acc_empty(ab));
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(S.acc_empty(ab));
+        else
+          mbar_arrive_cluster(mapa_shared(S.acc_empty(ab), 0));
+      }
     }
   }
 
@@ -638,16 +789,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   if (CL > 1) cluster_sync_all();  // no CTA leaves while peers may still write to it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
 }
 
-template <int MODE, int CL>
+template <int MODE, int CL, bool PAIR>
 cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_mma_kernel<MODE, CL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MODE>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(grouped_mma_kernel<MODE, CL, PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MODE, PAIR>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -657,7 +811,7 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
     cudaLaunchConfig_t q = {};
     q.gridDim = dim3(CL);
     q.blockDim = dim3(kThreads);
-    q.dynamicSmemBytes = Cfg<MODE>::SMEM;
+    q.dynamicSmemBytes = Cfg<MODE, PAIR>::SMEM;
     cudaLaunchAttribute a[1];
     a[0].id = cudaLaunchAttributeClusterDimension;
     a[0].val.clusterDim.x = CL;
@@ -666,7 +820,7 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
     q.attrs = a;
     q.numAttrs = 1;
     int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, grouped_mma_kernel<MODE, CL>, &q) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&ncl, grouped_mma_kernel<MODE, CL, PAIR>, &q) != cudaSuccess ||
         ncl <= 0) {
       cudaGetLastError();
       ncl = 0;
@@ -679,7 +833,7 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<MODE>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<MODE, PAIR>::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -688,12 +842,12 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_mma_kernel<MODE, CL>, p);
+  return cudaLaunchKernelEx(&cfg, grouped_mma_kernel<MODE, CL, PAIR>, p);
 }
 
 // CTAs per cluster for a grouped launch: a power of two dividing the units
-// of one tile.  Defaults measured on GB300 (T=4096, Zipf): gate/up 4, down 2;
-// MOE_GEMM_CLUSTER (1, 2, 4) overrides both for tuning.
+// of one tile.  Defaults measured on GB300 (T=4096, Zipf): gate/up 4, down 2
+// (one CTA per SM, cta_group::1); MOE_GEMM_CLUSTER (1, 2, 4) overrides both.
 int cluster_for(int mode, int units_per_tile) {
   static int env = -1;
   if (env < 0) {
@@ -704,6 +858,17 @@ int cluster_for(int mode, int units_per_tile) {
   int cl = env ? env : (mode == MMA_GATEUP ? 4 : 2);
   while (cl > 1 && units_per_tile % cl != 0) cl >>= 1;
   return cl;
+}
+
+// CTA pairs (tcgen05 cta_group::2) for the grouped GEMMs unless
+// MOE_GEMM_2SM=0; they need an even number of weight units per tile.
+bool pairs_for(int units_per_tile) {
+  static int env = -1;
+  if (env < 0) {
+    const char* e = getenv("MOE_GEMM_2SM");
+    env = (e && atoi(e) == 0) ? 0 : 1;
+  }
+  return env == 1 && units_per_tile % 2 == 0;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -744,16 +909,20 @@ cudaError_t make_tmap_16bit(CUtensorMap* map, const void* base, long long rows, 
 
 cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st) {
   if (grid <= 0) return cudaSuccess;
-  if (mode == MMA_ROUTER) return launch_mode<MMA_ROUTER, 1>(p, grid, st);
+  if (mode == MMA_ROUTER) return launch_mode<MMA_ROUTER, 1, false>(p, grid, st);
+  if (pairs_for(p.units_per_tile)) {
+    if (mode == MMA_GATEUP) return launch_mode<MMA_GATEUP, 2, true>(p, grid, st);
+    return launch_mode<MMA_DOWN, 2, true>(p, grid, st);
+  }
   const int cl = cluster_for(mode, p.units_per_tile);
   if (mode == MMA_GATEUP) {
-    if (cl == 4) return launch_mode<MMA_GATEUP, 4>(p, grid, st);
-    if (cl == 2) return launch_mode<MMA_GATEUP, 2>(p, grid, st);
-    return launch_mode<MMA_GATEUP, 1>(p, grid, st);
+    if (cl == 4) return launch_mode<MMA_GATEUP, 4, false>(p, grid, st);
+    if (cl == 2) return launch_mode<MMA_GATEUP, 2, false>(p, grid, st);
+    return launch_mode<MMA_GATEUP, 1, false>(p, grid, st);
   }
-  if (cl == 4) return launch_mode<MMA_DOWN, 4>(p, grid, st);
-  if (cl == 2) return launch_mode<MMA_DOWN, 2>(p, grid, st);
-  return launch_mode<MMA_DOWN, 1>(p, grid, st);
+  if (cl == 4) return launch_mode<MMA_DOWN, 4, false>(p, grid, st);
+  if (cl == 2) return launch_mode<MMA_DOWN, 2, false>(p, grid, st);
+  return launch_mode<MMA_DOWN, 1, false>(p, grid, st);
 }
 
 }  // namespace moe

@@ -12,7 +12,7 @@ namespace moe {
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 16;
 constexpr int kTokPerBlock = 32;  // tokens per block of the routing kernels
-constexpr int kTileRows = 256;    // largest token tile of the grouped GEMMs
+constexpr int kTileRows = 192;    // largest token tile of the grouped GEMMs (TMEM budget)
 constexpr int kUnitRows = 256;    // weight rows per tensor-core work unit (2 x M=128)
 constexpr int kCodeChunk = 9216;  // 256 rows x (32 B codes + 4 B scale/bias)
 constexpr int kRouterChunk = 32768;  // 256 rows x 64 bf16, pre-swizzled
