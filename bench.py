@@ -341,7 +341,7 @@ def run_prefill(args, torch, M, sd, gen, device, peaks):
         e2e={"value": args.world * PREFILL_T / e2e_s, "unit": "tokens/s",
              "h2d_bytes_per_step": PREFILL_T * D * 2 + E * 4,
              "d2h_bytes_per_step": PREFILL_T * D * 2},
-        gpu_launches=7 * args.steps, clocks=clocks, device_error=err)
+        gpu_launches=5 * args.steps, clocks=clocks, device_error=err)
 
 
 SWEEP_T = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072]
@@ -532,7 +532,7 @@ def config_for(workload):
     return {"workload": "qwen-shaped MoE prefill layer: T=4096, Zipf-skewed routing "
                         "(b_e = 1.5 ln(1/rank_e)), d=2048, E=256, top-8, I=512 + shared, 4-bit g64",
             "tokens_per_step": PREFILL_T, "l2": "flushed between timed steps (256 MB write)",
-            "launch": "one CUDA graph of the layer per step (8 kernels)"}
+            "launch": "one CUDA graph of the layer per step (5 kernels)"}
 
 
 def main():

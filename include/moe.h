@@ -204,10 +204,11 @@ moe_status moe_decode_host(moe_handle* const* layers, int L, const void* x_host,
 
 /* Per-stage timing of moe_forward (benchmark aid).  While enabled, every
  * moe_forward call records CUDA events around its stages on the caller's
- * stream: 0 router GEMM, 1 top-k, 2 scan + tile map, 3 scatter, 4 permuted
- * fp16 activations + shared gate, 5 gate/up GEMM, 6 down GEMM, 7 combine.
+ * stream: 0 router GEMM, 1 routing (top-k, histogram, scan + tile map,
+ * scatter, fp16 copy of the activations + shared gate: one kernel), 2 gate/up
+ * GEMM, 3 down GEMM, 4 combine.
  * moe_profile_read synchronises the device, writes the summed milliseconds
- * per stage into ms[0..n-1] (n <= 8) and the
+ * per stage into ms[0..n-1] (n <= 5) and the
  * number of timed chunks into *calls, and resets the sums.  At most 4096
  * chunks are kept between reads (later ones are not timed). */
 moe_status moe_profile_enable(moe_handle* h, int enable);

@@ -95,7 +95,7 @@ struct Cfg {
   static constexpr int CST = (MODE == MMA_DOWN) ? 8 : (MODE == MMA_GATEUP ? 6 : 0);
   static constexpr int CODE_STAGE = NA * kHalfChunk;
   // B ring: up to NMAX token rows (a pair's CTA holds half of them) x 64 K
-  static constexpr int B_STAGES = PAIR ? 8 : (TMEM_A ? 4 : 3);
+  static constexpr int B_STAGES = PAIR ? 8 : (MODE == MMA_GATEUP ? 6 : (TMEM_A ? 4 : 3));
   static constexpr int B_STAGE = (PAIR ? NMAX / 2 : NMAX) * 128;
   static constexpr int A_STAGE = TMEM_A ? 0 : NA * 16384;  // shared-memory A (router)
   // epilogue: per chunk of 16 rows, NSEG 64-byte segments per row (down: one
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       mbar_init(S.a_empty(s), C::NISS);
     }
     for (int s = 0; s < kBStages; ++s) {
-      mbar_init(S.b_full(s), 1);
+      // gate/up: one arrival per CTA of the pair (gathered rows, no byte count)
+      mbar_init(S.b_full(s), (MODE == MMA_GATEUP && PAIR) ? 2 : 1);
       mbar_init(S.b_empty(s), (PAIR ? 1 : CL) * C::NISS);
     }
     for (int b = 0; b < C::NACC; ++b) {
@@ -484,7 +485,75 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     return true;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && MODE == MMA_GATEUP) {
+    // ------------------------------------------------ B gathered (gate/up)
+    // Row n of the token tile is token perm[row0 + n]; this CTA loads rows
+    // [crank * npad / 2, ...) of a pair's tile (all of it without a pair)
+    // from the fp16 activations by 16-byte cp.async into the 128-byte
+    // swizzled layout (16-byte chunk c of row r at chunk c ^ (r % 8)); rows
+    // past the tile's tokens are zero.  A stage is announced kLag stages after
+    // its copies were issued: cp.async.wait_group, the proxy fence that makes
+    // the writes visible to the tensor core, then one arrival (in a pair on
+    // the even CTA's barrier, which counts one arrival per CTA).  (TMA 4-row
+    // gathers, which would count bytes on the even CTA's barrier directly,
+    // measured 26 % slower for this kernel: the gather rate bounds them.)
+    constexpr int kLag = kBStages > 4 ? 4 : kBStages - 1;  // below the ring depth
+    constexpr int kRowsPerLane = ((PAIR ? C::NMAX / 2 : C::NMAX) + 31) / 32;
+    const uint32_t fb0 = mapa_shared(S.b_full(0), 0);  // b_full(s) = fb0 + 8 s
+    auto announce = [&](uint32_t g) {
+      const int s = (int)(g % kBStages);
+      if (!PAIR || leader)
+        mbar_arrive(S.b_full(s));
+      else
+        mbar_arrive_cluster(fb0 + 8 * s);
+    };
+    uint32_t gb = 0;
+    bool ok = true;
+    for (int i = 0; i < nmy && ok; ++i) {
+      const Unit t = get_unit(p, MODE, cunit(i) * CL + crank, kPad);
+      const int hn = PAIR ? (t.npad >> 1) : t.npad;
+      const int hr0 = t.row0 + (PAIR ? crank * hn : 0);
+      int tok[kRowsPerLane];
+#pragma unroll
+      for (int m = 0; m < kRowsPerLane; ++m) {
+        const int r = lane + 32 * m;
+        tok[m] = (r < hn && hr0 + r < t.row0 + t.nrows) ? p.perm[hr0 + r] : -1;
+      }
+      for (int kb = 0; kb < kbu; ++kb) {
+        const int s = gb % kBStages;
+        if (!warp_wait(S.b_empty(s), ((gb / kBStages) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bs = S.b(s);
+#pragma unroll
+        for (int m = 0; m < kRowsPerLane; ++m) {
+          const int r = lane + 32 * m;
+          if (r < hn) {
+            const uint16_t* src = p.xg + (long long)(tok[m] < 0 ? 0 : tok[m]) * p.ldx + kb * 64;
+            const uint32_t nb = tok[m] < 0 ? 0u : 16u;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              cp_async16(bs + r * 128 + ((c ^ (r & 7)) << 4), src + c * 8, nb);
+          }
+        }
+        cp_async_commit();
+        ++gb;
+        if (gb > (uint32_t)kLag) {
+          cp_async_wait<kLag>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) announce(gb - 1 - kLag);
+        }
+      }
+    }
+    // the last stages (after a timeout every issued copy still completes)
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && ok)
+      for (uint32_t g = gb > (uint32_t)kLag ? gb - kLag : 0; g < gb; ++g) announce(g);
+  } else if (warp == 0) {
     // ------------------------------------------------------ B (+ router A)
     uint32_t gb = 0, ga = 0;
     bool ok = true;
@@ -845,10 +914,12 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, grouped_mma_kernel<MODE, CL, PAIR>, p);
 }
 
-// CTAs per cluster for a grouped launch: a power of two dividing the units
-// of one tile.  Defaults measured on GB300 (T=4096, Zipf): gate/up 4, down 2
-// (one CTA per SM, cta_group::1); MOE_GEMM_CLUSTER (1, 2, 4) overrides both.
+// CTAs per cluster for a grouped launch without pairs: a power of two
+// dividing the units of one tile.  Gate/up gathers its token rows (no
+// multicast): 1.  Down: 2 measured on GB300 (T=4096, Zipf); MOE_GEMM_CLUSTER
+// (1, 2, 4) overrides it.
 int cluster_for(int mode, int units_per_tile) {
+  if (mode == MMA_GATEUP) return 1;
   static int env = -1;
   if (env < 0) {
     const char* e = getenv("MOE_GEMM_CLUSTER");
@@ -914,12 +985,8 @@ cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStrea
     if (mode == MMA_GATEUP) return launch_mode<MMA_GATEUP, 2, true>(p, grid, st);
     return launch_mode<MMA_DOWN, 2, true>(p, grid, st);
   }
+  if (mode == MMA_GATEUP) return launch_mode<MMA_GATEUP, 1, false>(p, grid, st);
   const int cl = cluster_for(mode, p.units_per_tile);
-  if (mode == MMA_GATEUP) {
-    if (cl == 4) return launch_mode<MMA_GATEUP, 4, false>(p, grid, st);
-    if (cl == 2) return launch_mode<MMA_GATEUP, 2, false>(p, grid, st);
-    return launch_mode<MMA_GATEUP, 1, false>(p, grid, st);
-  }
   if (cl == 4) return launch_mode<MMA_DOWN, 4, false>(p, grid, st);
   if (cl == 2) return launch_mode<MMA_DOWN, 2, false>(p, grid, st);
   return launch_mode<MMA_DOWN, 1, false>(p, grid, st);

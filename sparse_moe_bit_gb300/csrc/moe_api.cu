@@ -167,10 +167,9 @@ moe_status alloc_all(Handle* h) {
   CK(dalloc(&w.ticket, 16), "alloc");
   CK(cudaMemset(w.ticket, 0, 16), "memset");
   if (h->layouts & MOE_LAYOUT_PREFILL) {
-    CK(dalloc(&w.xp, (size_t)T * k1 * c.d * 2), "alloc");
+    CK(dalloc(&w.xp, (size_t)T * c.d * 2), "alloc");
     CK(dalloc(&w.H, (size_t)T * k1 * c.I * 2), "alloc");
     CK(dalloc(&w.Y, (size_t)T * k1 * c.d * 2), "alloc");
-    CK(make_tmap_16bit(&h->tm_xp, w.xp, T * k1, c.d, 16, false), "tensor map (xp)");
     CK(make_tmap_16bit(&h->tm_h, w.H, T * k1, c.I, 16, false), "tensor map (H)");
   }
   CK(dalloc(&w.x_dev, (size_t)T * c.d * 2), "alloc");
@@ -185,9 +184,11 @@ void prof_mark(Handle* h, int i, cudaStream_t st) {
   cudaEventRecord(h->prof_ev[h->prof_calls * (Handle::kStagesTimed + 1) + i], st);
 }
 
-// router GEMM -> top-k (+ fp16 activations, shared gate) -> scan/tile map -> scatter
+// router GEMM -> fused routing (top-k, histogram, scan + tile map, scatter;
+// with_xp: also the fp16 copy of the activations that the gate/up GEMM
+// gathers its token rows from, and the shared gate)
 moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int T,
-                       const float* bias, cudaStream_t st) {
+                       const float* bias, bool with_xp, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const float* part = logits_in;
   int ks = 1;
@@ -215,11 +216,7 @@ moe_status run_routing(Handle* h, const uint16_t* x, const float* logits_in, int
     ks = rp.ks;
   }
   prof_mark(h, 1, st);
-  CK(launch_topk(h, part, ks, T, bias, st), "top-k launch");
-  prof_mark(h, 2, st);
-  CK(launch_scan_tiles(h, T, st), "scan launch");
-  prof_mark(h, 3, st);
-  CK(launch_scatter(h, T, st), "scatter launch");
+  CK(launch_route(h, part, ks, T, bias, with_xp ? x : nullptr, st), "routing launch");
   return MOE_OK;
 }
 
@@ -239,14 +236,14 @@ moe_status run_experts(Handle* h, const uint16_t* x, int T, uint16_t* y, cudaStr
   p.wA = h->pf_gu;
   p.a_unit_stride = (long long)(c.d / 64) * kCodeChunk;
   p.a_expert_stride = p.a_unit_stride * (c.I / 128);
-  p.tmB = h->tm_xp;
+  p.xg = w.xp;
+  p.perm = w.perm;
+  p.ldx = c.d;
   p.H = w.H;
   p.ldh = c.I;
   long long units = (long long)mt * p.m_units;
   int grid = units < h->num_sms ? (int)units : h->num_sms;
-  prof_mark(h, 4, st);
-  CK(launch_permute(h, x, T, st), "permute launch");
-  prof_mark(h, 5, st);
+  prof_mark(h, 2, st);
   CK(launch_grouped_mma(MMA_GATEUP, p, grid, st), "gate/up launch");
   // down projection + routing weight: one 128-row weight tile per unit
   p.kb_per_unit = c.I / 64;
@@ -262,11 +259,11 @@ moe_status run_experts(Handle* h, const uint16_t* x, int T, uint16_t* y, cudaStr
   p.row_scale = w.wrow;
   units = (long long)mt * p.m_units;
   grid = units < h->num_sms ? (int)units : h->num_sms;
-  prof_mark(h, 6, st);
+  prof_mark(h, 3, st);
   CK(launch_grouped_mma(MMA_DOWN, p, grid, st), "down launch");
-  prof_mark(h, 7, st);
+  prof_mark(h, 4, st);
   CK(launch_combine(h, T, y, st), "combine launch");
-  prof_mark(h, 8, st);
+  prof_mark(h, 5, st);
   if (h->prof && h->prof_calls < Handle::kProfCalls) ++h->prof_calls;
   return MOE_OK;
 }
@@ -368,7 +365,7 @@ moe_status moe_route(moe_handle* h, const void* x, int T, const float* logit_bia
   if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x NULL or not 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
-  s = run_routing(h, static_cast<const uint16_t*>(x), nullptr, T, logit_bias, st);
+  s = run_routing(h, static_cast<const uint16_t*>(x), nullptr, T, logit_bias, false, st);
   if (s != MOE_OK) return s;
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
@@ -394,7 +391,7 @@ moe_status moe_route_from_logits(moe_handle* h, const float* logits, int T,
   if (!logits || !aligned(logits, 4)) return fail(MOE_ERR_INVALID_ARG, "logits NULL or misaligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
-  s = run_routing(h, nullptr, logits, T, logit_bias, st);
+  s = run_routing(h, nullptr, logits, T, logit_bias, false, st);
   if (s != MOE_OK) return s;
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
@@ -436,7 +433,7 @@ moe_status moe_forward(moe_handle* h, const void* x, int T, const float* logit_b
     const int tc = (T - t0) < c.max_tokens ? (T - t0) : c.max_tokens;
     const uint16_t* xc = static_cast<const uint16_t*>(x) + (size_t)t0 * c.d;
     uint16_t* yc = static_cast<uint16_t*>(y) + (size_t)t0 * c.d;
-    s = run_routing(h, xc, nullptr, tc, logit_bias, st);
+    s = run_routing(h, xc, nullptr, tc, logit_bias, true, st);
     if (s != MOE_OK) return s;
     s = run_experts(h, xc, tc, yc, st);
     if (s != MOE_OK) return s;

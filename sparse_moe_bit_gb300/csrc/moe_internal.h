@@ -26,7 +26,7 @@ struct Workspace {
   int32_t* idx = nullptr;       // [Tmax][k]
   float* w = nullptr;           // [Tmax][k]
   float* sigma = nullptr;       // [Tmax]
-  uint16_t* xp = nullptr;       // [Tmax*(k+1)][d] fp16 activations in grouped-row order
+  uint16_t* xp = nullptr;       // [Tmax][d] fp16 copy of the activations (gate/up B rows)
   int32_t* hist = nullptr;      // [nblk][E]
   int32_t* base = nullptr;      // [nblk][E]
   int32_t* counts = nullptr;    // [E]
@@ -37,7 +37,7 @@ struct Workspace {
   float* wrow = nullptr;        // [Tmax*(k+1)] grouped row -> routing weight
   int4* tiles = nullptr;        // [max_tiles] {expert, row0, nrows, npad}
   int32_t* ntiles = nullptr;    // [1]
-  unsigned* ticket = nullptr;   // [1] blocks of the scan done (zero between calls)
+  unsigned* ticket = nullptr;   // [4]: [2], [3] the routing launch's grid barrier (zero between calls)
   uint16_t* H = nullptr;        // [Tmax*(k+1)][I] fp16 SwiGLU activations
   uint16_t* Y = nullptr;        // [Tmax*(k+1)][d] bf16 weighted contributions
   int max_tiles = 0;
@@ -64,10 +64,9 @@ struct Handle {
   uint16_t* w_router = nullptr;  // bf16 [E][d]
   uint16_t* w_sg = nullptr;      // bf16 [d]
   Workspace ws;
-  CUtensorMap tm_xp;   // gate/up B: xp [Tmax*(k+1)][d], 16-row box
   CUtensorMap tm_h;    // down B: H [Tmax*(k+1)][I], 16-row box
   // per-stage timing (moe_profile_enable)
-  static constexpr int kStagesTimed = 8;
+  static constexpr int kStagesTimed = 5;
   static constexpr int kProfCalls = 4096;
   bool prof = false;
   int prof_calls = 0;
@@ -101,8 +100,11 @@ struct MmaParams {
   long long a_expert_stride;  // bytes per expert
   long long a_unit_stride;    // bytes per 256-row unit
   int a_chunk;                // bytes per K block
-  // B operand rows: contiguous from row0 (16-row TMA tiles; gate/up reads the
-  // activations already permuted into grouped-row order)
+  // B operand rows: router and down contiguous from row0 (16-row TMA tiles);
+  // gate/up gathered by cp.async from row perm[row] of xg (fp16 [T][ldx])
+  const uint16_t* xg;
+  const int32_t* perm;
+  int ldx;
   // epilogue
   float* out_f32;             // router partials [KS][T][E]
   int E;
@@ -121,11 +123,10 @@ cudaError_t make_tmap_16bit(CUtensorMap* map, const void* base, long long rows, 
                             int box_rows, bool bf16);
 
 // ---- routing (routing.cu)
-cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
-                        cudaStream_t st);
-cudaError_t launch_permute(const Handle* h, const uint16_t* x, int T, cudaStream_t st);
-cudaError_t launch_scan_tiles(const Handle* h, int T, cudaStream_t st);
-cudaError_t launch_scatter(const Handle* h, int T, cudaStream_t st);
+// top-k, histogram, scan + tile map, scatter and (x non-null) the fp16 copy of
+// the activations with the shared-expert gate, in one cooperative launch
+cudaError_t launch_route(const Handle* h, const float* part, int KS, int T, const float* bias,
+                         const uint16_t* x, cudaStream_t st);
 cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st);
 
 // ---- repack (repack.cu)

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
 #include "softmax_df.cuh"
 
 namespace moe {
@@ -26,19 +27,133 @@ __device__ __forceinline__ uint32_t ord_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per token, 32 tokens per block (one block = one row of the
-// histogram).  Sums the router's K-split partial logits (fixed order), adds
-// the bias, keeps the top k by (logit desc, index asc) and computes the
-// renormalised softmax weights.  Each block counts its assignments per expert
-// (hist[block][e]).
-// Selection: lane l holds the order keys of experts l, l+32, ...; each round
-// every lane finds its best key not yet taken (first slot among equal keys,
-// i.e. the lowest index), the warp maximum of those and then the smallest
-// expert index among the lanes holding it name the winner (two warp
+// Top-k selection (topk_warp): the router's K-split partial logits are
+// summed in a fixed order, the bias added, and the top k kept by (logit
+// desc, index asc); lane l holds the order keys of experts l, l+32, ...; each
+// round every lane finds its best key not yet taken (first slot among equal
+// keys, i.e. the lowest index), the warp maximum of those and then the
+// smallest expert index among the lanes holding it name the winner (two warp
 // reductions per round).
 constexpr int kTopkThreads = 32 * kTokPerBlock;
 static_assert(kTopkThreads <= 1024, "one warp per token of a block");
 
+// Top-k of token t by one warp (t < T checked by the caller): the fixed-order
+// sum of the K-split partial logits and the bias, the logits row, the kept
+// experts idx[t][0..k) in order, their logits into s_vw[0..k) and one count
+// per kept expert into the block histogram cnt.
+template <int VPL>
+__device__ __forceinline__ void topk_warp(const float* __restrict__ part, int KS, int T, int E,
+                                          int k, const float* __restrict__ bias,
+                                          float* __restrict__ logits, int32_t* __restrict__ idx_out,
+                                          int t, float* s_vw, int* cnt, int* err) {
+  const int lane = threadIdx.x & 31;
+  float v[VPL];
+  uint32_t key[VPL];
+  bool nan_seen = false;
+  // all of the lane's loads first (one round trip), then the sums in the
+  // fixed order 0 + part_0 + part_1 + ... + bias
+  float pa[VPL], ba[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    pa[j] = (e < E) ? __ldg(part + (long long)t * E + e) : 0.0f;
+    ba[j] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
+  }
+  for (int q = 1; q < KS; ++q) {
+    float pq[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      pq[j] = (e < E) ? __ldg(part + ((long long)q * T + t) * E + e) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) pa[j] += pq[j];
+  }
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    float s = -INFINITY;
+    uint32_t kk = 0u;  // empty; every real key is larger
+    if (e < E) {
+      s = 0.0f + pa[j];
+      if (bias) s += ba[j];
+      logits[(long long)t * E + e] = s;
+      if (s != s) {
+        nan_seen = true;
+        s = -INFINITY;
+      }
+      kk = ord_key(s);
+    }
+    v[j] = s;
+    key[j] = kk;
+  }
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, MOE_DEVERR_NAN_LOGIT);
+
+  // lane r keeps the r-th choice
+  float my_v = -INFINITY;
+  int my_e = 0;
+  for (int r = 0; r < k; ++r) {
+    uint32_t bk = 0u;
+    int bj = 0;
+    float bv = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const bool better = key[j] > bk;
+      bk = better ? key[j] : bk;
+      bv = better ? v[j] : bv;
+      bj = better ? j : bj;
+    }
+    const uint32_t M = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t win =
+        __reduce_min_sync(0xffffffffu, bk == M ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+    const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31u));
+    if ((int)(win & 31u) == lane) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) key[j] = (j == (int)(win >> 5)) ? 0u : key[j];
+    }
+    if (lane == r) {
+      my_v = wv;
+      my_e = (int)win;
+    }
+  }
+  if (lane < k) {
+    idx_out[(long long)t * k + lane] = my_e;
+    s_vw[lane] = my_v;
+    atomicAdd(&cnt[my_e], 1);
+  }
+}
+
+// Routing weights of the tokens tb .. tb + kTokPerBlock - 1 (those < tend)
+// from their kept logits s_v (after a __syncthreads): w_r = exp(l_r - l_0) /
+// sum_i exp(l_i - l_0) in double-float arithmetic (within one ulp of the fp64
+// value; see softmax_df.cuh); with infinite logits the limit: +inf experts
+// share equally, all -inf share equally.  A warp takes 32 / kp tokens at once
+// (lane: token, slot), kp = 8 or 16 >= k; the sum over a token's slots is a
+// fixed butterfly (the same order on every run).
+__device__ __forceinline__ void softmax_weights(int tb, int tend, int k,
+                                                const float (*s_v)[kMaxK],
+                                                float* __restrict__ w_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kp = (k <= 8) ? 8 : 16;
+  const int tpw = 32 / kp;  // tokens per warp
+  const int tl = warp * tpw + lane / kp, r = lane % kp;
+  if (warp * tpw < kTokPerBlock) {
+    const int tt = tb + tl;
+    const bool on = tl < kTokPerBlock && tt < tend && r < k;
+    const dflt ex = on ? df_softmax_term(s_v[tl][r], s_v[tl][0]) : dflt{0.0f, 0.0f};
+    dflt den = ex;
+    for (int off = kp >> 1; off > 0; off >>= 1) {
+      const dflt o = {__shfl_xor_sync(0xffffffffu, den.hi, off),
+                      __shfl_xor_sync(0xffffffffu, den.lo, off)};
+      den = df_add(den, o);
+    }
+    if (on) w_out[(long long)tt * k + r] = df_div(ex, den).hi;
+  }
+}
+
+// One warp per token, 32 tokens per block (one block = one row of the
+// histogram): top-k of each token (topk_warp), then the block's weights and
+// its per-expert counts hist[block][e].
 template <int VPL>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float* __restrict__ part, int KS, int T, int E, int k, const float* __restrict__ bias,
@@ -46,182 +161,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     int32_t* __restrict__ hist, int* __restrict__ err) {
   __shared__ int cnt[kMaxE];
   __shared__ float s_v[kTokPerBlock][kMaxK];  // the kept logits of each token, in order
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-
   const int t = blockIdx.x * kTokPerBlock + warp;
-  if (t < T) {
-    float v[VPL];
-    uint32_t key[VPL];
-    bool nan_seen = false;
-    // all of the lane's loads first (one round trip), then the sums in the
-    // fixed order 0 + part_0 + part_1 + ... + bias
-    float pa[VPL], ba[VPL];
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      pa[j] = (e < E) ? __ldg(part + (long long)t * E + e) : 0.0f;
-      ba[j] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
-    }
-    for (int q = 1; q < KS; ++q) {
-      float pq[VPL];
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        pq[j] = (e < E) ? __ldg(part + ((long long)q * T + t) * E + e) : 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) pa[j] += pq[j];
-    }
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      float s = -INFINITY;
-      uint32_t kk = 0u;  // empty; every real key is larger
-      if (e < E) {
-        s = 0.0f + pa[j];
-        if (bias) s += ba[j];
-        logits[(long long)t * E + e] = s;
-        if (s != s) {
-          nan_seen = true;
-          s = -INFINITY;
-        }
-        kk = ord_key(s);
-      }
-      v[j] = s;
-      key[j] = kk;
-    }
-    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, MOE_DEVERR_NAN_LOGIT);
-
-    // lane r keeps the r-th choice
-    float my_v = -INFINITY;
-    int my_e = 0;
-    for (int r = 0; r < k; ++r) {
-      uint32_t bk = 0u;
-      int bj = 0;
-      float bv = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const bool better = key[j] > bk;
-        bk = better ? key[j] : bk;
-        bv = better ? v[j] : bv;
-        bj = better ? j : bj;
-      }
-      const uint32_t M = __reduce_max_sync(0xffffffffu, bk);
-      const uint32_t win =
-          __reduce_min_sync(0xffffffffu, bk == M ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
-      const float wv = __shfl_sync(0xffffffffu, bv, (int)(win & 31u));
-      if ((int)(win & 31u) == lane) {
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) key[j] = (j == (int)(win >> 5)) ? 0u : key[j];
-      }
-      if (lane == r) {
-        my_v = wv;
-        my_e = (int)win;
-      }
-    }
-    if (lane < k) {
-      idx_out[(long long)t * k + lane] = my_e;
-      s_v[warp][lane] = my_v;
-      atomicAdd(&cnt[my_e], 1);
-    }
-
-  }
+  if (t < T) topk_warp<VPL>(part, KS, T, E, k, bias, logits, idx_out, t, s_v[warp], cnt, err);
   __syncthreads();
-  // weights: w_r = exp(l_r - l_0) / sum_i exp(l_i - l_0) in double-float
-  // arithmetic (within one ulp of the fp64 value; see softmax_df.cuh); with
-  // infinite logits the limit: +inf experts share equally, all -inf share
-  // equally.  A warp takes 32 / kp tokens at once (lane: token, slot),
-  // kp = 8 or 16 >= k; the sum over a token's slots is a fixed butterfly
-  // (the same order on every run).
-  {
-    const int kp = (k <= 8) ? 8 : 16;
-    const int tpw = 32 / kp;  // tokens per warp
-    const int tl = warp * tpw + lane / kp, r = lane % kp;
-    if (warp * tpw < kTokPerBlock) {
-      const int tt = blockIdx.x * kTokPerBlock + tl;
-      const bool on = tl < kTokPerBlock && tt < T && r < k;
-      const dflt ex = on ? df_softmax_term(s_v[tl][r], s_v[tl][0]) : dflt{0.0f, 0.0f};
-      dflt den = ex;
-      for (int off = kp >> 1; off > 0; off >>= 1) {
-        const dflt o = {__shfl_xor_sync(0xffffffffu, den.hi, off),
-                        __shfl_xor_sync(0xffffffffu, den.lo, off)};
-        den = df_add(den, o);
-      }
-      if (on) w_out[(long long)tt * k + r] = df_div(ex, den).hi;
-    }
-  }
+  softmax_weights(blockIdx.x * kTokPerBlock, T, k, s_v, w_out);
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     hist[(long long)blockIdx.x * E + e] = cnt[e];
-}
-
-// The gate/up GEMM's B operand in grouped order: xp[r] = fp16(x[perm[r]])
-// for every grouped row r, so that the GEMM loads whole 16-row tiles by TMA
-// (a gather of 4 rows per operation measured as that kernel's limit).  One
-// warp per row, the row's loads issued together; the warp of a shared-expert
-// row (r = T k + t) also computes that token's gate sigma = sigmoid(w_sg . x)
-// and the row's weight.
-constexpr int kPermThreads = 256;
-constexpr int kPermRows = kPermThreads / 32;
-
-__global__ void __launch_bounds__(kPermThreads) permute_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int R, int Tk, int d,
-    const uint16_t* __restrict__ w_sg, int has_shared, float* __restrict__ sigma,
-    float* __restrict__ wrow, uint16_t* __restrict__ xp) {
-  extern __shared__ uint4 s_wsg[];  // d / 8
-  for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
-    s_wsg[i] = has_shared ? reinterpret_cast<const uint4*>(w_sg)[i] : make_uint4(0, 0, 0, 0);
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * kPermRows + warp;
-  if (r >= R) return;
-  const int t = perm[r];
-  const bool gate = has_shared && r >= Tk;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)t * d);
-  uint4* xo = reinterpret_cast<uint4*>(xp + (long long)r * d);
-  float dot = 0.0f;
-  for (int c0 = lane; c0 < d / 8; c0 += 32 * 8) {
-    uint4 raw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + 32 * i < d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c = c0 + 32 * i;
-      if (c < d / 8) {
-        const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        uint32_t hv[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(wv[q] << 16);
-          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
-          const __half2 h2 = __floats2half2_rn(lo, hi);
-          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        if (gate) {
-          const uint4 sg = s_wsg[c];
-          const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), dot);
-            dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
-                       dot);
-          }
-        }
-      }
-    }
-  }
-  if (gate) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    if (lane == 0) {
-      const float sg = 1.0f / (1.0f + expf(-dot));
-      sigma[t] = sg;
-      wrow[r] = sg;
-    }
-  }
 }
 
 // Exclusive scan of one value per thread over the whole block (<= 1024
@@ -254,6 +202,71 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   return r;
 }
 
+// Shared memory of offsets_and_tiles.
+struct TileSmem {
+  int warp_tot[32];
+  int total;
+  int clsb[17];
+  int wcls[32][16];  // per warp: experts of each remainder class
+};
+
+// Offsets over the routed experts and the tile map, from every expert's
+// count; one block, every thread (<= 1024, > E): thread e < E passes expert
+// e's count, thread E the shared expert's (T; 0 without one), the others 0.
+// Tile map: full kTileRows-row tiles first (expert order, shared last), then
+// each expert's remainder tile, larger remainders first (ties in expert
+// order).  The shared expert (index E, rows T*k .. T*k+T-1) takes part like
+// any expert.
+__device__ void offsets_and_tiles(int cnt, int T, int E, int k, int has_shared,
+                                  int32_t* __restrict__ offsets, int4* __restrict__ tiles,
+                                  int32_t* __restrict__ ntiles, TileSmem& sm) {
+  const int tid = threadIdx.x;
+  const int nexp = E + (has_shared ? 1 : 0);
+  // offsets over the routed experts
+  const int off = block_exclusive_scan(tid < E ? cnt : 0, sm.warp_tot, &sm.total);
+  if (tid <= E) offsets[tid] = (tid < E) ? off : sm.total;
+  // full tiles, all experts (shared last)
+  const int nf = (tid < nexp) ? cnt / kTileRows : 0;
+  const int full_off = block_exclusive_scan(nf, sm.warp_tot, &sm.total);
+  const int total_full = sm.total;
+  // remainder tiles: class c = npad/16 - 1, larger classes first
+  static_assert(kTileRows / 16 <= 16, "remainder classes");
+  const int tail = (tid < nexp) ? cnt % kTileRows : 0;
+  const int cls = tail ? ((tail + 15) >> 4) - 1 : -1;
+  if (tid < 17) sm.clsb[tid] = 0;
+  if (tid < 32 * 16) (&sm.wcls[0][0])[tid] = 0;
+  __syncthreads();
+  if (cls >= 0) atomicAdd(&sm.clsb[cls], 1);
+  // rank of the expert among the lower-indexed experts of its class: within
+  // the warp by matching lanes, then the counts of the earlier warps
+  const int lane = tid & 31, wid = tid >> 5;
+  const unsigned same = __match_any_sync(0xffffffffu, cls);
+  const int wrank = __popc(same & ((1u << lane) - 1u));
+  if (cls >= 0 && wrank == 0) sm.wcls[wid][cls] = __popc(same);
+  __syncthreads();
+  if (tid == 0) {
+    int run = total_full;
+    for (int c = 15; c >= 0; --c) {
+      const int n = sm.clsb[c];
+      sm.clsb[c] = run;
+      run += n;
+    }
+    *ntiles = run;
+  }
+  __syncthreads();
+  if (tid < nexp) {
+    const int e = tid;
+    const int row_base = (e < E) ? off : T * k;
+    for (int i = 0; i < nf; ++i)
+      tiles[full_off + i] = make_int4(e, row_base + i * kTileRows, kTileRows, kTileRows);
+    if (cls >= 0) {
+      int rank = wrank;
+      for (int w = 0; w < wid; ++w) rank += sm.wcls[w][cls];
+      tiles[sm.clsb[cls] + rank] = make_int4(e, row_base + nf * kTileRows, tail, (tail + 15) & ~15);
+    }
+  }
+}
+
 // Single block.  Per expert: exclusive scan of the block histograms over
 // blocks (base[b][e]), the total count, the exclusive scan over experts
 // (offsets), and the tile map: full 256-row tiles first (expert order), then
@@ -272,14 +285,10 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(
     const int32_t* __restrict__ hist, int nblk, int T, int E, int k, int has_shared,
     int32_t* __restrict__ base, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int4* __restrict__ tiles, int32_t* __restrict__ ntiles, unsigned* __restrict__ ticket) {
-  __shared__ int warp_tot[32];
-  __shared__ int s_total;
-  __shared__ int s_clsb[17];
+  __shared__ TileSmem tsm;
   __shared__ int s_part[1024];
-  __shared__ int s_wcls[32][16];  // per warp: experts of each remainder class
   __shared__ int s_last;
   const int tid = threadIdx.x;
-  const int nexp = E + (has_shared ? 1 : 0);
 
   const int EB = (E + gridDim.x - 1) / gridDim.x;  // experts of this block
   const int e0 = blockIdx.x * EB, ne = min(E, e0 + EB) - e0;
@@ -339,48 +348,7 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(
   if (tid == E && has_shared) cnt = T;
   if (tid == 0 && gridDim.x > 1) *ticket = 0u;  // for the next call
   __syncthreads();
-  // offsets over the routed experts
-  const int off = block_exclusive_scan(tid < E ? cnt : 0, warp_tot, &s_total);
-  if (tid <= E) offsets[tid] = (tid < E) ? off : s_total;
-  // full tiles, all experts (shared last)
-  const int nf = (tid < nexp) ? cnt / kTileRows : 0;
-  const int full_off = block_exclusive_scan(nf, warp_tot, &s_total);
-  const int total_full = s_total;
-  // remainder tiles: class c = npad/16 - 1 (0..15), larger classes first
-  const int tail = (tid < nexp) ? cnt % kTileRows : 0;
-  const int cls = tail ? ((tail + 15) >> 4) - 1 : -1;
-  if (tid < 17) s_clsb[tid] = 0;
-  if (tid < 32 * 16) (&s_wcls[0][0])[tid] = 0;
-  __syncthreads();
-  if (cls >= 0) atomicAdd(&s_clsb[cls], 1);
-  // rank of the expert among the lower-indexed experts of its class: within
-  // the warp by matching lanes, then the counts of the earlier warps
-  const int lane = tid & 31, wid = tid >> 5;
-  const unsigned same = __match_any_sync(0xffffffffu, cls);
-  const int wrank = __popc(same & ((1u << lane) - 1u));
-  if (cls >= 0 && wrank == 0) s_wcls[wid][cls] = __popc(same);
-  __syncthreads();
-  if (tid == 0) {
-    int run = total_full;
-    for (int c = 15; c >= 0; --c) {
-      const int n = s_clsb[c];
-      s_clsb[c] = run;
-      run += n;
-    }
-    *ntiles = run;
-  }
-  __syncthreads();
-  if (tid < nexp) {
-    const int e = tid;
-    const int row_base = (e < E) ? off : T * k;
-    for (int i = 0; i < nf; ++i)
-      tiles[full_off + i] = make_int4(e, row_base + i * kTileRows, kTileRows, kTileRows);
-    if (cls >= 0) {
-      int rank = wrank;
-      for (int w = 0; w < wid; ++w) rank += s_wcls[w][cls];
-      tiles[s_clsb[cls] + rank] = make_int4(e, row_base + nf * kTileRows, tail, (tail + 15) & ~15);
-    }
-  }
+  offsets_and_tiles(cnt, T, E, k, has_shared, offsets, tiles, ntiles, tsm);
 }
 
 // Scatter (stable counting sort by (expert, token)).  Row of assignment
@@ -438,6 +406,227 @@ __global__ void __launch_bounds__(256) scatter_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused routing: top-k + histogram, scan + tile map, scatter, and the fp16
+// activations the gate/up GEMM gathers from, with the shared-expert gate, in one
+// cooperative launch of G persistent blocks (one per SM at most).  Block b
+// owns the contiguous tokens [b tpb, (b+1) tpb); its per-expert counts are
+// row b of the histogram, so the block order is the token order and the
+// counting sort stays stable (rows of an expert group in ascending token
+// order).  The only grid-wide step is one barrier between the histogram and
+// the scan.
+constexpr int kRouteThreads = 1024;
+constexpr uint64_t kGridWaitNs = 2000000000ull;  // 2 s
+
+struct RouteParams {
+  const float* part;  // router partial logits [KS][T][E] (KS = 1: given logits)
+  int KS, T, E, k, has_shared, d;
+  const float* bias;       // [E] or null
+  const uint16_t* x;       // bf16 [T][d], or null: no permuted activations
+  const uint16_t* w_sg;    // bf16 [d] shared-expert gate (has_shared)
+  float* logits;           // [T][E]
+  int32_t* idx;            // [T][k]
+  float* w;                // [T][k]
+  float* sigma;            // [T]
+  int32_t* hist;           // [G][E]
+  int32_t* counts;         // [E]
+  int32_t* offsets;        // [E+1]
+  int32_t* perm;           // [T(k+1)] grouped row -> token
+  int32_t* slot;           // [T][k] -> grouped row
+  int32_t* dst;            // [T(k+1)] grouped row -> contribution row
+  float* wrow;             // [T(k+1)] grouped row -> routing weight / gate
+  int4* tiles;
+  int32_t* ntiles;
+  uint16_t* xp;            // fp16 [T][d]
+  unsigned* bar;           // [2] grid barrier: arrivals, generation
+  int* err;
+};
+
+// Grid-wide barrier of a cooperative launch (every block resident).  Gives
+// up after kGridWaitNs, setting MOE_DEVERR_GRID_TIMEOUT (the results are then
+// wrong, but the kernel ends).
+__device__ void route_grid_sync(unsigned* bar, int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned* gen = bar + 1;
+    const unsigned g = *gen;
+    __threadfence();
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);  // for the next launch
+      __threadfence();
+      atomicExch(bar + 1, g + 1);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (*gen == g) {
+        __nanosleep(100);
+        if (globaltimer_ns() - t0 > kGridWaitNs) {
+          atomicOr(err, MOE_DEVERR_GRID_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_constant__ RouteParams p) {
+  __shared__ int cnt[kMaxE];       // block histogram, then running ranks
+  __shared__ int row0[kMaxE];      // offsets[e] + this block's base for e
+  __shared__ uint32_t mask[kMaxE]; // tokens of a 32-token group choosing e
+  __shared__ float s_v[kTokPerBlock][kMaxK];
+  __shared__ TileSmem tsm;
+  __shared__ int s_before[kRouteThreads];  // partial column sums of the histogram
+  __shared__ int s_all[kRouteThreads];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.T, E = p.E, k = p.k, G = gridDim.x, b = blockIdx.x;
+  const int k1 = k + (p.has_shared ? 1 : 0);
+  const int tpb = (T + G - 1) / G;
+  const int t0 = min(T, b * tpb), t1 = min(T, t0 + tpb);
+
+  // ---- 1. top-k of the block's tokens (one warp per token), weights, counts
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int tb = t0; tb < t1; tb += kTokPerBlock) {
+    const int t = tb + warp;
+    if (warp < kTokPerBlock && t < t1)
+      topk_warp<VPL>(p.part, p.KS, T, E, k, p.bias, p.logits, p.idx, t, s_v[warp], cnt, p.err);
+    __syncthreads();
+    softmax_weights(tb, t1, k, s_v, p.w);
+    __syncthreads();
+  }
+  for (int e = tid; e < E; e += blockDim.x) p.hist[(long long)b * E + e] = cnt[e];
+  route_grid_sync(p.bar, p.err);
+
+  // ---- 2. per expert: this block's base (the counts of the blocks before
+  // it) and the total.  Thread tid = part * E + e sums part `part` of the
+  // blocks' counts of expert e; one thread per expert adds the parts in order.
+  {
+    const int nparts = kRouteThreads / E;  // >= 2 (E <= kMaxE = 512)
+    const int chunk = (G + nparts - 1) / nparts;
+    const int part = tid / E, e = tid - part * E;
+    if (part < nparts) {
+      const int g0 = min(G, part * chunk), g1 = min(G, g0 + chunk);
+      int before = 0, all = 0;
+#pragma unroll 8
+      for (int g = g0; g < g1; ++g) {
+        const int c = __ldcg(p.hist + (long long)g * E + e);
+        all += c;
+        before += (g < b) ? c : 0;
+      }
+      s_before[tid] = before;
+      s_all[tid] = all;
+    }
+    __syncthreads();
+  }
+  int tot = 0, base = 0;
+  if (tid < E) {
+    const int nparts = kRouteThreads / E;
+    for (int q = 0; q < nparts; ++q) {
+      tot += s_all[q * E + tid];
+      base += s_before[q * E + tid];
+    }
+  }
+  // exclusive scan over the experts' totals
+  const int off = block_exclusive_scan(tid < E ? tot : 0, tsm.warp_tot, &tsm.total);
+  if (tid < E) {
+    row0[tid] = off + base;
+    cnt[tid] = 0;  // running ranks of step 3
+    mask[tid] = 0u;
+  }
+  if (b == 0) {
+    if (tid < E) p.counts[tid] = tot;
+    int c = (tid < E) ? tot : 0;
+    if (tid == E && p.has_shared) c = T;
+    offsets_and_tiles(c, T, E, k, p.has_shared, p.offsets, p.tiles, p.ntiles, tsm);
+  }
+  __syncthreads();
+
+  // ---- 3. scatter, 32 tokens at a time: row of (t, j) with expert e =
+  // row0[e] + (tokens of this block before t that chose e)
+  for (int tb = t0; tb < t1; tb += 32) {
+    for (int a = tid; a < 32 * k; a += blockDim.x) {
+      const int tl = a / k, t = tb + tl;
+      if (t < t1) atomicOr(&mask[p.idx[(long long)t * k + (a - tl * k)]], 1u << tl);
+    }
+    __syncthreads();
+    for (int a = tid; a < 32 * k; a += blockDim.x) {
+      const int tl = a / k, j = a - tl * k, t = tb + tl;
+      if (t < t1) {
+        const int e = p.idx[(long long)t * k + j];
+        const int row = row0[e] + cnt[e] + __popc(mask[e] & ((1u << tl) - 1u));
+        p.perm[row] = t;
+        p.slot[(long long)t * k + j] = row;
+        p.wrow[row] = p.w[(long long)t * k + j];
+        p.dst[row] = t * k1 + j;
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+      cnt[e] += __popc(mask[e]);
+      mask[e] = 0u;
+    }
+    __syncthreads();
+  }
+  if (p.has_shared) {
+    for (int t = t0 + tid; t < t1; t += blockDim.x) {
+      p.perm[T * k + t] = t;
+      p.dst[T * k + t] = t * k1 + k;
+    }
+  }
+  if (!p.x) return;
+
+  // ---- 4. the fp16 copy of the activations, xp[t] = fp16(x[t]), from which
+  // the gate/up GEMM gathers its token rows (one warp per token); the shared
+  // gate sigma = sigmoid(w_sg . x) on the way
+  for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (long long)t * p.d);
+    uint4* xo = reinterpret_cast<uint4*>(p.xp + (long long)t * p.d);
+    float dot = 0.0f;
+    for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 8) {
+      uint4 raw[8];  // the lane's loads issued together
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + 32 * i;
+        if (c >= p.d / 8) break;
+        const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(wv[q] << 16);
+          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        if (p.has_shared) {
+          const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.w_sg) + c);
+          const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), dot);
+            dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
+                       dot);
+          }
+        }
+      }
+    }
+    if (p.has_shared) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (lane == 0) {
+        const float sg = 1.0f / (1.0f + expf(-dot));
+        p.sigma[t] = sg;
+        p.wrow[T * k + t] = sg;
+      }
+    }
+  }
+}
+
 // out[t][f] = sum_{j=0}^{k1-1} Y[t*k1 + j][f], fp32 in slot order (the
 // shared expert's term last), rounded once to bf16.  The routing weights were
 // applied when the rows of Y were written.  A thread's loads of all k1 rows
@@ -472,48 +661,69 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
+// Blocks of the fused routing launch: one per 32 tokens, at most as many as
+// can be resident at once (a cooperative launch; one per SM).
+template <int VPL>
+cudaError_t launch_route_vpl(const Handle* h, const RouteParams& p, cudaStream_t st) {
+  static int per_sm = -1;
+  if (per_sm < 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_kernel<VPL>, kRouteThreads,
+                                                      0) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      return cudaErrorLaunchOutOfResources;
+    }
+  }
+  const int want = (p.T + kTokPerBlock - 1) / kTokPerBlock;
+  const int cap = h->num_sms * per_sm;
+  const int G = want < cap ? want : cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_kernel<VPL>, p);
+}
+
 }  // namespace
 
-cudaError_t launch_topk(const Handle* h, const float* part, int KS, int T, const float* bias,
-                        cudaStream_t st) {
+cudaError_t launch_route(const Handle* h, const float* part, int KS, int T, const float* bias,
+                         const uint16_t* x, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const Workspace& ws = h->ws;
-  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
-  if (c.E <= 256)
-    topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, ws.logits, ws.idx,
-                                                  ws.w, ws.hist, h->dev_err);
-  else
-    topk_kernel<16><<<nblk, kTopkThreads, 0, st>>>(part, KS, T, c.E, c.k, bias, ws.logits, ws.idx,
-                                                   ws.w, ws.hist, h->dev_err);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_permute(const Handle* h, const uint16_t* x, int T, cudaStream_t st) {
-  const moe_config& c = h->cfg;
-  const Workspace& ws = h->ws;
-  const int R = T * (c.k + (c.has_shared ? 1 : 0));
-  permute_kernel<<<(R + kPermRows - 1) / kPermRows, kPermThreads, (size_t)c.d * 2, st>>>(
-      x, ws.perm, R, T * c.k, c.d, h->w_sg, c.has_shared, ws.sigma, ws.wrow, ws.xp);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scan_tiles(const Handle* h, int T, cudaStream_t st) {
-  const moe_config& c = h->cfg;
-  const Workspace& ws = h->ws;
-  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
-  const int nb = c.E >= 64 ? (c.E / 32 < 8 ? c.E / 32 : 8) : 1;  // experts split over blocks
-  scan_tiles_kernel<<<nb, 1024, 0, st>>>(ws.hist, nblk, T, c.E, c.k, c.has_shared, ws.base,
-                                         ws.counts, ws.offsets, ws.tiles, ws.ntiles, ws.ticket);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scatter(const Handle* h, int T, cudaStream_t st) {
-  const moe_config& c = h->cfg;
-  const Workspace& ws = h->ws;
-  const int nblk = (T + kTokPerBlock - 1) / kTokPerBlock;
-  scatter_kernel<<<nblk, 256, 0, st>>>(ws.idx, ws.w, ws.offsets, ws.base, T, c.E, c.k,
-                                       c.has_shared, ws.perm, ws.slot, ws.dst, ws.wrow);
-  return cudaGetLastError();
+  RouteParams p{};
+  p.part = part;
+  p.KS = KS;
+  p.T = T;
+  p.E = c.E;
+  p.k = c.k;
+  p.has_shared = c.has_shared;
+  p.d = c.d;
+  p.bias = bias;
+  p.x = x;
+  p.w_sg = h->w_sg;
+  p.logits = ws.logits;
+  p.idx = ws.idx;
+  p.w = ws.w;
+  p.sigma = ws.sigma;
+  p.hist = ws.hist;
+  p.counts = ws.counts;
+  p.offsets = ws.offsets;
+  p.perm = ws.perm;
+  p.slot = ws.slot;
+  p.dst = ws.dst;
+  p.wrow = ws.wrow;
+  p.tiles = ws.tiles;
+  p.ntiles = ws.ntiles;
+  p.xp = ws.xp;
+  p.bar = ws.ticket + 2;
+  p.err = h->dev_err;
+  return c.E <= 256 ? launch_route_vpl<8>(h, p, st) : launch_route_vpl<16>(h, p, st);
 }
 
 cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st) {

@@ -29,7 +29,7 @@ EXPORTS = ["moe_create", "moe_destroy", "moe_route", "moe_route_from_logits", "m
            "moe_profile_read", "moe_route_from_logits_noalloc", "moe_get_device_error",
            "moe_status_string", "moe_last_error", "moe_version"]
 
-STAGES = ["router", "topk", "scan", "scatter", "permute", "gate_up", "down", "combine"]
+STAGES = ["router", "routing", "gate_up", "down", "combine"]
 
 
 class MoEError(RuntimeError):
