@@ -58,7 +58,7 @@ extern "C" {
 typedef enum moe_status {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or config value   */
-  MOE_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. group != 64)   */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. group = 96)    */
   MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed                     */
   MOE_ERR_OOM = 4,         /* device allocation failed                       */
   MOE_ERR_DEVICE = 5       /* the device error word is set                   */
@@ -87,8 +87,13 @@ typedef struct moe_config {
   int E;           /* routed experts; 1..512                                 */
   int k;           /* experts kept per token; 1..min(E, 16)                  */
   int I;           /* expert intermediate size (routed and shared); mult. 128 */
-  int group;       /* quantisation group along K; must be 64                 */
-  int scale_dtype; /* MOE_SCALE_F16 (MOE_SCALE_BF16: MOE_ERR_UNSUPPORTED)    */
+  int group;       /* quantisation group along K: a multiple of 64 dividing
+                      d and I (64 on the pages); else MOE_ERR_UNSUPPORTED    */
+  int scale_dtype; /* MOE_SCALE_F16 or MOE_SCALE_BF16 (the pages' format;
+                      converted to fp16 at moe_create: exact for 0 and every
+                      magnitude in [2^-17, 65504]; a finite value with no
+                      exact fp16 value (above 65504, or tiny with bits below
+                      2^-24) makes moe_create return MOE_ERR_UNSUPPORTED)   */
   int max_tokens;  /* tokens per internal chunk (workspace is sized for it)  */
   int has_shared;  /* 1: one sigmoid-gated shared expert; 0: none            */
   int layouts;     /* MOE_LAYOUT_* bitmask, 0 = both                         */
@@ -99,11 +104,11 @@ typedef struct moe_config {
  * moe_create, which makes the handle's own repacked copy; the caller may free
  * them once moe_create returns).
  *   Codes: uint8, two 4-bit codes per byte, the even K index in the low
- *   nibble; matrices are [out][in] row-major, groups of 64 contiguous along in.
+ *   nibble; matrices are [out][in] row-major, groups contiguous along in.
  *   Scales and biases: 16-bit (scale_dtype), [out][in / group].
- *   gu_*: [E][2I][d/2] codes, [E][2I][d/64] s and beta; rows 0..I-1 are the
- *         gate projection, rows I..2I-1 the up projection.
- *   dn_*: [E][d][I/2] codes, [E][d][I/64] s and beta.
+ *   gu_*: [E][2I][d/2] codes, [E][2I][d/group] s and beta; rows 0..I-1 are
+ *         the gate projection, rows I..2I-1 the up projection.
+ *   dn_*: [E][d][I/2] codes, [E][d][I/group] s and beta.
  *   sh_*: the shared expert, same layouts with E = 1 (ignored if !has_shared).
  *   w_router: bf16 [E][d].   w_shared_gate: bf16 [d] (ignored if !has_shared).
  */

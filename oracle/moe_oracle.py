@@ -51,13 +51,22 @@ def unpack_codes(packed: np.ndarray) -> np.ndarray:
     return out
 
 
+def scale_values(a) -> np.ndarray:
+    """Exact fp64 values of a scale or bias array: np.uint16 arrays are bf16
+    bit patterns (the checkpoint format on the pages, §"Dequantize weights
+    during matrix multiplication"), anything else holds values (fp16)."""
+    a = np.asarray(a)
+    return bf16_values(a) if a.dtype == np.uint16 else a.astype(F64)
+
+
 def dequantize(packed, scale, bias, group: int = 64) -> np.ndarray:
     """Reconstruct a [rows, K] matrix: w[n, c] = s[n, c // g] * q[n, c] + beta[n, c // g].
 
-    ``scale`` and ``bias`` are fp16 or bf16-valued arrays [rows, K/g]."""
+    ``scale`` and ``bias`` are [rows, K/g]: fp16 values, or bf16 bit patterns
+    (np.uint16); ``g`` is the quantisation group along K."""
     q = unpack_codes(packed).astype(F64)
-    s = np.repeat(np.asarray(scale).astype(F64), group, axis=-1)
-    b = np.repeat(np.asarray(bias).astype(F64), group, axis=-1)
+    s = np.repeat(scale_values(scale), group, axis=-1)
+    b = np.repeat(scale_values(bias), group, axis=-1)
     assert s.shape == q.shape, (s.shape, q.shape)
     return s * q + b
 

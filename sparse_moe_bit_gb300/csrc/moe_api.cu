@@ -109,10 +109,10 @@ moe_status validate_config(const moe_config* c) {
     return fail(MOE_ERR_INVALID_ARG, "k=%d not in [1, min(E, %d)]", c->k, kMaxK);
   if (c->I < 128 || c->I % 128 != 0 || c->I > 8192)
     return fail(MOE_ERR_INVALID_ARG, "I=%d must be a multiple of 128 in [128, 8192]", c->I);
-  if (c->group != 64) return fail(MOE_ERR_UNSUPPORTED, "group=%d: only 64 is implemented", c->group);
-  if (c->scale_dtype == MOE_SCALE_BF16)
-    return fail(MOE_ERR_UNSUPPORTED, "bf16 scale/bias is not implemented");
-  if (c->scale_dtype != MOE_SCALE_F16)
+  if (c->group < 64 || c->group % 64 != 0 || c->d % c->group != 0 || c->I % c->group != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "group=%d: must be a multiple of 64 dividing d=%d and I=%d",
+                c->group, c->d, c->I);
+  if (c->scale_dtype != MOE_SCALE_F16 && c->scale_dtype != MOE_SCALE_BF16)
     return fail(MOE_ERR_INVALID_ARG, "scale_dtype=%d unknown", c->scale_dtype);
   if (c->max_tokens < 1 || c->max_tokens > (1 << 20))
     return fail(MOE_ERR_INVALID_ARG, "max_tokens=%d not in [1, 2^20]", c->max_tokens);
@@ -334,11 +334,20 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, void* stream,
     return s;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = launch_repack(h, w, st);
+  e = cudaMemsetAsync(h->dev_err, 0, 16, st);  // ordered before the repack's flag
+  if (e == cudaSuccess) e = launch_repack(h, w, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  int rerr = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&rerr, h->dev_err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) {
     free_handle(h);
     return cuda_fail(e, "repack");
+  }
+  if (rerr & kRepackScaleInexact) {
+    free_handle(h);
+    return fail(MOE_ERR_UNSUPPORTED,
+                "a bf16 scale/bias has no exact fp16 value (magnitude above 65504, or below "
+                "2^-17 with bits under 2^-24)");
   }
   h->last_stream = st;
   *out = h;

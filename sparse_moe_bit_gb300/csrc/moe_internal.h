@@ -16,6 +16,9 @@ constexpr int kTileRows = 192;    // largest token tile of the grouped GEMMs (TM
 constexpr int kUnitRows = 256;    // weight rows per tensor-core work unit (2 x M=128)
 constexpr int kCodeChunk = 9216;  // 256 rows x (32 B codes + 4 B scale/bias)
 constexpr int kRouterChunk = 32768;  // 256 rows x 64 bf16, pre-swizzled
+// device error word bit set by the repack when a bf16 scale/bias has no exact
+// fp16 value (moe_create then refuses the weights; never seen by callers)
+constexpr int kRepackScaleInexact = 1 << 30;
 
 // Per-handle scratch, sized for cfg.max_tokens tokens.
 struct Workspace {

@@ -16,6 +16,14 @@
 // block kb: two 128 x 64 bf16 tiles in the 128-byte swizzled K-major order of
 // the tensor-core operand (16-byte chunk c of row r stored at chunk c ^ (r%8)).
 //
+// Scale and bias: the kernels read one 32-bit word per row and 64-wide K
+// block (fp16 scale | fp16 bias << 16).  The caller's pairs may cover groups
+// of any multiple of 64 along K (each pair is repeated over its blocks, which
+// is exact) and may be bf16: bf16 -> fp16 is exact for 0 and for magnitudes
+// 2^-17 .. 65504 (fp16 keeps bf16's 8 significant bits there); a finite value
+// that does not survive the conversion sets a flag on which moe_create
+// refuses the weights.
+//
 // Decode layout: one array over all experts (shared expert last) in which
 // everything a CTA reads for a run of features is contiguous, so that one
 // bulk copy brings it in.  Gate/up: per expert, per feature f, one unit of
@@ -25,6 +33,7 @@
 // each output row the block's 16 bytes of codes (all rows of a block
 // contiguous), then the rows' scale/bias words per input group of 64.  Codes
 // keep their canonical nibble order.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
@@ -42,14 +51,33 @@ struct ExpertSrc {
   int E;
   int R;  // rows per expert
   int K;  // inner size
+  int group;  // quantisation group along K (a multiple of 64)
+  int bf16;   // scale/bias are bf16 (else fp16)
+  int* bad;   // kRepackScaleInexact set here when a bf16 value has no exact fp16
 };
+
+// 16-bit scale or bias as fp16 bits
+__device__ __forceinline__ uint32_t f16_bits(const ExpertSrc& s, uint16_t v) {
+  if (!s.bf16) return v;
+  const float f = __uint_as_float((uint32_t)v << 16);
+  const __half h = __float2half_rn(f);
+  if (f == f && __half2float(h) != f) atomicOr(s.bad, kRepackScaleInexact);
+  return __half_as_ushort(h);
+}
+
+// kernel word of row `row`, 64-wide K block `kb` (fp16 scale | fp16 bias << 16)
+__device__ __forceinline__ uint32_t sb_word(const ExpertSrc& s, const uint16_t* sc,
+                                            const uint16_t* bi, int row, int kb) {
+  const long long gi = (long long)row * (s.K / s.group) + kb / (s.group / 64);
+  return f16_bits(s, sc[gi]) | (f16_bits(s, bi[gi]) << 16);
+}
 
 __device__ __forceinline__ void expert_ptrs(const ExpertSrc& s, int x, const uint8_t*& c,
                                             const uint16_t*& sc, const uint16_t*& bi) {
   if (x < s.E) {
     c = s.codes + (long long)x * s.R * (s.K / 2);
-    sc = s.scale + (long long)x * s.R * (s.K / 64);
-    bi = s.bias + (long long)x * s.R * (s.K / 64);
+    sc = s.scale + (long long)x * s.R * (s.K / s.group);
+    bi = s.bias + (long long)x * s.R * (s.K / s.group);
   } else {
     c = s.sh_codes;
     sc = s.sh_scale;
@@ -93,8 +121,7 @@ __global__ void repack_prefill_kernel(ExpertSrc s, int nexp, int MU, int gate_up
     uint4* dst = reinterpret_cast<uint4*>(chunk + r * 32);
     dst[0] = make_uint4(permute_word(a.x), permute_word(a.y), permute_word(a.z), permute_word(a.w));
     dst[1] = make_uint4(permute_word(b.x), permute_word(b.y), permute_word(b.z), permute_word(b.w));
-    const long long gi = (long long)row * (s.K / 64) + kb;
-    reinterpret_cast<uint32_t*>(chunk + 8192)[r] = (uint32_t)sc[gi] | ((uint32_t)bi[gi] << 16);
+    reinterpret_cast<uint32_t*>(chunk + 8192)[r] = sb_word(s, sc, bi, row, kb);
   }
 }
 
@@ -116,10 +143,6 @@ __global__ void repack_router_prefill_kernel(const uint16_t* __restrict__ wr, in
     *reinterpret_cast<uint4*>(chunk + (r >> 7) * 16384 + (r & 127) * 128 + ((c ^ (r & 7)) << 4)) =
         v;
   }
-}
-
-__device__ __forceinline__ uint32_t sb_word(const uint16_t* sc, const uint16_t* bi, long long gi) {
-  return (uint32_t)sc[gi] | ((uint32_t)bi[gi] << 16);
 }
 
 // decode gate/up units: thread per 16-byte piece of a unit
@@ -144,9 +167,8 @@ __global__ void repack_decode_gu_kernel(ExpertSrc s, int nexp, int I, uint8_t* _
       const int w = (o - d) / 4;  // first of four words
       const int row = (w < ng) ? f : I + f;
       const int g = (w < ng) ? w : w - ng;
-      const long long gi = (long long)row * ng + g;
-      v = make_uint4(sb_word(sc, bi, gi), sb_word(sc, bi, gi + 1), sb_word(sc, bi, gi + 2),
-                     sb_word(sc, bi, gi + 3));
+      v = make_uint4(sb_word(s, sc, bi, row, g), sb_word(s, sc, bi, row, g + 1),
+                     sb_word(s, sc, bi, row, g + 2), sb_word(s, sc, bi, row, g + 3));
     }
     *reinterpret_cast<uint4*>(out + unit * ub + o) = v;
   }
@@ -178,7 +200,7 @@ __global__ void repack_decode_dn_kernel(ExpertSrc s, int nexp, uint8_t* __restri
       const long long xg = w / d;
       const int g = (int)(xg % ng), x = (int)(xg / ng);
       expert_ptrs(s, x, c, sc, bi);
-      sb_out[w] = sb_word(sc, bi, (long long)f * ng + g);
+      sb_out[w] = sb_word(s, sc, bi, f, g);
     }
   }
 }
@@ -201,9 +223,12 @@ __global__ void repack_router_decode_kernel(const uint16_t* __restrict__ wr,
   }
 }
 
-ExpertSrc make_src(const moe_weights* w, const moe_config& c, bool gu) {
+ExpertSrc make_src(const moe_weights* w, const moe_config& c, bool gu, int* bad) {
   ExpertSrc s;
   s.E = c.E;
+  s.group = c.group;
+  s.bf16 = c.scale_dtype == MOE_SCALE_BF16;
+  s.bad = bad;
   if (gu) {
     s.codes = (const uint8_t*)w->gu_codes;
     s.scale = (const uint16_t*)w->gu_scale;
@@ -231,8 +256,8 @@ ExpertSrc make_src(const moe_weights* w, const moe_config& c, bool gu) {
 cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const int grid = h->num_sms * 8;
-  const ExpertSrc gu = make_src(w, c, true);
-  const ExpertSrc dn = make_src(w, c, false);
+  const ExpertSrc gu = make_src(w, c, true, h->dev_err);
+  const ExpertSrc dn = make_src(w, c, false, h->dev_err);
   if (h->layouts & MOE_LAYOUT_PREFILL) {
     repack_prefill_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.I / 128, 1, c.I, h->pf_gu);
     repack_prefill_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, c.d / 256, 0, c.I, h->pf_dn);

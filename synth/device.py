@@ -98,13 +98,14 @@ def make_x(seed: int, T: int, d: int, row0: int = 0, layer: int = 0, device="cud
 def host_layer_to_device(lw: gen.LayerWeights, has_shared=True, device="cuda") -> dict:
     """Upload a host-generated synth.gen.LayerWeights in the canonical layout."""
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
-    bf = lambda bits: t(bits.view(np.int16)).view(torch.bfloat16)
-    w = dict(gu_codes=t(lw.gu_codes), gu_scale=t(lw.gu_scale), gu_bias=t(lw.gu_bias),
-             dn_codes=t(lw.dn_codes), dn_scale=t(lw.dn_scale), dn_bias=t(lw.dn_bias),
+    bf = lambda bits: t(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    sc = lambda a: bf(a) if a.dtype == np.uint16 else t(a)  # bf16 bits or fp16 scales
+    w = dict(gu_codes=t(lw.gu_codes), gu_scale=sc(lw.gu_scale), gu_bias=sc(lw.gu_bias),
+             dn_codes=t(lw.dn_codes), dn_scale=sc(lw.dn_scale), dn_bias=sc(lw.dn_bias),
              w_router=bf(lw.w_router))
     if has_shared:
-        w.update(sh_gu_codes=t(lw.sh_gu_codes), sh_gu_scale=t(lw.sh_gu_scale),
-                 sh_gu_bias=t(lw.sh_gu_bias), sh_dn_codes=t(lw.sh_dn_codes),
-                 sh_dn_scale=t(lw.sh_dn_scale), sh_dn_bias=t(lw.sh_dn_bias),
+        w.update(sh_gu_codes=t(lw.sh_gu_codes), sh_gu_scale=sc(lw.sh_gu_scale),
+                 sh_gu_bias=sc(lw.sh_gu_bias), sh_dn_codes=t(lw.sh_dn_codes),
+                 sh_dn_scale=sc(lw.sh_dn_scale), sh_dn_bias=sc(lw.sh_dn_bias),
                  w_shared_gate=bf(lw.w_shared_gate))
     return w

@@ -23,8 +23,9 @@ Every value is a pure function of (seed, tag, layer, expert, element index):
 
 Quantiser (per group of ``group`` consecutive values along K)
 -----------------------------------------------------------
-``s = fp16((max - min) / 15)``, ``beta = fp16(min)`` (fp32 arithmetic, one
-rounding per step, round-to-nearest-even), and
+``s = r((max - min) / 15)``, ``beta = r(min)`` with r the rounding to the
+scale type, fp16 or bf16 (fp32 arithmetic, one rounding per step,
+round-to-nearest-even), and
 ``q = clamp(rint((w - beta) / s), 0, 15)`` computed with the ROUNDED s and beta;
 ``q = 0`` where ``s == 0``.  Two codes share a byte, the even K index in the
 low nibble.  Weights are [out, in] row-major with the groups contiguous along
@@ -125,11 +126,12 @@ def bf16_bits_to_fp32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def quantize_rows(w: np.ndarray, group: int = 64):
+def quantize_rows(w: np.ndarray, group: int = 64, scale_dtype: str = "f16"):
     """Group-affine 4-bit quantiser.  ``w``: fp32 [rows, K].
 
-    Returns (packed uint8 [rows, K/2], scale fp16 [rows, K/group],
-    bias fp16 [rows, K/group]).
+    Returns (packed uint8 [rows, K/2], scale [rows, K/group],
+    bias [rows, K/group]); scale and bias are fp16 (np.float16) or, with
+    ``scale_dtype="bf16"``, bf16 bit patterns (np.uint16).
     """
     w = np.ascontiguousarray(w, dtype=np.float32)
     rows, K = w.shape
@@ -137,10 +139,17 @@ def quantize_rows(w: np.ndarray, group: int = 64):
     g = w.reshape(rows, K // group, group)
     mn = g.min(axis=2)
     mx = g.max(axis=2)
-    s16 = ((mx - mn) / np.float32(15.0)).astype(np.float16)
-    b16 = mn.astype(np.float16)
-    s = s16.astype(np.float32)[:, :, None]
-    b = b16.astype(np.float32)[:, :, None]
+    if scale_dtype == "bf16":
+        s16 = round_to_bf16_bits((mx - mn) / np.float32(15.0))
+        b16 = round_to_bf16_bits(mn)
+        s = bf16_bits_to_fp32(s16)[:, :, None]
+        b = bf16_bits_to_fp32(b16)[:, :, None]
+    else:
+        assert scale_dtype == "f16"
+        s16 = ((mx - mn) / np.float32(15.0)).astype(np.float16)
+        b16 = mn.astype(np.float16)
+        s = s16.astype(np.float32)[:, :, None]
+        b = b16.astype(np.float32)[:, :, None]
     with np.errstate(divide="ignore", invalid="ignore"):
         t = (g - b) / s
     q = np.where(s == 0, np.float32(0), np.rint(t))
@@ -149,11 +158,11 @@ def quantize_rows(w: np.ndarray, group: int = 64):
     return packed, s16, b16
 
 
-def quantized_matrix(seed, tag, layer, expert, rows, K, std=0.02, group=64):
+def quantized_matrix(seed, tag, layer, expert, rows, K, std=0.02, group=64, scale_dtype="f16"):
     """Quantised [rows, K] weight matrix of one stream (fp32 draws -> 4-bit)."""
     key = stream_key(seed, tag, layer, expert)
     w = normal_fp32(key, 0, rows * K, std).reshape(rows, K)
-    return quantize_rows(w, group)
+    return quantize_rows(w, group, scale_dtype)
 
 
 def bf16_matrix(seed, tag, layer, expert, rows, K, std, row0=0):
@@ -170,6 +179,7 @@ class MoEShape:
     k: int
     I: int
     group: int = 64
+    scale_dtype: str = "f16"  # "f16" (np.float16) or "bf16" (bit patterns, np.uint16)
 
 
 @dataclass
@@ -179,11 +189,11 @@ class LayerWeights:
     w_router: np.ndarray      # uint16 [E, d]
     w_shared_gate: np.ndarray  # uint16 [d]
     gu_codes: np.ndarray      # uint8 [E, 2I, d/2]  rows 0..I-1 gate, I..2I-1 up
-    gu_scale: np.ndarray      # fp16 [E, 2I, d/g]
-    gu_bias: np.ndarray       # fp16 [E, 2I, d/g]
+    gu_scale: np.ndarray      # fp16 or bf16 bits [E, 2I, d/g]
+    gu_bias: np.ndarray       # fp16 or bf16 bits [E, 2I, d/g]
     dn_codes: np.ndarray      # uint8 [E, d, I/2]
-    dn_scale: np.ndarray      # fp16 [E, d, I/g]
-    dn_bias: np.ndarray       # fp16 [E, d, I/g]
+    dn_scale: np.ndarray      # fp16 or bf16 bits [E, d, I/g]
+    dn_bias: np.ndarray       # fp16 or bf16 bits [E, d, I/g]
     sh_gu_codes: np.ndarray   # uint8 [2I, d/2]
     sh_gu_scale: np.ndarray
     sh_gu_bias: np.ndarray
@@ -195,24 +205,25 @@ class LayerWeights:
 def expert_weights(seed, layer, expert, shape: MoEShape, std=0.02):
     """(gu_codes, gu_scale, gu_bias, dn_codes, dn_scale, dn_bias) of one
     routed expert (``expert`` < E) or of the shared expert (``expert`` == E)."""
-    d, I, g = shape.d, shape.I, shape.group
+    d, I, g, sd = shape.d, shape.I, shape.group, shape.scale_dtype
     if expert == shape.E:
-        gu = quantized_matrix(seed, TAG_SH_GATE_UP, layer, 0, 2 * I, d, std, g)
-        dn = quantized_matrix(seed, TAG_SH_DOWN, layer, 0, d, I, std, g)
+        gu = quantized_matrix(seed, TAG_SH_GATE_UP, layer, 0, 2 * I, d, std, g, sd)
+        dn = quantized_matrix(seed, TAG_SH_DOWN, layer, 0, d, I, std, g, sd)
     else:
-        gu = quantized_matrix(seed, TAG_GATE_UP, layer, expert, 2 * I, d, std, g)
-        dn = quantized_matrix(seed, TAG_DOWN, layer, expert, d, I, std, g)
+        gu = quantized_matrix(seed, TAG_GATE_UP, layer, expert, 2 * I, d, std, g, sd)
+        dn = quantized_matrix(seed, TAG_DOWN, layer, expert, d, I, std, g, sd)
     return gu + dn
 
 
 def make_layer(seed: int, layer: int, shape: MoEShape, std=0.02) -> LayerWeights:
     """All weights of one layer on the host (use for small shapes)."""
     E, d, I, g = shape.E, shape.d, shape.I, shape.group
+    sdt = np.uint16 if shape.scale_dtype == "bf16" else np.float16
     gu_c = np.empty((E, 2 * I, d // 2), np.uint8)
-    gu_s = np.empty((E, 2 * I, d // g), np.float16)
+    gu_s = np.empty((E, 2 * I, d // g), sdt)
     gu_b = np.empty_like(gu_s)
     dn_c = np.empty((E, d, I // 2), np.uint8)
-    dn_s = np.empty((E, d, I // g), np.float16)
+    dn_s = np.empty((E, d, I // g), sdt)
     dn_b = np.empty_like(dn_s)
     for e in range(E):
         gu_c[e], gu_s[e], gu_b[e], dn_c[e], dn_s[e], dn_b[e] = expert_weights(

@@ -52,6 +52,12 @@ def near_tie_tokens(logits: np.ndarray, k: int, gap: float = 1e-4) -> np.ndarray
     return (s[:, k - 1] - s[:, k]) < gap
 
 
+def scale_dtype_code(shape) -> int:
+    """The C ABI's scale_dtype for a synth.gen.MoEShape."""
+    from sparse_moe_bit_gb300 import moe as _moe
+    return _moe.MOE_SCALE_BF16 if shape.scale_dtype == "bf16" else _moe.MOE_SCALE_F16
+
+
 class HostCase:
     """A layer generated on the host (small shapes), uploaded to the GPU."""
 
@@ -60,7 +66,8 @@ class HostCase:
         self.lw = gen.make_layer(seed, layer, shape)
         self.vals = O.layer_values(self.lw, has_shared=has_shared)
         self.w = sd.host_layer_to_device(self.lw, has_shared=has_shared)
-        self.cfg = M.MoEConfig(d=shape.d, E=shape.E, k=shape.k, I=shape.I,
+        self.cfg = M.MoEConfig(d=shape.d, E=shape.E, k=shape.k, I=shape.I, group=shape.group,
+                               scale_dtype=scale_dtype_code(shape),
                                max_tokens=max_tokens, has_shared=int(has_shared), layouts=layouts)
         self.moe = M.MoE(self.cfg, self.w)
 

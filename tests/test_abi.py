@@ -52,7 +52,7 @@ def _cfg(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(d=100), 1), (dict(d=0), 1), (dict(E=0), 1), (dict(E=513), 1), (dict(k=0), 1),
     (dict(k=17, E=32), 1), (dict(k=3, E=2), 1), (dict(I=100), 1), (dict(group=32), 2),
-    (dict(scale_dtype=2), 2), (dict(scale_dtype=7), 1), (dict(max_tokens=0), 1),
+    (dict(group=96), 2), (dict(group=256), 2), (dict(scale_dtype=7), 1), (dict(max_tokens=0), 1),
     (dict(has_shared=2), 1), (dict(layouts=9), 1)])
 def test_create_rejects_bad_config(lib, kw, status):
     from sparse_moe_bit_gb300 import moe
@@ -61,6 +61,16 @@ def test_create_rejects_bad_config(lib, kw, status):
     assert lib.moe_create(ctypes.byref(_cfg(**kw)), ctypes.byref(w), None, ctypes.byref(h)) == status
     assert h.value is None
     assert len(lib.moe_last_error()) > 0
+
+
+@pytest.mark.parametrize("kw", [dict(scale_dtype=2), dict(group=128), dict(group=128, scale_dtype=2)])
+def test_bf16_scales_and_group128_pass_validation(lib, kw):
+    # valid configurations: moe_create gets as far as the weight pointers
+    from sparse_moe_bit_gb300 import moe
+    w = moe._Weights()  # all NULL
+    h = ctypes.c_void_p()
+    assert lib.moe_create(ctypes.byref(_cfg(**kw)), ctypes.byref(w), None, ctypes.byref(h)) == 1
+    assert b"weight" in lib.moe_last_error()
 
 
 def test_create_rejects_null_or_misaligned_weights(lib):

@@ -13,8 +13,13 @@ SRC = os.path.join(ROOT, "oracle", "moe_oracle.py")
 MUTATIONS = [
     ("dropped bias term", "return s * q + b", "return s * q"),
     ("nibble order", "out[..., 0::2] = packed & 0x0F", "out[..., 0::2] = packed >> 4"),
-    ("group index", "s = np.repeat(np.asarray(scale).astype(F64), group, axis=-1)",
-     "s = np.tile(np.asarray(scale).astype(F64), group)"),
+    ("group index", "s = np.repeat(scale_values(scale), group, axis=-1)",
+     "s = np.tile(scale_values(scale), group)"),
+    ("group fixed at 64", "s = np.repeat(scale_values(scale), group, axis=-1)",
+     "s = np.repeat(scale_values(scale), 64, axis=-1)"),
+    ("bf16 scale bits read as fp16",
+     "return bf16_values(a) if a.dtype == np.uint16 else a.astype(F64)",
+     "return a.view(np.float16).astype(F64) if a.dtype == np.uint16 else a.astype(F64)"),
     ("router bias sign", "lg = lg + np.asarray(logit_bias, F64)[None, :]",
      "lg = lg - np.asarray(logit_bias, F64)[None, :]"),
     ("tie-break", "order = np.lexsort((ids, -lg), axis=-1)",

@@ -59,6 +59,38 @@ def test_dequant_hand_example():
     assert np.array_equal(w[1], np.array([float(v) for v in g["expect1"]]))
 
 
+def test_dequant_bf16_group128_hand_example():
+    # bf16 scale/bias given as bit patterns, one pair per 128 weights
+    g = _golden("dequant_bf16_g128.txt")
+    packed = np.array([[int(b, 16) for b in g["bytes0"]],
+                       [int(b, 16) for b in g["bytes1"]]], dtype=np.uint8)
+    scale = np.array([[int(v, 16)] for v in g["scale_bits"]], dtype=np.uint16)
+    bias = np.array([[int(v, 16)] for v in g["bias_bits"]], dtype=np.uint16)
+    w = O.dequantize(packed, scale, bias, 128)
+    assert np.array_equal(w[0], np.array([float(v) for v in g["expect0"]]))
+    assert np.array_equal(w[1], np.array([float(v) for v in g["expect1"]]))
+
+
+def test_bf16_scale_bits_decode_as_bf16():
+    # the same 16 bits mean different numbers in bf16 and fp16
+    assert O.scale_values(np.array([0x3C00], np.uint16))[0] == 2.0 ** -7
+    assert O.scale_values(np.array([0x3C00], np.uint16).view(np.float16))[0] == 1.0
+    assert O.scale_values(np.array([0xC0A0], np.uint16))[0] == -5.0
+
+
+def test_dequant_group128_boundaries():
+    # with 128-wide groups, elements 0..127 use pair 0 and 128..255 pair 1
+    q = np.zeros((1, 256), np.uint8)
+    q[0, 127] = 3
+    q[0, 128] = 5
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    s = np.array([[0.5, 2.0]], np.float16)
+    b = np.array([[1.0, -4.0]], np.float16)
+    w = O.dequantize(packed, s, b, 128)
+    assert w[0, 0] == 1.0 and w[0, 64] == 1.0 and w[0, 127] == 1.0 + 0.5 * 3
+    assert w[0, 128] == -4.0 + 2.0 * 5 and w[0, 255] == -4.0
+
+
 def test_nibble_order_low_is_even():
     q = O.unpack_codes(np.array([[0x21, 0xF0]], np.uint8))
     assert q.tolist() == [[1, 2, 0, 15]]

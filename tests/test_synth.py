@@ -74,3 +74,21 @@ def test_zipf_bias():
     assert sorted(rank.tolist()) == list(range(1, 257))
     assert b[rank == 1][0] == 0.0
     np.testing.assert_allclose(b, (1.5 * np.log(1.0 / rank)).astype(np.float32))
+
+
+def test_quantiser_bf16_scales_group128():
+    # bf16 scale/bias (bit patterns), 128-wide groups: s and beta are the RNE
+    # bf16 roundings of (max - min)/15 and min; the error bound grows by the
+    # coarser rounding (2^-8 relative) of beta and of 15 s
+    w = gen.normal_fp32(gen.stream_key(2, gen.TAG_GATE_UP), 0, 32 * 512, 0.02).reshape(32, 512)
+    packed, s, b = gen.quantize_rows(w, 128, "bf16")
+    assert s.dtype == np.uint16 and b.dtype == np.uint16 and s.shape == (32, 4)
+    g = w.reshape(32, 4, 128)
+    assert np.array_equal(s, gen.round_to_bf16_bits((g.max(2) - g.min(2)) / np.float32(15.0)))
+    assert np.array_equal(b, gen.round_to_bf16_bits(g.min(2)))
+    q = np.empty(w.shape, np.float64); q[:, 0::2] = packed & 15; q[:, 1::2] = packed >> 4
+    sf = np.repeat(gen.bf16_bits_to_fp32(s).astype(np.float64), 128, axis=1)
+    bf = np.repeat(gen.bf16_bits_to_fp32(b).astype(np.float64), 128, axis=1)
+    err = np.abs(sf * q + bf - w)
+    bound = sf / 2 + np.abs(bf) * 2.0 ** -8 + 15 * sf * 2.0 ** -8 + 1e-9
+    assert np.all(err <= bound)
