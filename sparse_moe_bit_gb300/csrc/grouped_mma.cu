@@ -363,21 +363,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 
   const int nunits =
       (MODE == MMA_ROUTER) ? p.nunits_host : (*p.ntiles_dev) * p.units_per_tile;
-  // work: the i-th cluster unit of cluster cid is cunit(i), snake order over
-  // the tile list (sorted by size: full tiles first, then remainders largest
-  // first), so that every cluster gets a similar mix; the CTA of rank r takes
-  // unit cu * CL + r (same tile for the whole cluster, weight unit m =
-  // consecutive)
+  // work: the i-th cluster unit of cluster cid is cunit(i) over the tile list
+  // (sorted by size: full tiles first, then remainders largest first); the
+  // CTA of rank r takes unit cu * CL + r (same tile for the whole cluster,
+  // weight unit m = consecutive)
   const int ncu = nunits / CL;
   const int cid = (CL == 1) ? (int)blockIdx.x : (int)cluster_id();
   const int ncl = (CL == 1) ? (int)gridDim.x : (int)cluster_count();
   const int crank = (CL == 1) ? 0 : (int)cluster_rank();
   if (cid >= ncu) return;  // uniform over the cluster
+  // With ncu = q ncl + r units, r clusters must take q + 1 of them: those
+  // clusters take the r (q + 1) smallest units (the end of the sorted list)
+  // and the other ncl - r clusters q of the largest.  A unit's cost is mostly
+  // fixed (its K loop of weight blocks) and only partly proportional to its
+  // tokens, so dealing the extra units at random made the clusters holding
+  // one more unit the kernel's tail.  Within each group, snake order.
+  // (Heavy clusters are the first r, so that with fewer units than clusters
+  // the ones left without work are the last, as the early return assumes.)
+  const int q = ncu / ncl, r = ncu % ncl;
+  const int nlight = ncl - r;  // clusters with q units
+  const bool heavy = cid < r;
+  const int gsize = heavy ? r : nlight, gid = heavy ? cid : cid - r;
+  const int gbase = heavy ? nlight * q : 0;
   auto cunit = [&](int i) {
-    const int base = i * ncl;
-    return (i & 1) ? base + (ncl - 1 - cid) : base + cid;
+    const int base = gbase + i * gsize;
+    return (i & 1) ? base + (gsize - 1 - gid) : base + gid;
   };
-  const int nmy = ncu / ncl + ((cunit(ncu / ncl) < ncu) ? 1 : 0);  // this cluster's units
+  const int nmy = heavy ? q + 1 : q;  // this cluster's units
   const bool leader = !PAIR || crank == 0;  // issues the MMAs
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
