@@ -83,7 +83,12 @@ struct Cfg {
   static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
   static constexpr int NISS = NA;  // MMA-issuing threads (one per weight tile)
   static constexpr int NMAX = TMEM_A ? kTileRows : 256;
-  static constexpr int A_COLS = NA * 32;  // TMEM columns of one A stage
+  // KPS: 64-wide K blocks per pipeline stage.  The down projection (one
+  // weight tile, 4 MMAs per K block, one issuing thread) was bound by the
+  // issuer's per-stage work (two barrier tests, a commit); two K blocks per
+  // stage halve it.
+  static constexpr int KPS = (MODE == MMA_DOWN) ? 2 : 1;
+  static constexpr int A_COLS = NA * 32 * KPS;  // TMEM columns of one A stage
   static constexpr int A_COL0 = NMAX * (NA == 2 ? 2 : NACC);
   // as many A stages as the rest of TMEM holds (at most 8): the ring's depth
   // bounds the pipeline, whose round trip (dequantise, signal, MMA, commit)
@@ -92,11 +97,14 @@ struct Cfg {
       TMEM_A ? ((512 - A_COL0) / A_COLS < 8 ? (512 - A_COL0) / A_COLS : 8) : 2;
   static_assert(!TMEM_A || A_COL0 + A_STAGES * A_COLS <= 512, "TMEM budget");
   static_assert(TMEM_A || NA * NMAX <= 512, "TMEM budget");
-  static constexpr int CST = (MODE == MMA_DOWN) ? 8 : (MODE == MMA_GATEUP ? 6 : 0);
-  static constexpr int CODE_STAGE = NA * kHalfChunk;
+  static constexpr int CST = (MODE == MMA_DOWN) ? 4 : (MODE == MMA_GATEUP ? 6 : 0);
+  static constexpr int CODE_KB = NA * kHalfChunk;  // code bytes of one K block
+  static constexpr int CODE_STAGE = CODE_KB * KPS;
   // B ring: up to NMAX token rows (a pair's CTA holds half of them) x 64 K
-  static constexpr int B_STAGES = PAIR ? 8 : (MODE == MMA_GATEUP ? 6 : (TMEM_A ? 4 : 3));
-  static constexpr int B_STAGE = (PAIR ? NMAX / 2 : NMAX) * 128;
+  // per K block (B_SUB bytes), KPS K blocks per stage
+  static constexpr int B_STAGES = PAIR ? (KPS == 2 ? 4 : 8) : (MODE == MMA_GATEUP ? 6 : 3);
+  static constexpr int B_SUB = (PAIR ? NMAX / 2 : NMAX) * 128;
+  static constexpr int B_STAGE = B_SUB * KPS;
   static constexpr int A_STAGE = TMEM_A ? 0 : NA * 16384;  // shared-memory A (router)
   // epilogue: per chunk of 16 rows, NSEG 64-byte segments per row (down: one
   // per weight tile; gate/up: one, the SwiGLU of the tile pair)
@@ -432,12 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kbu = p.kb_per_unit;
+  const int kbs = kbu / C::KPS;  // pipeline stages per unit
 
-  // Dequantise K block g (the g-th of this CTA's sequence) into its A stage in
-  // TMEM: thread t (0..255 of a group of 8 warps) takes row t of the unit
-  // (two tiles: tile t >> 7) or row t & 127, K half t >> 7 (one tile).  The
-  // warp's TMEM lane quarter (lanes 32 (warp % 4) ..) holds rows (t & 127).
-  // Returns false on a timeout.
+  // Dequantise stage g (the g-th of this CTA's sequence: KPS K blocks) into
+  // its A stage in TMEM: thread t (0..255 of a group of 8 warps) takes row t
+  // of the unit (two tiles: tile t >> 7) or row t & 127, K half t >> 7 (one
+  // tile).  The warp's TMEM lane quarter (lanes 32 (warp % 4) ..) holds rows
+  // (t & 127).  Returns false on a timeout.
   auto dequant_kb = [&](int g, int t) -> bool {
     const int row = (C::NA == 2) ? t : (t & 127);
     const int kh = (C::NA == 2) ? 0 : (t >> 7);
@@ -461,29 +470,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       free_ok = warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err);
     }
     if (!warp_wait(S.c_full(sc), (g / kCst) & 1, abort_flag, p.err) || !free_ok) return false;
-    // row `row` of the ring stage: codes, then the s,b word
-    const uint4 a0 = ld_shared_v4(S.code(sc) + row * 32 + kh * 16);
-    const uint4 a1 = (C::NA == 2) ? ld_shared_v4(S.code(sc) + row * 32 + 16) : a0;
-    const uint32_t sb = ld_shared_u32(S.code(sc) + 32 * 128 * C::NA + row * 4);
-    const uint32_t s2 = __byte_perm(sb, 0, 0x1010);
-    const uint32_t b2 = __byte_perm(sb, 0, 0x3232);
-    const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    uint32_t v[4 * NW];  // column 4 i + j = K pair (8 i + 2 j, 8 i + 2 j + 1)
-#pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      const uint4 d4 = dequant_word(w[i], s2, b2);
-      v[4 * i] = d4.x;
-      v[4 * i + 1] = d4.y;
-      v[4 * i + 2] = d4.z;
-      v[4 * i + 3] = d4.w;
-    }
     // the MMAs that read this A stage before have completed (a_empty)
     tc_fence_after();
-    const uint32_t ta = tmem + a_lane + C::A_COL0 + sa * C::A_COLS + a_off;
-    if constexpr (NW == 8)
-      tmem_st32(ta, v);
-    else
-      tmem_st16(ta, v);
+#pragma unroll
+    for (int k2 = 0; k2 < C::KPS; ++k2) {
+      // row `row` of K block k2 of the ring stage: codes, then the s,b word
+      const uint32_t cs = S.code(sc) + k2 * C::CODE_KB;
+      const uint4 a0 = ld_shared_v4(cs + row * 32 + kh * 16);
+      const uint4 a1 = (C::NA == 2) ? ld_shared_v4(cs + row * 32 + 16) : a0;
+      const uint32_t sb = ld_shared_u32(cs + 32 * 128 * C::NA + row * 4);
+      const uint32_t s2 = __byte_perm(sb, 0, 0x1010);
+      const uint32_t b2 = __byte_perm(sb, 0, 0x3232);
+      const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      uint32_t v[4 * NW];  // column 4 i + j = K pair (8 i + 2 j, 8 i + 2 j + 1)
+#pragma unroll
+      for (int i = 0; i < NW; ++i) {
+        const uint4 d4 = dequant_word(w[i], s2, b2);
+        v[4 * i] = d4.x;
+        v[4 * i + 1] = d4.y;
+        v[4 * i + 2] = d4.z;
+        v[4 * i + 3] = d4.w;
+      }
+      // K block k2's columns follow block k2 - 1's (NA x 32 per block)
+      const uint32_t ta =
+          tmem + a_lane + C::A_COL0 + sa * C::A_COLS + k2 * (C::NA * 32) + a_off;
+      if constexpr (NW == 8)
+        tmem_st32(ta, v);
+      else
+        tmem_st16(ta, v);
+    }
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -575,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank, kPad);
       const int k0 = t.ks * kbu;
       const uint8_t* asrc = p.wA + (long long)t.m * p.a_unit_stride + (long long)k0 * p.a_chunk;
-      for (int kb = 0; kb < kbu; ++kb) {
+      for (int kb = 0; kb < kbs; ++kb) {
         if (MODE == MMA_ROUTER) {
           const int s = ga % kAStages;
           if (!warp_wait(S.a_empty(s), ((ga / kAStages) & 1) ^ 1, abort_flag, p.err)) {
@@ -594,24 +609,30 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
           break;
         }
         const uint32_t bs = S.b(s);
-        const int x = (k0 + kb) * 64;
         if constexpr (PAIR) {
           // this CTA's half of the tile (rows crank * npad / 2 ..), counted on
           // the even CTA's barrier, which expects the bytes of both halves
-          if (lane == 0 && leader) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
+          if (lane == 0 && leader)
+            mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128 * C::KPS);
           __syncwarp();
           const int half = t.npad >> 1;
           const uint32_t fb = mapa_shared(S.b_full(s), 0);
-          for (int sl = lane; sl < (half >> 4); sl += 32)
-            tma_tile_2d_pair(bs + sl * 2048, &p.tmB, x, t.row0 + crank * half + 16 * sl, fb);
+#pragma unroll
+          for (int k2 = 0; k2 < C::KPS; ++k2)
+            for (int sl = lane; sl < (half >> 4); sl += 32)
+              tma_tile_2d_pair(bs + k2 * C::B_SUB + sl * 2048, &p.tmB,
+                               (k0 + kb * C::KPS + k2) * 64, t.row0 + crank * half + 16 * sl, fb);
         } else {
           // the whole tile arrives in every CTA; this CTA fetches 16-row slabs
           // crank, crank + CL, ... (one 2-D tile per slab)
-          if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128);
+          if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128 * C::KPS);
           __syncwarp();
           const int nslab = t.npad >> 4;
-          for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
-            tma_tile_2d<CL>(bs + sl * 2048, &p.tmB, x, t.row0 + 16 * sl, S.b_full(s));
+#pragma unroll
+          for (int k2 = 0; k2 < C::KPS; ++k2)
+            for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
+              tma_tile_2d<CL>(bs + k2 * C::B_SUB + sl * 2048, &p.tmB,
+                              (k0 + kb * C::KPS + k2) * 64, t.row0 + 16 * sl, S.b_full(s));
         }
         ++gb;
       }
@@ -635,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         tc_fence_after();
         const uint32_t idesc = idesc_f16(PAIR ? 256 : 128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
         bool ok = true;
-        for (int kb = 0; kb < kbu; ++kb) {
+        for (int kb = 0; kb < kbs; ++kb) {
           // both operands' barriers tested at once (the two tests' latencies
           // overlap; a test costs ~130 cycles even on a completed phase, and
           // the issuing thread is the pipeline's bottleneck at small N)
@@ -647,29 +668,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          // K step kk: both operands advance by 32 bytes (2 in the
-          // descriptor's address field, which holds the address / 16)
-          const uint64_t bd = sdesc_k_sw128(S.b(sb));
 #pragma unroll
-          for (int j = 0; j < C::NA; ++j) {
-            if (C::NISS == 2 && j != q) continue;
-            // NA == 2: tile j -> columns NMAX j; NACC == 2: buffer ab -> columns NMAX ab
-            const uint32_t dcol = tmem + C::NMAX * (C::NA == 2 ? j : ab);
-            if constexpr (C::TMEM_A) {
-              // A: 8 TMEM columns per K step of 16
-              const uint32_t at = tmem + C::A_COL0 + sa * C::A_COLS + j * 32;
+          for (int k2 = 0; k2 < C::KPS; ++k2) {
+            // K step kk: both operands advance by 32 bytes (2 in the
+            // descriptor's address field, which holds the address / 16)
+            const uint64_t bd = sdesc_k_sw128(S.b(sb) + k2 * C::B_SUB);
+            const uint32_t acc = (kb | k2) ? 1u : 0u;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                if constexpr (PAIR)
-                  tc_mma_f16_ts_pair(dcol, at + 8 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
-                else
-                  tc_mma_f16_ts(dcol, at + 8 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+            for (int j = 0; j < C::NA; ++j) {
+              if (C::NISS == 2 && j != q) continue;
+              // NA == 2: tile j -> columns NMAX j; NACC == 2: buffer ab -> columns NMAX ab
+              const uint32_t dcol = tmem + C::NMAX * (C::NA == 2 ? j : ab);
+              if constexpr (C::TMEM_A) {
+                // A: 8 TMEM columns per K step of 16; K block k2 after k2 - 1
+                const uint32_t at = tmem + C::A_COL0 + sa * C::A_COLS + k2 * (C::NA * 32) + j * 32;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  if constexpr (PAIR)
+                    tc_mma_f16_ts_pair(dcol, at + 8 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
+                  else
+                    tc_mma_f16_ts(dcol, at + 8 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
+                }
+              } else {
+                const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc_mma_f16(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
               }
-            } else {
-              const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
             }
           }
           if constexpr (PAIR) {
@@ -700,36 +725,39 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   } else if (warp == 2 && MODE != MMA_ROUTER) {
     // ------------------------------------------------ code ring
     if (lane == 0) {
-      const int total = nmy * kbu;
+      const int total = nmy * kbs;
       for (int g = 0; g < total; ++g) {
         constexpr int kCst = C::CST > 0 ? C::CST : 1;
         const int s = g % kCst;
         if (!thread_wait(S.c_empty(s), ((g / kCst) & 1) ^ 1, abort_flag, p.err)) break;
-        const int j = g / kbu;
+        const int j = g / kbs;
         const Unit u = get_unit(p, MODE, cunit(j) * CL + crank, kPad);
-        if (C::NA == 2) {  // the whole chunk of unit m
-          const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
-                              (long long)u.m * p.a_unit_stride +
-                              (long long)(g - j * kbu) * p.a_chunk;
-          mbar_arrive_expect_tx(S.c_full(s), kCodeChunk);
-          bulk_g2s(S.code(s), ch, kCodeChunk, S.c_full(s));
-        } else {  // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, s,b words
-          const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
-                              (long long)(u.m >> 1) * p.a_unit_stride +
-                              (long long)(g - j * kbu) * p.a_chunk;
-          const int h = u.m & 1;
-          mbar_arrive_expect_tx(S.c_full(s), kHalfChunk);
-          bulk_g2s(S.code(s), ch + h * 4096, 4096, S.c_full(s));
-          bulk_g2s(S.code(s) + 4096, ch + 8192 + h * 512, 512, S.c_full(s));
+        mbar_arrive_expect_tx(S.c_full(s), C::CODE_STAGE);
+#pragma unroll
+        for (int k2 = 0; k2 < C::KPS; ++k2) {
+          const int kbk = (g - j * kbs) * C::KPS + k2;  // K block within the unit
+          const uint32_t dst = S.code(s) + k2 * C::CODE_KB;
+          if (C::NA == 2) {  // the whole chunk of unit m
+            const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
+                                (long long)u.m * p.a_unit_stride + (long long)kbk * p.a_chunk;
+            bulk_g2s(dst, ch, kCodeChunk, S.c_full(s));
+          } else {  // rows 128 (m % 2) .. +127 of chunk unit m / 2: codes, s,b words
+            const uint8_t* ch = p.wA + (long long)u.expert * p.a_expert_stride +
+                                (long long)(u.m >> 1) * p.a_unit_stride +
+                                (long long)kbk * p.a_chunk;
+            const int h = u.m & 1;
+            bulk_g2s(dst, ch + h * 4096, 4096, S.c_full(s));
+            bulk_g2s(dst + 4096, ch + 8192 + h * 512, 512, S.c_full(s));
+          }
         }
       }
     }
   } else if (warp >= 4 && warp < 4 + kDeqWarps) {
     // ------------------------------------------------ dequantise
     if constexpr (MODE != MMA_ROUTER) {
-      const int total = nmy * kbu;
+      const int total = nmy * kbs;
       // gate/up: these warps take the even K blocks, the epilogue warps the
-      // odd ones (kbu is even, so the parity of g is that of the K block)
+      // odd ones (kbs is even, so the parity of g is that of the K block)
       for (int g = 0; g < total; g += kDeqSplit ? 2 : 1)
         if (!dequant_kb(g, threadIdx.x - 32 * 4)) break;
     }
@@ -748,8 +776,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         // the odd K blocks of this unit (the MMAs of the next unit cannot
         // start before this unit's epilogue has drained its accumulators)
         bool ok = true;
-        for (int kb = 1; kb < kbu && ok; kb += 2)
-          ok = dequant_kb(i * kbu + kb, threadIdx.x - 32 * kEpiWarp0);
+        for (int kb = 1; kb < kbs && ok; kb += 2)
+          ok = dequant_kb(i * kbs + kb, threadIdx.x - 32 * kEpiWarp0);
         if (!ok) break;
       }
       const int c0 = half * C::EPI_COLS;

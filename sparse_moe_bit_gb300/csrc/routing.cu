@@ -50,24 +50,31 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ part, int KS
   float v[VPL];
   uint32_t key[VPL];
   bool nan_seen = false;
-  // all of the lane's loads first (one round trip), then the sums in the
-  // fixed order 0 + part_0 + part_1 + ... + bias
+  // all of the lane's loads first (one round trip for up to kKsBatch
+  // splits), then the sums in the fixed order 0 + part_0 + part_1 + ... + bias
+  constexpr int kKsBatch = VPL <= 8 ? 4 : 2;
   float pa[VPL], ba[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
-    pa[j] = (e < E) ? __ldg(part + (long long)t * E + e) : 0.0f;
     ba[j] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
+    pa[j] = 0.0f;
   }
-  for (int q = 1; q < KS; ++q) {
-    float pq[VPL];
+  for (int q0 = 0; q0 < KS; q0 += kKsBatch) {
+    float pq[kKsBatch][VPL];
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      pq[j] = (e < E) ? __ldg(part + ((long long)q * T + t) * E + e) : 0.0f;
-    }
+    for (int qq = 0; qq < kKsBatch; ++qq)
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) pa[j] += pq[j];
+      for (int j = 0; j < VPL; ++j) {
+        const int e = lane + 32 * j;
+        pq[qq][j] = (e < E && q0 + qq < KS)
+                        ? __ldg(part + ((long long)(q0 + qq) * T + t) * E + e) : 0.0f;
+      }
+#pragma unroll
+    for (int qq = 0; qq < kKsBatch; ++qq)
+      if (q0 + qq < KS)
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) pa[j] += pq[qq][j];
   }
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
