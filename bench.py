@@ -443,7 +443,22 @@ def run_sweep(args, torch, M, sd, gen, device, peaks):
                  "empty_experts": int((counts == 0).sum().item())}
     layer.close()
     stress.close()
-    return points, stress_pt
+    # a few tokens (speculative-verify shape): a handle with both layouts runs
+    # T <= 4 as one decode pass per token, larger T on the tensor-core path
+    small = M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=64), sd.make_layer(0, 0, shape, device=device))
+    torch.cuda.empty_cache()
+    small_pts = []
+    for T in (1, 2, 3, 4, 8):
+        xs, ys = x[:T], out[:T]
+        for _ in range(2):
+            small.forward(xs, None, out=ys)
+        us = time_call(torch, lambda: small.forward(xs, None, out=ys), flush, 10, stream)
+        t_roof, bound = point_roofline(T, touched(small, xs, None, 64), 1, peaks)
+        small_pts.append({"T": T, "us": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
+                          "path": "decode kernel per token" if T <= 4 else "tensor-core",
+                          "bound": bound, "roofline_frac": round(t_roof / (us * 1e-6), 4)})
+    small.close()
+    return points, stress_pt, small_pts
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -621,6 +636,10 @@ def main():
         line["imbalance_T32768"] = dict(
             sweep[1], config="8 hot experts take half of the assignments, 64 experts get "
                              "none; one unchunked call")
+        line["small_T"] = {
+            "config": "same layer, uniform routing, a handle with both layouts; T <= 4 runs "
+                      "one decode-kernel pass per token; L2 flushed, median of 10",
+            "points": sweep[2]}
     if ws == 1:
         try:
             line["cpu_baseline"] = cpu_baseline(primary)

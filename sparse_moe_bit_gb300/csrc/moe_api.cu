@@ -5,6 +5,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -413,6 +414,21 @@ moe_status moe_route_from_logits(moe_handle* h, const float* logits, int T,
   return MOE_OK;
 }
 
+// Largest T that moe_forward runs through the decode kernel, one token per
+// pass (handles with the DECODE layout): below it the tensor-core path's
+// fixed costs (routing, tile map, K loops of whole weight tiles) exceed T
+// weight-bound passes.  Measured on GB300 (Qwen shape); MOE_SMALL_T
+// (1..64; 0 or 1: T = 1 only) overrides it.
+static int small_t_limit() {
+  static int lim = -1;
+  if (lim < 0) {
+    const char* e = getenv("MOE_SMALL_T");
+    lim = e ? atoi(e) : 4;
+    if (lim < 1 || lim > 64) lim = (e && atoi(e) == 0) ? 1 : 4;
+  }
+  return lim;
+}
+
 moe_status moe_forward(moe_handle* h, const void* x, int T, const float* logit_bias, void* y,
                        void* stream) {
   moe_status s = check_handle(h);
@@ -429,11 +445,15 @@ moe_status moe_forward(moe_handle* h, const void* x, int T, const float* logit_b
   if (xb < yb + bytes && yb < xb + bytes) return fail(MOE_ERR_INVALID_ARG, "x and y overlap");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
-  if (T == 1 && (h->layouts & MOE_LAYOUT_DECODE)) {
+  if (T <= small_t_limit() && (h->layouts & MOE_LAYOUT_DECODE)) {
+    // a few tokens: one pass of the bandwidth-bound decode kernel per token
+    // (each token's output depends on that token only)
     moe_handle* one[1] = {h};
-    CK(launch_decode(reinterpret_cast<Handle* const*>(one), 1, static_cast<const uint16_t*>(x),
-                     logit_bias, 1e-6f, static_cast<uint16_t*>(y), nullptr, st),
-       "decode launch");
+    for (int t = 0; t < T; ++t)
+      CK(launch_decode(reinterpret_cast<Handle* const*>(one), 1,
+                       static_cast<const uint16_t*>(x) + (size_t)t * c.d, logit_bias, 1e-6f,
+                       static_cast<uint16_t*>(y) + (size_t)t * c.d, nullptr, st),
+         "decode launch");
     return MOE_OK;
   }
   if (!(h->layouts & MOE_LAYOUT_PREFILL))

@@ -115,6 +115,26 @@ def test_forward_parity_mid(mid, T):
     check_output(y.float().cpu().numpy(), ref["out"], f"mid T={T}")
 
 
+@pytest.mark.parametrize("T", [2, 3, 4, 5])
+def test_forward_parity_small_t_both_paths(mid, T):
+    # a handle with the decode layout runs T <= 4 as one decode pass per
+    # token; a prefill-only handle runs the tensor-core path: both match the
+    # oracle, and the decode-path rows equal single-token calls bit for bit
+    bits, x = _x(mid, T, seed=20 + T)
+    pf = HostCase(MID, seed=1, layouts=M.MOE_LAYOUT_PREFILL)
+    for case in (mid, pf):
+        y = case.moe.forward(x)
+        r = case.moe.route(x)
+        torch.cuda.synchronize()
+        ref = case.oracle(bits, logits=r["logits"].cpu().numpy())
+        check_output(y.float().cpu().numpy(), ref["out"], f"mid T={T}")
+    if T <= 4:
+        y = mid.moe.forward(x)
+        rows = torch.stack([mid.moe.forward(x[t:t + 1])[0] for t in range(T)])
+        torch.cuda.synchronize()
+        assert torch.equal(y, rows)
+
+
 def test_forward_independent_routing_mid(mid):
     # the oracle routes from its own fp64 logits; near-tie tokens excluded
     T = 400
