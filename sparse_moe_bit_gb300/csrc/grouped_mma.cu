@@ -1,41 +1,48 @@
 // Grouped tensor-core GEMM for sm_103a: tcgen05.mma with TMEM accumulators,
-// token-row operands staged in shared memory by the tensor memory accelerator
-// (2-D tensor tiles multicast across a cluster), 4-bit weights dequantised
-// tile by tile inside the pipeline.
+// 4-bit weights dequantised tile by tile inside the pipeline, token rows
+// staged in shared memory.
 //
-// One work unit computes two 128-row weight tiles (A0, A1) against one token
-// tile of up to 256 rows (B), over K in blocks of 64 (one quantisation group
+// A work unit computes one or two 128-row weight tiles against one token
+// tile of up to 192 rows (B), over K in blocks of 64 (one quantisation group
 // per block):
-//   router : A = router rows e..e+255 (bf16), B = token rows of x (bf16),
+//   router : A0, A1 = router rows e..e+255 (bf16, pre-swizzled, by bulk copy
+//            into shared memory), B = token rows of x (bf16, 2-D TMA tiles),
 //            out = fp32 partial logits of one K split.
 //   gate/up: A0 = gate rows f..f+127, A1 = up rows f..f+127 of one expert
-//            (dequantised to fp16), B = the expert's grouped token rows of x
-//            (fp16, already permuted into grouped-row order); epilogue
-//            H = silu(A0 x) * (A1 x) -> fp16.
-//   down   : A = down rows f..f+127 (dequantised), B = the expert's rows of
-//            H; epilogue Y[dst] = w_row * (A x) -> bf16, written to the
-//            token's contribution row (deterministic combine later).
+//            (dequantised to fp16 straight into TMEM), B = the tile's tokens
+//            gathered through perm from the fp16 copy of x (cp.async);
+//            epilogue H = silu(A0 x) * (A1 x) -> fp16.
+//   down   : A = down rows f..f+127 (dequantised into TMEM), B = the
+//            expert's rows of H (2-D TMA tiles), two K blocks per stage;
+//            epilogue Y[dst] = w_row * (A x) -> bf16, written to the token's
+//            contribution row (deterministic combine later).
+// Gate/up and down run as CTA pairs (tcgen05 cta_group::2): the even CTA of
+// a cluster of two issues M = 256 MMAs over both CTAs' A tiles (consecutive
+// weight units) and each CTA holds half of the token tile.
 // Source: Perplexity, "Optimizing on-device inference for Apple Silicon",
 // §"Dequantize weights during matrix multiplication" (one small weight tile
-// at a time is expanded to 16-bit in on-chip memory and multiplied with the
-// routed activation rows; fp32 accumulation; the full matrix is never
-// written out) and §"Match tile size to expert load" (tile shape from the
-// expert's row count: the token dimension N of each tile is the expert's
-// remaining row count rounded up to 16, at most 256).
+// at a time is expanded to 16-bit on chip and multiplied with the routed
+// activation rows; fp32 accumulation; the full matrix is never written out)
+// and §"Match tile size to expert load" (tile shape from the expert's row
+// count: the token dimension N of each tile is the expert's remaining row
+// count rounded up to 16 (32 for pairs), at most 192).
 //
 // Warp roles (640 threads, one CTA per SM, persistent over the unit list):
-//   warp 0       B producer (the warp's lanes issue the 16-row TMA tiles)
-//                and, for the router, the A bulk copies
-//   warp 1       lane 0 issues tcgen05.mma; the warp owns the TMEM allocation
+//   warp 0       B producer (TMA tiles, or the gate/up row gather) and, for
+//                the router, the A bulk copies
+//   warps 1, 3   lane 0 issues tcgen05.mma, one thread per weight tile (in a
+//                pair, the even CTA's); warp 1 owns the TMEM allocation
 //   warp 2       lane 0 issues the bulk copies of the code ring
 //   warps 4..11  dequantise the weight codes from the ring into fp16 A tiles
-//                (128-byte swizzled, K-major): gate/up one row per thread,
-//                down half a row per thread
+//                in TMEM (gate/up one row per thread, every other K block;
+//                down half a row per thread)
 //   warps 12..19 epilogue: tcgen05.ld, activation / scaling, staging in
-//                shared memory, 16-byte stores of 64-byte row segments
-// Rings: A 2 stages, B 3 stages, codes 4 (gate/up) or 8 (down).  TMEM: two
-// fp32 accumulators of 256 columns (gate/up and router: tiles A0 and A1 of
-// one unit; down: two units in turn).
+//                shared memory, 16-byte stores of 64-byte row segments (and,
+//                in gate/up, the odd K blocks' dequantisation)
+// TMEM (512 columns): gate/up two 192-column accumulators (gate, up) and a
+// 2-stage A ring; down two 192-column accumulator buffers (the epilogue of a
+// unit overlaps the next one's MMAs) and a 2-stage A ring of two K blocks;
+// router two 256-column accumulators.  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

@@ -1,6 +1,7 @@
 // Inline-PTX wrappers for sm_103a: mbarrier, bulk (TMA) copies, cp.async,
 // proxy fences, and the fifth-generation tensor core (tcgen05: TMEM
-// allocation, MMA with shared-memory descriptors, commit, TMEM loads).
+// allocation, MMA with the A operand in shared or tensor memory, CTA pairs,
+// commit, TMEM loads and stores).
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -280,12 +281,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 
 // ------------------------------------------------------------------- misc
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
