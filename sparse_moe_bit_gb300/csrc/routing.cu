@@ -637,34 +637,41 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
 // out[t][f] = sum_{j=0}^{k1-1} Y[t*k1 + j][f], fp32 in slot order (the
 // shared expert's term last), rounded once to bf16.  The routing weights were
 // applied when the rows of Y were written.  A thread's loads of all k1 rows
-// are issued before the sum (k1 <= kMaxK + 1).
+// are issued before the sum.  K1 > 0: exactly K1 rows per token (registers
+// for K1 loads only, so more blocks are resident); K1 = 0: any k1 up to
+// kMaxK + 1.  Persistent blocks stride over the tokens (no partial last wave).
+template <int K1>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y, int k1,
-                                                     int d, uint16_t* __restrict__ out) {
-  const int t = blockIdx.x;
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    uint4 rv[kMaxK + 1];
+                                                     int d, int T, uint16_t* __restrict__ out) {
+  constexpr int NR = K1 > 0 ? K1 : kMaxK + 1;
+  const int nr = K1 > 0 ? K1 : k1;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint4 rv[NR];
 #pragma unroll
-    for (int j = 0; j < kMaxK + 1; ++j)
-      if (j < k1) rv[j] = __ldcs(reinterpret_cast<const uint4*>(Y + ((long long)t * k1 + j) * d + c));
+      for (int j = 0; j < NR; ++j)
+        if (j < nr)
+          rv[j] = __ldcs(reinterpret_cast<const uint4*>(Y + ((long long)t * nr + j) * d + c));
 #pragma unroll
-    for (int j = 0; j < kMaxK + 1; ++j) {
-      if (j >= k1) break;
-      const uint4 raw = rv[j];
-      const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int j = 0; j < NR; ++j) {
+        if (j >= nr) break;
+        const uint4 raw = rv[j];
+        const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] += __uint_as_float(v[q] << 16);
+          acc[2 * q + 1] += __uint_as_float(v[q] & 0xFFFF0000u);
+        }
+      }
+      uint32_t o[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        acc[2 * q] += __uint_as_float(v[q] << 16);
-        acc[2 * q + 1] += __uint_as_float(v[q] & 0xFFFF0000u);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        o[q] = *reinterpret_cast<const uint32_t*>(&b2);
       }
+      *reinterpret_cast<uint4*>(out + (long long)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-      o[q] = *reinterpret_cast<const uint32_t*>(&b2);
-    }
-    *reinterpret_cast<uint4*>(out + (long long)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -733,10 +740,32 @@ cudaError_t launch_route(const Handle* h, const float* part, int KS, int T, cons
   return c.E <= 256 ? launch_route_vpl<8>(h, p, st) : launch_route_vpl<16>(h, p, st);
 }
 
+namespace {
+// resident blocks of a combine variant (persistent grid)
+template <int K1>
+int combine_grid(const Handle* h, int threads, int T) {
+  static int per_sm = -1;
+  if (per_sm < 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<K1>, threads, 0) !=
+            cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+  }
+  const int cap = h->num_sms * per_sm;
+  return T < cap ? T : cap;
+}
+}  // namespace
+
 cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st) {
   const moe_config& c = h->cfg;
   const int threads = c.d / 8 < 256 ? c.d / 8 : 256;
-  combine_kernel<<<T, threads, 0, st>>>(h->ws.Y, c.k + (c.has_shared ? 1 : 0), c.d, y);
+  const int k1 = c.k + (c.has_shared ? 1 : 0);
+  if (k1 == 9)
+    combine_kernel<9><<<combine_grid<9>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y);
+  else
+    combine_kernel<0><<<combine_grid<0>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y);
   return cudaGetLastError();
 }
 
