@@ -37,6 +37,7 @@ ROUTER_BYTES = E * D * 2
 LAYER_BYTES_DECODE = 9 * EXPERT_BYTES + ROUTER_BYTES + D * 2 + 2 * D * 2   # 16,986,112
 FLOP_PER_TOKEN = 2 * D * E + K * (2 * D * 2 * I + 2 * I * D) + (2 * D * 2 * I + 2 * I * D) + 2 * D
 GATEUP_FLOP_PER_ROW = 2 * D * 2 * I
+METRIC = "MoE-layer tokens/s (prefill T=4096; decode T=1) and % of HBM/tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -576,9 +577,12 @@ def main():
         v = statistics.median(steps)
         cb = {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
               "sample": sample.sample}
-        line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": v,
-                "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
-                "higher_is_better": True, "dtype": "f64", "data": "synthetic",
+        tokens_per_step = PREFILL_T if args.workload == "prefill" else 1
+        line = {"impl": "reference", "metric": METRIC, "value": v,
+                "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1000.0 * tokens_per_step / v,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
                 "config": config_for(args.workload),
                 "cpu_baseline": cb,
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -604,7 +608,7 @@ def main():
     if rank != 0:
         return 0
     line = {
-        "metric": "MoE-layer tokens/s (prefill T=4096; decode T=1) and % of HBM/tensor roofline",
+        "metric": METRIC,
         "value": res["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
         "us_per_layer": res["us_per_layer"], "higher_is_better": True, "scaling": "weak",
