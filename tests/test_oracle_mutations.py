@@ -1,5 +1,6 @@
-"""Plant one plausible mistake at a time in a copy of the oracle (on the CPU)
-and check that the pins in test_oracle_pins.py catch every one of them."""
+"""Plant one plausible mistake at a time in a copy of an oracle (on the CPU)
+and check that its pins catch every one of them: test_oracle_pins.py for the
+MoE block, test_gdn_oracle_pins.py for the Gated DeltaNet scan."""
 import os
 import subprocess
 import sys
@@ -8,6 +9,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "moe_oracle.py")
+SRC_GDN = os.path.join(ROOT, "oracle", "gdn_oracle.py")
 
 # (name, original text, planted mistake)
 MUTATIONS = [
@@ -51,5 +53,46 @@ def test_pins_catch_planted_mistake(name, orig, bad, tmp_path):
     r = subprocess.run(
         [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"no pin caught the planted mistake '{name}'"
+
+
+WRITE = "        + beta[:, None, None] * v[:, :, None] * k[:, None, :]"
+MUTATIONS_GDN = [
+    ("gate applied to the write too", WRITE,
+     "        + alpha * beta[:, None, None] * v[:, :, None] * k[:, None, :]"),
+    ("write without beta", WRITE, "        + v[:, :, None] * k[:, None, :]"),
+    ("delta sign", "(S - beta[:, None, None] * Sk", "(S + beta[:, None, None] * Sk"),
+    ("readout before the write", 'o = scale * np.einsum("hij,hj->hi", S_new, q)',
+     'o = scale * np.einsum("hij,hj->hi", S, q)'),
+    ("readout with the key", 'o = scale * np.einsum("hij,hj->hi", S_new, q)',
+     'o = scale * np.einsum("hij,hj->hi", S_new, k)'),
+    ("delta read with the query", 'Sk = np.einsum("hij,hj->hi", S, k)',
+     'Sk = np.einsum("hij,hj->hi", S, q)'),
+    ("gate not exponentiated", "alpha = np.exp(g)[:, None, None]", "alpha = g[:, None, None]"),
+    ("head grouping modulo", "head_of = np.arange(Hv) // (Hv // Hk)",
+     "head_of = np.arange(Hv) % Hk"),
+    ("state carried across sequences", "S = states[n].copy()",
+     "S = S if n else states[n].copy()"),
+    ("initial state ignored", "states[:] = np.asarray(state0, F64)", "pass"),
+    ("default scale 1/dk", "scale = 1.0 / np.sqrt(dk)", "scale = 1.0 / dk"),
+    ("dense rule without beta on the write",
+     "S_new = S @ transition + F64(beta) * np.outer(v, k)",
+     "S_new = S @ transition + np.outer(v, k)"),
+    ("dense transition sign", "np.eye(dk) - F64(beta)", "np.eye(dk) + F64(beta)"),
+    ("bf16 bits misplaced", "<< np.uint32(16)", "<< np.uint32(15)"),
+]
+
+
+@pytest.mark.parametrize("name,orig,bad", MUTATIONS_GDN, ids=[m[0] for m in MUTATIONS_GDN])
+def test_gdn_pins_catch_planted_mistake(name, orig, bad, tmp_path):
+    src = open(SRC_GDN).read()
+    assert src.count(orig) == 1, f"mutation anchor not found once: {orig!r}"
+    mutant = tmp_path / "gdn_oracle_mutant.py"
+    mutant.write_text(src.replace(orig, bad))
+    env = dict(os.environ, GDN_ORACLE_FILE=str(mutant))
+    r = subprocess.run(
+        [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+         os.path.join(ROOT, "tests", "test_gdn_oracle_pins.py")],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"no pin caught the planted mistake '{name}'"

@@ -92,3 +92,21 @@ def test_quantiser_bf16_scales_group128():
     err = np.abs(sf * q + bf - w)
     bound = sf / 2 + np.abs(bf) * 2.0 ** -8 + 15 * sf * 2.0 ** -8 + 1e-9
     assert np.all(err <= bound)
+
+
+def test_gdn_inputs_recipe():
+    from synth import gdn
+    shape = gdn.GdnShape(Hk=2, Hv=4, dk=128, dv=64)
+    a = gdn.make_inputs(0, [5, 0, 11], shape, state_std=0.1)
+    b = gdn.make_inputs(0, [5, 0, 11], shape, state_std=0.1)
+    for x, y in ((a.q, b.q), (a.k, b.k), (a.v, b.v), (a.g, b.g), (a.beta, b.beta)):
+        assert np.array_equal(x, y)                       # seeded, reproducible
+    assert a.q.shape == (16, 2, 128) and a.v.shape == (16, 4, 64)
+    assert a.state0.shape == (3, 4, 64, 128)
+    assert list(a.offsets) == [0, 5, 5, 16]
+    qn = np.linalg.norm(gen.bf16_bits_to_fp32(a.q).astype(np.float64), axis=-1)
+    assert np.all(np.abs(qn - 1) < 4e-3)                  # unit norm up to bf16 rounding
+    alpha = np.exp(a.g.astype(np.float64))
+    assert np.all((alpha >= 0.9 - 1e-6) & (alpha < 1.0))
+    assert np.all((a.beta > 0) & (a.beta < 1))
+    assert not np.array_equal(a.q, a.k)
