@@ -349,6 +349,73 @@ SWEEP_T = [256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072]
 SWEEP_CHUNK = 8192
 
 
+# Gated DeltaNet prefill scan: one 2K-token prompt through a Qwen-shaped
+# linear-attention layer (16 query/key heads, 32 value heads, 128 x 128 fp32
+# state per value head).
+GDN_T = 2048
+GDN_SHAPE = dict(Hk=16, Hv=32, dk=128, dv=128)
+SM_MAX_MHZ = 2070.0
+FP32_LANES_PER_SM = 128
+
+
+def gdn_alu_ops(T, Hv, dv, dk):
+    """fp32 pipe operations the scan needs at least: per state element and
+    token, one multiply-add each for S.k and S.q and two operations for the
+    update alpha S + c k."""
+    return 4 * T * Hv * dv * dk
+
+
+def gdn_alu_peak(sm_count):
+    """fp32 lane operations per second at the maximum SM clock (T ops/s)."""
+    return sm_count * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12
+
+
+def run_gdn(args, torch, M, device):
+    import numpy as np
+    from synth import gdn
+    shape = gdn.GdnShape(**GDN_SHAPE)
+    inp = gdn.make_inputs(0, [GDN_T], shape)
+
+    def bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
+
+    q, k, v = bf16(inp.q), bf16(inp.k), bf16(inp.v)
+    g = torch.from_numpy(inp.g).to(device)
+    beta = torch.from_numpy(inp.beta).to(device)
+    o = torch.empty(GDN_T, shape.Hv, shape.dv, dtype=torch.bfloat16, device=device)
+    S = torch.empty(1, shape.Hv, shape.dv, shape.dk, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fn():
+        M.gdn_scan(q, k, v, g, beta, o=o, state_out=S, stream=stream)
+
+    flush = l2_flush_buffer(torch, device)
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    clk = ClockSampler(device.index)
+    clk.start()
+    us = time_call(torch, fn, flush, max(10, args.steps), stream)
+    clocks = clk.stop()
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    ops = gdn_alu_ops(GDN_T, shape.Hv, shape.dv, shape.dk)
+    achieved = ops / (us * 1e-6) / 1e12
+    peak = gdn_alu_peak(sm_count)
+    return {
+        "config": f"one {GDN_T}-token prompt, Hk={shape.Hk} query/key heads, Hv={shape.Hv} "
+                  f"value heads, dk=dv={shape.dk}; q, k unit-norm bf16, v bf16, alpha in "
+                  "[0.9, 1), beta = sigmoid(N(0,1)); L2 flushed between calls, median",
+        "us": us, "tokens_per_s": GDN_T / (us * 1e-6),
+        "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
+                     "unit": "T fp32 lane-ops/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "kernel": "gdn_scan_kernel",
+                     "algorithmic_ops_per_launch": ops,
+                     "peak_source": f"{sm_count} SMs x {FP32_LANES_PER_SM} fp32 lanes x "
+                                    f"{SM_MAX_MHZ:.0f} MHz"},
+        "gpu_launches": 1, "clocks": clocks,
+    }
+
+
 def point_roofline(T, experts_touched, chunks, peaks):
     """max(FLOP at peak, bytes at HBM bandwidth) for one call: the touched
     experts' 4.5-bit weights (counted per chunk), the router per chunk, x in
@@ -561,6 +628,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
     ap.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
                     help="layers of the decode chain (profiling captures use fewer)")
+    ap.add_argument("--no-gdn", action="store_true",
+                    help="skip the Gated DeltaNet prefill scan (one 2K prompt)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the prefill length sweep and the imbalance case")
     args = ap.parse_args()
@@ -604,6 +673,7 @@ def main():
     res = runner[primary](args, torch, M, sd, gen, device, peaks)
     sec = runner[secondary](args, torch, M, sd, gen, device, peaks) if secondary else None
     sweep = None if args.no_sweep else run_sweep(args, torch, M, sd, gen, device, peaks)
+    gdn_res = None if args.no_gdn else run_gdn(args, torch, M, device)
 
     if rank != 0:
         return 0
@@ -644,6 +714,8 @@ def main():
             "config": "same layer, uniform routing, a handle with both layouts; T <= 4 runs "
                       "one decode-kernel pass per token; L2 flushed, median of 10",
             "points": sweep[2]}
+    if gdn_res is not None:
+        line["gdn_scan"] = gdn_res
     if ws == 1:
         try:
             line["cpu_baseline"] = cpu_baseline(primary)

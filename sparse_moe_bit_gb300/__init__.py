@@ -1,10 +1,11 @@
 """Sparse 4-bit Mixture-of-Experts block for GB300 (sm_103a).
 
 The compute lives in libmoe.so (CUDA kernels behind the C ABI of
-include/moe.h); this package is its thin Python binding.
+include/moe.h, and the Gated DeltaNet prefill scan of include/gdn.h); this
+package is its thin Python binding.
 """
 from .moe import (MOE_LAYOUT_DECODE, MOE_LAYOUT_PREFILL, MOE_SCALE_F16, MoE, MoEConfig,
-                  MoEError, decode, decode_host, load_library)
+                  MoEError, decode, decode_host, gdn_scan, load_library)
 
-__all__ = ["MoE", "MoEConfig", "MoEError", "decode", "decode_host", "load_library",
+__all__ = ["MoE", "MoEConfig", "MoEError", "decode", "decode_host", "gdn_scan", "load_library",
            "MOE_SCALE_F16", "MOE_LAYOUT_PREFILL", "MOE_LAYOUT_DECODE"]

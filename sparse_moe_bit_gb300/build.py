@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["moe_api.cu", "grouped_mma.cu", "routing.cu", "repack.cu", "decode.cu"]
+SOURCES = ["moe_api.cu", "grouped_mma.cu", "routing.cu", "repack.cu", "decode.cu",
+           "gdn_scan.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

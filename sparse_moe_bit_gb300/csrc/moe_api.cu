@@ -9,6 +9,7 @@
 #include <cstring>
 #include <new>
 
+#include "gdn.h"
 #include "moe_internal.h"
 
 using namespace moe;
@@ -592,6 +593,48 @@ moe_status moe_get_device_error(moe_handle* h, int* code) {
   CK(cudaMemset(h->dev_err, 0, 4), "clear error word");
   *code = v;
   return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status gdn_scan(const void* q, const void* k, const void* v, const float* g,
+                    const float* beta, float scale, const int32_t* offsets, int N, int T,
+                    int Hk, int Hv, int dk, int dv, const float* state_in, float* state_out,
+                    void* o, void* stream) {
+  if (T > 0 && (!q || !k || !v || !g || !beta || !o))
+    return fail(MOE_ERR_INVALID_ARG, "NULL tensor");
+  if (T < 0 || N < 1 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1)
+    return fail(MOE_ERR_INVALID_ARG, "bad size (T=%d N=%d Hk=%d Hv=%d dk=%d dv=%d)", T, N, Hk,
+                Hv, dk, dv);
+  if (Hv % Hk != 0) return fail(MOE_ERR_INVALID_ARG, "Hv=%d is not a multiple of Hk=%d", Hv, Hk);
+  if (Hv > 65535 || N > 65535) return fail(MOE_ERR_INVALID_ARG, "Hv or N above 65535");
+  if (!offsets && N != 1) return fail(MOE_ERR_INVALID_ARG, "offsets is NULL but N=%d", N);
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+    return fail(MOE_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(state_in, 16) || !aligned(state_out, 16) || !aligned(g, 4) ||
+      !aligned(beta, 4) || !aligned(offsets, 4))
+    return fail(MOE_ERR_INVALID_ARG, "misaligned pointer");
+  if (dk != kGdnDk) return fail(MOE_ERR_UNSUPPORTED, "dk=%d (supported: %d)", dk, kGdnDk);
+  if (dv % kGdnRows != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "dv=%d is not a multiple of %d", dv, kGdnRows);
+  if (T == 0 && !state_out) return MOE_OK;
+  GdnParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.offsets = offsets;
+  p.state_in = state_in;
+  p.state_out = state_out;
+  p.o = static_cast<uint16_t*>(o);
+  p.scale = scale;
+  p.T = T;
+  p.Hk = Hk;
+  p.Hv = Hv;
+  p.dv = dv;
+  p.N = N;
+  CK(launch_gdn_scan(p, static_cast<cudaStream_t>(stream)), "gdn_scan launch");
+  return MOE_OK;
 }
 
 }  // extern "C"

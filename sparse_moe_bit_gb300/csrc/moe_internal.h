@@ -141,4 +141,23 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
                           cudaStream_t st);
 size_t decode_scratch_bytes(const Handle* h, int L);
 
+// Gated DeltaNet prefill scan (gdn_scan.cu).  Key width fixed at 128,
+// value rows in blocks of 32; see include/gdn.h for the layouts.
+struct GdnParams {
+  const uint16_t* q;        // bf16 [T][Hk][128]
+  const uint16_t* k;        // bf16 [T][Hk][128]
+  const uint16_t* v;        // bf16 [T][Hv][dv]
+  const float* g;           // [T][Hv] log of the gate
+  const float* beta;        // [T][Hv]
+  const int32_t* offsets;   // [N+1] or null (one sequence of T tokens)
+  const float* state_in;    // [N][Hv][dv][128] or null (zero state)
+  float* state_out;         // [N][Hv][dv][128] or null
+  uint16_t* o;              // bf16 [T][Hv][dv]
+  float scale;
+  int T, Hk, Hv, dv, N;
+};
+constexpr int kGdnDk = 128;
+constexpr int kGdnRows = 32;
+cudaError_t launch_gdn_scan(const GdnParams& p, cudaStream_t st);
+
 }  // namespace moe

@@ -27,7 +27,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
 EXPORTS = ["moe_create", "moe_destroy", "moe_route", "moe_route_from_logits", "moe_forward",
            "moe_forward_host", "moe_decode", "moe_decode_host", "moe_profile_enable",
            "moe_profile_read", "moe_route_from_logits_noalloc", "moe_get_device_error",
-           "moe_status_string", "moe_last_error", "moe_version"]
+           "moe_status_string", "moe_last_error", "moe_version", "gdn_scan"]
 
 STAGES = ["router", "routing", "gate_up", "down", "combine"]
 
@@ -81,6 +81,7 @@ def load_library() -> ctypes.CDLL:
         "moe_profile_read": [P, ctypes.POINTER(F), I, ctypes.POINTER(I)],
         "moe_route_from_logits_noalloc": [P, I, I, I, P, P, P, P, P, P, P, P],
         "moe_get_device_error": [P, ctypes.POINTER(I)],
+        "gdn_scan": [P, P, P, P, P, F, P, I, I, I, I, I, I, P, P, P, P],
         "moe_status_string": [I],
         "moe_last_error": [],
         "moe_version": [],
@@ -278,3 +279,29 @@ def route_from_logits_noalloc(logits: torch.Tensor, k: int, bias: torch.Tensor |
         _ptr(logits), T, E, k, _ptr(bias), _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["counts"]),
         _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["slot"]), _stream(stream)))
     return out
+
+
+def gdn_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+             beta: torch.Tensor, scale: float | None = None, offsets: torch.Tensor | None = None,
+             state: torch.Tensor | None = None, state_out: torch.Tensor | None = None,
+             o: torch.Tensor | None = None, stream=None):
+    """Gated DeltaNet prefill scan (include/gdn.h).
+
+    q, k bf16 [T, Hk, dk]; v bf16 [T, Hv, dv]; g, beta fp32 [T, Hv];
+    offsets int32 [N+1] (device) or None for one sequence; state fp32
+    [N, Hv, dv, dk] or None (zero).  Returns (o bf16 [T, Hv, dv], final state
+    fp32 [N, Hv, dv, dk]).  Outputs are made here with torch unless given."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = 1 if offsets is None else offsets.numel() - 1
+    if scale is None:
+        scale = dk ** -0.5
+    dev = q.device
+    if o is None:
+        o = torch.empty(T, Hv, dv, dtype=torch.bfloat16, device=dev)
+    if state_out is None:
+        state_out = torch.empty(N, Hv, dv, dk, dtype=torch.float32, device=dev)
+    _check(load_library().gdn_scan(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(offsets), N, T, Hk,
+        Hv, dk, dv, _ptr(state), _ptr(state_out), _ptr(o), _stream(stream)))
+    return o, state_out

@@ -1,4 +1,5 @@
-"""The C-ABI library loads, exports every function include/moe.h declares,
+"""The C-ABI library loads, exports every function include/moe.h and
+include/gdn.h declare,
 and rejects bad arguments before touching the GPU (no compute calls here)."""
 import ctypes
 import os
@@ -19,9 +20,12 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "moe.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    names = set()
+    for header in ("moe.h", "gdn.h"):
+        src = open(os.path.join(ROOT, "include", header)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b((?:moe|gdn)_[a-z_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_and_binding_agree():
@@ -94,3 +98,38 @@ def test_calls_on_null_handle_are_rejected(lib):
     code = ctypes.c_int()
     assert lib.moe_get_device_error(None, ctypes.byref(code)) == 1
     assert lib.moe_destroy(None) == 0
+
+
+# Fake, suitably aligned device addresses: every case below is refused during
+# argument checking, before anything could be enqueued.
+_A = 0x10000
+
+
+def _gdn_args(**kw):
+    a = dict(q=_A, k=_A, v=_A, g=_A, beta=_A, scale=0.088, offsets=None, N=1, T=64, Hk=2, Hv=4,
+             dk=128, dv=64, state_in=None, state_out=None, o=_A, stream=None)
+    a.update(kw)
+    return a
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(beta=None), 1), (dict(T=-1), 1), (dict(N=0), 1),
+    (dict(Hk=0), 1), (dict(Hv=6, Hk=4), 1), (dict(N=2), 1), (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1), (dict(q=_A + 8), 1), (dict(state_out=_A + 4), 1),
+    (dict(g=_A + 2), 1), (dict(Hv=70000, Hk=1), 1), (dict(dk=64), 2), (dict(dk=256), 2),
+    (dict(dv=48), 2), (dict(dv=0), 1)])
+def test_gdn_scan_rejects_bad_arguments(lib, kw, status):
+    a = _gdn_args(**kw)
+    r = lib.gdn_scan(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["offsets"], a["N"],
+                     a["T"], a["Hk"], a["Hv"], a["dk"], a["dv"], a["state_in"], a["state_out"],
+                     a["o"], a["stream"])
+    assert r == status, lib.moe_last_error()
+    assert lib.moe_last_error()
+
+
+def test_gdn_scan_empty_without_state_is_a_no_op(lib):
+    a = _gdn_args(T=0)
+    assert lib.gdn_scan(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], None, 1, 0, 2, 4,
+                        128, 64, None, None, a["o"], None) == 0
+    assert lib.gdn_scan(None, None, None, None, None, 1.0, None, 1, 0, 2, 4, 128, 64, None, None,
+                        None, None) == 0

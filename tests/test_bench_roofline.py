@@ -40,3 +40,11 @@ def test_point_roofline_bound_and_value():
     # large T, few experts: FLOPs dominate
     t, bound = bench.point_roofline(65536, 64, 8, peaks)
     assert bound == "tensor" and abs(t - bench.FLOP_PER_TOKEN * 65536 / 2000e12) < 1e-12
+
+
+def test_gdn_scan_alu_roofline():
+    # per state element and token: S.k, S.q (one multiply-add each) and the
+    # update alpha S + c k (two operations)
+    assert bench.gdn_alu_ops(2048, 32, 128, 128) == 4 * 2048 * 32 * 128 * 128
+    # 152 SMs x 128 fp32 lanes x 2.07 GHz
+    assert abs(bench.gdn_alu_peak(152) - 40.27392) < 1e-9
