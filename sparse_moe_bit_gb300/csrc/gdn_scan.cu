@@ -18,17 +18,19 @@
 //     o_t[i] = alpha_t (S_{t-1}[i] . q~_t) + c (k_t . q~_t),   q~ = scale q
 // (the readout from the identity S_t q = alpha S_{t-1} q + c (k . q), so one
 // pass over the row per token serves both dot products).  Eight lanes share
-// one row, 16 fp32 state values each, for the whole scan: the state never
-// leaves registers until the end.  The two dot products are summed across
-// the eight lanes by a shuffle butterfly, after which all eight hold the same
-// c (addition is commutative, so the butterfly gives every lane identical
-// bits).  A CTA of 256 threads holds 32 rows of one head; grid (dv/32, Hv,
-// sequences).  Tokens are staged 32 at a time in shared memory as fp32
-// (k and scaled q, the 32 rows' v values, alpha, beta and k . q~ per token),
-// double-buffered: the next block's global loads are issued into registers
-// before the current block is scanned and stored to the other buffer after.
-// Lane s of a row holds columns 32 m + 4 s + e (m, e < 4), so the eight
-// distinct float4 addresses one warp reads per load cover all 32 banks.
+// a pair of rows, 16 fp32 state values of each, for the whole scan: the
+// state never leaves registers until the end, and every k and q value a lane
+// reads from shared memory serves two rows.  The four dot products are
+// summed across the eight lanes by one shuffle butterfly, after which all
+// eight hold the same c (addition is commutative, so the butterfly gives
+// every lane identical bits).  A CTA of 128 threads holds 32 rows of one
+// head; grid (dv/32, Hv, sequences).  Tokens are staged 32 at a time in
+// shared memory as fp32 (k and scaled q, the 32 rows' v values, alpha, beta
+// and k . q~ per token), double-buffered: the next block's global loads are
+// issued into registers before the current block is scanned and stored to
+// the other buffer after.  Lane s holds columns 32 m + 4 s + e (m, e < 4),
+// so the eight distinct float4 addresses one warp reads per load cover all
+// 32 banks.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -40,14 +42,14 @@ namespace {
 
 constexpr int kDk = kGdnDk;             // state columns (key width)
 constexpr int kRows = kGdnRows;         // state rows per CTA
-constexpr int kLanes = 8;               // lanes per row
-constexpr int kThreads = kRows * kLanes;  // 256
+constexpr int kLanes = 8;               // lanes per pair of rows
+constexpr int kThreads = kRows / 2 * kLanes;  // 128
 constexpr int kChunk = 32;              // tokens per staged block
 constexpr int kVec = kDk / (4 * kLanes);  // float4 groups per lane (4)
+constexpr int kKQ = kChunk * kDk / 8 / kThreads;  // 16-byte pieces of k (and q) per thread
 
-static_assert(kThreads == 256 && kVec == 4, "layout below assumes these");
-static_assert(kChunk * kDk / 8 == 2 * kThreads, "two 16-byte loads of k (and q) per thread");
-static_assert(kChunk * kRows / 8 == kThreads / 2, "one 16-byte load of v per thread of the first half");
+static_assert(kThreads == 128 && kVec == 4 && kKQ == 4, "layout below assumes these");
+static_assert(kChunk * kRows / 8 == kThreads, "one 16-byte piece of v (and of o) per thread");
 
 struct __align__(16) GdnSmem {
   float k[2][kChunk][kDk];
@@ -59,7 +61,7 @@ struct __align__(16) GdnSmem {
 
 // One staged block, in flight in registers.
 struct Prefetch {
-  uint4 k[2], q[2], v;
+  uint4 k[kKQ], q[kKQ], v;
   float gb;
 };
 
@@ -74,12 +76,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return ua | (ub << 16);
 }
 
-// Issue the global loads of tokens t0 .. t0+n-1 (n <= kChunk; lanes past n
+// Issue the global loads of tokens t0 .. t0+n-1 (n <= kChunk; pieces past n
 // load nothing and hold zeros).
 __device__ __forceinline__ void load_block(Prefetch& pf, const GdnParams& p, int h, int hk,
                                            int r0, int t0, int n, int tid) {
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < kKQ; ++j) {
     const int i = tid + j * kThreads;          // 16-byte piece of the block's k (q)
     const int tt = i >> 4, c8 = (i & 15) * 8;  // token, first column
     pf.k[j] = make_uint4(0, 0, 0, 0);
@@ -90,19 +92,19 @@ __device__ __forceinline__ void load_block(Prefetch& pf, const GdnParams& p, int
       pf.q[j] = __ldg(reinterpret_cast<const uint4*>(p.q + off));
     }
   }
-  pf.v = make_uint4(0, 0, 0, 0);
-  pf.gb = 0.f;
-  if (tid < kThreads / 2) {
+  {
     const int tt = tid >> 2, c8 = (tid & 3) * 8;
+    pf.v = make_uint4(0, 0, 0, 0);
     if (tt < n)
       pf.v = __ldg(reinterpret_cast<const uint4*>(p.v + ((size_t)(t0 + tt) * p.Hv + h) * p.dv +
                                                   r0 + c8));
-  } else if (tid < kThreads / 2 + 2 * kChunk) {
-    const int tt = (tid - kThreads / 2) & (kChunk - 1);
-    const bool is_beta = tid >= kThreads / 2 + kChunk;
+  }
+  pf.gb = 0.f;
+  if (tid < 2 * kChunk) {
+    const int tt = tid & (kChunk - 1);
     if (tt < n) {
       const size_t off = (size_t)(t0 + tt) * p.Hv + h;
-      pf.gb = is_beta ? __ldg(p.beta + off) : __ldg(p.g + off);
+      pf.gb = tid >= kChunk ? __ldg(p.beta + off) : __ldg(p.g + off);
     }
   }
 }
@@ -110,7 +112,7 @@ __device__ __forceinline__ void load_block(Prefetch& pf, const GdnParams& p, int
 __device__ __forceinline__ void store_block(GdnSmem& sm, int b, const Prefetch& pf, float scale,
                                             int tid) {
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < kKQ; ++j) {
     const int i = tid + j * kThreads;
     const int tt = i >> 4, c8 = (i & 15) * 8;
     const uint32_t* kw = reinterpret_cast<const uint32_t*>(&pf.k[j]);
@@ -124,44 +126,110 @@ __device__ __forceinline__ void store_block(GdnSmem& sm, int b, const Prefetch& 
     qd[1] = make_float4(scale * bf16_lo(qw[2]), scale * bf16_hi(qw[2]), scale * bf16_lo(qw[3]),
                         scale * bf16_hi(qw[3]));
   }
-  if (tid < kThreads / 2) {
+  {
     const int tt = tid >> 2, c8 = (tid & 3) * 8;
     const uint32_t* vw = reinterpret_cast<const uint32_t*>(&pf.v);
     float4* vd = reinterpret_cast<float4*>(&sm.v[b][tt][c8]);
     vd[0] = make_float4(bf16_lo(vw[0]), bf16_hi(vw[0]), bf16_lo(vw[1]), bf16_hi(vw[1]));
     vd[1] = make_float4(bf16_lo(vw[2]), bf16_hi(vw[2]), bf16_lo(vw[3]), bf16_hi(vw[3]));
-  } else if (tid < kThreads / 2 + kChunk) {
-    sm.sc[b][tid - kThreads / 2].x = expf(pf.gb);        // alpha, fp32
-  } else if (tid < kThreads / 2 + 2 * kChunk) {
-    sm.sc[b][tid - kThreads / 2 - kChunk].y = pf.gb;     // beta
+  }
+  if (tid < kChunk)
+    sm.sc[b][tid].x = expf(pf.gb);                       // alpha, fp32
+  else if (tid < 2 * kChunk)
+    sm.sc[b][tid - kChunk].y = pf.gb;                    // beta
+}
+
+// k . q~ of each staged token: eight threads per token (two tokens per
+// thread), same column split as the state rows.
+__device__ __forceinline__ void block_kq(GdnSmem& sm, int b, int tid) {
+  const int s = tid & 7;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int tt = (tid >> 3) + half * (kChunk / 2);
+    float acc = 0.f;
+#pragma unroll
+    for (int m = 0; m < kVec; ++m) {
+      const float4 a = *reinterpret_cast<const float4*>(&sm.k[b][tt][32 * m + 4 * s]);
+      const float4 c = *reinterpret_cast<const float4*>(&sm.q[b][tt][32 * m + 4 * s]);
+      acc = fmaf(a.x, c.x, acc);
+      acc = fmaf(a.y, c.y, acc);
+      acc = fmaf(a.z, c.z, acc);
+      acc = fmaf(a.w, c.w, acc);
+    }
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
+    if (s == 0) sm.sc[b][tt].z = acc;
   }
 }
 
-// k . q~ of each staged token: eight threads per token, same column split as
-// the state rows.
-__device__ __forceinline__ void block_kq(GdnSmem& sm, int b, int tid) {
-  const int tt = tid >> 3, s = tid & 7;
-  float acc = 0.f;
+__device__ __forceinline__ void load_kq(const GdnSmem& sm, int b, int t, int s, float4 (&kk)[kVec],
+                                        float4 (&qq)[kVec]) {
 #pragma unroll
   for (int m = 0; m < kVec; ++m) {
-    const float4 a = *reinterpret_cast<const float4*>(&sm.k[b][tt][32 * m + 4 * s]);
-    const float4 c = *reinterpret_cast<const float4*>(&sm.q[b][tt][32 * m + 4 * s]);
-    acc = fmaf(a.x, c.x, acc);
-    acc = fmaf(a.y, c.y, acc);
-    acc = fmaf(a.z, c.z, acc);
-    acc = fmaf(a.w, c.w, acc);
+    kk[m] = *reinterpret_cast<const float4*>(&sm.k[b][t][32 * m + 4 * s]);
+    qq[m] = *reinterpret_cast<const float4*>(&sm.q[b][t][32 * m + 4 * s]);
   }
-  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
-  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
-  if (s == 0) sm.sc[b][tt].z = acc;
+}
+
+// One token for the lane's two rows (2 pr, 2 pr + 1).
+__device__ __forceinline__ void scan_token(GdnSmem& sm, int b, int t, int pr, int s,
+                                           float (&SA)[kVec][4], float (&SB)[kVec][4],
+                                           const float4 (&kk)[kVec], const float4 (&qq)[kVec]) {
+  float uA0 = 0.f, uA1 = 0.f, wA0 = 0.f, wA1 = 0.f;   // S.k and S.q~ of row A, two chains each
+  float uB0 = 0.f, uB1 = 0.f, wB0 = 0.f, wB1 = 0.f;
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) {
+    uA0 = fmaf(SA[m][0], kk[m].x, uA0);
+    wA0 = fmaf(SA[m][0], qq[m].x, wA0);
+    uB0 = fmaf(SB[m][0], kk[m].x, uB0);
+    wB0 = fmaf(SB[m][0], qq[m].x, wB0);
+    uA1 = fmaf(SA[m][1], kk[m].y, uA1);
+    wA1 = fmaf(SA[m][1], qq[m].y, wA1);
+    uB1 = fmaf(SB[m][1], kk[m].y, uB1);
+    wB1 = fmaf(SB[m][1], qq[m].y, wB1);
+    uA0 = fmaf(SA[m][2], kk[m].z, uA0);
+    wA0 = fmaf(SA[m][2], qq[m].z, wA0);
+    uB0 = fmaf(SB[m][2], kk[m].z, uB0);
+    wB0 = fmaf(SB[m][2], qq[m].z, wB0);
+    uA1 = fmaf(SA[m][3], kk[m].w, uA1);
+    wA1 = fmaf(SA[m][3], qq[m].w, wA1);
+    uB1 = fmaf(SB[m][3], kk[m].w, uB1);
+    wB1 = fmaf(SB[m][3], qq[m].w, wB1);
+  }
+  float uA = uA0 + uA1, wA = wA0 + wA1, uB = uB0 + uB1, wB = wB0 + wB1;
+#pragma unroll
+  for (int lv = 1; lv < kLanes; lv <<= 1) {
+    uA += __shfl_xor_sync(0xFFFFFFFFu, uA, lv);
+    wA += __shfl_xor_sync(0xFFFFFFFFu, wA, lv);
+    uB += __shfl_xor_sync(0xFFFFFFFFu, uB, lv);
+    wB += __shfl_xor_sync(0xFFFFFFFFu, wB, lv);
+  }
+  const float4 sc = sm.sc[b][t];                        // alpha, beta, k . q~
+  const float2 vv = *reinterpret_cast<const float2*>(&sm.v[b][t][2 * pr]);
+  const float cA = sc.y * (vv.x - sc.x * uA);
+  const float cB = sc.y * (vv.y - sc.x * uB);
+  if (s == 0)
+    *reinterpret_cast<float2*>(&sm.o[t][2 * pr]) =
+        make_float2(fmaf(sc.x, wA, cA * sc.z), fmaf(sc.x, wB, cB * sc.z));
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) {
+    SA[m][0] = fmaf(sc.x, SA[m][0], cA * kk[m].x);
+    SA[m][1] = fmaf(sc.x, SA[m][1], cA * kk[m].y);
+    SA[m][2] = fmaf(sc.x, SA[m][2], cA * kk[m].z);
+    SA[m][3] = fmaf(sc.x, SA[m][3], cA * kk[m].w);
+    SB[m][0] = fmaf(sc.x, SB[m][0], cB * kk[m].x);
+    SB[m][1] = fmaf(sc.x, SB[m][1], cB * kk[m].y);
+    SB[m][2] = fmaf(sc.x, SB[m][2], cB * kk[m].z);
+    SB[m][3] = fmaf(sc.x, SB[m][3], cB * kk[m].w);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(const GdnParams p) {
   extern __shared__ float4 gdn_smem_raw[];
   GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gdn_smem_raw);
   const int tid = threadIdx.x;
-  const int row = tid >> 3, s = tid & 7;
+  const int pr = tid >> 3, s = tid & 7;                 // row pair, lane within it
   const int r0 = blockIdx.x * kRows, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
 
@@ -171,14 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(const GdnParams p
     end = min(max(__ldg(p.offsets + n + 1), beg), p.T);
   }
 
-  // The row's 16 state values: columns 32 m + 4 s + e.
-  const size_t srow = (((size_t)n * p.Hv + h) * p.dv + r0 + row) * kDk + 4 * s;
-  float S[kVec][4];
+  // 16 state values of each of the two rows: columns 32 m + 4 s + e.
+  const size_t srow = (((size_t)n * p.Hv + h) * p.dv + r0 + 2 * pr) * kDk + 4 * s;
+  float SA[kVec][4], SB[kVec][4];
 #pragma unroll
   for (int m = 0; m < kVec; ++m) {
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (p.state_in) x = __ldg(reinterpret_cast<const float4*>(p.state_in + srow + 32 * m));
-    S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+    if (p.state_in) {
+      a = __ldg(reinterpret_cast<const float4*>(p.state_in + srow + 32 * m));
+      c = __ldg(reinterpret_cast<const float4*>(p.state_in + srow + kDk + 32 * m));
+    }
+    SA[m][0] = a.x; SA[m][1] = a.y; SA[m][2] = a.z; SA[m][3] = a.w;
+    SB[m][0] = c.x; SB[m][1] = c.y; SB[m][2] = c.z; SB[m][3] = c.w;
   }
 
   const int nblocks = (end - beg + kChunk - 1) / kChunk;
@@ -197,60 +269,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(const GdnParams p
       const bool more = blk + 1 < nblocks;
       if (more) load_block(pf, p, h, hk, r0, t0 + kChunk, min(kChunk, end - t0 - kChunk), tid);
 
-      float4 kk[kVec], qq[kVec];
-#pragma unroll
-      for (int m = 0; m < kVec; ++m) {
-        kk[m] = *reinterpret_cast<const float4*>(&sm.k[b][0][32 * m + 4 * s]);
-        qq[m] = *reinterpret_cast<const float4*>(&sm.q[b][0][32 * m + 4 * s]);
+      // Two tokens per iteration, k and q of the next token loaded during
+      // the current one (the block is zero-padded up to kChunk tokens).
+      float4 k0[kVec], q0[kVec], k1[kVec], q1[kVec];
+      load_kq(sm, b, 0, s, k0, q0);
+      int t = 0;
+      for (; t + 1 < ntok; t += 2) {
+        load_kq(sm, b, t + 1, s, k1, q1);
+        scan_token(sm, b, t, pr, s, SA, SB, k0, q0);
+        if (t + 2 < kChunk) load_kq(sm, b, t + 2, s, k0, q0);
+        scan_token(sm, b, t + 1, pr, s, SA, SB, k1, q1);
       }
-      for (int t = 0; t < ntok; ++t) {
-        // next token's k and q (the block is zero-padded, so t + 1 < kChunk is enough)
-        float4 kn[kVec], qn[kVec];
-        const int tn = t + 1 < kChunk ? t + 1 : t;
-#pragma unroll
-        for (int m = 0; m < kVec; ++m) {
-          kn[m] = *reinterpret_cast<const float4*>(&sm.k[b][tn][32 * m + 4 * s]);
-          qn[m] = *reinterpret_cast<const float4*>(&sm.q[b][tn][32 * m + 4 * s]);
-        }
-        float u0 = 0.f, u1 = 0.f, w0 = 0.f, w1 = 0.f;   // S.k and S.q~, two chains each
-#pragma unroll
-        for (int m = 0; m < kVec; ++m) {
-          u0 = fmaf(S[m][0], kk[m].x, u0);
-          w0 = fmaf(S[m][0], qq[m].x, w0);
-          u1 = fmaf(S[m][1], kk[m].y, u1);
-          w1 = fmaf(S[m][1], qq[m].y, w1);
-          u0 = fmaf(S[m][2], kk[m].z, u0);
-          w0 = fmaf(S[m][2], qq[m].z, w0);
-          u1 = fmaf(S[m][3], kk[m].w, u1);
-          w1 = fmaf(S[m][3], qq[m].w, w1);
-        }
-        float u = u0 + u1, w = w0 + w1;
-        u += __shfl_xor_sync(0xFFFFFFFFu, u, 1);
-        w += __shfl_xor_sync(0xFFFFFFFFu, w, 1);
-        u += __shfl_xor_sync(0xFFFFFFFFu, u, 2);
-        w += __shfl_xor_sync(0xFFFFFFFFu, w, 2);
-        u += __shfl_xor_sync(0xFFFFFFFFu, u, 4);
-        w += __shfl_xor_sync(0xFFFFFFFFu, w, 4);
-
-        const float4 sc = sm.sc[b][t];                  // alpha, beta, k . q~
-        const float vi = sm.v[b][t][row];
-        const float c = sc.y * (vi - sc.x * u);
-        if (s == 0) sm.o[t][row] = fmaf(sc.x, w, c * sc.z);
-#pragma unroll
-        for (int m = 0; m < kVec; ++m) {
-          S[m][0] = fmaf(sc.x, S[m][0], c * kk[m].x);
-          S[m][1] = fmaf(sc.x, S[m][1], c * kk[m].y);
-          S[m][2] = fmaf(sc.x, S[m][2], c * kk[m].z);
-          S[m][3] = fmaf(sc.x, S[m][3], c * kk[m].w);
-          kk[m] = kn[m];
-          qq[m] = qn[m];
-        }
-      }
+      if (t < ntok) scan_token(sm, b, t, pr, s, SA, SB, k0, q0);
 
       if (more) store_block(sm, b ^ 1, pf, p.scale, tid);
       __syncthreads();
-      // o of this block: 32 tokens x 32 rows, 16 bytes per thread of the first half
-      if (tid < kThreads / 2) {
+      // o of this block: 32 tokens x 32 rows, one 16-byte piece per thread
+      {
         const int tt = tid >> 2, c8 = (tid & 3) * 8;
         if (tt < ntok) {
           const float* src = &sm.o[tt][c8];
@@ -269,9 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(const GdnParams p
 
   if (p.state_out) {
 #pragma unroll
-    for (int m = 0; m < kVec; ++m)
+    for (int m = 0; m < kVec; ++m) {
       *reinterpret_cast<float4*>(p.state_out + srow + 32 * m) =
-          make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
+          make_float4(SA[m][0], SA[m][1], SA[m][2], SA[m][3]);
+      *reinterpret_cast<float4*>(p.state_out + srow + kDk + 32 * m) =
+          make_float4(SB[m][0], SB[m][1], SB[m][2], SB[m][3]);
+    }
   }
 }
 
