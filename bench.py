@@ -365,6 +365,12 @@ def gdn_alu_ops(T, Hv, dv, dk):
     return 4 * T * Hv * dv * dk
 
 
+def gdn_bytes(T, Hk, Hv, dk, dv):
+    """Bytes one scan must move: q, k, v in and o out (bf16), g and beta
+    (fp32), the final state out (fp32)."""
+    return 2 * T * Hk * dk * 2 + T * Hv * dv * 2 * 2 + T * Hv * 4 * 2 + Hv * dv * dk * 4
+
+
 def gdn_alu_peak(sm_count):
     """fp32 lane operations per second at the maximum SM clock (T ops/s)."""
     return sm_count * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12
@@ -401,6 +407,7 @@ def run_gdn(args, torch, M, device):
     ops = gdn_alu_ops(GDN_T, shape.Hv, shape.dv, shape.dk)
     achieved = ops / (us * 1e-6) / 1e12
     peak = gdn_alu_peak(sm_count)
+    kv = profiled_traffic("gdn_scan_kernel")
     return {
         "config": f"one {GDN_T}-token prompt, Hk={shape.Hk} query/key heads, Hv={shape.Hv} "
                   f"value heads, dk=dv={shape.dk}; q, k unit-norm bf16, v bf16, alpha in "
@@ -408,10 +415,13 @@ def run_gdn(args, torch, M, device):
         "us": us, "tokens_per_s": GDN_T / (us * 1e-6),
         "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
                      "unit": "T fp32 lane-ops/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "kernel": "gdn_scan_kernel",
+                     "traffic": int(kv["bytes_per_launch"]) if kv else None,
+                     "kernel": "gdn_scan_kernel",
                      "algorithmic_ops_per_launch": ops,
                      "peak_source": f"{sm_count} SMs x {FP32_LANES_PER_SM} fp32 lanes x "
                                     f"{SM_MAX_MHZ:.0f} MHz"},
+        "algorithmic_bytes_per_launch": gdn_bytes(GDN_T, shape.Hk, shape.Hv, shape.dk,
+                                                  shape.dv),
         "gpu_launches": 1, "clocks": clocks,
     }
 

@@ -48,3 +48,10 @@ def test_gdn_scan_alu_roofline():
     assert bench.gdn_alu_ops(2048, 32, 128, 128) == 4 * 2048 * 32 * 128 * 128
     # 152 SMs x 128 fp32 lanes x 2.07 GHz
     assert abs(bench.gdn_alu_peak(152) - 40.27392) < 1e-9
+
+
+def test_gdn_scan_bytes():
+    # q, k 16 heads x 128, v and o 32 heads x 128 (bf16), g and beta (fp32), state (fp32)
+    assert bench.gdn_bytes(2048, 16, 32, 128, 128) == (
+        2 * 2048 * 16 * 128 * 2 + 2 * 2048 * 32 * 128 * 2 + 2 * 2048 * 32 * 4 + 32 * 128 * 128 * 4)
+    assert bench.gdn_bytes(2048, 16, 32, 128, 128) == 52953088
