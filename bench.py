@@ -408,6 +408,19 @@ def run_gdn(args, torch, M, device):
     achieved = ops / (us * 1e-6) / 1e12
     peak = gdn_alu_peak(sm_count)
     kv = profiled_traffic("gdn_scan_kernel")
+    cpu = None
+    if getattr(args, "world", 1) == 1:   # the fp64 oracle on the host, a bounded sample
+        try:
+            from oracle import gdn_oracle as G
+            n = 256
+            t_start = time.perf_counter()
+            G.gdn_scan(inp.q[:n], inp.k[:n], inp.v[:n], inp.g[:n], inp.beta[:n])
+            cpu = {"value": n / (time.perf_counter() - t_start), "unit": "tokens/s", "cores": 1,
+                   "kind": "oracle",
+                   "sample": f"fp64 oracle, the first {n} tokens of the same prompt, all "
+                             f"{shape.Hv} value heads (numpy, one thread)"}
+        except Exception as ex:  # informative only; never fail the bench on it
+            cpu = {"error": str(ex)}
     return {
         "config": f"one {GDN_T}-token prompt, Hk={shape.Hk} query/key heads, Hv={shape.Hv} "
                   f"value heads, dk=dv={shape.dk}; q, k unit-norm bf16, v bf16, alpha in "
@@ -422,7 +435,7 @@ def run_gdn(args, torch, M, device):
                                     f"{SM_MAX_MHZ:.0f} MHz"},
         "algorithmic_bytes_per_launch": gdn_bytes(GDN_T, shape.Hk, shape.Hv, shape.dk,
                                                   shape.dv),
-        "gpu_launches": 1, "clocks": clocks,
+        "gpu_launches": 1, "clocks": clocks, "cpu_baseline": cpu,
     }
 
 
