@@ -1,9 +1,10 @@
 """Pins of the Gated DeltaNet scan oracle to facts fixed by the pages and by
 mathematics: a hand-worked example (tests/golden/gdn_hand.txt), closed forms
 of special cases (no write, pure overwrite, no decay), the delta rule as one
-gradient step of an online regression loss (checked with autograd), and the
-structure of the scan (state carried across chunks, sequences independent,
-grouped heads, readout scale).  A dropped term, a wrong sign, a swapped
+gradient step of an online regression loss (checked with autograd), an
+independent chunked evaluation (a triangular solve per chunk of tokens), and
+the structure of the scan (state carried across chunks, sequences
+independent, grouped heads, readout scale).  A dropped term, a wrong sign, a swapped
 operand or a wrong head index in oracle/gdn_oracle.py fails at least one.
 """
 import importlib.util
@@ -249,3 +250,47 @@ def test_value_heads_share_their_query_key_head():
 def test_bf16_bit_inputs_read_exactly():
     bits = np.array([[[0x3F80, 0xC000, 0x3E80, 0x0000]]], dtype=np.uint16)   # 1, -2, 0.25, 0
     np.testing.assert_array_equal(G.as_values(bits), [[[1.0, -2.0, 0.25, 0.0]]])
+
+
+def _chunked_scan(q, k, v, g, beta, scale, S0, C):
+    """The same rule evaluated a chunk of C tokens at a time, derived
+    independently of the oracle's token loop.  Unrolling the rule inside a
+    chunk that starts from state S_0, with gamma_i the product of the gates up
+    to token i and c_i = beta_i (v_i - alpha_i S_{i-1} k_i):
+        S_i = gamma_i S_0 + sum_{j<=i} (gamma_i / gamma_j) c_j k_j^T,
+    so the c_i solve the unit lower-triangular system
+        c_i + beta_i sum_{j<i} (gamma_i/gamma_j)(k_i.k_j) c_j
+            = beta_i (v_i - gamma_i S_0 k_i),
+    and o_i = scale (gamma_i S_0 q_i + sum_{j<=i} (gamma_i/gamma_j)(q_i.k_j) c_j).
+    One head: q, k [T, dk], v [T, dv], g, beta [T], S0 [dv, dk]."""
+    from scipy.linalg import solve_triangular
+    T = q.shape[0]
+    S = S0.copy()
+    o = np.zeros((T, v.shape[1]))
+    for a in range(0, T, C):
+        b = min(T, a + C)
+        Q, K, V = q[a:b], k[a:b], v[a:b]
+        gam = np.exp(np.cumsum(g[a:b]))
+        ratio = gam[:, None] / gam[None, :]
+        L = np.tril(beta[a:b, None] * ratio * (K @ K.T), -1)
+        rhs = beta[a:b, None] * (V - gam[:, None] * (K @ S.T))
+        Cm = solve_triangular(np.eye(b - a) + L, rhs, lower=True, unit_diagonal=True)
+        M = np.tril(ratio * (Q @ K.T))
+        o[a:b] = scale * (gam[:, None] * (Q @ S.T) + M @ Cm)
+        S = gam[-1] * S + Cm.T @ ((gam[-1] / gam)[:, None] * K)
+    return o, S
+
+
+@pytest.mark.parametrize("C", [1, 4, 16])
+def test_chunked_form_matches_the_token_loop(C):
+    """An independent evaluation (chunks, a triangular solve, matrix
+    products: the blockwise way the pages mention) gives the same outputs and
+    state as the oracle's token-by-token scan."""
+    rng = np.random.default_rng(12)
+    T, dk, dv = 37, 8, 5
+    q, k, v, g, beta = _random(rng, T, 1, 1, dk, dv)
+    S0 = rng.standard_normal((1, 1, dv, dk))
+    o, S = G.gdn_scan(q, k, v, g, beta, scale=0.6, state0=S0)
+    oc, Sc = _chunked_scan(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], 0.6, S0[0, 0], C)
+    np.testing.assert_allclose(o[:, 0], oc, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(S[0, 0], Sc, rtol=1e-10, atol=1e-11)
