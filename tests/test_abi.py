@@ -133,3 +133,19 @@ def test_gdn_scan_empty_without_state_is_a_no_op(lib):
                         128, 64, None, None, a["o"], None) == 0
     assert lib.gdn_scan(None, None, None, None, None, 1.0, None, 1, 0, 2, 4, 128, 64, None, None,
                         None, None) == 0
+
+
+def test_create_without_a_device_fails_cleanly(lib):
+    """On a machine with no usable CUDA device moe_create returns
+    MOE_ERR_CUDA with a message and no handle (it must not crash).  Skipped
+    where a device exists: there the fake weight addresses would be read."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    from sparse_moe_bit_gb300 import moe
+    h = ctypes.c_void_p(0x1234)
+    w = moe._Weights(*([0x10000] * 14))
+    r = lib.moe_create(ctypes.byref(_cfg()), ctypes.byref(w), None, ctypes.byref(h))
+    assert r == 3, lib.moe_last_error()
+    assert h.value is None
+    assert lib.moe_last_error()
