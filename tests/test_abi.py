@@ -149,3 +149,29 @@ def test_create_without_a_device_fails_cleanly(lib):
     assert r == 3, lib.moe_last_error()
     assert h.value is None
     assert lib.moe_last_error()
+
+
+def test_gdn_binding_fails_loudly_without_a_device(lib):
+    """The binding marshals the scan's arguments (N from the offsets, the
+    default scale) and surfaces the library's status: with no device the call
+    passes argument checking and then fails with MOE_ERR_CUDA; there is no
+    CPU fallback.  Skipped where a device exists (the tensors here live on
+    the host)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    import types
+    import sparse_moe_bit_gb300 as M
+    legacy = types.SimpleNamespace(cuda_stream=0)          # torch cannot make a stream here
+    T, Hk, Hv = 8, 1, 2
+    q = torch.zeros(T, Hk, 128, dtype=torch.bfloat16)
+    v = torch.zeros(T, Hv, 32, dtype=torch.bfloat16)
+    g = torch.zeros(T, Hv)
+    off = torch.tensor([0, 3, 8], dtype=torch.int32)
+    with pytest.raises(M.MoEError) as ex:
+        M.gdn_scan(q, q, v, g, g, offsets=off, stream=legacy)
+    assert ex.value.status == 3
+    bad = torch.zeros(T, Hk, 64, dtype=torch.bfloat16)     # dk = 64: refused before any launch
+    with pytest.raises(M.MoEError) as ex:
+        M.gdn_scan(bad, bad, v, g, g, stream=legacy)
+    assert ex.value.status == 2
