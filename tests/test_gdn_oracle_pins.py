@@ -294,3 +294,45 @@ def test_chunked_form_matches_the_token_loop(C):
     oc, Sc = _chunked_scan(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], 0.6, S0[0, 0], C)
     np.testing.assert_allclose(o[:, 0], oc, rtol=1e-10, atol=1e-11)
     np.testing.assert_allclose(S[0, 0], Sc, rtol=1e-10, atol=1e-11)
+
+
+def _wy_scan(q, k, v, g, beta, scale, S0, C):
+    """The chunked form with everything that depends on the inputs alone
+    folded into four per-chunk matrices, so that the sequential pass over the
+    chunks touches the state only through products with them:
+        A = (I + L)^{-1} diag(beta)          (L as in _chunked_scan)
+        U = A V,   W = A diag(gamma) K,   P = diag(gamma) Q~ - M W,   R = M U
+        c-vectors  C = U - W S_0^T
+        outputs    O = P S_0^T + R
+        end state  S = gamma_C S_0 + C^T diag(gamma_C / gamma) K."""
+    from scipy.linalg import solve_triangular
+    T = q.shape[0]
+    S = S0.copy()
+    o = np.zeros((T, v.shape[1]))
+    for a in range(0, T, C):
+        b = min(T, a + C)
+        Q, K, V = scale * q[a:b], k[a:b], v[a:b]
+        gam = np.exp(np.cumsum(g[a:b]))
+        ratio = gam[:, None] / gam[None, :]
+        L = np.tril(beta[a:b, None] * ratio * (K @ K.T), -1)
+        A = solve_triangular(np.eye(b - a) + L, np.diag(beta[a:b]), lower=True,
+                             unit_diagonal=True)
+        M = np.tril(ratio * (Q @ K.T))
+        U, W = A @ V, A @ (gam[:, None] * K)
+        P, R = gam[:, None] * Q - M @ W, M @ U
+        Cm = U - W @ S.T
+        o[a:b] = P @ S.T + R
+        S = gam[-1] * S + Cm.T @ ((gam[-1] / gam)[:, None] * K)
+    return o, S
+
+
+@pytest.mark.parametrize("C", [3, 16, 64])
+def test_input_only_chunk_matrices_reproduce_the_scan(C):
+    rng = np.random.default_rng(13)
+    T, dk, dv = 70, 8, 6
+    q, k, v, g, beta = _random(rng, T, 1, 1, dk, dv)
+    S0 = rng.standard_normal((1, 1, dv, dk))
+    o, S = G.gdn_scan(q, k, v, g, beta, scale=0.4, state0=S0)
+    ow, Sw = _wy_scan(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], 0.4, S0[0, 0], C)
+    np.testing.assert_allclose(o[:, 0], ow, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(S[0, 0], Sw, rtol=1e-10, atol=1e-11)
