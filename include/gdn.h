@@ -45,9 +45,11 @@ extern "C" {
  *   scale     readout scale (1/sqrt(dk) in the usual layer); finite
  *   offsets   int32 [N+1] device array of sequence boundaries (sequence n
  *             is tokens offsets[n] .. offsets[n+1]-1), or NULL for a single
- *             sequence of T tokens (then N must be 1).  The kernel clamps
- *             each boundary into [0, T] and makes them non-decreasing, so
- *             bad offsets cannot address memory outside the buffers; tokens
+ *             sequence of T tokens (then N must be 1).  Offsets must be
+ *             non-decreasing within [0, T]; the kernel clamps each
+ *             sequence's range into [0, T] with end >= start, so bad offsets
+ *             cannot address memory outside the buffers (ranges that then
+ *             overlap write the same rows of o in no defined order).  Tokens
  *             outside every sequence are not written.
  *   state_in  fp32 [N][Hv][dv][dk], 16-byte aligned, or NULL (zero state)
  *   state_out fp32 [N][Hv][dv][dk], 16-byte aligned, or NULL (not written);
