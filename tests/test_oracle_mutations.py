@@ -40,6 +40,19 @@ MUTATIONS = [
     ("perm index", "perm = (order // k).astype(np.int32)", "perm = (order % k).astype(np.int32)"),
     ("offsets shift", "offsets[1:] = np.cumsum(counts)", "offsets[:-1] = np.cumsum(counts)"),
     ("rms of v, not v^2", "np.mean(v * v, axis=-1, keepdims=True)", "np.mean(v, axis=-1, keepdims=True)"),
+    ("rms eps dropped", "np.mean(v * v, axis=-1, keepdims=True) + eps)",
+     "np.mean(v * v, axis=-1, keepdims=True))"),
+    ("silu of the product", "return (silu(g) * u) @ w_down.T", "return silu(g * u) @ w_down.T"),
+    ("scale used as bias", "return s * q + b", "return s * q + s"),
+    ("full-softmax denominator", "w = ex / ex.sum(axis=1, keepdims=True)",
+     "w = ex / np.exp(lg - m).sum(axis=1, keepdims=True)"),
+    ("shared weighted by 1 - sigma", "out += sigma[:, None] * swiglu_expert(x, wg, wu, wd)",
+     "out += (1 - sigma)[:, None] * swiglu_expert(x, wg, wu, wd)"),
+    ("weight of slot 0 for every slot", "out += w[:, j:j + 1] * y[:, j]",
+     "out += w[:, 0:1] * y[:, j]"),
+    ("+inf logits: weight to every kept expert", "hit = (top[pos] == np.inf).astype(F64)",
+     "hit = np.ones_like(top[pos])"),
+    ("all -inf logits: no weight", "w[neg] = 1.0 / k", "w[neg] = 0.0"),
 ]
 
 
