@@ -233,14 +233,15 @@ def test_sequences_are_independent():
     np.testing.assert_array_equal(S[1], S0[1])                 # empty sequence
 
 
-def test_value_heads_share_their_query_key_head():
-    """Hv = 4 value heads over Hk = 2 query/key heads: value heads 0, 1 read
-    q/k head 0 and value heads 2, 3 read q/k head 1."""
+@pytest.mark.parametrize("Hk,Hv", [(2, 4), (4, 8), (2, 6)])
+def test_value_heads_share_their_query_key_head(Hk, Hv):
+    """Hv value heads over Hk query/key heads: value head h reads q/k head
+    h // (Hv / Hk) (e.g. Hv = 4 over Hk = 2: heads 0, 1 read 0 and 2, 3 read 1)."""
     rng = np.random.default_rng(11)
-    q, k, v, g, beta = _random(rng, 6, 2, 4, 4, 3)
+    q, k, v, g, beta = _random(rng, 6, Hk, Hv, 4, 3)
     o, S = G.gdn_scan(q, k, v, g, beta)
-    for h in range(4):
-        hk = h // 2
+    for h in range(Hv):
+        hk = h // (Hv // Hk)
         oh, Sh = G.gdn_scan(q[:, hk:hk + 1], k[:, hk:hk + 1], v[:, h:h + 1], g[:, h:h + 1],
                             beta[:, h:h + 1])
         np.testing.assert_allclose(o[:, h], oh[:, 0], rtol=1e-13, atol=1e-14)

@@ -94,6 +94,15 @@ MUTATIONS_GDN = [
      "S_new = S @ transition + np.outer(v, k)"),
     ("dense transition sign", "np.eye(dk) - F64(beta)", "np.eye(dk) + F64(beta)"),
     ("bf16 bits misplaced", "<< np.uint32(16)", "<< np.uint32(15)"),
+    ("gate squared", "alpha = np.exp(g)[:, None, None]", "alpha = np.exp(2 * g)[:, None, None]"),
+    ("beta twice on the erase", "(S - beta[:, None, None] * Sk",
+     "(S - beta[:, None, None] ** 2 * Sk"),
+    ("readout unscaled", 'o = scale * np.einsum("hij,hj->hi", S_new, q)',
+     'o = np.einsum("hij,hj->hi", S_new, q)'),
+    ("last sequence dropped", "for n in range(N):", "for n in range(max(N - 1, 1)):"),
+    ("first initial state for every sequence", "states[:] = np.asarray(state0, F64)",
+     "states[:] = np.asarray(state0, F64)[:1]"),
+    ("q/k head h // Hk", "head_of = np.arange(Hv) // (Hv // Hk)", "head_of = np.arange(Hv) // Hk"),
 ]
 
 
