@@ -228,8 +228,10 @@ moe_status moe_profile_read(moe_handle* h, float* ms, int n, int* calls);
  * whose device memory is entirely owned by another framework.
  *   Scratch: one file-scope device array of about 2.5 MB inside this library,
  *   held by every GPU that loads the library until the process exits.  Limits:
- *   T <= 2048, E <= 256, k <= 16 and k <= E; larger sizes return
- *   MOE_ERR_INVALID_ARG before anything is enqueued.
+ *   T <= 2048, E <= 256, k <= 16 and k <= E; larger sizes, a NULL output and
+ *   a pointer that is not 4-byte aligned return MOE_ERR_INVALID_ARG before
+ *   anything is enqueued; a launch that fails returns MOE_ERR_CUDA (errors
+ *   of earlier, unrelated launches are neither reported nor cleared).
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   All calls share the one array: calls that overlap on the GPU (different

@@ -18,8 +18,8 @@ Source: Perplexity, "Optimizing on-device inference for Apple Silicon"
 * §"Reduce intermediate and state traffic": the expert output projection is
   combined with its routing score and with the shared expert's result.
 
-Where the pages leave a step open this module takes the plain reading (all of
-them are listed in the design doc): softmax over the router logits, keep the top k
+Where the pages leave a step open this module takes the plain reading:
+softmax over the router logits, keep the top k
 ordered by (logit descending, expert index ascending) and renormalise over
 those k; SwiGLU experts ``down(silu(gate x) * (up x))``; the shared expert
 weighted by ``sigmoid(w_sg . x)``; dequantised value ``s * q + beta``.

@@ -273,26 +273,15 @@ __device__ __forceinline__ float silu_tanh(float z) {
   return fmaf(hz, t, hz);
 }
 
-// TMA load of B: a 2-D tile (16 rows).  With CL > 1 the data is multicast to
-// the same shared-memory offset of every CTA of the cluster and each CTA's
-// barrier at `bar` receives its bytes.
-template <int CL>
+// TMA load of B: a 2-D tile (16 rows) into this CTA's shared memory, its
+// bytes counted on this CTA's barrier at `bar`.
 __device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             uint32_t bar) {
-  if (CL == 1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(tm), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-  } else {
-    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(tm), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-  }
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 // TMA load of this CTA's half of a pair's B tile (a 16-row slab into its own
@@ -305,21 +294,6 @@ __device__ __forceinline__ void tma_tile_2d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(tm), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
-}
-
-// tcgen05 commit that arrives on `bar` in every CTA of the cluster
-template <int CL>
-__device__ __forceinline__ void tc_commit_cluster(uint32_t bar) {
-  if (CL == 1) {
-    tc_commit(bar);
-  } else {
-    const uint16_t mask = (uint16_t)((1u << CL) - 1u);
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-  }
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -346,20 +320,19 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// CL: CTAs per cluster.  The CL CTAs of a cluster work on the same token tile
-// (consecutive weight units m), each fetching every CL-th 16-row slab of B and
-// multicasting it to all of them; a B slot is reused only after every CTA's
-// MMAs have read it (each MMA commit arrives on the slot's barrier in all CTAs).
-// PAIR (CL = 2, grouped modes): the two CTAs form a tcgen05 pair.  The even
-// CTA issues MMAs of M = 256 over both CTAs' A tiles (its own weight unit m
-// and the odd CTA's m + 1, each dequantised into its own TMEM); each CTA
-// loads half of the token tile into its own shared memory, so that every
-// B byte is written to and read from one SM's shared memory only once for
-// 256 weight rows.  The odd CTA's dequantising and epilogue warps arrive on
-// the even CTA's barriers; the even CTA's commits arrive on both CTAs'.
+// CL: CTAs per cluster, 1 without pairs.
+// PAIR (CL = 2, grouped modes): the two CTAs form a tcgen05 pair working on
+// the same token tile.  The even CTA issues MMAs of M = 256 over both CTAs'
+// A tiles (its own weight unit m and the odd CTA's m + 1, each dequantised
+// into its own TMEM); each CTA loads half of the token tile into its own
+// shared memory, so that every B byte is written to and read from one SM's
+// shared memory only once for 256 weight rows.  The odd CTA's dequantising
+// and epilogue warps arrive on the even CTA's barriers; the even CTA's
+// commits arrive on both CTAs'.
 template <int MODE, int CL, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_constant__ MmaParams p) {
-  static_assert(!PAIR || (CL == 2 && MODE != MMA_ROUTER), "pairs: two CTAs, grouped modes");
+  static_assert(PAIR ? (CL == 2 && MODE != MMA_ROUTER) : CL == 1,
+                "pairs: two CTAs, grouped modes; otherwise one CTA");
   using C = Cfg<MODE, PAIR>;
   constexpr int kPad = PAIR ? 32 : 16;
   // gate/up: the epilogue warps, idle while a unit's MMAs run (its single
@@ -418,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     for (int s = 0; s < kBStages; ++s) {
       // gate/up: one arrival per CTA of the pair (gathered rows, no byte count)
       mbar_init(S.b_full(s), (MODE == MMA_GATEUP && PAIR) ? 2 : 1);
-      mbar_init(S.b_empty(s), (PAIR ? 1 : CL) * C::NISS);
+      mbar_init(S.b_empty(s), C::NISS);
     }
     for (int b = 0; b < C::NACC; ++b) {
       mbar_init(S.acc_full(b), C::NISS);
@@ -443,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
+  if (CL > 1) cluster_sync_all();  // the peer's barriers are initialised before it arrives
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int kbu = p.kb_per_unit;
@@ -630,15 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
               tma_tile_2d_pair(bs + k2 * C::B_SUB + sl * 2048, &p.tmB,
                                (k0 + kb * C::KPS + k2) * 64, t.row0 + crank * half + 16 * sl, fb);
         } else {
-          // the whole tile arrives in every CTA; this CTA fetches 16-row slabs
-          // crank, crank + CL, ... (one 2-D tile per slab)
+          // the whole tile, one 2-D tile per 16-row slab
           if (lane == 0) mbar_arrive_expect_tx(S.b_full(s), (uint32_t)t.npad * 128 * C::KPS);
           __syncwarp();
           const int nslab = t.npad >> 4;
 #pragma unroll
           for (int k2 = 0; k2 < C::KPS; ++k2)
-            for (int sl = crank + CL * lane; sl < nslab; sl += 32 * CL)
-              tma_tile_2d<CL>(bs + k2 * C::B_SUB + sl * 2048, &p.tmB,
+            for (int sl = lane; sl < nslab; sl += 32)
+              tma_tile_2d(bs + k2 * C::B_SUB + sl * 2048, &p.tmB,
                               (k0 + kb * C::KPS + k2) * 64, t.row0 + 16 * sl, S.b_full(s));
         }
         ++gb;
@@ -710,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
             tc_commit_pair_mc(S.b_empty(sb), 3);
           } else {
             tc_commit(S.a_empty(sa));
-            tc_commit_cluster<CL>(S.b_empty(sb));
+            tc_commit(S.b_empty(sb));
           }
           if (++sa == kAStages) { sa = 0; pa ^= 1; }
           if (++sb == (uint32_t)kBStages) { sb = 0; pb ^= 1; }
@@ -961,23 +933,6 @@ cudaError_t launch_mode(const MmaParams& p, int grid, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, grouped_mma_kernel<MODE, CL, PAIR>, p);
 }
 
-// CTAs per cluster for a grouped launch without pairs: a power of two
-// dividing the units of one tile.  Gate/up gathers its token rows (no
-// multicast): 1.  Down: 2 measured on GB300 (T=4096, Zipf); MOE_GEMM_CLUSTER
-// (1, 2, 4) overrides it.
-int cluster_for(int mode, int units_per_tile) {
-  if (mode == MMA_GATEUP) return 1;
-  static int env = -1;
-  if (env < 0) {
-    const char* e = getenv("MOE_GEMM_CLUSTER");
-    env = e ? atoi(e) : 0;
-    if (env != 1 && env != 2 && env != 4) env = 0;
-  }
-  int cl = env ? env : (mode == MMA_GATEUP ? 4 : 2);
-  while (cl > 1 && units_per_tile % cl != 0) cl >>= 1;
-  return cl;
-}
-
 // CTA pairs (tcgen05 cta_group::2) for the grouped GEMMs unless
 // MOE_GEMM_2SM=0; they need an even number of weight units per tile.
 bool pairs_for(int units_per_tile) {
@@ -1033,9 +988,6 @@ cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStrea
     return launch_mode<MMA_DOWN, 2, true>(p, grid, st);
   }
   if (mode == MMA_GATEUP) return launch_mode<MMA_GATEUP, 1, false>(p, grid, st);
-  const int cl = cluster_for(mode, p.units_per_tile);
-  if (cl == 4) return launch_mode<MMA_DOWN, 4, false>(p, grid, st);
-  if (cl == 2) return launch_mode<MMA_DOWN, 2, false>(p, grid, st);
   return launch_mode<MMA_DOWN, 1, false>(p, grid, st);
 }
 

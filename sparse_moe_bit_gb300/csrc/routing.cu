@@ -835,6 +835,11 @@ extern "C" moe_status moe_route_from_logits_noalloc(const float* logits, int T, 
     return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!logits || !idx || !w || !counts || !offsets || !perm || !slot) return MOE_ERR_INVALID_ARG;
+  // the same alignment as the handle-based routing calls: 4-byte elements
+  auto al4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+  if (!al4(logits) || !al4(logit_bias) || !al4(idx) || !al4(w) || !al4(counts) ||
+      !al4(offsets) || !al4(perm) || !al4(slot))
+    return MOE_ERR_INVALID_ARG;
   unsigned char* s = nullptr;
   if (na_scratch(&s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -843,14 +848,32 @@ extern "C" moe_status moe_route_from_logits_noalloc(const float* logits, int T, 
   int32_t* base = reinterpret_cast<int32_t*>(s + kNaBase);
   int4* tiles = reinterpret_cast<int4*>(s + kNaTilesOff);
   int32_t* ntiles = reinterpret_cast<int32_t*>(s + kNaNtiles);
-  // every scratch word is written before it is read: nothing to clear
-  topk_kernel<8><<<nblk, kTopkThreads, 0, st>>>(
-      logits, 1, T, E, k, logit_bias, reinterpret_cast<float*>(s + kNaLogits), idx, w, hist,
-      reinterpret_cast<int*>(s + kNaErr));
-  scan_tiles_kernel<<<1, 1024, 0, st>>>(hist, nblk, T, E, k, 0, base, counts, offsets, tiles,
-                                        ntiles, nullptr);
-  scatter_kernel<<<nblk, 256, 0, st>>>(idx, w, offsets, base, T, E, k, 0, perm, slot,
-                                       reinterpret_cast<int32_t*>(s + kNaDst),
-                                       reinterpret_cast<float*>(s + kNaWrow));
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  float* lg = reinterpret_cast<float*>(s + kNaLogits);
+  int* err = reinterpret_cast<int*>(s + kNaErr);
+  int32_t* dst = reinterpret_cast<int32_t*>(s + kNaDst);
+  float* wrow = reinterpret_cast<float*>(s + kNaWrow);
+  // Every scratch word is written before it is read: nothing to clear.  Each
+  // launch's own status is checked (an error left by an earlier, unrelated
+  // launch is neither reported here nor cleared).
+  auto cfg = [&](int grid, int threads) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(grid);
+    c.blockDim = dim3(threads);
+    c.stream = st;
+    return c;
+  };
+  cudaLaunchConfig_t c1 = cfg(nblk, kTopkThreads);
+  if (cudaLaunchKernelEx(&c1, topk_kernel<8>, logits, 1, T, E, k, logit_bias, lg, idx, w, hist,
+                         err) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  cudaLaunchConfig_t c2 = cfg(1, 1024);
+  if (cudaLaunchKernelEx(&c2, scan_tiles_kernel, (const int32_t*)hist, nblk, T, E, k, 0, base,
+                         counts, offsets, tiles, ntiles, (unsigned*)nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  cudaLaunchConfig_t c3 = cfg(nblk, 256);
+  if (cudaLaunchKernelEx(&c3, scatter_kernel, (const int32_t*)idx, (const float*)w,
+                         (const int32_t*)offsets, (const int32_t*)base, T, E, k, 0, perm, slot,
+                         dst, wrow) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import sparse_moe_bit_gb300 as M
+from oracle import moe_oracle as O
 from sparse_moe_bit_gb300 import moe as MM
 from tests.moe_cases import MID, HostCase
 
@@ -38,6 +39,50 @@ def test_noalloc_routing_matches_handle_routing_twice():
         got = MM.route_from_logits_noalloc(logits, MID.k, bias)
         torch.cuda.synchronize()
         _same(got, ref)
+
+
+def _matches_oracle(got, lg, k, E):
+    """Routing of fp32 logits against the oracle's selection and grouping:
+    indices, counts, offsets, perm and slot bit for bit, weights within 1 ulp
+    of fp32 of the fp64 weights."""
+    idx, w = O.select_top_k(lg.astype(np.float64), k)
+    counts, offsets, perm, slot = O.group_by_expert(idx, E)
+    assert np.array_equal(got["idx"].cpu().numpy(), idx)
+    assert np.array_equal(got["counts"].cpu().numpy(), counts)
+    assert np.array_equal(got["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(got["perm"].cpu().numpy(), perm)
+    assert np.array_equal(got["slot"].cpu().numpy(), slot)
+    w32 = w.astype(np.float32)
+    assert np.all(np.abs(got["w"].cpu().numpy() - w32) <= np.spacing(np.abs(w32)))
+
+
+@pytest.mark.parametrize("E,k", [(256, 16), (256, 8)])
+def test_noalloc_routing_at_its_limits(E, k):
+    """The largest sizes the entry point takes (T = 2048 with E = 256 and
+    k = 16: every lane slot of the selection, the largest tile map and scratch
+    offsets) and the Qwen-shaped router (E = 256, k = 8), twice in a row."""
+    rng = np.random.default_rng(E + k)
+    for T in (2048, 1999):
+        lg = (rng.standard_normal((T, E)) * 1.5).astype(np.float32)
+        lg[:64] = np.round(lg[:64] * 2) / 2  # exact ties
+        hot = rng.choice(E, 4, replace=False)
+        lg[:, hot] += 3.0  # a few experts take most rows: several full tiles
+        got = MM.route_from_logits_noalloc(torch.from_numpy(lg).cuda(), k)
+        torch.cuda.synchronize()
+        _matches_oracle(got, lg, k, E)
+
+
+def test_noalloc_rejects_misaligned_pointers():
+    lib = M.load_library()
+    x = torch.zeros(64, 16, device="cuda")
+    o = torch.zeros(1 << 16, dtype=torch.int32, device="cuda")
+    p = o.data_ptr()
+    assert lib.moe_route_from_logits_noalloc(x.data_ptr() + 2, 4, 16, 2, None, p, p, p, p, p, p,
+                                             None) == 1
+    assert lib.moe_route_from_logits_noalloc(x.data_ptr(), 4, 16, 2, None, p + 1, p, p, p, p, p,
+                                             None) == 1
+    assert lib.moe_route_from_logits_noalloc(x.data_ptr(), 4, 16, 2, x.data_ptr() + 2, p, p, p,
+                                             p, p, p, None) == 1
 
 
 def test_noalloc_rejects_sizes_beyond_its_limit():
