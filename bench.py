@@ -565,34 +565,39 @@ def cpu_threads():
 class OracleSample:
     """A bounded sample of the workload for the fp64 oracle on host cores.
     Weights are generated once (outside timing); run() times oracle work only.
-      decode : the first `n_layers` layers of the 40-layer chain, one token;
-               value scaled to a full 40-layer token
+      decode : the whole 40-layer chain for one token (router, top-k,
+               dequantisation of the 9 experts of every layer, experts,
+               combine, RMS normalisation): one step is one full token
       prefill: `n_tok` tokens of the T=4096 Zipf layer (router, top-k,
                dequantisation of every touched expert, experts, combine)."""
 
-    def __init__(self, workload, n_layers=2, n_tok=256):
+    def __init__(self, workload, n_layers=DECODE_LAYERS, n_tok=256):
         import numpy as np
         from oracle import moe_oracle as O
         from synth import gen
         self.O, self.workload = O, workload
         shape = gen.MoEShape(d=D, E=E, k=K, I=I)
         if workload == "decode":
+            from concurrent.futures import ThreadPoolExecutor
             self.layers = []
             x = O.bf16_values(gen.make_x(1, 1, D))
             self.x0 = x
-            for l in range(n_layers):
-                wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, l, 0, E, D, 0.02))
-                wsg = O.bf16_values(gen.bf16_matrix(0, gen.TAG_SHARED_GATE, l, 0, 1, D, 0.02)[0])
-                idx, _ = O.select_top_k(O.router_logits(x, wr), K)
-                cache = {int(e): gen.expert_weights(0, l, int(e), shape) for e in idx[0]}
-                cache[E] = gen.expert_weights(0, l, E, shape)
-                vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr, w_shared_gate=wsg,
-                            experts=None, shared=None)
-                self.layers.append((vals, cache))
-                x = O.rms_norm(O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"])
-            self.units = n_layers
-            self.sample = (f"fp64 oracle, layers 0-{n_layers - 1} of the 40-layer decode chain "
-                           f"(one token), scaled to 40 layers")
+            with ThreadPoolExecutor(max_workers=16) as pool:
+                for l in range(n_layers):
+                    wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, l, 0, E, D, 0.02))
+                    wsg = O.bf16_values(
+                        gen.bf16_matrix(0, gen.TAG_SHARED_GATE, l, 0, 1, D, 0.02)[0])
+                    idx, _ = O.select_top_k(O.router_logits(x, wr), K)
+                    need = [int(e) for e in idx[0]] + [E]
+                    ws = pool.map(lambda e, l=l: gen.expert_weights(0, l, e, shape), need)
+                    cache = dict(zip(need, ws))
+                    vals = dict(E=E, k=K, group=64, has_shared=True, w_router=wr,
+                                w_shared_gate=wsg, experts=None, shared=None)
+                    self.layers.append((vals, cache))
+                    x = O.rms_norm(O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"])
+            self.units = 1
+            self.sample = (f"fp64 oracle, the whole {n_layers}-layer decode chain for one token "
+                           f"per step")
         else:
             self.x = O.bf16_values(gen.make_x(0, n_tok, D))
             wr = O.bf16_values(gen.bf16_matrix(0, gen.TAG_ROUTER, 0, 0, E, D, 0.02))
@@ -615,17 +620,37 @@ class OracleSample:
             x = self.x0
             for vals, cache in self.layers:
                 x = O.rms_norm(O.moe_layer(x, vals, expert_source=lambda e: cache[e])["out"])
-            sec = time.perf_counter() - t0
-            return 1.0 / (sec / self.units * DECODE_LAYERS)
+            return self.units / (time.perf_counter() - t0)
         O.moe_layer(self.x, self.vals, logit_bias=self.bias, expert_source=lambda e: self.cache[e])
         return self.units / (time.perf_counter() - t0)
+
+
+_ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                   "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def single_thread_rate(workload, steps):
+    """The same oracle sample in a child process whose BLAS runs one thread
+    (the thread count is fixed when numpy loads, hence the process)."""
+    env = dict(os.environ, **{k: "1" for k in _ONE_THREAD_ENV})
+    code = ("import sys, json, statistics; sys.path.insert(0, %r); import bench; "
+            "s = bench.OracleSample(%r); s.run(); "
+            "print(json.dumps(statistics.median([s.run() for _ in range(%d)])))"
+            % (ROOT, workload, max(1, steps)))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True,
+                           text=True, timeout=900)
+        v = float(r.stdout.strip().splitlines()[-1])
+    except Exception as ex:  # informative only
+        return {"error": str(ex)[:200]}
+    return {"value": v, "unit": "tokens/s", "cores": 1}
 
 
 def cpu_baseline(workload, steps=1):
     s = OracleSample(workload)
     v = statistics.median([s.run() for _ in range(max(1, steps))])
     return {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": s.sample}
+            "sample": s.sample, "single_thread": single_thread_rate(workload, steps)}
 
 
 # ------------------------------------------------------------------ main
@@ -665,14 +690,16 @@ def main():
         sample = OracleSample(args.workload)
         for _ in range(args.warmup):
             sample.run()
-        steps = [sample.run() for _ in range(args.steps)]
-        v = statistics.median(steps)
+        t0 = time.perf_counter()
+        rates = [sample.run() for _ in range(args.steps)]
+        ms_step = 1000.0 * (time.perf_counter() - t0) / args.steps  # measured, not scaled
+        v = statistics.median(rates)
         cb = {"value": v, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-              "sample": sample.sample}
-        tokens_per_step = PREFILL_T if args.workload == "prefill" else 1
+              "sample": sample.sample,
+              "single_thread": single_thread_rate(args.workload, min(2, args.steps))}
         line = {"impl": "reference", "metric": METRIC, "value": v,
                 "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": 1000.0 * tokens_per_step / v,
+                "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic",
                 "config": config_for(args.workload),

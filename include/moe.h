@@ -78,8 +78,14 @@ enum {
   MOE_DEVERR_WAIT_TIMEOUT = 1,   /* a pipeline wait passed its time limit    */
   MOE_DEVERR_NAN_LOGIT = 2,      /* a router logit was NaN (treated as -inf) */
   MOE_DEVERR_GRID_TIMEOUT = 4,   /* a wait on another CTA passed its limit   */
-  MOE_DEVERR_RANGE = 8           /* a decode router partial sum was outside
+  MOE_DEVERR_RANGE = 8,          /* a decode router partial sum was outside
                                     +-2^20 (clamped; fixed-point range)     */
+  MOE_DEVERR_FP16_RANGE = 16     /* prefill: an fp16 operand overflowed: a
+                                    token whose largest activation is above
+                                    2^61 (beyond the per-token scaling), or
+                                    a scaled silu(gate)*up beyond 65504 (for
+                                    weights far outside N(0, 0.02)); that
+                                    token's output is not valid              */
 };
 
 typedef struct moe_config {

@@ -189,13 +189,18 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
 // scale 2^e per group of 64, e = floor(log2 amax) - 13 so that every value of
 // the group is below 2^14 units: a bf16 value within 2^6 of its group's
 // maximum is represented exactly, any other value to within 2^-15 of the
-// group maximum.  (e >= -127 keeps 2^-e a normal float; smaller groups are
-// below 2^-114 everywhere.)
+// group maximum.  This holds over fp32's whole range: amax below 2^-99
+// (subnormal included) is scaled by 2^64 before its exponent is read, and
+// e >= -149 keeps the scale 2^e representable.
 __device__ __forceinline__ int group_exponent(float amax) {
-  const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;  // floor(log2 amax)
-  return max(ex - 13, -127);
+  int ex;  // floor(log2 amax)
+  if (amax < 1.0e-30f)
+    ex = (int)((__float_as_uint(amax * 18446744073709551616.0f) >> 23) & 0xFFu) - 127 - 64;
+  else
+    ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+  return max(ex - 13, -149);
 }
-// 2^-e for a group exponent e
+// 2^-e for a group exponent e >= -126 (a normal float)
 __device__ __forceinline__ float inv_pow2(int e) { return __int_as_float((127 - e) << 23); }
 // 2^e, exact also where it is subnormal (two power-of-two factors)
 __device__ __forceinline__ float pow2(int e) {
@@ -203,9 +208,12 @@ __device__ __forceinline__ float pow2(int e) {
   return __int_as_float((a + 127) << 23) * __int_as_float((b + 127) << 23);
 }
 // fp32 bits whose low 16 bits are round(v * 2^-e) as a 16-bit integer:
-// adding 1.5 * 2^23 leaves the rounded integer in the low mantissa bits
-__device__ __forceinline__ uint32_t quant_bits(float v, float inv) {
-  return __float_as_uint(fmaf(v, inv, 12582912.0f));
+// adding 1.5 * 2^23 leaves the rounded integer in the low mantissa bits.
+// Below e = -126, 2^-e exceeds fp32's range: v is first scaled by 2^64
+// (exact: such groups are below 2^-99).
+__device__ __forceinline__ uint32_t quant_bits(float v, int e) {
+  if (e >= -126) return __float_as_uint(fmaf(v, inv_pow2(e), 12582912.0f));
+  return __float_as_uint(fmaf(v * 18446744073709551616.0f, inv_pow2(e + 64), 12582912.0f));
 }
 // the low 16 bits of lo and of hi as one signed 16-bit pair
 __device__ __forceinline__ uint32_t pack_lo16(uint32_t lo, uint32_t hi) {
@@ -248,9 +256,11 @@ __device__ __forceinline__ void red_add_u64(unsigned long long* a, unsigned long
   asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
 }
 
-// Pacing of a poll on another CTA's data: a short sleep per round; gives up
-// (true) when another CTA gave up or, recording the error, after kWaitNs.
-__device__ __forceinline__ bool poll_give_up(const DecParams& p, uint64_t& t0, uint32_t& n) {
+// Pacing of a poll on another CTA's data (each round is one L2 round trip;
+// no sleep: a sleeping poller measured up to ~2 us late); gives up (true)
+// when another CTA gave up or, recording the error, after kWaitNs.
+template <class PP>
+__device__ __forceinline__ bool poll_give_up(const PP& p, uint64_t& t0, uint32_t& n) {
   ++n;
   if ((n & 15u) == 1u) {
     if (*(volatile int*)p.abort_flag) return true;
@@ -263,7 +273,6 @@ __device__ __forceinline__ bool poll_give_up(const DecParams& p, uint64_t& t0, u
       return true;
     }
   }
-  __nanosleep(20);
   return false;
 }
 
@@ -326,7 +335,8 @@ __device__ __forceinline__ float unfix32(long long s) {
 
 // Bounded wait on an mbarrier phase; the thread sleeps in hardware between
 // checks.  On time-out (or when another CTA gave up) records the error.
-__device__ __forceinline__ bool copy_wait(const DecParams& p, uint32_t bar, uint32_t parity) {
+template <class PP>
+__device__ __forceinline__ bool copy_wait(const PP& p, uint32_t bar, uint32_t parity) {
   if (mbar_try_wait_sleep(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
@@ -338,6 +348,117 @@ __device__ __forceinline__ bool copy_wait(const DecParams& p, uint32_t bar, uint
       return false;
     }
   }
+}
+
+// Four consecutive activations v0..v3 at index i0 (a multiple of 4; the 16
+// lanes of a half-warp hold one group of 64) -> 16-bit integers with the
+// group's power-of-two scale, stored as the packed pairs the integer dot
+// products take: word m of group g holds (x0,x2), (x4,x6), (x1,x3),
+// (x5,x7) of K indices 8m..8m+7.  Also the group's scale and sum.  Every
+// lane of the warp takes part (shuffles); act = false contributes nothing.
+__device__ __forceinline__ void quant_x4_into(float v0, float v1, float v2, float v3, int i0,
+                                              bool act, uint4* xq, float* xsc, float* xg, int ng,
+                                              int lane) {
+  float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+  float sum = (v0 + v1) + (v2 + v3);
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) {
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  }
+  const int e = group_exponent(am);
+  const uint32_t b0 = quant_bits(v0, e), b1 = quant_bits(v1, e);
+  const uint32_t b2 = quant_bits(v2, e), b3 = quant_bits(v3, e);
+  if (act) {
+    const int g = i0 >> 6, kk = i0 & 63;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(xq + (kk >> 3) * ng + g);
+    const int h4 = (kk & 4) ? 1 : 0;  // second half of the word: x4..x7
+    wp[h4] = pack_lo16(b0, b2);
+    wp[2 + h4] = pack_lo16(b1, b3);
+    if ((lane & 15) == 0) {
+      xsc[g] = pow2(e);
+      xg[g] = sum;
+    }
+  }
+}
+
+// One warp's share of a block's gate/up: the warp's two features (units t =
+// 0, 1 at ub0, gu_unit bytes each: gate codes, up codes, gate s,b, up s,b);
+// lane: one group of 64 inputs at a time, its activations in registers for
+// both units.  ag/au: the lane's partial sums (the caller sums the warp).
+// sum_i (s q_i + beta) x_i = s sum_i q_i x_i + beta X per group (X = sum_i x_i).
+__device__ __forceinline__ void gateup_pair(const uint8_t* ub0, int gu_unit, int d, int ng,
+                                            const uint4* xq, const float* xsc, const float* xg,
+                                            int lane, float (&ag)[2], float (&au)[2]) {
+  ag[0] = ag[1] = au[0] = au[1] = 0.f;
+  for (int g = lane; g < ng; g += 32) {
+    uint4 xw[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) xw[m] = xq[m * ng + g];
+    const float sc = xsc[g], X = xg[g];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint8_t* ub = ub0 + t * gu_unit;
+      const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
+      const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
+      const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
+      const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
+      int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
+      int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
+      pg0 = dot8i(cg0.z, xw[2], pg0);
+      pg1 = dot8i(cg0.w, xw[3], pg1);
+      pu0 = dot8i(cu0.z, xw[2], pu0);
+      pu1 = dot8i(cu0.w, xw[3], pu1);
+      pg0 = dot8i(cg1.x, xw[4], pg0);
+      pg1 = dot8i(cg1.y, xw[5], pg1);
+      pu0 = dot8i(cu1.x, xw[4], pu0);
+      pu1 = dot8i(cu1.y, xw[5], pu1);
+      pg0 = dot8i(cg1.z, xw[6], pg0);
+      pg1 = dot8i(cg1.w, xw[7], pg1);
+      pu0 = dot8i(cu1.z, xw[6], pu0);
+      pu1 = dot8i(cu1.w, xw[7], pu1);
+      const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
+      const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
+      ag[t] += s_of(sbg) * (sc * (float)(pg0 + pg1)) + b_of(sbg) * X;
+      au[t] += s_of(sbu) * (sc * (float)(pu0 + pu1)) + b_of(sbu) * X;
+    }
+  }
+}
+
+// h of a 32-feature block (lane = feature, one warp) -> 16-bit integers with
+// one power-of-two scale, packed as the integer dot products take them
+// (word m: features 8m..8m+7); also the scale and the sum of h.  qt: 32 words
+// of scratch.
+__device__ __forceinline__ void quant_h32(float v, uint32_t* qt, uint4* hpk, float* hsc, float* hs,
+                                          int lane) {
+  float am = fabsf(v), s = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+  }
+  const int e = group_exponent(am);
+  qt[lane] = quant_bits(v, e);
+  __syncwarp();
+  if (lane < kBlk / 8) {
+    const uint32_t* q8 = qt + lane * 8;
+    hpk[lane] = make_uint4(pack_lo16(q8[0], q8[2]), pack_lo16(q8[4], q8[6]),
+                           pack_lo16(q8[1], q8[3]), pack_lo16(q8[5], q8[7]));
+  }
+  if (lane == 0) {
+    *hsc = pow2(e);
+    *hs = s;
+  }
+}
+
+// One output row's share of a block's down projection, times the routing
+// weight wj: wj (s sum_i q_i h_i + beta H) over the block's 32 features
+// (cw: their codes in row f; sb: the row's scale/bias word of the block's
+// input group; h packed as quant_h32 leaves it).
+__device__ __forceinline__ float down_value(uint4 cw, uint32_t sb, uint4 h0, uint4 h1, uint4 h2,
+                                            uint4 h3, float hsc, float Hs, float wj) {
+  const int a = (dot8i(cw.x, h0, 0) + dot8i(cw.y, h1, 0)) + (dot8i(cw.z, h2, 0) + dot8i(cw.w, h3, 0));
+  return wj * (s_of(sb) * (hsc * (float)a) + b_of(sb) * Hs);
 }
 
 __device__ __forceinline__ void stamp(const DecParams& p, int l, int i) {
@@ -439,35 +560,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
              (uint32_t)(d * 4), dn_bar);
   };
 
-  // Four consecutive activations v0..v3 at index i0 (a multiple of 4; the 16
-  // lanes of a half-warp hold one group of 64) -> 16-bit integers with the
-  // group's power-of-two scale, stored as the packed pairs the integer dot
-  // products take: word m of group g holds (x0,x2), (x4,x6), (x1,x3),
-  // (x5,x7) of K indices 8m..8m+7.  Also the group's scale and sum.  Every
-  // lane of the warp takes part (shuffles); act = false contributes nothing.
   auto quant_x4 = [&](float v0, float v1, float v2, float v3, int i0, bool act) {
-    float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
-    float sum = (v0 + v1) + (v2 + v3);
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    }
-    const int e = group_exponent(am);
-    const float inv = inv_pow2(e);
-    const uint32_t b0 = quant_bits(v0, inv), b1 = quant_bits(v1, inv);
-    const uint32_t b2 = quant_bits(v2, inv), b3 = quant_bits(v3, inv);
-    if (act) {
-      const int g = i0 >> 6, kk = i0 & 63;
-      uint32_t* wp = reinterpret_cast<uint32_t*>(xq + (kk >> 3) * ng + g);
-      const int h4 = (kk & 4) ? 1 : 0;  // second half of the word: x4..x7
-      wp[h4] = pack_lo16(b0, b2);
-      wp[2 + h4] = pack_lo16(b1, b3);
-      if ((lane & 15) == 0) {
-        xsc[g] = pow2(e);
-        xg[g] = sum;
-      }
-    }
+    quant_x4_into(v0, v1, v2, v3, i0, act, xq, xsc, xg, ng, lane);
   };
 
   // x (bf16 [d]) -> quantised activations in shared memory, with optional
@@ -545,10 +639,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   };
 
   // The router sum of entry e of P_ln, once every copy's count is complete.
-  auto poll_P = [&](const unsigned long long* Ps, int e, long long& sum) -> bool {
+  // With `ow` (not null), the four tagged output words at `osrc` are polled
+  // in the same loop until each carries the tag `otag`: the previous layer's
+  // outputs are published before its router sums, so both are ready
+  // together and one round trip serves both.
+  auto poll_P = [&](const unsigned long long* Ps, int e, long long& sum,
+                    const uint32_t* osrc = nullptr, uint32_t otag = 0u,
+                    uint4* ow = nullptr) -> bool {
     unsigned long long w[kPCopies];
 #pragma unroll
     for (int q = 0; q < kPCopies; ++q) w[q] = ld_relaxed_u64(Ps + q * (E + 1) + e);
+    if (ow) *ow = ld_relaxed_v4(osrc);
     uint64_t t0 = 0;
     uint32_t n = 0;
     for (;;) {
@@ -558,11 +659,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const unsigned want = (G > q) ? (unsigned)((G - q + kPCopies - 1) / kPCopies) : 0u;
         if ((unsigned)(w[q] >> kCountShift) != want) pend |= 1u << q;
       }
-      if (!pend) break;
+      const bool opend = ow && ((ow->x >> 16) != otag || (ow->y >> 16) != otag ||
+                                (ow->z >> 16) != otag || (ow->w >> 16) != otag);
+      if (!pend && !opend) break;
       if (poll_give_up(p, t0, n)) return false;
 #pragma unroll
       for (int q = 0; q < kPCopies; ++q)
         if ((pend >> q) & 1u) w[q] = ld_relaxed_u64(Ps + q * (E + 1) + e);
+      if (opend) *ow = ld_relaxed_v4(osrc);
     }
     sum = 0;
 #pragma unroll
@@ -602,19 +706,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     //      and the previous output, polled in one pass
     bool bad = false;
     const unsigned long long* Ps = p.P + (long long)l * kPCopies * (E + 1);
+    const uint32_t* osrc = p.out + (long long)((l - 1) & 1) * d;
+    const uint32_t otag = (uint32_t)l;  // tag of layer l-1's outputs
+    // this thread's first four output words ride along with its P entry
+    const bool o_first = l > 0 && tid <= E && 4 * tid < d;
+    uint4 oraw = make_uint4(0u, 0u, 0u, 0u);
     long long ps0 = 0, ps1 = 0;
-    if (tid <= E && !poll_P(Ps, tid, ps0)) bad = true;
+    if (tid <= E && !poll_P(Ps, tid, ps0, osrc + 4 * tid, otag, o_first ? &oraw : nullptr))
+      bad = true;
     if (tid + kDecThreads <= E && !poll_P(Ps, tid + kDecThreads, ps1)) bad = true;
     if (l > 0) {
-      const uint32_t* src = p.out + (long long)((l - 1) & 1) * d;
-      const uint32_t want = (uint32_t)l;  // tag of layer l-1
+      const uint32_t* src = osrc;
+      const uint32_t want = otag;
       float ss = 0.f;
       for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
         const int i0 = ib + 4 * tid;
         const bool act = i0 < d;
         uint4 raw = make_uint4(0u, 0u, 0u, 0u);
         if (act && !bad) {
-          raw = ld_relaxed_v4(src + i0);
+          raw = (ib == 0 && o_first) ? oraw : ld_relaxed_v4(src + i0);
           uint64_t t0 = 0;
           uint32_t n = 0;
           while ((raw.x >> 16) != want || (raw.y >> 16) != want || (raw.z >> 16) != want ||
@@ -730,39 +840,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       ph_gu ^= 1;
       {
         const uint8_t* ub0 = gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit;
-        float ag[2] = {0.f, 0.f}, au[2] = {0.f, 0.f};
-        for (int g = lane; g < ng; g += 32) {
-          uint4 xw[8];
-#pragma unroll
-          for (int m = 0; m < 8; ++m) xw[m] = xq[m * ng + g];
-          const float sc = xsc[g], X = xg[g];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const uint8_t* ub = ub0 + t * gu_unit;
-            const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
-            const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
-            const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
-            const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
-            int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
-            int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
-            pg0 = dot8i(cg0.z, xw[2], pg0);
-            pg1 = dot8i(cg0.w, xw[3], pg1);
-            pu0 = dot8i(cu0.z, xw[2], pu0);
-            pu1 = dot8i(cu0.w, xw[3], pu1);
-            pg0 = dot8i(cg1.x, xw[4], pg0);
-            pg1 = dot8i(cg1.y, xw[5], pg1);
-            pu0 = dot8i(cu1.x, xw[4], pu0);
-            pu1 = dot8i(cu1.y, xw[5], pu1);
-            pg0 = dot8i(cg1.z, xw[6], pg0);
-            pg1 = dot8i(cg1.w, xw[7], pg1);
-            pu0 = dot8i(cu1.z, xw[6], pu0);
-            pu1 = dot8i(cu1.w, xw[7], pu1);
-            const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
-            const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
-            ag[t] += s_of(sbg) * (sc * (float)(pg0 + pg1)) + b_of(sbg) * X;
-            au[t] += s_of(sbu) * (sc * (float)(pu0 + pu1)) + b_of(sbu) * X;
-          }
-        }
+        float ag[2], au[2];
+        gateup_pair(ub0, gu_unit, d, ng, xq, xsc, xg, lane, ag, au);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const float gv = warp_sum(ag[t]) * r, uv = warp_sum(au[t]) * r;
@@ -772,28 +851,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       __syncthreads();
       // h of the block -> 16-bit integers with one power-of-two scale, packed
       // as the integer dot products take them (word m: features 8m..8m+7)
-      if (warp == 0) {
-        const float v = hb[lane];
-        float am = fabsf(v), hs = v;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-          hs += __shfl_xor_sync(0xffffffffu, hs, o);
-        }
-        const int e = group_exponent(am);
-        uint32_t* qt = reinterpret_cast<uint32_t*>(red2);
-        qt[lane] = quant_bits(v, inv_pow2(e));
-        __syncwarp();
-        if (lane < kBlk / 8) {
-          const uint32_t* q8 = qt + lane * 8;
-          hpk[lane] = make_uint4(pack_lo16(q8[0], q8[2]), pack_lo16(q8[4], q8[6]),
-                                 pack_lo16(q8[1], q8[3]), pack_lo16(q8[5], q8[7]));
-        }
-        if (lane == 0) {
-          misc[2] = pow2(e);
-          misc[3] = hs;
-        }
-      }
+      if (warp == 0)
+        quant_h32(hb[lane], reinterpret_cast<uint32_t*>(red2), hpk, &misc[2], &misc[3], lane);
       if (!copy_wait(p, dn_bar, ph_dn)) {
         drain();
         return;
@@ -810,11 +869,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         unsigned long long* pb = p.part + (long long)b * d;
         const unsigned long long tg = (unsigned long long)ptag << 32;
         for (int f = tid; f < d; f += kDecThreads) {
-          const uint4 cw = dnc[f];
-          const uint32_t sb = dnsb[f];
-          const int a = (dot8i(cw.x, h0, 0) + dot8i(cw.y, h1, 0)) +
-                        (dot8i(cw.z, h2, 0) + dot8i(cw.w, h3, 0));
-          const float v = wj * (s_of(sb) * (hsc * (float)a) + b_of(sb) * Hs);
+          const float v = down_value(dnc[f], dnsb[f], h0, h1, h2, h3, hsc, Hs, wj);
           st_relaxed_u64(pb + f, tg | __float_as_uint(v));
         }
       }
@@ -897,6 +952,530 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       ph_rt ^= 1;
       router_partial(l + 1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// A few tokens (2 <= T <= kFewMax) of one layer in one launch: every token is
+// routed on the device, the union of the experts the tokens picked is formed,
+// and each block of an expert in that union is streamed once, for every token
+// that picked it (the speculative-verify shape: a handful of rows that pick
+// different experts, where one pass of the one-row path per token reads the
+// shared experts' weights T times and the matrix path pays whole-tile costs).
+// Source: Perplexity, "Optimizing on-device inference for Apple Silicon",
+// §"Limits of further optimization" (verify passes of 2-5 rows that pick
+// different experts fall between the one-row weight path and the matrix
+// path) and §"Optimizing the one-row weight path".
+//
+// Per token the arithmetic is the decode kernel's (router sums as counted
+// 64-bit fixed point over the owned features, the same top-k and softmax, the
+// same integer dot products, the same fixed-order sum of the partials), so a
+// token's output does not depend on the other tokens of the launch: T copies
+// of one token give the decode kernel's single-layer output, bit for bit.
+//
+// Union entry u = 0 is the shared expert (when there is one), then the routed
+// experts in ascending index.  Block b: entry b / bpe, features (b % bpe) *
+// 32 .. + 31; CTA c takes blocks c, c + G, ...  The shared expert's blocks do
+// not depend on the routing, so CTAs c < bpe issue their first copies at the
+// start.  A block computes h for each token that picked its expert and that
+// token's partial over all d outputs, tagged, at part[t][slot][b % bpe][f]; a
+// warp's gate/up rows of the CTA's next block load as soon as the warp has
+// used its current ones, the next down columns once the current ones are
+// used.  CTA c owns output features [c d / G, (c+1) d / G) of every token.
+constexpr int kFewMax = 8;
+constexpr int kFewUnion = kFewMax * kMaxK + 1;  // union entries at most
+constexpr int kFewPairs = 2;  // (token, entry) router sums polled together per thread
+
+struct FewParams {
+  DecLayer W;
+  int T, d, E, k, I, has_shared, Ep, nf_max;
+  unsigned epoch;
+  const uint16_t* x;         // bf16 [T][d]
+  const float* bias;         // [E] or null
+  uint16_t* y;               // bf16 [T][d]
+  float* logits;             // [T][E] (written by CTA 0)
+  unsigned long long* part;  // [T][k1][bpe][d] tagged partials
+  unsigned long long* P;     // [T][kPCopies][E+1] counted router sums, zero at launch
+  int* abort_flag;           // zero at launch
+  int* err;
+};
+
+struct FewSmem {
+  size_t xq, xsc, xg, gu, dnc, dnsb, rt, outs, lg, sel_e, sel_w, sig, umask, ubase, ulist,
+      uslot, hb, hpk, hsc, hsum, qt, red2, misc, infl, bars, total;
+};
+__host__ __device__ inline FewSmem few_smem(int T, int d, int E, int Ep, int nf_max) {
+  FewSmem s;
+  size_t o = 0;
+  s.xq = dec_take(o, (size_t)T * d * 2, 16);
+  s.xsc = dec_take(o, (size_t)T * (d / 64) * 4, 16);
+  s.xg = dec_take(o, (size_t)T * (d / 64) * 4, 16);
+  s.gu = dec_take(o, (size_t)kBlk * (d + d / 8), 128);
+  s.dnc = dec_take(o, (size_t)d * 16, 128);
+  s.dnsb = dec_take(o, (size_t)d * 4, 128);
+  s.rt = dec_take(o, (size_t)nf_max * Ep * 2, 128);
+  s.outs = dec_take(o, (size_t)T * nf_max * 4, 16);
+  s.lg = dec_take(o, (size_t)T * (E + 1) * 4, 16);
+  s.sel_e = dec_take(o, (size_t)T * kMaxK * 4, 16);
+  s.sel_w = dec_take(o, (size_t)T * kMaxK * 4, 16);
+  s.sig = dec_take(o, (size_t)T * 4, 16);
+  s.umask = dec_take(o, (size_t)(kMaxE / 32) * 4, 16);
+  s.ubase = dec_take(o, (size_t)(kMaxE / 32) * 4, 16);
+  s.ulist = dec_take(o, (size_t)kFewUnion * 4, 16);
+  s.uslot = dec_take(o, (size_t)kFewUnion * kFewMax, 16);
+  s.hb = dec_take(o, (size_t)T * kBlk * 4, 16);
+  s.hpk = dec_take(o, (size_t)T * (kBlk / 8) * 16, 16);
+  s.hsc = dec_take(o, (size_t)T * 4, 16);
+  s.hsum = dec_take(o, (size_t)T * 4, 16);
+  s.qt = dec_take(o, (size_t)kFewMax * kBlk * 4, 16);
+  s.red2 = dec_take(o, (size_t)kRedChunks * 16 * 4, 16);
+  s.misc = dec_take(o, 16, 16);
+  s.infl = dec_take(o, (kDecWarps + 2) * 4, 16);
+  s.bars = dec_take(o, (kDecWarps + 2) * 8, 8);
+  s.total = o;
+  return s;
+}
+
+// Top-k of one token by one warp from its logits in shared memory (NaN taken
+// as -inf), ranked by (value descending, index ascending).  Lane l holds the
+// order keys of experts l + 32 j.  Each round every lane finds its best key
+// not yet taken (strictly larger wins: the lane's lowest index among equal
+// keys), then the warp maximum and the smallest expert index among the lanes
+// holding it name the round's winner.
+template <int VPL>
+__device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int* sel_e, int lane) {
+  uint32_t key[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    float v = (e < E) ? lg[e] : 0.0f;
+    if (v != v) v = -INFINITY;
+    key[j] = (e < E) ? ord_key(v) : 0u;  // 0: empty (every real key is larger)
+  }
+  for (int r = 0; r < k; ++r) {
+    uint32_t bk = 0u;
+    int bj = 0;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const bool better = key[j] > bk;
+      bk = better ? key[j] : bk;
+      bj = better ? j : bj;
+    }
+    const uint32_t M = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t win =
+        __reduce_min_sync(0xffffffffu, bk == M ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+    if ((int)(win & 31u) == lane) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) key[j] = (j == (int)(win >> 5)) ? 0u : key[j];
+    }
+    if (lane == 0) sel_e[r] = (int)win;
+  }
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_constant__ FewParams p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  const int T = p.T, d = p.d, E = p.E, k = p.k, I = p.I, Ep = p.Ep;
+  const int ng = d / 64;
+  const int bpe = I / kBlk;
+  const int k1 = k + (p.has_shared ? 1 : 0);
+  const FewSmem L = few_smem(T, d, E, Ep, p.nf_max);
+  uint4* xq = reinterpret_cast<uint4*>(dsm + L.xq);    // [T][8 words][ng] packed int16 x
+  float* xsc = reinterpret_cast<float*>(dsm + L.xsc);  // [T][ng]
+  float* xg = reinterpret_cast<float*>(dsm + L.xg);    // [T][ng]
+  uint8_t* gu_buf = dsm + L.gu;
+  const uint4* dnc = reinterpret_cast<const uint4*>(dsm + L.dnc);
+  const uint32_t* dnsb = reinterpret_cast<const uint32_t*>(dsm + L.dnsb);
+  const uint16_t* rt_buf = reinterpret_cast<const uint16_t*>(dsm + L.rt);
+  float* outs = reinterpret_cast<float*>(dsm + L.outs);  // [T][nf_max] owned input values
+  float* lg = reinterpret_cast<float*>(dsm + L.lg);      // [T][E+1]; entry E: shared gate
+  int* sel_e = reinterpret_cast<int*>(dsm + L.sel_e);    // [T][kMaxK]
+  float* sel_w = reinterpret_cast<float*>(dsm + L.sel_w);
+  float* sig = reinterpret_cast<float*>(dsm + L.sig);    // [T]
+  uint32_t* umask = reinterpret_cast<uint32_t*>(dsm + L.umask);
+  int* ubase = reinterpret_cast<int*>(dsm + L.ubase);
+  int* ulist = reinterpret_cast<int*>(dsm + L.ulist);    // union entry -> expert
+  int8_t* uslot = reinterpret_cast<int8_t*>(dsm + L.uslot);  // [entry][kFewMax] slot, -1 none
+  float* hb = reinterpret_cast<float*>(dsm + L.hb);      // [T][32]
+  uint4* hpk = reinterpret_cast<uint4*>(dsm + L.hpk);    // [T][4]
+  float* hsc = reinterpret_cast<float*>(dsm + L.hsc);
+  float* hsum = reinterpret_cast<float*>(dsm + L.hsum);
+  uint32_t* qt = reinterpret_cast<uint32_t*>(dsm + L.qt);  // [kFewMax][32]
+  float* red2 = reinterpret_cast<float*>(dsm + L.red2);
+  int* misc = reinterpret_cast<int*>(dsm + L.misc);      // [0] union entries
+  volatile int* infl = reinterpret_cast<volatile int*>(dsm + L.infl);
+  const uint32_t bar0 = smem_u32(dsm + L.bars);
+  const int kDnBar = kDecWarps, kRtBar = kDecWarps + 1;
+  const uint32_t dn_bar = bar0 + 8 * kDnBar;
+  const uint32_t rt_bar = bar0 + 8 * kRtBar;
+  constexpr int kDnTid = (kDecWarps - 2) * 32 + 1, kRtTid = (kDecWarps - 1) * 32 + 31;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int f0 = (int)((long long)c * d / G), f1 = (int)((long long)(c + 1) * d / G);
+  const int nf = f1 - f0;
+  const int gu_unit = d + d / 8;
+  const DecLayer& W = p.W;
+
+  if (tid == 0) {
+    for (int i = 0; i < kDecWarps + 2; ++i) mbar_init(bar0 + 8 * i, 1);
+    fence_mbar_init();
+  }
+  if (tid < kDecWarps + 2) infl[tid] = -1;
+  __syncthreads();
+  uint32_t ph_gu = 0, ph_dn = 0;
+
+  auto drain = [&]() {
+    if (lane != 0) return;
+    for (int i = 0; i < kDecWarps + 2; ++i) {
+      const int pty = infl[i];
+      if (pty < 0) continue;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar0 + 8 * i, (uint32_t)pty)) {
+        if (globaltimer_ns() - t0 > kDrainNs) break;
+      }
+    }
+  };
+  // copies of block b of expert ex: the warp's gate/up rows (lane 0 of each
+  // warp), the block's down columns and their scale/bias words (one thread)
+  auto issue_gu = [&](int b, long long ex) {
+    const int i0 = (b % bpe) * kBlk;
+    const uint32_t bar = bar0 + 8 * warp;
+    const uint32_t bytes = (uint32_t)(kUnitsPerWarp * gu_unit);
+    infl[warp] = (int)ph_gu;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_u32(gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit),
+             W.gu + (ex * I + i0 + warp * kUnitsPerWarp) * gu_unit, bytes, bar);
+  };
+  auto issue_dn = [&](int b, long long ex) {
+    const int i0 = (b % bpe) * kBlk;
+    infl[kDnBar] = (int)ph_dn;
+    mbar_arrive_expect_tx(dn_bar, (uint32_t)(d * 20));
+    bulk_g2s(smem_u32(dsm + L.dnc), W.dnc + (ex * bpe + i0 / kBlk) * (long long)d * 16,
+             (uint32_t)(d * 16), dn_bar);
+    bulk_g2s(smem_u32(dsm + L.dnsb), W.dnsb + (ex * (I / 64) + i0 / 64) * (long long)d,
+             (uint32_t)(d * 4), dn_bar);
+  };
+
+  // ---- the shared expert's first block (no routing needed) and the router
+  //      rows of the owned features
+  const bool pre = p.has_shared && c < bpe;
+  if (pre) {
+    if (lane == 0) issue_gu(c, E);
+    if (tid == kDnTid) issue_dn(c, E);
+  }
+  if (tid == kRtTid && nf > 0) {
+    const uint32_t bytes = (uint32_t)nf * Ep * 2;
+    infl[kRtBar] = 0;
+    mbar_arrive_expect_tx(rt_bar, bytes);
+    bulk_g2s(smem_u32(dsm + L.rt), W.w_rt + (long long)f0 * Ep, bytes, rt_bar);
+  }
+
+  // ---- every token's activations -> quantised, and the owned features' values
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* src = p.x + (long long)t * d;
+    for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
+      const int i0 = ib + 4 * tid;
+      const bool act = i0 < d;
+      uint2 raw = make_uint2(0u, 0u);
+      if (act) raw = __ldg(reinterpret_cast<const uint2*>(src + i0));
+      const float v[4] = {bf16f(raw.x & 0xFFFFu), bf16f(raw.x >> 16), bf16f(raw.y & 0xFFFFu),
+                          bf16f(raw.y >> 16)};
+      quant_x4_into(v[0], v[1], v[2], v[3], i0, act, xq + (size_t)t * 8 * ng, xsc + t * ng,
+                    xg + t * ng, ng, lane);
+      if (act) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (i0 + q >= f0 && i0 + q < f1) outs[t * p.nf_max + i0 + q - f0] = v[q];
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- router sums of every token over the owned features (CTA c adds into
+  //      copy c % kPCopies of each entry, zero without owned features)
+  if (nf > 0) {
+    if (!copy_wait(p, rt_bar, 0)) {
+      drain();
+      return;
+    }
+    if (tid == kRtTid) infl[kRtBar] = -1;
+  }
+  {
+    bool range_err = false;
+    for (int e = tid; e <= E; e += kDecThreads) {
+      for (int t = 0; t < T; ++t) {
+        const float* ot = outs + t * p.nf_max;
+        float acc = 0.f;
+        for (int fb = 0; fb < nf; fb += kMaxOwned) {
+          uint16_t wv[kMaxOwned];
+          float ov[kMaxOwned];
+#pragma unroll
+          for (int i = 0; i < kMaxOwned; ++i) {
+            wv[i] = (fb + i < nf) ? rt_buf[(fb + i) * Ep + e] : (uint16_t)0;
+            ov[i] = (fb + i < nf) ? ot[fb + i] : 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < kMaxOwned; ++i) acc = fmaf(ov[i], bf16f(wv[i]), acc);
+        }
+        long long v;
+        if (fabsf(acc) < 1048575.0f) {
+          v = fix32(acc);
+        } else {
+          v = (acc > 0.0f) ? kPMaxAbs : -kPMaxAbs;
+          range_err = true;
+        }
+        red_add_u64(p.P + ((long long)t * kPCopies + (c % kPCopies)) * (E + 1) + e,
+                    (1ull << kCountShift) + (unsigned long long)(v + kPOffset));
+      }
+    }
+    if (range_err) atomicOr(p.err, MOE_DEVERR_RANGE);
+  }
+
+  // ---- the router sums, kFewPairs (token, entry) pairs at a time per thread
+  bool bad = false, nan_seen = false;
+  {
+    const int npairs = T * (E + 1);
+    for (int pb = tid; pb < npairs && !bad; pb += kFewPairs * kDecThreads) {
+      unsigned long long w[kFewPairs][kPCopies];
+      const unsigned long long* src[kFewPairs];
+#pragma unroll
+      for (int i = 0; i < kFewPairs; ++i) {
+        const int pp = pb + i * kDecThreads;
+        const int t = pp / (E + 1), e = pp - t * (E + 1);
+        src[i] = p.P + (long long)t * kPCopies * (E + 1) + e;
+#pragma unroll
+        for (int q = 0; q < kPCopies; ++q)
+          w[i][q] = (pp < npairs) ? ld_relaxed_u64(src[i] + q * (E + 1)) : 0ull;
+      }
+      uint64_t t0 = 0;
+      uint32_t n = 0;
+      for (;;) {
+        unsigned pend = 0;
+#pragma unroll
+        for (int i = 0; i < kFewPairs; ++i) {
+          if (pb + i * kDecThreads >= npairs) continue;
+#pragma unroll
+          for (int q = 0; q < kPCopies; ++q) {
+            const unsigned want = (G > q) ? (unsigned)((G - q + kPCopies - 1) / kPCopies) : 0u;
+            if ((unsigned)(w[i][q] >> kCountShift) != want) pend |= 1u << (i * kPCopies + q);
+          }
+        }
+        if (!pend) break;
+        if (poll_give_up(p, t0, n)) {
+          bad = true;
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < kFewPairs; ++i)
+#pragma unroll
+          for (int q = 0; q < kPCopies; ++q)
+            if ((pend >> (i * kPCopies + q)) & 1u) w[i][q] = ld_relaxed_u64(src[i] + q * (E + 1));
+      }
+      if (bad) break;
+#pragma unroll
+      for (int i = 0; i < kFewPairs; ++i) {
+        const int pp = pb + i * kDecThreads;
+        if (pp >= npairs) continue;
+        const int t = pp / (E + 1), e = pp - t * (E + 1);
+        long long sum = 0;
+#pragma unroll
+        for (int q = 0; q < kPCopies; ++q) {
+          const long long cnt = (long long)(w[i][q] >> kCountShift);
+          sum += (long long)(w[i][q] & ((1ull << kCountShift) - 1ull)) - cnt * kPOffset;
+        }
+        float v = unfix32(sum);
+        if (e < E) {
+          if (p.bias) v += __ldg(p.bias + e);
+          if (c == 0) p.logits[(long long)t * E + e] = v;
+          if (v != v) nan_seen = true;
+        }
+        lg[t * (E + 1) + e] = v;
+      }
+    }
+  }
+  if (tid < kMaxE / 32) umask[tid] = 0u;
+  for (int i = tid; i < kFewUnion * kFewMax; i += kDecThreads) uslot[i] = (int8_t)-1;
+  if (__syncthreads_or(bad)) {
+    drain();
+    return;
+  }
+  if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
+
+  // ---- top-k, routing weights and shared gate of token t (warp t)
+  if (warp < T) {
+    const float* lt = lg + warp * (E + 1);
+    int* se = sel_e + warp * kMaxK;
+    if (E <= 256)
+      warp_topk<8>(lt, E, k, se, lane);
+    else
+      warp_topk<16>(lt, E, k, se, lane);
+    __syncwarp();
+    // softmax over the k chosen logits in double-float arithmetic (within
+    // one ulp of fp64), as in the decode kernel
+    const int my_e = (lane < k) ? se[lane] : 0;
+    float my_v = (lane < k) ? lt[my_e] : -INFINITY;
+    if (my_v != my_v) my_v = -INFINITY;
+    float top = lt[se[0]];
+    if (top != top) top = -INFINITY;
+    const dflt ex = (lane < k) ? df_softmax_term(my_v, top) : dflt{0.0f, 0.0f};
+    dflt den = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const dflt ot = {__shfl_xor_sync(0xffffffffu, den.hi, o),
+                       __shfl_xor_sync(0xffffffffu, den.lo, o)};
+      den = df_add(den, ot);
+    }
+    if (lane < k) sel_w[warp * kMaxK + lane] = df_div(ex, den).hi;
+    if (lane == 0) sig[warp] = p.has_shared ? 1.0f / (1.0f + expf(-lt[E])) : 0.0f;
+  }
+  __syncthreads();
+
+  // ---- the union of the chosen experts, ascending (after the shared expert)
+  for (int a = tid; a < T * k; a += kDecThreads) {
+    const int e = sel_e[(a / k) * kMaxK + a % k];
+    atomicOr(&umask[e >> 5], 1u << (e & 31));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int cnt = (lane < kMaxE / 32) ? __popc(umask[lane]) : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane < kMaxE / 32) ubase[lane] = incl - cnt + p.has_shared;
+    if (lane == 31) misc[0] = incl + p.has_shared;
+  }
+  __syncthreads();
+  for (int a = tid; a < T * k; a += kDecThreads) {
+    const int t = a / k, j = a - t * k;
+    const int e = sel_e[t * kMaxK + j];
+    const int u = ubase[e >> 5] + __popc(umask[e >> 5] & ((1u << (e & 31)) - 1u));
+    ulist[u] = e;
+    uslot[u * kFewMax + t] = (int8_t)j;
+  }
+  if (p.has_shared) {
+    if (tid < T) uslot[tid] = (int8_t)k;
+    if (tid == 0) ulist[0] = E;
+  }
+  __syncthreads();
+  const int NB = misc[0] * bpe;
+  const uint32_t ptag = (p.epoch << 6) | 0x80000000u;
+
+  // ---- the CTA's blocks
+  if (!pre && c < NB) {
+    if (lane == 0) issue_gu(c, ulist[c / bpe]);
+    if (tid == kDnTid) issue_dn(c, ulist[c / bpe]);
+  }
+  for (int b = c; b < NB; b += G) {
+    const int u = b / bpe, blk = b - u * bpe;
+    unsigned tmask = 0u;
+    for (int t = 0; t < T; ++t)
+      if (uslot[u * kFewMax + t] >= 0) tmask |= 1u << t;
+    if (!copy_wait(p, bar0 + 8 * warp, ph_gu)) {
+      drain();
+      return;
+    }
+    if (lane == 0) infl[warp] = -1;
+    ph_gu ^= 1;
+    {
+      const uint8_t* ub0 = gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit;
+      for (unsigned m = tmask; m; m &= m - 1u) {
+        const int t = __ffs(m) - 1;
+        float ag[2], au[2];
+        gateup_pair(ub0, gu_unit, d, ng, xq + (size_t)t * 8 * ng, xsc + t * ng, xg + t * ng, lane,
+                    ag, au);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float gv = warp_sum(ag[q]), uv = warp_sum(au[q]);
+          if (lane == 0) hb[t * kBlk + warp * kUnitsPerWarp + q] = gv / (1.0f + expf(-gv)) * uv;
+        }
+      }
+    }
+    // this warp's rows are used: the next block's rows for it load now
+    if (b + G < NB && lane == 0) issue_gu(b + G, ulist[(b + G) / bpe]);
+    __syncthreads();
+    if (warp < T && ((tmask >> warp) & 1u))
+      quant_h32(hb[warp * kBlk + lane], qt + warp * kBlk, hpk + warp * (kBlk / 8), &hsc[warp],
+                &hsum[warp], lane);
+    if (!copy_wait(p, dn_bar, ph_dn)) {
+      drain();
+      return;
+    }
+    if (tid == kDnTid) infl[kDnBar] = -1;
+    ph_dn ^= 1;
+    __syncthreads();
+    {
+      const unsigned long long tg = (unsigned long long)ptag << 32;
+      for (int f = tid; f < d; f += kDecThreads) {
+        const uint4 cw = dnc[f];
+        const uint32_t sb = dnsb[f];
+        for (unsigned m = tmask; m; m &= m - 1u) {
+          const int t = __ffs(m) - 1;
+          const int j = uslot[u * kFewMax + t];
+          const float wj = (j < k) ? sel_w[t * kMaxK + j] : sig[t];
+          const uint4* ht = hpk + t * (kBlk / 8);
+          const float v = down_value(cw, sb, ht[0], ht[1], ht[2], ht[3], hsc[t], hsum[t], wj);
+          st_relaxed_u64(p.part + (((long long)t * k1 + j) * bpe + blk) * d + f,
+                         tg | __float_as_uint(v));
+        }
+      }
+    }
+    __syncthreads();  // the down columns and h are no longer read
+    if (b + G < NB && tid == kDnTid) issue_dn(b + G, ulist[(b + G) / bpe]);
+  }
+
+  // ---- owned outputs of every token: the fixed-order sum of its partials
+  const int npart = k1 * bpe;
+  for (int t = 0; t < T; ++t) {
+    const unsigned long long* pt = p.part + (long long)t * npart * d;
+    for (int fl0 = 0; fl0 < nf; fl0 += 16) {
+      const int fl = fl0 + (tid & 15), ch = tid >> 4;
+      float s = 0.f;
+      if (fl < nf) {
+        const unsigned long long* pf = pt + f0 + fl;
+        for (int bp = ch; bp < npart && !bad; bp += kRedChunks * kPollMax) {
+          unsigned long long v[kPollMax];
+#pragma unroll
+          for (int i = 0; i < kPollMax; ++i) {
+            const int bb = bp + i * kRedChunks;
+            v[i] = (bb < npart) ? ld_relaxed_u64(pf + (long long)bb * d)
+                                : ((unsigned long long)ptag << 32);
+          }
+          uint64_t t0 = 0;
+          uint32_t n = 0;
+          for (;;) {
+            unsigned pend = 0;
+#pragma unroll
+            for (int i = 0; i < kPollMax; ++i)
+              if ((uint32_t)(v[i] >> 32) != ptag) pend |= 1u << i;
+            if (!pend) break;
+            if (poll_give_up(p, t0, n)) {
+              bad = true;
+              break;
+            }
+#pragma unroll
+            for (int i = 0; i < kPollMax; ++i)
+              if ((pend >> i) & 1u) v[i] = ld_relaxed_u64(pf + (long long)(bp + i * kRedChunks) * d);
+          }
+#pragma unroll
+          for (int i = 0; i < kPollMax; ++i)
+            if (bp + i * kRedChunks < npart) s += __uint_as_float((uint32_t)v[i]);
+        }
+      }
+      red2[ch * 16 + (tid & 15)] = s;
+      if (__syncthreads_or(bad)) {
+        drain();
+        return;
+      }
+      if (tid < 16 && fl0 + tid < nf) {
+        float o = 0.f;
+        for (int q = 0; q < kRedChunks; ++q) o += red2[q * 16 + tid];
+        p.y[(long long)t * d + f0 + fl0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      }
+      __syncthreads();
     }
   }
 }
@@ -997,6 +1576,78 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+size_t few_scratch_bytes(const Handle* h) {
+  const moe_config& c = h->cfg;
+  const int k1 = c.k + (c.has_shared ? 1 : 0);
+  auto r256 = [](size_t b) { return (b + 255) / 256 * 256; };
+  return 256 + r256((size_t)kFewMax * kPCopies * (c.E + 1) * 8) +
+         r256((size_t)kFewMax * k1 * (c.I / kBlk) * c.d * 8);
+}
+
+int few_max_tokens() { return kFewMax; }
+
+bool few_supported(const Handle* h, int T) {
+  if (T < 2 || T > kFewMax || !h->ws.few) return false;
+  const moe_config& c = h->cfg;
+  const int G = h->num_sms;
+  if ((G + kPCopies - 1) / kPCopies > kMaxPerCopy) return false;
+  const int nf_max = (c.d + G - 1) / G;
+  return few_smem(T, c.d, c.E, decode_router_pitch(c.E), nf_max).total <= 227 * 1024;
+}
+
+cudaError_t launch_few(Handle* h, const uint16_t* x, int T, const float* bias, uint16_t* y,
+                       cudaStream_t st) {
+  const moe_config& c = h->cfg;
+  const int G = h->num_sms;
+  const int k1 = c.k + (c.has_shared ? 1 : 0);
+  const int nf_max = (c.d + G - 1) / G;
+  const int Ep = decode_router_pitch(c.E);
+  const FewSmem sm = few_smem(T, c.d, c.E, Ep, nf_max);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(few_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  auto r256 = [](size_t b) { return (b + 255) / 256 * 256; };
+  // scratch: [abort | P] (zeroed before every launch) | partials
+  uint8_t* q = h->ws.few;
+  int* abort_flag = reinterpret_cast<int*>(q);
+  unsigned long long* P = reinterpret_cast<unsigned long long*>(q + 256);
+  const size_t zero_bytes = 256 + (size_t)T * kPCopies * (c.E + 1) * 8;
+  unsigned long long* part = reinterpret_cast<unsigned long long*>(
+      q + 256 + r256((size_t)kFewMax * kPCopies * (c.E + 1) * 8));
+  (void)k1;
+  FewParams p;
+  p.W.gu = h->dc_gu;
+  p.W.dnc = h->dc_dn;
+  p.W.dnsb = reinterpret_cast<const uint32_t*>(h->dc_dn + (size_t)h->n_exp * c.I / 2 * c.d);
+  p.W.w_rt = h->dc_router_t;
+  p.T = T;
+  p.d = c.d;
+  p.E = c.E;
+  p.k = c.k;
+  p.I = c.I;
+  p.has_shared = c.has_shared;
+  p.Ep = Ep;
+  p.nf_max = nf_max;
+  p.epoch = ++h->dec_epoch;
+  p.x = x;
+  p.bias = bias;
+  p.y = y;
+  p.logits = h->ws.logits;
+  p.part = part;
+  p.P = P;
+  p.abort_flag = abort_flag;
+  p.err = h->dev_err;
+  cudaError_t e = cudaMemsetAsync(q, 0, zero_bytes, st);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&p};
+  return cudaLaunchCooperativeKernel((const void*)few_kernel, dim3(G), dim3(kDecThreads), args,
+                                     sm.total, st);
 }
 
 }  // namespace moe

@@ -763,15 +763,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       const int c1 = min(c0 + C::EPI_COLS, t.npad);
       // row data of the warp's 128 columns, fetched while the MMAs run:
       // lane l holds rows c0 + l + 32 v, v = 0..3
-      float rsc4[4] = {0.f, 0.f, 0.f, 0.f};
+      // (down: the routing weight and contribution row; gate/up: the power of
+      // two that scaled the row's fp16 activations)
+      constexpr float kR0 = (MODE == MMA_GATEUP) ? 1.f : 0.f;
+      float rsc4[4] = {kR0, kR0, kR0, kR0};
       int rdst4[4] = {0, 0, 0, 0};
-      if (MODE == MMA_DOWN) {
+      if (MODE != MMA_ROUTER) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int n = c0 + lane + 32 * v;
           if (n < t.nrows) {
-            rsc4[v] = p.row_scale[t.row0 + n];
-            rdst4[v] = p.dst_row[t.row0 + n];
+            if (MODE == MMA_DOWN) {
+              rsc4[v] = p.row_scale[t.row0 + n];
+              rdst4[v] = p.dst_row[t.row0 + n];
+            } else {
+              rsc4[v] = p.row_xscale[t.row0 + n];
+            }
           }
         }
       }
@@ -819,12 +826,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         const uint32_t sbuf = S.stage(e, nst & 1);
         __syncwarp();  // the buffer's previous reads are done
         if (nvalid > 0) {
+          bool ovf = false;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float v0 = __uint_as_float(r0[j]);
             if (MODE == MMA_GATEUP) {
+              // The row's activations entered as x / s (s a power of two), so
+              // the accumulators are v0 = g / s and v1 = u / s.  H holds
+              // silu(g) u / s^2 = silu(s v0) * (v1 / s), bounded by |v0 v1|
+              // (|silu(z)| <= |z|); the down projection's row weight carries
+              // the s^2 back.  s = 1 for activations within [2^-6, 2^6).
+              const float ps = __shfl_sync(0xffffffffu, rsc, j);
+              const float pinv = __int_as_float(0x7F000000 - __float_as_int(ps));  // 1/s, exact
               const float v1 = __uint_as_float(r1[j]);
-              const float h = silu_tanh(v0) * v1;
+              const float h = silu_tanh(v0 * ps) * (v1 * pinv);
+              ovf |= fabsf(h) >= 65520.0f;  // fp16 rounding would give inf
               st_shared_u16(sbuf + j * 64 + lane * 2, __half_as_ushort(__float2half_rn(h)));
             } else {
               const float sc = __shfl_sync(0xffffffffu, rsc, j);
@@ -835,6 +851,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
                               __bfloat16_as_ushort(__float2bfloat16_rn(sc * __uint_as_float(r1[j]))));
             }
           }
+          if (MODE == MMA_GATEUP && __any_sync(0xffffffffu, ovf) && lane == 0)
+            atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
         }
         __syncwarp();
         // 16 rows x NSEG segments x four 16-byte pieces: piece pi = lane + 32 it

@@ -84,8 +84,9 @@ void free_handle(Handle* h) {
   void* ptrs[] = {h->pf_gu, h->pf_dn, h->pf_router, h->dc_gu, h->dc_dn, h->dc_router_t,
                   h->w_router, h->w_sg, h->dev_err, h->ws.logit_part, h->ws.logits,
                   h->ws.idx, h->ws.w, h->ws.sigma, h->ws.xp, h->ws.hist, h->ws.base,
-                  h->ws.counts, h->ws.offsets, h->ws.perm, h->ws.slot, h->ws.dst, h->ws.wrow,
-                  h->ws.tiles, h->ws.ntiles, h->ws.ticket, h->ws.H, h->ws.Y, h->ws.x_dev, h->ws.y_dev,
+                  h->ws.counts, h->ws.offsets, h->ws.perm, h->ws.slot, h->ws.dst, h->ws.wrow, h->ws.xrow,
+                  h->ws.tiles, h->ws.ntiles, h->ws.ticket, h->ws.H, h->ws.Y, h->ws.few,
+                  h->ws.x_dev, h->ws.y_dev,
                   h->ws.bias_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -164,6 +165,7 @@ moe_status alloc_all(Handle* h) {
   CK(dalloc(&w.slot, (size_t)T * c.k * 4), "alloc");
   CK(dalloc(&w.dst, (size_t)T * k1 * 4), "alloc");
   CK(dalloc(&w.wrow, (size_t)T * k1 * 4), "alloc");
+  CK(dalloc(&w.xrow, (size_t)T * k1 * 4), "alloc");
   CK(dalloc(&w.tiles, (size_t)w.max_tiles * sizeof(int4)), "alloc");
   CK(dalloc(&w.ntiles, 16), "alloc");
   CK(dalloc(&w.ticket, 16), "alloc");
@@ -174,6 +176,9 @@ moe_status alloc_all(Handle* h) {
     CK(dalloc(&w.Y, (size_t)T * k1 * c.d * 2), "alloc");
     CK(make_tmap_16bit(&h->tm_h, w.H, T * k1, c.I, 16, false), "tensor map (H)");
   }
+  // the few-token path (2..8 tokens on the decode layout), when its scratch is modest
+  if ((h->layouts & MOE_LAYOUT_DECODE) && T >= 2 && few_scratch_bytes(h) <= ((size_t)256 << 20))
+    CK(dalloc(&w.few, few_scratch_bytes(h)), "alloc");
   CK(dalloc(&w.x_dev, (size_t)T * c.d * 2), "alloc");
   CK(dalloc(&w.y_dev, (size_t)T * c.d * 2), "alloc");
   CK(dalloc(&w.bias_dev, (size_t)c.E * 4 * 64), "alloc");  // [64][E]: moe_decode_host
@@ -240,6 +245,7 @@ moe_status run_experts(Handle* h, const uint16_t* x, int T, uint16_t* y, cudaStr
   p.a_expert_stride = p.a_unit_stride * (c.I / 128);
   p.xg = w.xp;
   p.perm = w.perm;
+  p.row_xscale = w.xrow;
   p.ldx = c.d;
   p.H = w.H;
   p.ldh = c.I;
@@ -415,17 +421,20 @@ moe_status moe_route_from_logits(moe_handle* h, const float* logits, int T,
   return MOE_OK;
 }
 
-// Largest T that moe_forward runs through the decode kernel, one token per
-// pass (handles with the DECODE layout): below it the tensor-core path's
-// fixed costs (routing, tile map, K loops of whole weight tiles) exceed T
-// weight-bound passes.  Measured on GB300 (Qwen shape); MOE_SMALL_T
-// (1..64; 0 or 1: T = 1 only) overrides it.
+// Largest T that moe_forward runs on the bandwidth path of the DECODE layout:
+// T = 1 through the decode kernel, 2 <= T <= 8 through the few-token kernel
+// (one launch streaming the union of the tokens' experts once; one decode
+// pass per token where its scratch was not built).  Below it the tensor-core
+// path's fixed costs (routing, tile map, K loops of whole weight tiles)
+// exceed the weight streaming.  MOE_SMALL_T (1..8; 0 or 1: T = 1 only)
+// overrides it.
 static int small_t_limit() {
   static int lim = -1;
   if (lim < 0) {
     const char* e = getenv("MOE_SMALL_T");
-    lim = e ? atoi(e) : 4;
-    if (lim < 1 || lim > 64) lim = (e && atoi(e) == 0) ? 1 : 4;
+    const int def = few_max_tokens();
+    lim = e ? atoi(e) : def;
+    if (lim < 1 || lim > def) lim = (e && atoi(e) == 0) ? 1 : def;
   }
   return lim;
 }
@@ -447,8 +456,14 @@ moe_status moe_forward(moe_handle* h, const void* x, int T, const float* logit_b
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   if (T <= small_t_limit() && (h->layouts & MOE_LAYOUT_DECODE)) {
-    // a few tokens: one pass of the bandwidth-bound decode kernel per token
-    // (each token's output depends on that token only)
+    if (T >= 2 && few_supported(h, T)) {
+      CK(launch_few(h, static_cast<const uint16_t*>(x), T, logit_bias, static_cast<uint16_t*>(y),
+                    st),
+         "few-token launch");
+      return MOE_OK;
+    }
+    // one pass of the bandwidth-bound decode kernel per token (each token's
+    // output depends on that token only)
     moe_handle* one[1] = {h};
     for (int t = 0; t < T; ++t)
       CK(launch_decode(reinterpret_cast<Handle* const*>(one), 1,

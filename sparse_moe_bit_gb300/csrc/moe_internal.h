@@ -37,13 +37,16 @@ struct Workspace {
   int32_t* perm = nullptr;      // [Tmax*(k+1)] grouped row -> token
   int32_t* slot = nullptr;      // [Tmax][k]
   int32_t* dst = nullptr;       // [Tmax*(k+1)] grouped row -> contribution row
-  float* wrow = nullptr;        // [Tmax*(k+1)] grouped row -> routing weight
+  float* wrow = nullptr;        // [Tmax*(k+1)] grouped row -> routing weight (times s^2)
+  float* xrow = nullptr;        // [Tmax*(k+1)] grouped row -> activation scale s
   int4* tiles = nullptr;        // [max_tiles] {expert, row0, nrows, npad}
   int32_t* ntiles = nullptr;    // [1]
   unsigned* ticket = nullptr;   // [4]: [2], [3] the routing launch's grid barrier (zero between calls)
   uint16_t* H = nullptr;        // [Tmax*(k+1)][I] fp16 SwiGLU activations
   uint16_t* Y = nullptr;        // [Tmax*(k+1)][d] bf16 weighted contributions
   int max_tiles = 0;
+  // few-token launches: abort flag, router sums, partials (null: not built)
+  uint8_t* few = nullptr;
   // staging for moe_forward_host
   void* x_dev = nullptr;
   void* y_dev = nullptr;
@@ -117,6 +120,9 @@ struct MmaParams {
   int ldy;
   const int32_t* dst_row;
   const float* row_scale;
+  // gate/up: per grouped row, the power of two s that divided its fp16
+  // activations (the epilogue undoes it)
+  const float* row_xscale;
   int* err;
 };
 cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st);
@@ -140,6 +146,13 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
                           float eps, uint16_t* y, const moe_decode_trace* trace,
                           cudaStream_t st);
 size_t decode_scratch_bytes(const Handle* h, int L);
+// a few tokens (2..few_max_tokens()) of one layer in one launch (decode.cu):
+// the union of the tokens' experts streamed once
+size_t few_scratch_bytes(const Handle* h);
+int few_max_tokens();
+bool few_supported(const Handle* h, int T);
+cudaError_t launch_few(Handle* h, const uint16_t* x, int T, const float* bias, uint16_t* y,
+                       cudaStream_t st);
 
 // Gated DeltaNet prefill scan (gdn_scan.cu).  Key width fixed at 128,
 // value rows in blocks of 32; see include/gdn.h for the layouts.

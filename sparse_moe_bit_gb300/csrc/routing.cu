@@ -441,7 +441,8 @@ struct RouteParams {
   int32_t* perm;           // [T(k+1)] grouped row -> token
   int32_t* slot;           // [T][k] -> grouped row
   int32_t* dst;            // [T(k+1)] grouped row -> contribution row
-  float* wrow;             // [T(k+1)] grouped row -> routing weight / gate
+  float* wrow;             // [T(k+1)] grouped row -> routing weight / gate (times s^2)
+  float* xrow;             // [T(k+1)] grouped row -> activation scale s of its token
   int4* tiles;
   int32_t* ntiles;
   uint16_t* xp;            // fp16 [T][d]
@@ -584,32 +585,33 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
   }
   if (!p.x) return;
 
-  // ---- 4. the fp16 copy of the activations, xp[t] = fp16(x[t]), from which
-  // the gate/up GEMM gathers its token rows (one warp per token); the shared
-  // gate sigma = sigmoid(w_sg . x) on the way
+  // ---- 4. the fp16 copy of the activations, from which the gate/up GEMM
+  // gathers its token rows (one warp per token); the shared gate
+  // sigma = sigmoid(w_sg . x) on the way.
+  // fp16 holds less range than bf16, so each token's row is divided by a
+  // power of two s first: s = 1 while the row's largest magnitude is in
+  // [2^-6, 2^6) (the usual activations: the copy is exact up to fp16
+  // rounding), else 2^(floor(log2 max) - 1), which brings the largest value
+  // into [2, 4); log2 s is clamped to [-60, 60].  The gate/up epilogue and
+  // the row weights of the down projection (times s^2) undo it exactly.
   for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
     const uint4* xr = reinterpret_cast<const uint4*>(p.x + (long long)t * p.d);
     uint4* xo = reinterpret_cast<uint4*>(p.xp + (long long)t * p.d);
-    float dot = 0.0f;
-    for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 8) {
-      uint4 raw[8];  // the lane's loads issued together
+    float dot = 0.0f, amax = 0.0f;
+    for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 4) {
+      uint4 raw[4];  // the lane's loads issued together
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
         if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int c = c0 + 32 * i;
         if (c >= p.d / 8) break;
         const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        uint32_t hv[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(wv[q] << 16);
-          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
-          const __half2 h2 = __floats2half2_rn(lo, hi);
-          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        for (int q = 0; q < 4; ++q)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[q] << 16)),
+                                   fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
         if (p.has_shared) {
           const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.w_sg) + c);
           const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
@@ -622,13 +624,54 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
         }
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int ex = 0;  // log2 s
+    if (amax > 0.0f && (amax < 0.015625f || amax >= 64.0f)) {
+      ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 128;  // floor(log2 max) - 1
+      ex = min(max(ex, -60), 60);
+    }
+    const float s_t = __int_as_float((127 + ex) << 23);
+    const float inv = __int_as_float((127 - ex) << 23);
+    if (lane == 0 && !(amax * inv < 65520.0f) && amax == amax) atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
+    for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 4) {
+      uint4 raw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = c0 + 32 * i;
+        if (c >= p.d / 8) break;
+        const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(wv[q] << 16) * inv;
+          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u) * inv;
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+    }
+    // the token's rows: the scale for the gate/up epilogue, s^2 into the
+    // row weights of the down projection (rows written in step 3 by this block)
+    const float s2 = s_t * s_t;
+    if (lane < k) {
+      const int row = p.slot[(long long)t * k + lane];
+      p.xrow[row] = s_t;
+      p.wrow[row] *= s2;
+    }
     if (p.has_shared) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
       if (lane == 0) {
         const float sg = 1.0f / (1.0f + expf(-dot));
         p.sigma[t] = sg;
-        p.wrow[T * k + t] = sg;
+        p.wrow[T * k + t] = sg * s2;
+        p.xrow[T * k + t] = s_t;
       }
     }
   }
@@ -732,6 +775,7 @@ cudaError_t launch_route(const Handle* h, const float* part, int KS, int T, cons
   p.slot = ws.slot;
   p.dst = ws.dst;
   p.wrow = ws.wrow;
+  p.xrow = ws.xrow;
   p.tiles = ws.tiles;
   p.ntiles = ws.ntiles;
   p.xp = ws.xp;

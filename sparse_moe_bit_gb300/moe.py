@@ -19,6 +19,12 @@ MOE_SCALE_F16 = 1
 MOE_SCALE_BF16 = 2
 MOE_LAYOUT_PREFILL = 1
 MOE_LAYOUT_DECODE = 2
+# device error word bits (include/moe.h)
+MOE_DEVERR_WAIT_TIMEOUT = 1
+MOE_DEVERR_NAN_LOGIT = 2
+MOE_DEVERR_GRID_TIMEOUT = 4
+MOE_DEVERR_RANGE = 8
+MOE_DEVERR_FP16_RANGE = 16
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
           4: "out of device memory", 5: "device error"}

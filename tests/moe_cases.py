@@ -98,12 +98,27 @@ class DeviceLayer:
             self._cache[e] = gen.expert_weights(self.seed, self.layer, e, self.shape)
         return self._cache[e]
 
+    def prefetch(self, experts):
+        """Generate the given experts' weights on the host, several at once
+        (numpy releases the GIL inside the generator's array operations)."""
+        from concurrent.futures import ThreadPoolExecutor
+        need = sorted({int(e) for e in experts} - set(self._cache))
+        if not need:
+            return
+        with ThreadPoolExecutor(max_workers=min(16, len(need))) as ex:
+            for e, w in zip(need, ex.map(
+                    lambda e: gen.expert_weights(self.seed, self.layer, e, self.shape), need)):
+                self._cache[e] = w
+
     def values(self):
         s = self.shape
         return dict(E=s.E, k=s.k, group=s.group, has_shared=True, w_router=self.w_router,
                     w_shared_gate=self.w_sg, experts=None, shared=None)
 
     def oracle(self, x_vals, logits=None, bias=None):
+        if logits is not None:
+            idx, _ = O.select_top_k(np.asarray(logits, np.float64), self.shape.k)
+            self.prefetch(list(np.unique(idx)) + [self.shape.E])
         return O.moe_layer(x_vals, self.values(), logit_bias=bias, logits=logits,
                            expert_source=self.expert)
 

@@ -117,9 +117,9 @@ def test_forward_parity_mid(mid, T):
 
 @pytest.mark.parametrize("T", [2, 3, 4, 5])
 def test_forward_parity_small_t_both_paths(mid, T):
-    # a handle with the decode layout runs T <= 4 as one decode pass per
-    # token; a prefill-only handle runs the tensor-core path: both match the
-    # oracle, and the decode-path rows equal single-token calls bit for bit
+    # a handle with the decode layout runs 2 <= T <= 8 through the few-token
+    # kernel; a prefill-only handle runs the tensor-core path: both match the
+    # oracle, and the few-token rows equal single-token calls bit for bit
     bits, x = _x(mid, T, seed=20 + T)
     pf = HostCase(MID, seed=1, layouts=M.MOE_LAYOUT_PREFILL)
     for case in (mid, pf):

@@ -2,9 +2,10 @@
 expert, 4-bit g64) under uniform and Zipf-skewed routing, processed in
 chunks of 8192 tokens above that length.  The routing of every token is
 checked bit-exact given the GPU's logits (chunk by chunk: a token's logits do
-not depend on the chunk it shares), outputs on sampled tokens against the
-fp64 oracle.  The sweep's longer lengths (up to 128K tokens) are measured by
-bench.py; their kernels and chunk loop are the ones exercised here."""
+not depend on the chunk it shares); outputs against the fp64 oracle for every
+token up to 2048 tokens and for 4096 sampled tokens from 16K on.  The sweep's
+longer lengths (up to 128K tokens) are measured by bench.py; their kernels
+and chunk loop are the ones exercised here."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +20,8 @@ pytestmark = pytest.mark.gpu
 CHUNK = 8192
 
 
-@pytest.mark.parametrize("T,zipf", [(256, False), (256, True), (2048, False), (16384, True)])
+@pytest.mark.parametrize("T,zipf", [(256, False), (256, True), (2048, False), (16384, True),
+                                    (32768, False)])
 def test_prefill_sweep_length(T, zipf):
     chunk = min(T, CHUNK)
     layer = DeviceLayer(QWEN, seed=0, layer=0, max_tokens=chunk)
@@ -38,7 +40,13 @@ def test_prefill_sweep_length(T, zipf):
     lg = np.concatenate(lgs)
     idx = np.concatenate(idxs)
     counts = np.bincount(idx.ravel(), minlength=QWEN.E)
-    toks = _sample_tokens(idx, counts, 24, 8, np.random.default_rng(T + zipf))
+    # short prompts: every token; 16K and longer: 4096 sampled tokens (with
+    # every near-tie token and tokens of the hottest expert)
+    if T <= 2048:
+        toks = np.arange(T)
+    else:
+        toks = _sample_tokens(idx, counts, 4096, 256, np.random.default_rng(T + zipf), lg)
+        assert len(toks) >= 4096
     e, m = _check_sampled(layer, 0, lg, y.float().cpu().numpy(), toks, bias_np)
     print(f"T={T} {'zipf' if zipf else 'uniform'}: experts touched {int((counts > 0).sum())}, "
           f"sampled {len(toks)} tokens rel-L2 {e:.2e}")
