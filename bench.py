@@ -535,18 +535,21 @@ def run_sweep(args, torch, M, sd, gen, device, peaks):
     layer.close()
     stress.close()
     # a few tokens (speculative-verify shape): a handle with both layouts runs
-    # T <= 4 as one decode pass per token, larger T on the tensor-core path
+    # T = 1 on the decode kernel, 2 <= T <= 8 on the few-token kernel (one
+    # launch streaming the union of the tokens' experts once), larger T on the
+    # tensor-core path
     small = M.MoE(M.MoEConfig(d=D, E=E, k=K, I=I, max_tokens=64), sd.make_layer(0, 0, shape, device=device))
     torch.cuda.empty_cache()
     small_pts = []
-    for T in (1, 2, 3, 4, 8):
+    for T in (1, 2, 3, 4, 5, 6, 8, 12, 16):
         xs, ys = x[:T], out[:T]
         for _ in range(2):
             small.forward(xs, None, out=ys)
         us = time_call(torch, lambda: small.forward(xs, None, out=ys), flush, 10, stream)
         t_roof, bound = point_roofline(T, touched(small, xs, None, 64), 1, peaks)
         small_pts.append({"T": T, "us": round(us, 1), "tokens_per_s": round(T / (us * 1e-6), 1),
-                          "path": "decode kernel per token" if T <= 4 else "tensor-core",
+                          "path": ("decode kernel" if T == 1 else
+                                   "few-token kernel" if T <= 8 else "tensor-core"),
                           "bound": bound, "roofline_frac": round(t_roof / (us * 1e-6), 4)})
     small.close()
     return points, stress_pt, small_pts
@@ -732,7 +735,10 @@ def main():
         "value": res["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
         "us_per_layer": res["us_per_layer"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp16-operands/fp32-accumulate (prefill), fp32 CUDA-core (decode)",
+        "vs_baseline": None,
+        "dtype": ("decode: int16 activations (a power-of-two scale per 64-group) x 4-bit codes, "
+                  "exact int32 dot products (dp2a), fp32 scale/bias and sums; prefill: fp16 "
+                  "tensor-core operands (per-token power-of-two scaled), fp32 accumulate"),
         "data": "synthetic (seeded counter-based generator; random-init weights)",
         "config": dict(config_for(primary), parallelism=f"replicas x{ws}"),
         "roofline": dict(res["roofline"], peak_source=peak_src),
@@ -761,8 +767,10 @@ def main():
             sweep[1], config="8 hot experts take half of the assignments, 64 experts get "
                              "none; one unchunked call")
         line["small_T"] = {
-            "config": "same layer, uniform routing, a handle with both layouts; T <= 4 runs "
-                      "one decode-kernel pass per token; L2 flushed, median of 10",
+            "config": "same layer, uniform routing, a handle with both layouts: T = 1 on the "
+                      "decode kernel, 2..8 on the few-token kernel (the union of the tokens' "
+                      "experts streamed once), more on the tensor-core path; roofline from the "
+                      "bytes of the experts touched; L2 flushed, median of 10",
             "points": sweep[2]}
     if gdn_res is not None:
         line["gdn_scan"] = gdn_res

@@ -82,10 +82,12 @@ enum {
                                     +-2^20 (clamped; fixed-point range)     */
   MOE_DEVERR_FP16_RANGE = 16     /* prefill: an fp16 operand overflowed: a
                                     token whose largest activation is above
-                                    2^61 (beyond the per-token scaling), or
-                                    a scaled silu(gate)*up beyond 65504 (for
-                                    weights far outside N(0, 0.02)); that
-                                    token's output is not valid              */
+                                    2^61 times fp16's range (beyond the
+                                    per-token scaling), or a non-finite
+                                    output (an intermediate silu(gate)*up
+                                    beyond fp16's range, for weights far
+                                    outside N(0, 0.02), or a non-finite
+                                    input); such outputs are not valid      */
 };
 
 typedef struct moe_config {

@@ -76,7 +76,6 @@ constexpr int kMaxPerCopy = 31;                      // 31 * 2^53 < 2^58: no car
 constexpr int kRedChunks = 32;  // partial sums per owned feature in the reduction
 constexpr int kPollMax = 8;     // partials in flight per thread in one polling pass
 constexpr int kMaxOwned = 16;   // owned output features summed per pass (router sums)
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
 
 struct DecLayer {
@@ -108,6 +107,10 @@ struct DecParams {
   unsigned long long* P;  // [L][kPCopies][E+1] counted fixed-point router sums, zero at launch
   int* abort_flag;      // zero at launch
   int* err;
+  uint64_t wait_ns;     // a wait on another CTA or a copy gives up after this
+  // test of the give-up path: wait for one more router-sum arrival than any
+  // CTA makes (a flag that nothing sets); the wait must run out
+  int unset_flag;
 };
 
 // shared-memory carve-up (the host sizes the launch with the same function)
@@ -258,7 +261,7 @@ __device__ __forceinline__ void red_add_u64(unsigned long long* a, unsigned long
 
 // Pacing of a poll on another CTA's data (each round is one L2 round trip;
 // no sleep: a sleeping poller measured up to ~2 us late); gives up (true)
-// when another CTA gave up or, recording the error, after kWaitNs.
+// when another CTA gave up or, recording the error, after p.wait_ns.
 template <class PP>
 __device__ __forceinline__ bool poll_give_up(const PP& p, uint64_t& t0, uint32_t& n) {
   ++n;
@@ -267,7 +270,7 @@ __device__ __forceinline__ bool poll_give_up(const PP& p, uint64_t& t0, uint32_t
     const uint64_t t = globaltimer_ns();
     if (n == 1u) {
       t0 = t;
-    } else if (t - t0 > kWaitNs) {
+    } else if (t - t0 > p.wait_ns) {
       atomicOr(p.err, MOE_DEVERR_GRID_TIMEOUT);
       atomicExch(p.abort_flag, 1);
       return true;
@@ -276,41 +279,48 @@ __device__ __forceinline__ bool poll_give_up(const PP& p, uint64_t& t0, uint32_t
   return false;
 }
 
-// Top-k over the whole CTA, ranked by (value descending, index ascending).
-// keys[e] (e < 32 * chunks) = order key of expert e's logit << 32 | ~e, 0
-// past E: distinct, larger is better; cand[] zero; both written by the
-// caller before a barrier.  An expert's rank within its chunk of 32 makes
-// the chunk's k best candidates (an expert of the overall top k has fewer
-// than k better experts anywhere, so also in its chunk); a candidate's rank
-// among all candidates is then its overall rank: sel_e[rank] for rank < k.
-// Two threads count for a key (16 comparisons each), and 512 / (candidates)
-// threads, a power of two, for a candidate.
+// Top-k of T tokens over the whole CTA, ranked by (value descending, index
+// ascending).  keys[t][e] (e < 32 * chunks) = order key of expert e's logit
+// << 32 | ~e, 0 past E: distinct, larger is better; cand[] zero; both
+// written by the caller before a barrier.  An expert's rank within its chunk
+// of 32 makes the chunk's k best candidates (an expert of the overall top k
+// has fewer than k better experts anywhere, so also in its chunk); a
+// candidate's rank among its token's candidates is then its overall rank:
+// sel_e[t * kMaxK + rank] for rank < k.  Two threads count for a key (16
+// comparisons each), and 512 / (all candidates) threads, a power of two, for
+// a candidate.
 __device__ __forceinline__ void cta_topk(const unsigned long long* keys, unsigned long long* cand,
-                                         int E, int k, int* sel_e, int tid) {
-  const int nch = (E + 31) >> 5, nc = nch * k;
+                                         int E, int k, int T, int* sel_e, int tid) {
+  const int nch = (E + 31) >> 5, nkey = 32 * nch, nc = nch * k;
   // whole warps in every pass (the shuffles); keys past E are 0
-  for (int t = tid; t < 64 * nch; t += kDecThreads) {
-    const int e = t >> 1, h = t & 1;
-    const unsigned long long my = keys[e];
-    const unsigned long long* kc = keys + (e & ~31) + 16 * h;
+  for (int it = tid; it < T * 64 * nch; it += kDecThreads) {
+    const int tok = it / (64 * nch), r = it - tok * 64 * nch;
+    const int e = r >> 1, h = r & 1;
+    const unsigned long long* kt = keys + tok * nkey;
+    const unsigned long long my = kt[e];
+    const unsigned long long* kc = kt + (e & ~31) + 16 * h;
     int rank = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) rank += (kc[i] > my) ? 1 : 0;
     rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-    if (h == 0 && e < E && rank < k) cand[(e >> 5) * k + rank] = my;
+    if (h == 0 && e < E && rank < k) cand[tok * nc + (e >> 5) * k + rank] = my;
   }
   __syncthreads();
   int tpc = 32;  // threads per candidate
-  while (tpc > 1 && tpc * nc > kDecThreads) tpc >>= 1;
-  const int tot = (nc * tpc + 31) & ~31;
-  for (int t = tid; t < tot; t += kDecThreads) {
-    const int ci = t / tpc, part = t % tpc;
-    const unsigned long long my = (ci < nc) ? cand[ci] : 0ull;
+  while (tpc > 1 && tpc * nc * T > kDecThreads) tpc >>= 1;
+  const int tot = (T * nc * tpc + 31) & ~31;
+  for (int it = tid; it < tot; it += kDecThreads) {
+    const int ci = it / tpc, part = it % tpc;  // candidate over all tokens
+    const bool ok = ci < T * nc;
+    const int tok = ok ? ci / nc : 0;
+    const unsigned long long* ct = cand + tok * nc;
+    const unsigned long long my = ok ? ct[ci - tok * nc] : 0ull;
     int rank = 0;
-    if (ci < nc)
-      for (int j = part; j < nc; j += tpc) rank += (cand[j] > my) ? 1 : 0;
+    if (ok)
+      for (int j = part; j < nc; j += tpc) rank += (ct[j] > my) ? 1 : 0;
     for (int o = 1; o < tpc; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (part == 0 && my != 0ull && rank < k) sel_e[rank] = (int)(0xFFFFFFFFu - (uint32_t)my);
+    if (part == 0 && my != 0ull && rank < k)
+      sel_e[tok * kMaxK + rank] = (int)(0xFFFFFFFFu - (uint32_t)my);
   }
   __syncthreads();
 }
@@ -342,7 +352,7 @@ __device__ __forceinline__ bool copy_wait(const PP& p, uint32_t bar, uint32_t pa
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*(volatile int*)p.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) {
+    if (globaltimer_ns() - t0 > p.wait_ns) {
       atomicOr(p.err, MOE_DEVERR_WAIT_TIMEOUT);
       atomicExch(p.abort_flag, 1);
       return false;
@@ -382,45 +392,63 @@ __device__ __forceinline__ void quant_x4_into(float v0, float v1, float v2, floa
   }
 }
 
-// One warp's share of a block's gate/up: the warp's two features (units t =
-// 0, 1 at ub0, gu_unit bytes each: gate codes, up codes, gate s,b, up s,b);
-// lane: one group of 64 inputs at a time, its activations in registers for
-// both units.  ag/au: the lane's partial sums (the caller sums the warp).
-// sum_i (s q_i + beta) x_i = s sum_i q_i x_i + beta X per group (X = sum_i x_i).
-__device__ __forceinline__ void gateup_pair(const uint8_t* ub0, int gu_unit, int d, int ng,
+// One warp's share of a block's gate/up: the warp's two features (units u =
+// 0, 1 at ub0, gu_unit bytes each: gate codes, up codes, gate s,b, up s,b),
+// for each token t < NTOK in tmask (its activations at xq + t * xstride, its
+// group scales and sums at xsc, xg + t * sstride); lane: one group of 64
+// inputs at a time, the group's code words loaded once for every token.
+// acc[t] = the lane's partial sums (gate u0, up u0, gate u1, up u1); the
+// caller sums the warp.  sum_i (s q_i + beta) x_i = s sum_i q_i x_i + beta X
+// per group (X = sum_i x_i); the same expressions for every NTOK, so a
+// token's sums do not depend on the other tokens.
+template <int NTOK>
+__device__ __forceinline__ void gateup_rows(const uint8_t* ub0, int gu_unit, int d, int ng,
                                             const uint4* xq, const float* xsc, const float* xg,
-                                            int lane, float (&ag)[2], float (&au)[2]) {
-  ag[0] = ag[1] = au[0] = au[1] = 0.f;
+                                            int xstride, int sstride, unsigned tmask, int lane,
+                                            float (&acc)[NTOK][4]) {
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
   for (int g = lane; g < ng; g += 32) {
-    uint4 xw[8];
+    uint4 cw[2][4];
+    uint32_t sbg[2], sbu[2];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) xw[m] = xq[m * ng + g];
-    const float sc = xsc[g], X = xg[g];
+    for (int u = 0; u < 2; ++u) {
+      const uint8_t* ub = ub0 + u * gu_unit;
+      cw[u][0] = *reinterpret_cast<const uint4*>(ub + g * 32);
+      cw[u][1] = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
+      cw[u][2] = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
+      cw[u][3] = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
+      sbg[u] = reinterpret_cast<const uint32_t*>(ub + d)[g];
+      sbu[u] = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
+    }
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const uint8_t* ub = ub0 + t * gu_unit;
-      const uint4 cg0 = *reinterpret_cast<const uint4*>(ub + g * 32);
-      const uint4 cg1 = *reinterpret_cast<const uint4*>(ub + g * 32 + 16);
-      const uint4 cu0 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32);
-      const uint4 cu1 = *reinterpret_cast<const uint4*>(ub + d / 2 + g * 32 + 16);
-      int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
-      int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
-      pg0 = dot8i(cg0.z, xw[2], pg0);
-      pg1 = dot8i(cg0.w, xw[3], pg1);
-      pu0 = dot8i(cu0.z, xw[2], pu0);
-      pu1 = dot8i(cu0.w, xw[3], pu1);
-      pg0 = dot8i(cg1.x, xw[4], pg0);
-      pg1 = dot8i(cg1.y, xw[5], pg1);
-      pu0 = dot8i(cu1.x, xw[4], pu0);
-      pu1 = dot8i(cu1.y, xw[5], pu1);
-      pg0 = dot8i(cg1.z, xw[6], pg0);
-      pg1 = dot8i(cg1.w, xw[7], pg1);
-      pu0 = dot8i(cu1.z, xw[6], pu0);
-      pu1 = dot8i(cu1.w, xw[7], pu1);
-      const uint32_t sbg = reinterpret_cast<const uint32_t*>(ub + d)[g];
-      const uint32_t sbu = reinterpret_cast<const uint32_t*>(ub + d + d / 16)[g];
-      ag[t] += s_of(sbg) * (sc * (float)(pg0 + pg1)) + b_of(sbg) * X;
-      au[t] += s_of(sbu) * (sc * (float)(pu0 + pu1)) + b_of(sbu) * X;
+    for (int t = 0; t < NTOK; ++t) {
+      if (!((tmask >> t) & 1u)) continue;
+      const uint4* xt = xq + t * xstride;
+      uint4 xw[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) xw[m] = xt[m * ng + g];
+      const float sc = xsc[t * sstride + g], X = xg[t * sstride + g];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint4 cg0 = cw[u][0], cg1 = cw[u][1], cu0 = cw[u][2], cu1 = cw[u][3];
+        int pg0 = dot8i(cg0.x, xw[0], 0), pg1 = dot8i(cg0.y, xw[1], 0);
+        int pu0 = dot8i(cu0.x, xw[0], 0), pu1 = dot8i(cu0.y, xw[1], 0);
+        pg0 = dot8i(cg0.z, xw[2], pg0);
+        pg1 = dot8i(cg0.w, xw[3], pg1);
+        pu0 = dot8i(cu0.z, xw[2], pu0);
+        pu1 = dot8i(cu0.w, xw[3], pu1);
+        pg0 = dot8i(cg1.x, xw[4], pg0);
+        pg1 = dot8i(cg1.y, xw[5], pg1);
+        pu0 = dot8i(cu1.x, xw[4], pu0);
+        pu1 = dot8i(cu1.y, xw[5], pu1);
+        pg0 = dot8i(cg1.z, xw[6], pg0);
+        pg1 = dot8i(cg1.w, xw[7], pg1);
+        pu0 = dot8i(cu1.z, xw[6], pu0);
+        pu1 = dot8i(cu1.w, xw[7], pu1);
+        acc[t][2 * u] += s_of(sbg[u]) * (sc * (float)(pg0 + pg1)) + b_of(sbg[u]) * X;
+        acc[t][2 * u + 1] += s_of(sbu[u]) * (sc * (float)(pu0 + pu1)) + b_of(sbu[u]) * X;
+      }
     }
   }
 }
@@ -656,7 +684,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       unsigned pend = 0;
 #pragma unroll
       for (int q = 0; q < kPCopies; ++q) {
-        const unsigned want = (G > q) ? (unsigned)((G - q + kPCopies - 1) / kPCopies) : 0u;
+        const unsigned want = ((G > q) ? (unsigned)((G - q + kPCopies - 1) / kPCopies) : 0u) +
+                              ((q == 0 && p.unset_flag) ? 1u : 0u);
         if ((unsigned)(w[q] >> kCountShift) != want) pend |= 1u << q;
       }
       const bool opend = ow && ((ow->x >> 16) != otag || (ow->y >> 16) != otag ||
@@ -785,7 +814,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int e = E + tid; e < nch * 32; e += kDecThreads) keys[e] = 0ull;
     for (int i = tid; i < nch * k; i += kDecThreads) cand[i] = 0ull;
     if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
-    cta_topk(keys, cand, E, k, sel_e, tid);
+    cta_topk(keys, cand, E, k, 1, sel_e, tid);
     if (c < NB && !pre) {
       if (lane == 0) issue_gu(c, W);
       if (tid == kDnTid) issue_dn(c, W);
@@ -840,11 +869,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       ph_gu ^= 1;
       {
         const uint8_t* ub0 = gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit;
-        float ag[2], au[2];
-        gateup_pair(ub0, gu_unit, d, ng, xq, xsc, xg, lane, ag, au);
+        float acc[1][4];
+        gateup_rows<1>(ub0, gu_unit, d, ng, xq, xsc, xg, 0, 0, 1u, lane, acc);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const float gv = warp_sum(ag[t]) * r, uv = warp_sum(au[t]) * r;
+          const float gv = warp_sum(acc[0][2 * t]) * r, uv = warp_sum(acc[0][2 * t + 1]) * r;
           if (lane == 0) hb[warp * kUnitsPerWarp + t] = gv / (1.0f + expf(-gv)) * uv;
         }
       }
@@ -999,11 +1028,12 @@ struct FewParams {
   unsigned long long* P;     // [T][kPCopies][E+1] counted router sums, zero at launch
   int* abort_flag;           // zero at launch
   int* err;
+  uint64_t wait_ns;          // a wait on another CTA or a copy gives up after this
 };
 
 struct FewSmem {
-  size_t xq, xsc, xg, gu, dnc, dnsb, rt, outs, lg, sel_e, sel_w, sig, umask, ubase, ulist,
-      uslot, hb, hpk, hsc, hsum, qt, red2, misc, infl, bars, total;
+  size_t xq, xsc, xg, gu, dnc, dnsb, rt, outs, lg, keys, cand, sel_e, sel_w, sig, umask, ubase,
+      ulist, uslot, hb, hpk, hsc, hsum, qt, red2, misc, infl, bars, total;
 };
 __host__ __device__ inline FewSmem few_smem(int T, int d, int E, int Ep, int nf_max) {
   FewSmem s;
@@ -1017,6 +1047,8 @@ __host__ __device__ inline FewSmem few_smem(int T, int d, int E, int Ep, int nf_
   s.rt = dec_take(o, (size_t)nf_max * Ep * 2, 128);
   s.outs = dec_take(o, (size_t)T * nf_max * 4, 16);
   s.lg = dec_take(o, (size_t)T * (E + 1) * 4, 16);
+  s.keys = dec_take(o, (size_t)T * ((E + 31) / 32) * 32 * 8, 16);
+  s.cand = dec_take(o, (size_t)T * ((E + 31) / 32) * kMaxK * 8, 16);
   s.sel_e = dec_take(o, (size_t)T * kMaxK * 4, 16);
   s.sel_w = dec_take(o, (size_t)T * kMaxK * 4, 16);
   s.sig = dec_take(o, (size_t)T * 4, 16);
@@ -1029,48 +1061,12 @@ __host__ __device__ inline FewSmem few_smem(int T, int d, int E, int Ep, int nf_
   s.hsc = dec_take(o, (size_t)T * 4, 16);
   s.hsum = dec_take(o, (size_t)T * 4, 16);
   s.qt = dec_take(o, (size_t)kFewMax * kBlk * 4, 16);
-  s.red2 = dec_take(o, (size_t)kRedChunks * 16 * 4, 16);
+  s.red2 = dec_take(o, (size_t)2 * kRedChunks * 16 * 4, 16);
   s.misc = dec_take(o, 16, 16);
   s.infl = dec_take(o, (kDecWarps + 2) * 4, 16);
   s.bars = dec_take(o, (kDecWarps + 2) * 8, 8);
   s.total = o;
   return s;
-}
-
-// Top-k of one token by one warp from its logits in shared memory (NaN taken
-// as -inf), ranked by (value descending, index ascending).  Lane l holds the
-// order keys of experts l + 32 j.  Each round every lane finds its best key
-// not yet taken (strictly larger wins: the lane's lowest index among equal
-// keys), then the warp maximum and the smallest expert index among the lanes
-// holding it name the round's winner.
-template <int VPL>
-__device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int* sel_e, int lane) {
-  uint32_t key[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    float v = (e < E) ? lg[e] : 0.0f;
-    if (v != v) v = -INFINITY;
-    key[j] = (e < E) ? ord_key(v) : 0u;  // 0: empty (every real key is larger)
-  }
-  for (int r = 0; r < k; ++r) {
-    uint32_t bk = 0u;
-    int bj = 0;
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const bool better = key[j] > bk;
-      bk = better ? key[j] : bk;
-      bj = better ? j : bj;
-    }
-    const uint32_t M = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t win =
-        __reduce_min_sync(0xffffffffu, bk == M ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
-    if ((int)(win & 31u) == lane) {
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) key[j] = (j == (int)(win >> 5)) ? 0u : key[j];
-    }
-    if (lane == 0) sel_e[r] = (int)win;
-  }
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_constant__ FewParams p) {
@@ -1089,6 +1085,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
   const uint16_t* rt_buf = reinterpret_cast<const uint16_t*>(dsm + L.rt);
   float* outs = reinterpret_cast<float*>(dsm + L.outs);  // [T][nf_max] owned input values
   float* lg = reinterpret_cast<float*>(dsm + L.lg);      // [T][E+1]; entry E: shared gate
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(dsm + L.keys);  // [T][nch*32]
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(dsm + L.cand);  // [T][nch*k]
   int* sel_e = reinterpret_cast<int*>(dsm + L.sel_e);    // [T][kMaxK]
   float* sel_w = reinterpret_cast<float*>(dsm + L.sel_w);
   float* sig = reinterpret_cast<float*>(dsm + L.sig);    // [T]
@@ -1171,14 +1169,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
     bulk_g2s(smem_u32(dsm + L.rt), W.w_rt + (long long)f0 * Ep, bytes, rt_bar);
   }
 
-  // ---- every token's activations -> quantised, and the owned features' values
-  for (int t = 0; t < T; ++t) {
-    const uint16_t* src = p.x + (long long)t * d;
-    for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
-      const int i0 = ib + 4 * tid;
-      const bool act = i0 < d;
-      uint2 raw = make_uint2(0u, 0u);
-      if (act) raw = __ldg(reinterpret_cast<const uint2*>(src + i0));
+  // ---- every token's activations -> quantised, and the owned features'
+  //      values (the loads of all tokens first)
+  for (int ib = 0; ib < d; ib += 4 * kDecThreads) {
+    const int i0 = ib + 4 * tid;
+    const bool act = i0 < d;
+    uint2 rawt[kFewMax];
+#pragma unroll
+    for (int t = 0; t < kFewMax; ++t)
+      rawt[t] = (act && t < T) ? __ldg(reinterpret_cast<const uint2*>(p.x + (long long)t * d + i0))
+                               : make_uint2(0u, 0u);
+#pragma unroll
+    for (int t = 0; t < kFewMax; ++t) {
+      if (t >= T) break;
+      const uint2 raw = rawt[t];
       const float v[4] = {bf16f(raw.x & 0xFFFFu), bf16f(raw.x >> 16), bf16f(raw.y & 0xFFFFu),
                           bf16f(raw.y >> 16)};
       quant_x4_into(v[0], v[1], v[2], v[3], i0, act, xq + (size_t)t * 8 * ng, xsc + t * ng,
@@ -1205,6 +1209,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
     bool range_err = false;
     for (int e = tid; e <= E; e += kDecThreads) {
       for (int t = 0; t < T; ++t) {
+        // the decode kernel's order: owned features in chunks of kMaxOwned
         const float* ot = outs + t * p.nf_max;
         float acc = 0.f;
         for (int fb = 0; fb < nf; fb += kMaxOwned) {
@@ -1288,7 +1293,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
         if (e < E) {
           if (p.bias) v += __ldg(p.bias + e);
           if (c == 0) p.logits[(long long)t * E + e] = v;
-          if (v != v) nan_seen = true;
+          float kv = v;
+          if (v != v) {
+            nan_seen = true;
+            kv = -INFINITY;
+          }
+          keys[t * 32 * ((E + 31) >> 5) + e] = ((unsigned long long)ord_key(kv) << 32) |
+                                                 (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
         }
         lg[t * (E + 1) + e] = v;
       }
@@ -1296,21 +1307,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
   }
   if (tid < kMaxE / 32) umask[tid] = 0u;
   for (int i = tid; i < kFewUnion * kFewMax; i += kDecThreads) uslot[i] = (int8_t)-1;
+  {
+    const int nkey = 32 * ((E + 31) >> 5);
+    for (int i = tid; i < T * nkey; i += kDecThreads)
+      if (i % nkey >= E) keys[i] = 0ull;
+    for (int i = tid; i < T * ((E + 31) >> 5) * k; i += kDecThreads) cand[i] = 0ull;
+  }
   if (__syncthreads_or(bad)) {
     drain();
     return;
   }
   if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
 
-  // ---- top-k, routing weights and shared gate of token t (warp t)
+  // ---- top-k of every token over the whole CTA; routing weights and shared
+  //      gate of token t by warp t
+  cta_topk(keys, cand, E, k, T, sel_e, tid);
   if (warp < T) {
     const float* lt = lg + warp * (E + 1);
-    int* se = sel_e + warp * kMaxK;
-    if (E <= 256)
-      warp_topk<8>(lt, E, k, se, lane);
-    else
-      warp_topk<16>(lt, E, k, se, lane);
-    __syncwarp();
+    const int* se = sel_e + warp * kMaxK;
     // softmax over the k chosen logits in double-float arithmetic (within
     // one ulp of fp64), as in the decode kernel
     const int my_e = (lane < k) ? se[lane] : 0;
@@ -1382,14 +1396,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
     ph_gu ^= 1;
     {
       const uint8_t* ub0 = gu_buf + (size_t)warp * kUnitsPerWarp * gu_unit;
+      // one token at a time (compact code: each phase of this kernel runs
+      // once per launch, so its instructions are fetched cold)
       for (unsigned m = tmask; m; m &= m - 1u) {
         const int t = __ffs(m) - 1;
-        float ag[2], au[2];
-        gateup_pair(ub0, gu_unit, d, ng, xq + (size_t)t * 8 * ng, xsc + t * ng, xg + t * ng, lane,
-                    ag, au);
+        float acc[1][4];
+        gateup_rows<1>(ub0, gu_unit, d, ng, xq + (size_t)t * 8 * ng, xsc + t * ng, xg + t * ng, 0,
+                       0, 1u, lane, acc);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const float gv = warp_sum(ag[q]), uv = warp_sum(au[q]);
+          const float gv = warp_sum(acc[0][2 * q]), uv = warp_sum(acc[0][2 * q + 1]);
           if (lane == 0) hb[t * kBlk + warp * kUnitsPerWarp + q] = gv / (1.0f + expf(-gv)) * uv;
         }
       }
@@ -1428,52 +1444,70 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
   }
 
   // ---- owned outputs of every token: the fixed-order sum of its partials
+  //      (the decode kernel's order), two tokens' loads in flight together
   const int npart = k1 * bpe;
-  for (int t = 0; t < T; ++t) {
-    const unsigned long long* pt = p.part + (long long)t * npart * d;
+  for (int t0 = 0; t0 < T; t0 += 2) {
+    const int nt = min(2, T - t0);
     for (int fl0 = 0; fl0 < nf; fl0 += 16) {
       const int fl = fl0 + (tid & 15), ch = tid >> 4;
-      float s = 0.f;
+      float s2[2] = {0.f, 0.f};
       if (fl < nf) {
-        const unsigned long long* pf = pt + f0 + fl;
-        for (int bp = ch; bp < npart && !bad; bp += kRedChunks * kPollMax) {
-          unsigned long long v[kPollMax];
+        const unsigned long long* pf[2];
 #pragma unroll
-          for (int i = 0; i < kPollMax; ++i) {
-            const int bb = bp + i * kRedChunks;
-            v[i] = (bb < npart) ? ld_relaxed_u64(pf + (long long)bb * d)
-                                : ((unsigned long long)ptag << 32);
-          }
-          uint64_t t0 = 0;
+        for (int tt = 0; tt < 2; ++tt)
+          pf[tt] = p.part + (long long)(t0 + (tt < nt ? tt : 0)) * npart * d + f0 + fl;
+        for (int bp = ch; bp < npart && !bad; bp += kRedChunks * kPollMax) {
+          unsigned long long v[2][kPollMax];
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int i = 0; i < kPollMax; ++i) {
+              const int bb = bp + i * kRedChunks;
+              v[tt][i] = (bb < npart && tt < nt) ? ld_relaxed_u64(pf[tt] + (long long)bb * d)
+                                                 : ((unsigned long long)ptag << 32);
+            }
+          uint64_t tw = 0;
           uint32_t n = 0;
           for (;;) {
             unsigned pend = 0;
 #pragma unroll
-            for (int i = 0; i < kPollMax; ++i)
-              if ((uint32_t)(v[i] >> 32) != ptag) pend |= 1u << i;
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+              for (int i = 0; i < kPollMax; ++i)
+                if ((uint32_t)(v[tt][i] >> 32) != ptag) pend |= 1u << (tt * kPollMax + i);
             if (!pend) break;
-            if (poll_give_up(p, t0, n)) {
+            if (poll_give_up(p, tw, n)) {
               bad = true;
               break;
             }
 #pragma unroll
-            for (int i = 0; i < kPollMax; ++i)
-              if ((pend >> i) & 1u) v[i] = ld_relaxed_u64(pf + (long long)(bp + i * kRedChunks) * d);
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+              for (int i = 0; i < kPollMax; ++i)
+                if ((pend >> (tt * kPollMax + i)) & 1u)
+                  v[tt][i] = ld_relaxed_u64(pf[tt] + (long long)(bp + i * kRedChunks) * d);
           }
 #pragma unroll
-          for (int i = 0; i < kPollMax; ++i)
-            if (bp + i * kRedChunks < npart) s += __uint_as_float((uint32_t)v[i]);
+          for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+            for (int i = 0; i < kPollMax; ++i)
+              if (bp + i * kRedChunks < npart) s2[tt] += __uint_as_float((uint32_t)v[tt][i]);
         }
       }
-      red2[ch * 16 + (tid & 15)] = s;
+      red2[ch * 16 + (tid & 15)] = s2[0];
+      red2[(kRedChunks + ch) * 16 + (tid & 15)] = s2[1];
       if (__syncthreads_or(bad)) {
         drain();
         return;
       }
-      if (tid < 16 && fl0 + tid < nf) {
-        float o = 0.f;
-        for (int q = 0; q < kRedChunks; ++q) o += red2[q * 16 + tid];
-        p.y[(long long)t * d + f0 + fl0 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      if (tid < 32) {
+        const int tt = tid >> 4, fo = tid & 15;
+        if (tt < nt && fl0 + fo < nf) {
+          float o = 0.f;
+          for (int q = 0; q < kRedChunks; ++q) o += red2[(tt * kRedChunks + q) * 16 + fo];
+          p.y[(long long)(t0 + tt) * d + f0 + fl0 + fo] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        }
       }
       __syncthreads();
     }
@@ -1567,6 +1601,8 @@ cudaError_t launch_decode(Handle* const* layers, int L, const uint16_t* x, const
                    : nullptr;
     p.tr_ns = (trace && trace->timestamps) ? trace->timestamps + (long long)l0 * 4 : nullptr;
     p.err = h0->dev_err;
+    p.wait_ns = h0->wait_ns;
+    p.unset_flag = h0->test_unset_flag;
     // the abort flag, the tagged outputs and the router sums start at zero
     cudaError_t e = cudaMemsetAsync(scr, 0, zero_bytes, st);
     if (e != cudaSuccess) return e;
@@ -1589,8 +1625,9 @@ size_t few_scratch_bytes(const Handle* h) {
 int few_max_tokens() { return kFewMax; }
 
 bool few_supported(const Handle* h, int T) {
-  if (T < 2 || T > kFewMax || !h->ws.few) return false;
   const moe_config& c = h->cfg;
+  // the logits go to the workspace's [max_tokens][E] rows
+  if (T < 2 || T > kFewMax || T > c.max_tokens || !h->ws.few) return false;
   const int G = h->num_sms;
   if ((G + kPCopies - 1) / kPCopies > kMaxPerCopy) return false;
   const int nf_max = (c.d + G - 1) / G;
@@ -1643,6 +1680,7 @@ cudaError_t launch_few(Handle* h, const uint16_t* x, int T, const float* bias, u
   p.P = P;
   p.abort_flag = abort_flag;
   p.err = h->dev_err;
+  p.wait_ns = h->wait_ns;
   cudaError_t e = cudaMemsetAsync(q, 0, zero_bytes, st);
   if (e != cudaSuccess) return e;
   void* args[] = {&p};

@@ -47,6 +47,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdlib>
+#include <type_traits>
 
 #include "moe_internal.h"
 #include "ptx.cuh"
@@ -380,6 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
   const int nmy = heavy ? q + 1 : q;  // this cluster's units
   const bool leader = !PAIR || crank == 0;  // issues the MMAs
 
+  // some token of the call has an activation scale s != 1 (gate/up epilogue)
+  const bool xscaled = (MODE == MMA_GATEUP) && p.xscaled && *p.xscaled != 0;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -763,12 +766,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       const int c1 = min(c0 + C::EPI_COLS, t.npad);
       // row data of the warp's 128 columns, fetched while the MMAs run:
       // lane l holds rows c0 + l + 32 v, v = 0..3
-      // (down: the routing weight and contribution row; gate/up: the power of
-      // two that scaled the row's fp16 activations)
+      // (down: the routing weight and contribution row; gate/up, when some
+      // token of the call was scaled: the power of two that scaled the row's
+      // fp16 activations)
       constexpr float kR0 = (MODE == MMA_GATEUP) ? 1.f : 0.f;
       float rsc4[4] = {kR0, kR0, kR0, kR0};
       int rdst4[4] = {0, 0, 0, 0};
-      if (MODE != MMA_ROUTER) {
+      if (MODE == MMA_DOWN || (MODE == MMA_GATEUP && xscaled)) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int n = c0 + lane + 32 * v;
@@ -787,98 +791,108 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       if (!warp_wait(S.acc_full(ab), aph, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t tacc = tmem + lane_base + C::NMAX * ab;
-      for (int n0 = c0; n0 < c1; n0 += 16) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tacc + n0, r0);
-        if (C::NA == 2) tmem_ld16(tacc + C::NMAX + n0, r1);
-        const int nvalid = min(16, t.nrows - n0);
-        // this chunk's rows n0..n0+15 are held by lanes (n0 - c0) % 32 + j
-        // in register slot (n0 - c0) / 32
-        const int vsel = (n0 - c0) >> 5;
-        const int lsel = (n0 - c0) & 31;
-        float rsc_v = rsc4[0];
-        int rdst_v = rdst4[0];
-#pragma unroll
-        for (int v = 1; v < 4; ++v) {
-          if (vsel == v) {
-            rsc_v = rsc4[v];
-            rdst_v = rdst4[v];
+      // SC: some token of the call was scaled (gate/up; a separate copy of the
+      // chunk loop, so that the usual case runs without the scaling)
+      auto chunks = [&](auto sc_tag) {
+        constexpr bool SC = decltype(sc_tag)::value;
+        for (int n0 = c0; n0 < c1; n0 += 16) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tacc + n0, r0);
+          if (C::NA == 2) tmem_ld16(tacc + C::NMAX + n0, r1);
+          const int nvalid = min(16, t.nrows - n0);
+          // this chunk's rows n0..n0+15 are held by lanes (n0 - c0) % 32 + j
+          // in register slot (n0 - c0) / 32
+          const int vsel = (n0 - c0) >> 5;
+          const int lsel = (n0 - c0) & 31;
+          float rsc_v = rsc4[0];
+          int rdst_v = rdst4[0];
+  #pragma unroll
+          for (int v = 1; v < 4; ++v) {
+            if (vsel == v) {
+              rsc_v = rsc4[v];
+              rdst_v = rdst4[v];
+            }
           }
-        }
-        const float rsc = __shfl_sync(0xffffffffu, rsc_v, (lsel + lane) & 31);
-        const long long rdst = __shfl_sync(0xffffffffu, rdst_v, (lsel + lane) & 31);
-        tmem_ld_wait();
-        if (MODE == MMA_ROUTER) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (j >= nvalid) break;
-            const int row = t.row0 + n0 + j;
-            const int ex = t.m * 256 + q * 32 + lane;
-            float* o = p.out_f32 + ((long long)t.ks * p.rows_total + row) * p.E;
-            if (ex < p.E) o[ex] = __uint_as_float(r0[j]);
-            if (ex + 128 < p.E) o[ex + 128] = __uint_as_float(r1[j]);
+          const float rsc = __shfl_sync(0xffffffffu, rsc_v, (lsel + lane) & 31);
+          const long long rdst = __shfl_sync(0xffffffffu, rdst_v, (lsel + lane) & 31);
+          tmem_ld_wait();
+          if (MODE == MMA_ROUTER) {
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j >= nvalid) break;
+              const int row = t.row0 + n0 + j;
+              const int ex = t.m * 256 + q * 32 + lane;
+              float* o = p.out_f32 + ((long long)t.ks * p.rows_total + row) * p.E;
+              if (ex < p.E) o[ex] = __uint_as_float(r0[j]);
+              if (ex + 128 < p.E) o[ex + 128] = __uint_as_float(r1[j]);
+            }
+            continue;
           }
-          continue;
-        }
-        // stage [16 rows][NSEG x 32 values] in shared memory, then 16-byte
-        // vector stores of whole 64-byte row segments
-        constexpr int NSEG = C::NSEG;
-        const uint32_t sbuf = S.stage(e, nst & 1);
-        __syncwarp();  // the buffer's previous reads are done
-        if (nvalid > 0) {
-          bool ovf = false;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float v0 = __uint_as_float(r0[j]);
+          // stage [16 rows][NSEG x 32 values] in shared memory, then 16-byte
+          // vector stores of whole 64-byte row segments
+          constexpr int NSEG = C::NSEG;
+          const uint32_t sbuf = S.stage(e, nst & 1);
+          __syncwarp();  // the buffer's previous reads are done
+          if (nvalid > 0) {
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float v0 = __uint_as_float(r0[j]);
+              if (MODE == MMA_GATEUP) {
+                const float v1 = __uint_as_float(r1[j]);
+                float h;
+                if constexpr (SC) {
+                  // The row's activations entered as x / s (s a power of two),
+                  // so the accumulators are v0 = g / s and v1 = u / s.  H holds
+                  // silu(g) u / s^2 = silu(s v0) * (v1 / s), bounded by |v0 v1|
+                  // (|silu(z)| <= |z|); the down projection's row weight carries
+                  // the s^2 back.
+                  const float ps = __shfl_sync(0xffffffffu, rsc, j);
+                  const float pinv = __int_as_float(0x7F000000 - __float_as_int(ps));  // 1/s, exact
+                  h = silu_tanh(v0 * ps) * (v1 * pinv);
+                } else {
+                  h = silu_tanh(v0) * v1;
+                }
+                st_shared_u16(sbuf + j * 64 + lane * 2, __half_as_ushort(__float2half_rn(h)));
+              } else {
+                const float sc = __shfl_sync(0xffffffffu, rsc, j);
+                st_shared_u16(sbuf + j * 64 * NSEG + lane * 2,
+                              __bfloat16_as_ushort(__float2bfloat16_rn(sc * v0)));
+                if (NSEG == 2)
+                  st_shared_u16(sbuf + j * 128 + 64 + lane * 2,
+                                __bfloat16_as_ushort(__float2bfloat16_rn(sc * __uint_as_float(r1[j]))));
+              }
+            }
+          }
+          __syncwarp();
+          // 16 rows x NSEG segments x four 16-byte pieces: piece pi = lane + 32 it
+  #pragma unroll
+          for (int it = 0; it < 2 * NSEG; ++it) {
+            const int pi = lane + 32 * it;
+            const int j = pi / (4 * NSEG);
+            const int seg = (pi >> 2) % NSEG;
+            const int part = pi & 3;
             if (MODE == MMA_GATEUP) {
-              // The row's activations entered as x / s (s a power of two), so
-              // the accumulators are v0 = g / s and v1 = u / s.  H holds
-              // silu(g) u / s^2 = silu(s v0) * (v1 / s), bounded by |v0 v1|
-              // (|silu(z)| <= |z|); the down projection's row weight carries
-              // the s^2 back.  s = 1 for activations within [2^-6, 2^6).
-              const float ps = __shfl_sync(0xffffffffu, rsc, j);
-              const float pinv = __int_as_float(0x7F000000 - __float_as_int(ps));  // 1/s, exact
-              const float v1 = __uint_as_float(r1[j]);
-              const float h = silu_tanh(v0 * ps) * (v1 * pinv);
-              ovf |= fabsf(h) >= 65520.0f;  // fp16 rounding would give inf
-              st_shared_u16(sbuf + j * 64 + lane * 2, __half_as_ushort(__float2half_rn(h)));
+              if (j < nvalid) {
+                const uint4 v = ld_shared_v4(sbuf + j * 64 + part * 16);
+                const long long row = t.row0 + n0 + j;
+                *reinterpret_cast<uint4*>(p.H + row * p.ldh + t.m * 128 + q * 32 + part * 8) = v;
+              }
             } else {
-              const float sc = __shfl_sync(0xffffffffu, rsc, j);
-              st_shared_u16(sbuf + j * 64 * NSEG + lane * 2,
-                            __bfloat16_as_ushort(__float2bfloat16_rn(sc * v0)));
-              if (NSEG == 2)
-                st_shared_u16(sbuf + j * 128 + 64 + lane * 2,
-                              __bfloat16_as_ushort(__float2bfloat16_rn(sc * __uint_as_float(r1[j]))));
+              const long long dj = __shfl_sync(0xffffffffu, rdst, j);
+              if (j < nvalid) {
+                const uint4 v = ld_shared_v4(sbuf + j * 64 * NSEG + seg * 64 + part * 16);
+                uint16_t* yr = p.Y + dj * p.ldy + t.m * (128 * NSEG) + seg * 128 + q * 32 + part * 8;
+                *reinterpret_cast<uint4*>(yr) = v;
+              }
             }
           }
-          if (MODE == MMA_GATEUP && __any_sync(0xffffffffu, ovf) && lane == 0)
-            atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
+          ++nst;
         }
-        __syncwarp();
-        // 16 rows x NSEG segments x four 16-byte pieces: piece pi = lane + 32 it
-#pragma unroll
-        for (int it = 0; it < 2 * NSEG; ++it) {
-          const int pi = lane + 32 * it;
-          const int j = pi / (4 * NSEG);
-          const int seg = (pi >> 2) % NSEG;
-          const int part = pi & 3;
-          if (MODE == MMA_GATEUP) {
-            if (j < nvalid) {
-              const uint4 v = ld_shared_v4(sbuf + j * 64 + part * 16);
-              const long long row = t.row0 + n0 + j;
-              *reinterpret_cast<uint4*>(p.H + row * p.ldh + t.m * 128 + q * 32 + part * 8) = v;
-            }
-          } else {
-            const long long dj = __shfl_sync(0xffffffffu, rdst, j);
-            if (j < nvalid) {
-              const uint4 v = ld_shared_v4(sbuf + j * 64 * NSEG + seg * 64 + part * 16);
-              uint16_t* yr = p.Y + dj * p.ldy + t.m * (128 * NSEG) + seg * 128 + q * 32 + part * 8;
-              *reinterpret_cast<uint4*>(yr) = v;
-            }
-          }
-        }
-        ++nst;
-      }
+      };
+      if (MODE == MMA_GATEUP && xscaled)
+        chunks(std::true_type{});
+      else
+        chunks(std::false_type{});
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

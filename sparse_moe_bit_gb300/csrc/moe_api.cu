@@ -246,6 +246,7 @@ moe_status run_experts(Handle* h, const uint16_t* x, int T, uint16_t* y, cudaStr
   p.xg = w.xp;
   p.perm = w.perm;
   p.row_xscale = w.xrow;
+  p.xscaled = reinterpret_cast<const int*>(w.ticket + 1);
   p.ldx = c.d;
   p.H = w.H;
   p.ldh = c.I;
@@ -322,6 +323,11 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, void* stream,
   if (!h) return fail(MOE_ERR_OOM, "host allocation");
   h->cfg = *cfg;
   h->layouts = cfg->layouts ? cfg->layouts : (MOE_LAYOUT_PREFILL | MOE_LAYOUT_DECODE);
+  if (const char* wl = getenv("MOE_WAIT_LIMIT_NS")) {
+    const long long v = atoll(wl);
+    if (v >= 100000 && v <= 10000000000ll) h->wait_ns = (uint64_t)v;
+  }
+  if (const char* uf = getenv("MOE_TEST_UNSET_FLAG")) h->test_unset_flag = atoi(uf) == 1;
   h->n_exp = cfg->E + (cfg->has_shared ? 1 : 0);
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);

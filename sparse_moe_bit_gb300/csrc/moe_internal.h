@@ -41,7 +41,8 @@ struct Workspace {
   float* xrow = nullptr;        // [Tmax*(k+1)] grouped row -> activation scale s
   int4* tiles = nullptr;        // [max_tiles] {expert, row0, nrows, npad}
   int32_t* ntiles = nullptr;    // [1]
-  unsigned* ticket = nullptr;   // [4]: [2], [3] the routing launch's grid barrier (zero between calls)
+  unsigned* ticket = nullptr;   // [4]: [2], [3] the routing launch's grid barrier (zero between calls);
+                                // [1]: some token of the call has an activation scale s != 1
   uint16_t* H = nullptr;        // [Tmax*(k+1)][I] fp16 SwiGLU activations
   uint16_t* Y = nullptr;        // [Tmax*(k+1)][d] bf16 weighted contributions
   int max_tiles = 0;
@@ -79,6 +80,12 @@ struct Handle {
   cudaEvent_t* prof_ev = nullptr;  // [kProfCalls][kStagesTimed + 1]
   int* dev_err = nullptr;
   unsigned dec_epoch = 0;  // decode launches so far (tags the exchanged partials)
+  // the decode kernels' waits on other CTAs give up after wait_ns (2 s;
+  // MOE_WAIT_LIMIT_NS at moe_create); test_unset_flag (MOE_TEST_UNSET_FLAG=1
+  // at moe_create, tests only) makes the decode kernel wait on a flag that
+  // nothing sets, so that the give-up path runs
+  uint64_t wait_ns = 2000000000ull;
+  int test_unset_flag = 0;
   cudaStream_t last_stream = nullptr;
 };
 
@@ -121,8 +128,10 @@ struct MmaParams {
   const int32_t* dst_row;
   const float* row_scale;
   // gate/up: per grouped row, the power of two s that divided its fp16
-  // activations (the epilogue undoes it)
+  // activations (the epilogue undoes it); xscaled: nonzero when some token of
+  // the call has s != 1 (otherwise the rows' scales are not read)
   const float* row_xscale;
+  const int* xscaled;
   int* err;
 };
 cudaError_t launch_grouped_mma(int mode, const MmaParams& p, int grid, cudaStream_t st);

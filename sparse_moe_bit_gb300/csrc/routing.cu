@@ -443,6 +443,7 @@ struct RouteParams {
   int32_t* dst;            // [T(k+1)] grouped row -> contribution row
   float* wrow;             // [T(k+1)] grouped row -> routing weight / gate (times s^2)
   float* xrow;             // [T(k+1)] grouped row -> activation scale s of its token
+  int* xscaled;            // set when some token of the call has s != 1
   int4* tiles;
   int32_t* ntiles;
   uint16_t* xp;            // fp16 [T][d]
@@ -505,6 +506,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
     __syncthreads();
   }
   for (int e = tid; e < E; e += blockDim.x) p.hist[(long long)b * E + e] = cnt[e];
+  if (b == 0 && tid == 0 && p.x) *p.xscaled = 0;  // set in step 4, after the barrier
   route_grid_sync(p.bar, p.err);
 
   // ---- 2. per expert: this block's base (the counts of the blocks before
@@ -594,49 +596,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
   // rounding), else 2^(floor(log2 max) - 1), which brings the largest value
   // into [2, 4); log2 s is clamped to [-60, 60].  The gate/up epilogue and
   // the row weights of the down projection (times s^2) undo it exactly.
-  for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
-    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (long long)t * p.d);
-    uint4* xo = reinterpret_cast<uint4*>(p.xp + (long long)t * p.d);
-    float dot = 0.0f, amax = 0.0f;
+  // One pass converts with s = 1 while finding the largest magnitude; a
+  // token that needs another s is converted again.
+  auto convert = [&](const uint4* xr, uint4* xo, float inv, float* amax, float* dot) {
     for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 4) {
       uint4 raw[4];  // the lane's loads issued together
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = c0 + 32 * i;
-        if (c >= p.d / 8) break;
-        const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[q] << 16)),
-                                   fabsf(__uint_as_float(wv[q] & 0xFFFF0000u))));
-        if (p.has_shared) {
-          const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.w_sg) + c);
-          const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), dot);
-            dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
-                       dot);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    int ex = 0;  // log2 s
-    if (amax > 0.0f && (amax < 0.015625f || amax >= 64.0f)) {
-      ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 128;  // floor(log2 max) - 1
-      ex = min(max(ex, -60), 60);
-    }
-    const float s_t = __int_as_float((127 + ex) << 23);
-    const float inv = __int_as_float((127 - ex) << 23);
-    if (lane == 0 && !(amax * inv < 65520.0f) && amax == amax) atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
-    for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 4) {
-      uint4 raw[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
@@ -648,13 +612,46 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
         uint32_t hv[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(wv[q] << 16) * inv;
-          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u) * inv;
-          const __half2 h2 = __floats2half2_rn(lo, hi);
+          const float lo = __uint_as_float(wv[q] << 16);
+          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
+          if (amax) *amax = fmaxf(*amax, fmaxf(fabsf(lo), fabsf(hi)));
+          const __half2 h2 = __floats2half2_rn(lo * inv, hi * inv);
           hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
         }
         xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        if (dot && p.has_shared) {
+          const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.w_sg) + c);
+          const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            *dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), *dot);
+            *dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
+                        *dot);
+          }
+        }
       }
+    }
+  };
+  for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (long long)t * p.d);
+    uint4* xo = reinterpret_cast<uint4*>(p.xp + (long long)t * p.d);
+    float dot = 0.0f, amax = 0.0f;
+    convert(xr, xo, 1.0f, &amax, &dot);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int ex = 0;  // log2 s
+    if (amax > 0.0f && (amax < 0.015625f || amax >= 64.0f)) {
+      ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 128;  // floor(log2 max) - 1
+      ex = min(max(ex, -60), 60);
+    }
+    const float s_t = __int_as_float((127 + ex) << 23);
+    const float inv = __int_as_float((127 - ex) << 23);
+    if (lane == 0 && !(amax * inv < 65520.0f) && amax == amax) atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
+    if (ex != 0) {
+      __syncwarp();  // the first pass's stores of this row are done (same lanes)
+      convert(xr, xo, inv, nullptr, nullptr);
+      if (lane == 0) atomicOr(p.xscaled, 1);
     }
     // the token's rows: the scale for the gate/up epilogue, s^2 into the
     // row weights of the down projection (rows written in step 3 by this block)
@@ -683,11 +680,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
 // are issued before the sum.  K1 > 0: exactly K1 rows per token (registers
 // for K1 loads only, so more blocks are resident); K1 = 0: any k1 up to
 // kMaxK + 1.  Persistent blocks stride over the tokens (no partial last wave).
+// A non-finite output (an intermediate beyond fp16's range on the way: the
+// prefill path's H is fp16) sets MOE_DEVERR_FP16_RANGE.
 template <int K1>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y, int k1,
-                                                     int d, int T, uint16_t* __restrict__ out) {
+                                                     int d, int T, uint16_t* __restrict__ out,
+                                                     int* __restrict__ err) {
   constexpr int NR = K1 > 0 ? K1 : kMaxK + 1;
   const int nr = K1 > 0 ? K1 : k1;
+  bool bad = false;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -712,10 +713,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
       for (int q = 0; q < 4; ++q) {
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
         o[q] = *reinterpret_cast<const uint32_t*>(&b2);
+        bad |= !(fabsf(acc[2 * q]) <= 3.4e38f) || !(fabsf(acc[2 * q + 1]) <= 3.4e38f);
       }
       *reinterpret_cast<uint4*>(out + (long long)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
+  if (bad) atomicOr(err, MOE_DEVERR_FP16_RANGE);
 }
 
 // Blocks of the fused routing launch: one per 32 tokens, at most as many as
@@ -776,6 +779,7 @@ cudaError_t launch_route(const Handle* h, const float* part, int KS, int T, cons
   p.dst = ws.dst;
   p.wrow = ws.wrow;
   p.xrow = ws.xrow;
+  p.xscaled = reinterpret_cast<int*>(ws.ticket + 1);
   p.tiles = ws.tiles;
   p.ntiles = ws.ntiles;
   p.xp = ws.xp;
@@ -807,9 +811,11 @@ cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st)
   const int threads = c.d / 8 < 256 ? c.d / 8 : 256;
   const int k1 = c.k + (c.has_shared ? 1 : 0);
   if (k1 == 9)
-    combine_kernel<9><<<combine_grid<9>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y);
+    combine_kernel<9><<<combine_grid<9>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y,
+                                                                          h->dev_err);
   else
-    combine_kernel<0><<<combine_grid<0>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y);
+    combine_kernel<0><<<combine_grid<0>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y,
+                                                                          h->dev_err);
   return cudaGetLastError();
 }
 
