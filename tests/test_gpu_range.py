@@ -18,6 +18,7 @@ import torch
 
 import sparse_moe_bit_gb300 as M
 from oracle import moe_oracle as O
+from synth import device as sd
 from synth import gen
 from tests.moe_cases import MID, HostCase, bits_to_dev, check_output, dev_to_bits
 
@@ -90,3 +91,38 @@ def test_prefill_flags_activations_beyond_its_scaling():
     case.moe.forward(x)
     torch.cuda.synchronize()
     assert case.moe.device_error() & M.MOE_DEVERR_FP16_RANGE
+
+
+def test_large_intermediates_flagged_on_prefill_exact_on_decode():
+    """Gate/up weights 1000 times N(0, 0.02)-scale make silu(gate)*up reach
+    ~1e5 and more: beyond fp16, which holds the prefill path's H, so the
+    prefill path reports MOE_DEVERR_FP16_RANGE (a non-finite output); the
+    decode path, which keeps H in fp32 and 16-bit integers with a
+    power-of-two scale per block, matches the oracle."""
+    from dataclasses import replace
+    lw = gen.make_layer(4, 0, MID)
+    big = dict(gu_scale=(lw.gu_scale.astype(np.float32) * 1000).astype(np.float16),
+               gu_bias=(lw.gu_bias.astype(np.float32) * 1000).astype(np.float16),
+               sh_gu_scale=(lw.sh_gu_scale.astype(np.float32) * 1000).astype(np.float16),
+               sh_gu_bias=(lw.sh_gu_bias.astype(np.float32) * 1000).astype(np.float16))
+    lw = replace(lw, **big)
+    vals = O.layer_values(lw)
+    w = sd.host_layer_to_device(lw)
+    bits = gen.make_x(12, 8, MID.d)
+    x = bits_to_dev(bits)
+    pf = M.MoE(M.MoEConfig(d=MID.d, E=MID.E, k=MID.k, I=MID.I, max_tokens=16,
+                           layouts=M.MOE_LAYOUT_PREFILL), w)
+    pf.forward(x)
+    torch.cuda.synchronize()
+    assert pf.device_error() & M.MOE_DEVERR_FP16_RANGE
+    dec = M.MoE(M.MoEConfig(d=MID.d, E=MID.E, k=MID.k, I=MID.I, max_tokens=16,
+                            layouts=M.MOE_LAYOUT_DECODE), w)
+    outs, lgs = [], []
+    for t in range(8):
+        y, tr = M.decode([dec], x[t], trace=True)
+        torch.cuda.synchronize()
+        outs.append(O.bf16_values(dev_to_bits(y)))
+        lgs.append(tr["logits"][0].cpu().numpy())
+    assert dec.device_error() == 0
+    ref = O.moe_layer(O.bf16_values(bits), vals, logits=np.stack(lgs))["out"]
+    check_output(np.stack(outs), ref, "decode, large intermediates")
