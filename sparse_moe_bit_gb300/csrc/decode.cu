@@ -77,6 +77,11 @@ constexpr int kRedChunks = 32;  // partial sums per owned feature in the reducti
 constexpr int kPollMax = 8;     // partials in flight per thread in one polling pass
 constexpr int kMaxOwned = 16;   // owned output features summed per pass (router sums)
 constexpr uint64_t kDrainNs = 100000000ull;
+// A wait looks at the abort flag (another CTA gave up) only once it has run
+// this long: the flag is a global load, one loaded L2 round trip (1-2 us while
+// the weights stream), which a wait that reads it at its first retry adds to
+// every exchange and copy it waits for.
+constexpr uint64_t kAbortCheckNs = 20000ull;
 
 struct DecLayer {
   const uint8_t* gu;     // [n_exp][I] units of d + d/8 bytes (gate, up codes; their s,b)
@@ -115,7 +120,7 @@ struct DecParams {
 
 // shared-memory carve-up (the host sizes the launch with the same function)
 struct DecSmem {
-  size_t xq, xsc, xg, gu, dnc, dnsb, hb, hpk, rt, outs, red2, lg, lb, keys, cand, sel_e, sel_w,
+  size_t xq, xsc, xg, xraw, gu, dnc, dnsb, hb, hpk, rt, outs, red2, lg, lb, keys, cand, sel_e, sel_w,
       misc, red, infl, bars, total;
 };
 __host__ __device__ inline size_t dec_take(size_t& o, size_t bytes, size_t align) {
@@ -131,6 +136,7 @@ __host__ __device__ inline DecSmem dec_smem(int d, int E, int Ep, int nf_max) {
   s.xq = dec_take(o, (size_t)d * 2, 16);
   s.xsc = dec_take(o, (size_t)(d / 64) * 4, 16);
   s.xg = dec_take(o, (size_t)(d / 64) * 4, 16);
+  s.xraw = dec_take(o, (size_t)d * 2, 16);
   s.gu = dec_take(o, (size_t)kBlk * (d + d / 8), 128);
   s.dnc = dec_take(o, (size_t)d * 16, 128);
   s.dnsb = dec_take(o, (size_t)d * 4, 128);
@@ -141,7 +147,7 @@ __host__ __device__ inline DecSmem dec_smem(int d, int E, int Ep, int nf_max) {
   s.red2 = dec_take(o, (size_t)kRedChunks * 16 * 4, 16);
   s.lg = dec_take(o, (size_t)(E + 1) * 4, 16);
   s.lb = dec_take(o, (size_t)E * 4, 16);
-  s.keys = dec_take(o, (size_t)nch * 32 * 8, 16);
+  s.keys = dec_take(o, (size_t)max(nch, 8) * 32 * 8, 16);   // >= 256 keys (small top-k)
   s.cand = dec_take(o, (size_t)nch * kMaxK * 8, 16);
   s.sel_e = dec_take(o, kMaxK * 4, 16);
   s.sel_w = dec_take(o, kMaxK * 4, 16);
@@ -261,19 +267,22 @@ __device__ __forceinline__ void red_add_u64(unsigned long long* a, unsigned long
 
 // Pacing of a poll on another CTA's data (each round is one L2 round trip;
 // no sleep: a sleeping poller measured up to ~2 us late); gives up (true)
-// when another CTA gave up or, recording the error, after p.wait_ns.
+// when another CTA gave up (looked at after kAbortCheckNs) or, recording the
+// error, after p.wait_ns.
 template <class PP>
 __device__ __forceinline__ bool poll_give_up(const PP& p, uint64_t& t0, uint32_t& n) {
   ++n;
   if ((n & 15u) == 1u) {
-    if (*(volatile int*)p.abort_flag) return true;
     const uint64_t t = globaltimer_ns();
     if (n == 1u) {
       t0 = t;
-    } else if (t - t0 > p.wait_ns) {
-      atomicOr(p.err, MOE_DEVERR_GRID_TIMEOUT);
-      atomicExch(p.abort_flag, 1);
-      return true;
+    } else if (t - t0 > kAbortCheckNs) {
+      if (*(volatile int*)p.abort_flag) return true;
+      if (t - t0 > p.wait_ns) {
+        atomicOr(p.err, MOE_DEVERR_GRID_TIMEOUT);
+        atomicExch(p.abort_flag, 1);
+        return true;
+      }
     }
   }
   return false;
@@ -325,6 +334,54 @@ __device__ __forceinline__ void cta_topk(const unsigned long long* keys, unsigne
   __syncthreads();
 }
 
+// Top-k of one token for E <= 256 in one warp, ranked like cta_topk.  Lane l
+// takes keys[8l .. 8l+7] (as cta_topk takes them, 0 past E) and sorts them
+// descending (Batcher's 19-comparator network); then k rounds: the largest
+// list head over the warp (a warp max of the heads' high words, the order key
+// of the logit; equal logits: the lowest lane holds the lowest expert index),
+// whose lane drops it.  A lane holds 8 experts, so it wins at most 8 rounds.
+// sel_e[r] for r < k (k <= 16); the caller synchronises before reading it.
+__device__ __forceinline__ void warp_topk256(const unsigned long long* keys, int k, int* sel_e,
+                                             int lane) {
+  unsigned long long s[8];
+  {
+    const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(keys + 8 * lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const ulonglong2 q = kp[i];
+      s[2 * i] = q.x;
+      s[2 * i + 1] = q.y;
+    }
+  }
+#define MOE_CE(a, b)                                  \
+  {                                                   \
+    const unsigned long long x_ = s[a], y_ = s[b];    \
+    const bool sw_ = x_ < y_;                         \
+    s[a] = sw_ ? y_ : x_;                             \
+    s[b] = sw_ ? x_ : y_;                             \
+  }
+  MOE_CE(0, 1) MOE_CE(2, 3) MOE_CE(4, 5) MOE_CE(6, 7)
+  MOE_CE(0, 2) MOE_CE(1, 3) MOE_CE(4, 6) MOE_CE(5, 7)
+  MOE_CE(1, 2) MOE_CE(5, 6)
+  MOE_CE(0, 4) MOE_CE(1, 5) MOE_CE(2, 6) MOE_CE(3, 7)
+  MOE_CE(2, 4) MOE_CE(3, 5)
+  MOE_CE(1, 2) MOE_CE(3, 4) MOE_CE(5, 6)
+#undef MOE_CE
+  int mine = 0;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t hi = (uint32_t)(s[0] >> 32);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t bal = __ballot_sync(0xffffffffu, hi == m);
+    const bool win = (bal & ((2u << lane) - 1u)) == (1u << lane);  // lowest lane with m
+    const int ew = __shfl_sync(0xffffffffu, (int)(0xFFFFFFFFu - (uint32_t)s[0]), __ffs(bal) - 1);
+    if (lane == r) mine = ew;
+#pragma unroll
+    for (int i = 0; i < 7; ++i) s[i] = win ? s[i + 1] : s[i];
+    s[7] = win ? 0ull : s[7];
+  }
+  if (lane < k) sel_e[lane] = mine;
+}
+
 // round(v * 2^32) as a 64-bit integer for |v| < 2^20, from 32-bit
 // conversions (the 64-bit ones are slow): x = v 2^32 is exact; its high part
 // floor(x / 2^24) and the remainder x - hi 2^24 (in [0, 2^24), exact) convert
@@ -351,8 +408,10 @@ __device__ __forceinline__ bool copy_wait(const PP& p, uint32_t bar, uint32_t pa
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t = globaltimer_ns();
+    if (t - t0 < kAbortCheckNs) continue;
     if (*(volatile int*)p.abort_flag) return false;
-    if (globaltimer_ns() - t0 > p.wait_ns) {
+    if (t - t0 > p.wait_ns) {
       atomicOr(p.err, MOE_DEVERR_WAIT_TIMEOUT);
       atomicExch(p.abort_flag, 1);
       return false;
@@ -506,6 +565,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   uint4* xq = reinterpret_cast<uint4*>(dsm + L.xq);   // [8 words][ng] packed int16 x
   float* xsc = reinterpret_cast<float*>(dsm + L.xsc);  // [ng] scale of a group of x
   float* xg = reinterpret_cast<float*>(dsm + L.xg);    // [ng] sum of a group of x
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(dsm + L.xraw);  // [d] previous output, bf16
   uint8_t* gu_buf = dsm + L.gu;                        // [32 units] of d + d/8 bytes
   const uint4* dnc = reinterpret_cast<const uint4*>(dsm + L.dnc);        // [d] block codes
   const uint32_t* dnsb = reinterpret_cast<const uint32_t*>(dsm + L.dnsb);  // [d] s,b words
@@ -771,7 +831,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         ss = fmaf(v1, v1, ss);
         ss = fmaf(v2, v2, ss);
         ss = fmaf(v3, v3, ss);
-        quant_x4(v0, v1, v2, v3, i0, act);
+        // quantised after the copies are issued (off the routing's path)
+        if (act)
+          *reinterpret_cast<uint2*>(xraw + i0) =
+              make_uint2(pack_lo16(raw.x, raw.y), pack_lo16(raw.z, raw.w));
       }
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
@@ -811,16 +874,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (c == 0) p.sigma[l] = sg;
       }
     }
-    for (int e = E + tid; e < nch * 32; e += kDecThreads) keys[e] = 0ull;
-    for (int i = tid; i < nch * k; i += kDecThreads) cand[i] = 0ull;
+    for (int e = E + tid; e < max(nch, 8) * 32; e += kDecThreads) keys[e] = 0ull;
+    if (E > 256)
+      for (int i = tid; i < nch * k; i += kDecThreads) cand[i] = 0ull;
     if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
-    cta_topk(keys, cand, E, k, 1, sel_e, tid);
+    if (E <= 256) {
+      if (warp == 0) warp_topk256(keys, k, sel_e, lane);
+      __syncthreads();
+    } else {
+      cta_topk(keys, cand, E, k, 1, sel_e, tid);
+    }
     if (c < NB && !pre) {
       if (lane == 0) issue_gu(c, W);
       if (tid == kDnTid) issue_dn(c, W);
     }
     pre = false;
     stamp(p, l, 1);
+    if (l > 0) {  // the previous output -> quantised activations
+      for (int ib = 0; ib < d; ib += 4 * kDecThreads) {  // whole warps (shuffles)
+        const int i0 = ib + 4 * tid;
+        const bool act = i0 < d;
+        uint2 raw = make_uint2(0u, 0u);
+        if (act) raw = *reinterpret_cast<const uint2*>(xraw + i0);
+        quant_x4(bf16f(raw.x & 0xFFFFu), bf16f(raw.x >> 16), bf16f(raw.y & 0xFFFFu),
+                 bf16f(raw.y >> 16), i0, act);
+      }
+      __syncthreads();
+    }
     if (warp == wwarp) {
       // routing weights (softmax over the k chosen logits in double-float
       // arithmetic, within one ulp of fp64), off the path of the copies and
