@@ -58,6 +58,7 @@
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "softmax_df.cuh"
+#include "topk_warp.cuh"
 
 namespace moe {
 namespace {
@@ -174,12 +175,6 @@ __device__ __forceinline__ float b_of(uint32_t sb) {
   return __half2float(__ushort_as_half((uint16_t)(sb >> 16)));
 }
 
-// order-preserving key of a float (larger value, larger key); -0 taken as +0
-__device__ __forceinline__ uint32_t ord_key(float v) {
-  if (v == 0.0f) v = 0.0f;
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (.lo) or bytes 2, 3 (.hi);
 // a signed 16-bit pairs, b unsigned bytes
@@ -332,54 +327,6 @@ __device__ __forceinline__ void cta_topk(const unsigned long long* keys, unsigne
       sel_e[tok * kMaxK + rank] = (int)(0xFFFFFFFFu - (uint32_t)my);
   }
   __syncthreads();
-}
-
-// Top-k of one token for E <= 256 in one warp, ranked like cta_topk.  Lane l
-// takes keys[8l .. 8l+7] (as cta_topk takes them, 0 past E) and sorts them
-// descending (Batcher's 19-comparator network); then k rounds: the largest
-// list head over the warp (a warp max of the heads' high words, the order key
-// of the logit; equal logits: the lowest lane holds the lowest expert index),
-// whose lane drops it.  A lane holds 8 experts, so it wins at most 8 rounds.
-// sel_e[r] for r < k (k <= 16); the caller synchronises before reading it.
-__device__ __forceinline__ void warp_topk256(const unsigned long long* keys, int k, int* sel_e,
-                                             int lane) {
-  unsigned long long s[8];
-  {
-    const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(keys + 8 * lane);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const ulonglong2 q = kp[i];
-      s[2 * i] = q.x;
-      s[2 * i + 1] = q.y;
-    }
-  }
-#define MOE_CE(a, b)                                  \
-  {                                                   \
-    const unsigned long long x_ = s[a], y_ = s[b];    \
-    const bool sw_ = x_ < y_;                         \
-    s[a] = sw_ ? y_ : x_;                             \
-    s[b] = sw_ ? x_ : y_;                             \
-  }
-  MOE_CE(0, 1) MOE_CE(2, 3) MOE_CE(4, 5) MOE_CE(6, 7)
-  MOE_CE(0, 2) MOE_CE(1, 3) MOE_CE(4, 6) MOE_CE(5, 7)
-  MOE_CE(1, 2) MOE_CE(5, 6)
-  MOE_CE(0, 4) MOE_CE(1, 5) MOE_CE(2, 6) MOE_CE(3, 7)
-  MOE_CE(2, 4) MOE_CE(3, 5)
-  MOE_CE(1, 2) MOE_CE(3, 4) MOE_CE(5, 6)
-#undef MOE_CE
-  int mine = 0;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t hi = (uint32_t)(s[0] >> 32);
-    const uint32_t m = __reduce_max_sync(0xffffffffu, hi);
-    const uint32_t bal = __ballot_sync(0xffffffffu, hi == m);
-    const bool win = (bal & ((2u << lane) - 1u)) == (1u << lane);  // lowest lane with m
-    const int ew = __shfl_sync(0xffffffffu, (int)(0xFFFFFFFFu - (uint32_t)s[0]), __ffs(bal) - 1);
-    if (lane == r) mine = ew;
-#pragma unroll
-    for (int i = 0; i < 7; ++i) s[i] = win ? s[i + 1] : s[i];
-    s[7] = win ? 0ull : s[7];
-  }
-  if (lane < k) sel_e[lane] = mine;
 }
 
 // round(v * 2^32) as a 64-bit integer for |v| < 2^20, from 32-bit
@@ -878,8 +825,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (E > 256)
       for (int i = tid; i < nch * k; i += kDecThreads) cand[i] = 0ull;
     if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
-    if (E <= 256) {
-      if (warp == 0) warp_topk256(keys, k, sel_e, lane);
+    if (E <= 256) {  // one warp: lane l takes experts 8l .. 8l+7
+      if (warp == 0) {
+        unsigned long long s8[8];
+        const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(keys + 8 * lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const ulonglong2 q = kp[i];
+          s8[2 * i] = q.x;
+          s8[2 * i + 1] = q.y;
+        }
+        const unsigned long long kw = warp_topk_lists(s8, k, lane);
+        if (lane < k) sel_e[lane] = (int)(0xFFFFFFFFu - (uint32_t)kw);
+      }
       __syncthreads();
     } else {
       cta_topk(keys, cand, E, k, 1, sel_e, tid);
@@ -1399,9 +1357,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) few_kernel(const __grid_consta
   }
   if (__syncthreads_or(nan_seen) && c == 0 && tid == 0) atomicOr(p.err, MOE_DEVERR_NAN_LOGIT);
 
-  // ---- top-k of every token over the whole CTA; routing weights and shared
-  //      gate of token t by warp t
-  cta_topk(keys, cand, E, k, T, sel_e, tid);
+  // ---- top-k of every token (up to 256 experts: warp t takes token t, lane l
+  //      experts 8l .. 8l+7; else over the whole CTA); routing weights and
+  //      shared gate of token t by warp t
+  if (E <= 256) {
+    if (warp < T) {
+      const int nkey = 32 * ((E + 31) >> 5);
+      const unsigned long long* kt = keys + warp * nkey;
+      unsigned long long s8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s8[i] = (8 * lane + i < nkey) ? kt[8 * lane + i] : 0ull;
+      const unsigned long long kw = warp_topk_lists(s8, k, lane);
+      if (lane < k) sel_e[warp * kMaxK + lane] = (int)(0xFFFFFFFFu - (uint32_t)kw);
+    }
+    __syncthreads();
+  } else {
+    cta_topk(keys, cand, E, k, T, sel_e, tid);
+  }
   if (warp < T) {
     const float* lt = lg + warp * (E + 1);
     const int* se = sel_e + warp * kMaxK;

@@ -84,7 +84,7 @@ void free_handle(Handle* h) {
   void* ptrs[] = {h->pf_gu, h->pf_dn, h->pf_router, h->dc_gu, h->dc_dn, h->dc_router_t,
                   h->w_router, h->w_sg, h->dev_err, h->ws.logit_part, h->ws.logits,
                   h->ws.idx, h->ws.w, h->ws.sigma, h->ws.xp, h->ws.hist, h->ws.base,
-                  h->ws.counts, h->ws.offsets, h->ws.perm, h->ws.slot, h->ws.dst, h->ws.wrow, h->ws.xrow,
+                  h->ws.counts, h->ws.offsets, h->ws.perm, h->ws.slot, h->ws.dst, h->ws.wrow, h->ws.xrow, h->ws.xtok,
                   h->ws.tiles, h->ws.ntiles, h->ws.ticket, h->ws.H, h->ws.Y, h->ws.few,
                   h->ws.x_dev, h->ws.y_dev,
                   h->ws.bias_dev};
@@ -166,6 +166,7 @@ moe_status alloc_all(Handle* h) {
   CK(dalloc(&w.dst, (size_t)T * k1 * 4), "alloc");
   CK(dalloc(&w.wrow, (size_t)T * k1 * 4), "alloc");
   CK(dalloc(&w.xrow, (size_t)T * k1 * 4), "alloc");
+  CK(dalloc(&w.xtok, (size_t)T * 4), "alloc");
   CK(dalloc(&w.tiles, (size_t)w.max_tiles * sizeof(int4)), "alloc");
   CK(dalloc(&w.ntiles, 16), "alloc");
   CK(dalloc(&w.ticket, 16), "alloc");

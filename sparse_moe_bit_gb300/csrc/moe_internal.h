@@ -39,6 +39,7 @@ struct Workspace {
   int32_t* dst = nullptr;       // [Tmax*(k+1)] grouped row -> contribution row
   float* wrow = nullptr;        // [Tmax*(k+1)] grouped row -> routing weight (times s^2)
   float* xrow = nullptr;        // [Tmax*(k+1)] grouped row -> activation scale s
+  float* xtok = nullptr;        // [Tmax] activation scale s of each token
   int4* tiles = nullptr;        // [max_tiles] {expert, row0, nrows, npad}
   int32_t* ntiles = nullptr;    // [1]
   unsigned* ticket = nullptr;   // [4]: [2], [3] the routing launch's grid barrier (zero between calls);

@@ -16,16 +16,10 @@
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "softmax_df.cuh"
+#include "topk_warp.cuh"
 
 namespace moe {
 namespace {
-
-// order-preserving key of a float (larger value, larger key); -0 taken as +0
-__device__ __forceinline__ uint32_t ord_key(float v) {
-  if (v == 0.0f) v = 0.0f;
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Top-k selection (topk_warp): the router's K-split partial logits are
 // summed in a fixed order, the bias added, and the top k kept by (logit
@@ -126,6 +120,95 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ part, int KS
   if (lane < k) {
     idx_out[(long long)t * k + lane] = my_e;
     s_vw[lane] = my_v;
+    atomicAdd(&cnt[my_e], 1);
+  }
+}
+
+// topk_warp for E <= 256 with lane l holding experts 8l .. 8l+7 (contiguous
+// loads; the ranking of warp_topk_lists): the same fixed-order sums, outputs
+// and counts.
+__device__ __forceinline__ void topk_warp8(const float* __restrict__ part, int KS, int T, int E,
+                                           int k, const float* __restrict__ bias,
+                                           float* __restrict__ logits,
+                                           int32_t* __restrict__ idx_out, int t, float* s_vw,
+                                           int* cnt, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int e0 = 8 * lane;
+  const bool vec = (E & 7) == 0;  // whole 32-byte groups: vector loads
+  float pa[8], ba[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    pa[i] = 0.0f;
+    ba[i] = 0.0f;
+  }
+  if (bias && e0 < E) {
+    if (vec) {
+      const float4 b0 = __ldg(reinterpret_cast<const float4*>(bias + e0));
+      const float4 b1 = __ldg(reinterpret_cast<const float4*>(bias + e0) + 1);
+      ba[0] = b0.x; ba[1] = b0.y; ba[2] = b0.z; ba[3] = b0.w;
+      ba[4] = b1.x; ba[5] = b1.y; ba[6] = b1.z; ba[7] = b1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ba[i] = (e0 + i < E) ? __ldg(bias + e0 + i) : 0.0f;
+    }
+  }
+  // the lane's loads of two splits at a time, then the sums in the fixed
+  // order 0 + part_0 + part_1 + ... + bias
+  for (int q0 = 0; q0 < KS; q0 += 2) {
+    float pq[2][8];
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      const float* src = part + ((long long)(q0 + qq) * T + t) * E + e0;
+      const bool on = q0 + qq < KS && e0 < E;
+      if (vec) {
+        const float4 a0 = on ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 a1 = on ? __ldg(reinterpret_cast<const float4*>(src) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        pq[qq][0] = a0.x; pq[qq][1] = a0.y; pq[qq][2] = a0.z; pq[qq][3] = a0.w;
+        pq[qq][4] = a1.x; pq[qq][5] = a1.y; pq[qq][6] = a1.z; pq[qq][7] = a1.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pq[qq][i] = (on && e0 + i < E) ? __ldg(src + i) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq)
+      if (q0 + qq < KS)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pa[i] += pq[qq][i];
+  }
+  bool nan_seen = false;
+  unsigned long long s8[8];
+  float lv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = e0 + i;
+    float s = 0.0f + pa[i];
+    if (bias) s += ba[i];
+    lv[i] = s;
+    if (s != s) {
+      nan_seen = true;
+      s = -INFINITY;
+    }
+    s8[i] = (e < E) ? (((unsigned long long)ord_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e))
+                    : 0ull;
+  }
+  float* lo = logits + (long long)t * E + e0;
+  if (vec) {
+    if (e0 < E) {
+      reinterpret_cast<float4*>(lo)[0] = make_float4(lv[0], lv[1], lv[2], lv[3]);
+      reinterpret_cast<float4*>(lo)[1] = make_float4(lv[4], lv[5], lv[6], lv[7]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (e0 + i < E) lo[i] = lv[i];
+  }
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, MOE_DEVERR_NAN_LOGIT);
+  const unsigned long long kw = warp_topk_lists(s8, k, lane);
+  if (lane < k) {
+    const int my_e = (int)(0xFFFFFFFFu - (uint32_t)kw);
+    idx_out[(long long)t * k + lane] = my_e;
+    s_vw[lane] = ord_value((uint32_t)(kw >> 32));
     atomicAdd(&cnt[my_e], 1);
   }
 }
@@ -443,6 +526,7 @@ struct RouteParams {
   int32_t* dst;            // [T(k+1)] grouped row -> contribution row
   float* wrow;             // [T(k+1)] grouped row -> routing weight / gate (times s^2)
   float* xrow;             // [T(k+1)] grouped row -> activation scale s of its token
+  float* xtok;             // [T] activation scale s of each token
   int* xscaled;            // set when some token of the call has s != 1
   int4* tiles;
   int32_t* ntiles;
@@ -451,30 +535,32 @@ struct RouteParams {
   int* err;
 };
 
-// Grid-wide barrier of a cooperative launch (every block resident).  Gives
-// up after kGridWaitNs, setting MOE_DEVERR_GRID_TIMEOUT (the results are then
-// wrong, but the kernel ends).
+// Grid-wide barrier of a cooperative launch (every block resident), passed
+// once per launch: a block adds its arrival to bar[0] without waiting for
+// the result and polls the count until every block has arrived (one L2 round
+// trip after the last arrival); bar[1] counts the blocks that have left, and
+// the last of them zeroes both for the next launch.  Gives up after
+// kGridWaitNs, setting MOE_DEVERR_GRID_TIMEOUT (the results are then wrong,
+// but the kernel ends).
 __device__ void route_grid_sync(unsigned* bar, int* err) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile unsigned* gen = bar + 1;
-    const unsigned g = *gen;
     __threadfence();
-    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-      atomicExch(bar, 0u);  // for the next launch
-      __threadfence();
-      atomicExch(bar + 1, g + 1);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (*gen == g) {
-        __nanosleep(100);
-        if (globaltimer_ns() - t0 > kGridWaitNs) {
-          atomicOr(err, MOE_DEVERR_GRID_TIMEOUT);
-          break;
-        }
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+      if (v >= gridDim.x) break;
+      if ((n & 63u) == 0 && globaltimer_ns() - t0 > kGridWaitNs) {
+        atomicOr(err, MOE_DEVERR_GRID_TIMEOUT);
+        break;
       }
     }
-    __threadfence();
+    if (atomicAdd(bar + 1, 1u) == gridDim.x - 1) {  // every block has left the wait
+      bar[0] = 0u;
+      bar[1] = 0u;
+    }
   }
   __syncthreads();
 }
@@ -488,6 +574,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
   __shared__ TileSmem tsm;
   __shared__ int s_before[kRouteThreads];  // partial column sums of the histogram
   __shared__ int s_all[kRouteThreads];
+  __shared__ int s_scaled;  // some token of this block has s != 1
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = p.T, E = p.E, k = p.k, G = gridDim.x, b = blockIdx.x;
   const int k1 = k + (p.has_shared ? 1 : 0);
@@ -496,34 +583,130 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
 
   // ---- 1. top-k of the block's tokens (one warp per token), weights, counts
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  if (tid == 0) s_scaled = 0;
   __syncthreads();
   for (int tb = t0; tb < t1; tb += kTokPerBlock) {
     const int t = tb + warp;
-    if (warp < kTokPerBlock && t < t1)
-      topk_warp<VPL>(p.part, p.KS, T, E, k, p.bias, p.logits, p.idx, t, s_v[warp], cnt, p.err);
+    if (warp < kTokPerBlock && t < t1) {
+      if constexpr (VPL == 8)
+        topk_warp8(p.part, p.KS, T, E, k, p.bias, p.logits, p.idx, t, s_v[warp], cnt, p.err);
+      else
+        topk_warp<VPL>(p.part, p.KS, T, E, k, p.bias, p.logits, p.idx, t, s_v[warp], cnt, p.err);
+    }
     __syncthreads();
     softmax_weights(tb, t1, k, s_v, p.w);
     __syncthreads();
   }
   for (int e = tid; e < E; e += blockDim.x) p.hist[(long long)b * E + e] = cnt[e];
-  if (b == 0 && tid == 0 && p.x) *p.xscaled = 0;  // set in step 4, after the barrier
-  route_grid_sync(p.bar, p.err);
+  if (b == 0 && tid == 0 && p.x) *p.xscaled = 0;  // set after the barrier
 
-  // ---- 2. per expert: this block's base (the counts of the blocks before
+  // ---- 2. the fp16 copy of the activations, from which the gate/up GEMM
+  // gathers its token rows (one warp per token), and the shared gate sigma =
+  // sigmoid(w_sg . x) on the way; before the barrier, which does not order
+  // it (it needs no routing), so that its loads overlap the barrier's wait.
+  // fp16 holds less range than bf16, so each token's row is divided by a
+  // power of two s first: s = 1 while the row's largest magnitude is in
+  // [2^-6, 2^6) (the usual activations: the copy is exact up to fp16
+  // rounding), else 2^(floor(log2 max) - 1), which brings the largest value
+  // into [2, 4); log2 s is clamped to [-60, 60].  The gate/up epilogue and
+  // the row weights of the down projection (times s^2, step 4) undo it
+  // exactly.  One pass converts with s = 1 while finding the largest
+  // magnitude; a token that needs another s is converted again.
+  if (p.x) {
+    // a lane's loads of a row are issued together, 4 at a time
+    auto convert = [&](const uint4* xr, uint4* xo, float inv, float* amax, float* dot) {
+      for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 4) {
+        uint4 raw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = c0 + 32 * i;
+          if (c >= p.d / 8) break;
+          const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          uint32_t hv[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(wv[q] << 16);
+            const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
+            if (amax) *amax = fmaxf(*amax, fmaxf(fabsf(lo), fabsf(hi)));
+            const __half2 h2 = __floats2half2_rn(lo * inv, hi * inv);
+            hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          if (dot && p.has_shared) {
+            const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.w_sg) + c);
+            const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              *dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), *dot);
+              *dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
+                          *dot);
+            }
+          }
+        }
+      }
+    };
+    for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
+      const uint4* xr = reinterpret_cast<const uint4*>(p.x + (long long)t * p.d);
+      uint4* xo = reinterpret_cast<uint4*>(p.xp + (long long)t * p.d);
+      float dot = 0.0f, amax = 0.0f;
+      convert(xr, xo, 1.0f, &amax, &dot);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      int ex = 0;  // log2 s
+      if (amax > 0.0f && (amax < 0.015625f || amax >= 64.0f)) {
+        ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 128;  // floor(log2 max) - 1
+        ex = min(max(ex, -60), 60);
+      }
+      const float s_t = __int_as_float((127 + ex) << 23);
+      const float inv = __int_as_float((127 - ex) << 23);
+      if (lane == 0 && !(amax * inv < 65520.0f) && amax == amax) atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
+      if (ex != 0) {
+        __syncwarp();  // the first pass's stores of this row are done (same lanes)
+        convert(xr, xo, inv, nullptr, nullptr);
+        if (lane == 0) s_scaled = 1;
+      }
+      if (lane == 0) p.xtok[t] = s_t;
+      if (p.has_shared) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        if (lane == 0) {
+          const float sg = 1.0f / (1.0f + expf(-dot));
+          p.sigma[t] = sg;
+          p.wrow[T * k + t] = sg * (s_t * s_t);
+          p.xrow[T * k + t] = s_t;
+        }
+      }
+    }
+  }
+  route_grid_sync(p.bar, p.err);
+  if (tid == 0 && s_scaled) atomicOr(p.xscaled, 1);
+
+  // ---- 3. per expert: this block's base (the counts of the blocks before
   // it) and the total.  Thread tid = part * E + e sums part `part` of the
-  // blocks' counts of expert e; one thread per expert adds the parts in order.
+  // blocks' counts of expert e (its loads issued together, kHistBatch at a
+  // time); one thread per expert adds the parts in order.
   {
+    constexpr int kHistBatch = 20;
     const int nparts = kRouteThreads / E;  // >= 2 (E <= kMaxE = 512)
     const int chunk = (G + nparts - 1) / nparts;
     const int part = tid / E, e = tid - part * E;
     if (part < nparts) {
       const int g0 = min(G, part * chunk), g1 = min(G, g0 + chunk);
       int before = 0, all = 0;
-#pragma unroll 8
-      for (int g = g0; g < g1; ++g) {
-        const int c = __ldcg(p.hist + (long long)g * E + e);
-        all += c;
-        before += (g < b) ? c : 0;
+      for (int gb = g0; gb < g1; gb += kHistBatch) {
+        int cv[kHistBatch];
+#pragma unroll
+        for (int i = 0; i < kHistBatch; ++i)
+          cv[i] = (gb + i < g1) ? __ldcg(p.hist + (long long)(gb + i) * E + e) : 0;
+#pragma unroll
+        for (int i = 0; i < kHistBatch; ++i) {
+          all += cv[i];
+          before += (gb + i < b) ? cv[i] : 0;
+        }
       }
       s_before[tid] = before;
       s_all[tid] = all;
@@ -542,7 +725,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
   const int off = block_exclusive_scan(tid < E ? tot : 0, tsm.warp_tot, &tsm.total);
   if (tid < E) {
     row0[tid] = off + base;
-    cnt[tid] = 0;  // running ranks of step 3
+    cnt[tid] = 0;  // running ranks of step 4
     mask[tid] = 0u;
   }
   if (b == 0) {
@@ -553,8 +736,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
   }
   __syncthreads();
 
-  // ---- 3. scatter, 32 tokens at a time: row of (t, j) with expert e =
-  // row0[e] + (tokens of this block before t that chose e)
+  // ---- 4. scatter, 32 tokens at a time: row of (t, j) with expert e =
+  // row0[e] + (tokens of this block before t that chose e); the row weight
+  // carries s^2 of its token, the row's activation scale s
   for (int tb = t0; tb < t1; tb += 32) {
     for (int a = tid; a < 32 * k; a += blockDim.x) {
       const int tl = a / k, t = tb + tl;
@@ -566,9 +750,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
       if (t < t1) {
         const int e = p.idx[(long long)t * k + j];
         const int row = row0[e] + cnt[e] + __popc(mask[e] & ((1u << tl) - 1u));
+        const float st = p.x ? p.xtok[t] : 1.0f;
         p.perm[row] = t;
         p.slot[(long long)t * k + j] = row;
-        p.wrow[row] = p.w[(long long)t * k + j];
+        p.wrow[row] = p.w[(long long)t * k + j] * (st * st);
+        if (p.x) p.xrow[row] = st;
         p.dst[row] = t * k1 + j;
       }
     }
@@ -583,93 +769,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(const __grid_co
     for (int t = t0 + tid; t < t1; t += blockDim.x) {
       p.perm[T * k + t] = t;
       p.dst[T * k + t] = t * k1 + k;
-    }
-  }
-  if (!p.x) return;
-
-  // ---- 4. the fp16 copy of the activations, from which the gate/up GEMM
-  // gathers its token rows (one warp per token); the shared gate
-  // sigma = sigmoid(w_sg . x) on the way.
-  // fp16 holds less range than bf16, so each token's row is divided by a
-  // power of two s first: s = 1 while the row's largest magnitude is in
-  // [2^-6, 2^6) (the usual activations: the copy is exact up to fp16
-  // rounding), else 2^(floor(log2 max) - 1), which brings the largest value
-  // into [2, 4); log2 s is clamped to [-60, 60].  The gate/up epilogue and
-  // the row weights of the down projection (times s^2) undo it exactly.
-  // One pass converts with s = 1 while finding the largest magnitude; a
-  // token that needs another s is converted again.
-  auto convert = [&](const uint4* xr, uint4* xo, float inv, float* amax, float* dot) {
-    for (int c0 = lane; c0 < p.d / 8; c0 += 32 * 4) {
-      uint4 raw[4];  // the lane's loads issued together
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c0 + 32 * i < p.d / 8) raw[i] = __ldg(xr + c0 + 32 * i);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = c0 + 32 * i;
-        if (c >= p.d / 8) break;
-        const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        uint32_t hv[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(wv[q] << 16);
-          const float hi = __uint_as_float(wv[q] & 0xFFFF0000u);
-          if (amax) *amax = fmaxf(*amax, fmaxf(fabsf(lo), fabsf(hi)));
-          const __half2 h2 = __floats2half2_rn(lo * inv, hi * inv);
-          hv[q] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        xo[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        if (dot && p.has_shared) {
-          const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.w_sg) + c);
-          const uint32_t sv[4] = {sg.x, sg.y, sg.z, sg.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            *dot = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(sv[q] << 16), *dot);
-            *dot = fmaf(__uint_as_float(wv[q] & 0xFFFF0000u), __uint_as_float(sv[q] & 0xFFFF0000u),
-                        *dot);
-          }
-        }
-      }
-    }
-  };
-  for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
-    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (long long)t * p.d);
-    uint4* xo = reinterpret_cast<uint4*>(p.xp + (long long)t * p.d);
-    float dot = 0.0f, amax = 0.0f;
-    convert(xr, xo, 1.0f, &amax, &dot);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    int ex = 0;  // log2 s
-    if (amax > 0.0f && (amax < 0.015625f || amax >= 64.0f)) {
-      ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 128;  // floor(log2 max) - 1
-      ex = min(max(ex, -60), 60);
-    }
-    const float s_t = __int_as_float((127 + ex) << 23);
-    const float inv = __int_as_float((127 - ex) << 23);
-    if (lane == 0 && !(amax * inv < 65520.0f) && amax == amax) atomicOr(p.err, MOE_DEVERR_FP16_RANGE);
-    if (ex != 0) {
-      __syncwarp();  // the first pass's stores of this row are done (same lanes)
-      convert(xr, xo, inv, nullptr, nullptr);
-      if (lane == 0) atomicOr(p.xscaled, 1);
-    }
-    // the token's rows: the scale for the gate/up epilogue, s^2 into the
-    // row weights of the down projection (rows written in step 3 by this block)
-    const float s2 = s_t * s_t;
-    if (lane < k) {
-      const int row = p.slot[(long long)t * k + lane];
-      p.xrow[row] = s_t;
-      p.wrow[row] *= s2;
-    }
-    if (p.has_shared) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      if (lane == 0) {
-        const float sg = 1.0f / (1.0f + expf(-dot));
-        p.sigma[t] = sg;
-        p.wrow[T * k + t] = sg * s2;
-        p.xrow[T * k + t] = s_t;
-      }
     }
   }
 }
@@ -779,6 +878,7 @@ cudaError_t launch_route(const Handle* h, const float* part, int KS, int T, cons
   p.dst = ws.dst;
   p.wrow = ws.wrow;
   p.xrow = ws.xrow;
+  p.xtok = ws.xtok;
   p.xscaled = reinterpret_cast<int*>(ws.ticket + 1);
   p.tiles = ws.tiles;
   p.ntiles = ws.ntiles;
