@@ -42,7 +42,8 @@
 // TMEM (512 columns): gate/up two 192-column accumulators (gate, up) and a
 // 2-stage A ring; down two 192-column accumulator buffers (the epilogue of a
 // unit overlaps the next one's MMAs) and a 2-stage A ring of two K blocks;
-// router two 256-column accumulators.  Every wait is bounded.
+// router two 128-column accumulators (token tiles of at most 128 rows) and
+// 4-stage A and B rings.  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -90,7 +91,7 @@ struct Cfg {
   static constexpr int NA = (MODE == MMA_DOWN) ? 1 : 2;
   static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
   static constexpr int NISS = NA;  // MMA-issuing threads (one per weight tile)
-  static constexpr int NMAX = TMEM_A ? kTileRows : 256;
+  static constexpr int NMAX = TMEM_A ? kTileRows : 128;  // router token tiles: <= 128 rows
   // KPS: 64-wide K blocks per pipeline stage.  The down projection (one
   // weight tile, 4 MMAs per K block, one issuing thread) was bound by the
   // issuer's per-stage work (two barrier tests, a commit); two K blocks per
@@ -102,7 +103,7 @@ struct Cfg {
   // bounds the pipeline, whose round trip (dequantise, signal, MMA, commit)
   // is longer than one K block's MMAs
   static constexpr int A_STAGES =
-      TMEM_A ? ((512 - A_COL0) / A_COLS < 8 ? (512 - A_COL0) / A_COLS : 8) : 2;
+      TMEM_A ? ((512 - A_COL0) / A_COLS < 8 ? (512 - A_COL0) / A_COLS : 8) : 4;
   static_assert(!TMEM_A || A_COL0 + A_STAGES * A_COLS <= 512, "TMEM budget");
   static_assert(TMEM_A || NA * NMAX <= 512, "TMEM budget");
   static constexpr int CST = (MODE == MMA_DOWN) ? 4 : (MODE == MMA_GATEUP ? 6 : 0);
@@ -110,7 +111,8 @@ struct Cfg {
   static constexpr int CODE_STAGE = CODE_KB * KPS;
   // B ring: up to NMAX token rows (a pair's CTA holds half of them) x 64 K
   // per K block (B_SUB bytes), KPS K blocks per stage
-  static constexpr int B_STAGES = PAIR ? (KPS == 2 ? 4 : 8) : (MODE == MMA_GATEUP ? 6 : 3);
+  static constexpr int B_STAGES =
+      PAIR ? (KPS == 2 ? 4 : 8) : (MODE == MMA_GATEUP ? 6 : (MODE == MMA_ROUTER ? 4 : 3));
   static constexpr int B_SUB = (PAIR ? NMAX / 2 : NMAX) * 128;
   static constexpr int B_STAGE = B_SUB * KPS;
   static constexpr int A_STAGE = TMEM_A ? 0 : NA * 16384;  // shared-memory A (router)
@@ -119,7 +121,7 @@ struct Cfg {
   static constexpr int NSEG = (MODE == MMA_DOWN) ? NA : 1;
   static constexpr int STAGE_BUF = 16 * 64 * NSEG;
   // columns of the accumulator taken by each of the two epilogue halves
-  static constexpr int EPI_COLS = TMEM_A ? NMAX / 2 : 128;
+  static constexpr int EPI_COLS = NMAX / 2;
   static_assert(EPI_COLS % 16 == 0 && EPI_COLS <= 128, "epilogue column split");
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + A_STAGES * A_STAGE;
