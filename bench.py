@@ -407,7 +407,7 @@ def run_gdn(args, torch, M, device):
     ops = gdn_alu_ops(GDN_T, shape.Hv, shape.dv, shape.dk)
     achieved = ops / (us * 1e-6) / 1e12
     peak = gdn_alu_peak(sm_count)
-    kv = profiled_traffic("gdn_scan_kernel")
+    kv = profiled_traffic("gdn_chunk_kernel")
     cpu = None
     if getattr(args, "world", 1) == 1:   # the fp64 oracle on the host, a bounded sample
         try:
@@ -429,8 +429,11 @@ def run_gdn(args, torch, M, device):
         "roofline": {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
                      "unit": "T fp32 lane-ops/s", "frac": round(achieved / peak, 4),
                      "traffic": int(kv["bytes_per_launch"]) if kv else None,
-                     "kernel": "gdn_scan_kernel",
+                     "kernel": "gdn_chunk_kernel",
                      "algorithmic_ops_per_launch": ops,
+                     "note": "achieved counts the token-by-token rule's 4 fp32 operations per "
+                             "state element and token; the kernel evaluates the rule in chunks "
+                             "of 32 tokens with its products on the tensor cores",
                      "peak_source": f"{sm_count} SMs x {FP32_LANES_PER_SM} fp32 lanes x "
                                     f"{SM_MAX_MHZ:.0f} MHz"},
         "algorithmic_bytes_per_launch": gdn_bytes(GDN_T, shape.Hk, shape.Hv, shape.dk,

@@ -84,10 +84,11 @@ def test_scan_parity_qwen_prompt_2k():
     _check_state(S.cpu().numpy().astype(np.float64), s_ref)
 
 
-def test_chunked_prompt_is_bit_identical():
+def test_prompt_split_over_two_calls():
     """Scanning a prompt in two calls, the state carried in place between
-    them, gives exactly the bits of one call: every token's arithmetic is
-    independent of where the call boundaries fall."""
+    them, matches one call within the parity bars (the tensor-core scan
+    evaluates chunks of 32 tokens from the start of each call, so the two
+    ways round differently; the token-by-token kernel gave the same bits)."""
     shape = gdn.GdnShape(2, 4, 128, 64)
     inp = gdn.make_inputs(5, [300], shape, state_std=0.05)
     d = _to_dev(inp)
@@ -98,8 +99,11 @@ def test_chunked_prompt_is_bit_identical():
         M.gdn_scan(d["q"][a:b], d["k"][a:b], d["v"][a:b], d["g"][a:b], d["beta"][a:b],
                    state=st, state_out=st, o=o2[a:b])
     torch.cuda.synchronize()
-    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
-    assert torch.equal(S1, st)
+    o_ref, s_ref = G.gdn_scan(inp.q, inp.k, inp.v, inp.g, inp.beta, state0=inp.state0)
+    _check_o(_bf16_values(o2), o_ref)
+    _check_state(st.cpu().numpy().astype(np.float64), s_ref)
+    _check_o(_bf16_values(o2), _bf16_values(o1))
+    _check_state(st.cpu().numpy().astype(np.float64), S1.cpu().numpy().astype(np.float64))
 
 
 def test_grouped_heads_match_repeated_heads():
