@@ -788,15 +788,15 @@ cudaError_t launch_gdn_scan(const GdnParams& p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(gdn_scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    gdn_scan_kernel<<<grid, kThreads, smem, st>>>(p);
-  } else {
+    return launch_kernel(gdn_scan_kernel, grid, dim3(kThreads), smem, st, p);
+  }
+  {
     const int smem = (int)sizeof(ChunkSmem);
     cudaError_t e = cudaFuncSetAttribute(gdn_chunk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    gdn_chunk_kernel<<<grid, kCThreads, smem, st>>>(p);
+    return launch_kernel(gdn_chunk_kernel, grid, dim3(kCThreads), smem, st, p);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe

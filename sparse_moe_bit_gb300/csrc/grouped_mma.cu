@@ -440,23 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     constexpr int kCst = C::CST > 0 ? C::CST : 1;
     constexpr int NW = (C::NA == 2) ? 8 : 4;  // code words of the row (8 values each)
     const int sc = g % kCst, sa = g % kAStages;
-    // A stage sa is free once the MMAs of K block g - A_STAGES have completed.
-    // Pairs: those MMAs' commit arrives only on the B slot's barrier; the B
-    // ring is deeper than the A ring and K block g + B_STAGES - A_STAGES
-    // cannot complete before this one is dequantised, so the slot's phase
-    // for g - A_STAGES is still the one the parity names.
-    bool free_ok;
-    if constexpr (PAIR) {
-      static_assert(C::B_STAGES > C::A_STAGES, "B ring deeper than the A ring");
-      const int gp = g - kAStages;
-      free_ok = gp < 0 || warp_wait(S.b_empty(gp % C::B_STAGES), (gp / C::B_STAGES) & 1,
-                                    abort_flag, p.err);
-    } else {
-      free_ok = warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err);
-    }
-    if (!warp_wait(S.c_full(sc), (g / kCst) & 1, abort_flag, p.err) || !free_ok) return false;
-    // the MMAs that read this A stage before have completed (a_empty)
-    tc_fence_after();
+    // The codes are loaded and dequantised into registers first, while the
+    // MMAs that still read A stage sa run: only the TMEM store waits for the
+    // stage, so the chain from those MMAs' commit to the next arrival on
+    // a_full is the store alone.
+    if (!warp_wait(S.c_full(sc), (g / kCst) & 1, abort_flag, p.err)) return false;
+    uint32_t v[C::KPS][4 * NW];  // column 4 i + j = K pair (8 i + 2 j, 8 i + 2 j + 1)
 #pragma unroll
     for (int k2 = 0; k2 < C::KPS; ++k2) {
       // row `row` of K block k2 of the ring stage: codes, then the s,b word
@@ -467,28 +456,48 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
       const uint32_t s2 = __byte_perm(sb, 0, 0x1010);
       const uint32_t b2 = __byte_perm(sb, 0, 0x3232);
       const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      uint32_t v[4 * NW];  // column 4 i + j = K pair (8 i + 2 j, 8 i + 2 j + 1)
 #pragma unroll
       for (int i = 0; i < NW; ++i) {
         const uint4 d4 = dequant_word(w[i], s2, b2);
-        v[4 * i] = d4.x;
-        v[4 * i + 1] = d4.y;
-        v[4 * i + 2] = d4.z;
-        v[4 * i + 3] = d4.w;
+        v[k2][4 * i] = d4.x;
+        v[k2][4 * i + 1] = d4.y;
+        v[k2][4 * i + 2] = d4.z;
+        v[k2][4 * i + 3] = d4.w;
       }
+    }
+    // the code stage is read (the loads above have returned their values)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(S.c_empty(sc));
+    // A stage sa is free once the MMAs of K block g - A_STAGES have completed.
+    // Pairs: those MMAs' commit arrives only on the B slot's barrier; the B
+    // ring is deeper than the A ring and K block g + B_STAGES - A_STAGES
+    // cannot complete before this one is dequantised, so the slot's phase
+    // for g - A_STAGES is still the one the parity names.
+    if constexpr (PAIR) {
+      static_assert(C::B_STAGES > C::A_STAGES, "B ring deeper than the A ring");
+      const int gp = g - kAStages;
+      if (gp >= 0 && !warp_wait(S.b_empty(gp % C::B_STAGES), (gp / C::B_STAGES) & 1, abort_flag,
+                                p.err))
+        return false;
+    } else {
+      if (!warp_wait(S.a_empty(sa), ((g / kAStages) & 1) ^ 1, abort_flag, p.err)) return false;
+    }
+    // the MMAs that read this A stage before have completed
+    tc_fence_after();
+#pragma unroll
+    for (int k2 = 0; k2 < C::KPS; ++k2) {
       // K block k2's columns follow block k2 - 1's (NA x 32 per block)
       const uint32_t ta =
           tmem + a_lane + C::A_COL0 + sa * C::A_COLS + k2 * (C::NA * 32) + a_off;
       if constexpr (NW == 8)
-        tmem_st32(ta, v);
+        tmem_st32(ta, v[k2]);
       else
-        tmem_st16(ta, v);
+        tmem_st16(ta, v[k2]);
     }
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(S.c_empty(sc));
       if (leader)
         mbar_arrive(S.a_full(sa));
       else

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "moe.h"
 
@@ -89,6 +90,20 @@ struct Handle {
   int test_unset_flag = 0;
   cudaStream_t last_stream = nullptr;
 };
+
+// Launches kern and returns that launch's own status (cudaGetLastError after a
+// <<<>>> launch would also report, and clear, an error left by an earlier,
+// unrelated launch).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = smem;
+  c.stream = st;
+  return cudaLaunchKernelEx(&c, kern, std::forward<Args>(args)...);
+}
 
 // row pitch (elements) of the decode router layout: E router columns, the
 // shared-gate column, zero padding to a 16-byte multiple

@@ -258,30 +258,34 @@ cudaError_t launch_repack(Handle* h, const moe_weights* w, cudaStream_t st) {
   const int grid = h->num_sms * 8;
   const ExpertSrc gu = make_src(w, c, true, h->dev_err);
   const ExpertSrc dn = make_src(w, c, false, h->dev_err);
+  cudaError_t e = cudaSuccess;
+  const dim3 G(grid), B(256);
   if (h->layouts & MOE_LAYOUT_PREFILL) {
-    repack_prefill_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.I / 128, 1, c.I, h->pf_gu);
-    repack_prefill_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, c.d / 256, 0, c.I, h->pf_dn);
-    repack_router_prefill_kernel<<<grid, 256, 0, st>>>((const uint16_t*)w->w_router, c.E, c.d,
-                                                       (c.E + 255) / 256, h->pf_router);
+    if ((e = launch_kernel(repack_prefill_kernel, G, B, 0, st, gu, h->n_exp, c.I / 128, 1, c.I,
+                           h->pf_gu)) != cudaSuccess ||
+        (e = launch_kernel(repack_prefill_kernel, G, B, 0, st, dn, h->n_exp, c.d / 256, 0, c.I,
+                           h->pf_dn)) != cudaSuccess ||
+        (e = launch_kernel(repack_router_prefill_kernel, G, B, 0, st, (const uint16_t*)w->w_router,
+                           c.E, c.d, (c.E + 255) / 256, h->pf_router)) != cudaSuccess)
+      return e;
   }
   if (h->layouts & MOE_LAYOUT_DECODE) {
-    repack_decode_gu_kernel<<<grid, 256, 0, st>>>(gu, h->n_exp, c.I, h->dc_gu);
-    repack_decode_dn_kernel<<<grid, 256, 0, st>>>(dn, h->n_exp, h->dc_dn);
-    repack_router_decode_kernel<<<grid, 256, 0, st>>>(
-        (const uint16_t*)w->w_router, c.has_shared ? (const uint16_t*)w->w_shared_gate : nullptr,
-        c.E, c.d, decode_router_pitch(c.E), h->dc_router_t);
+    if ((e = launch_kernel(repack_decode_gu_kernel, G, B, 0, st, gu, h->n_exp, c.I, h->dc_gu)) !=
+            cudaSuccess ||
+        (e = launch_kernel(repack_decode_dn_kernel, G, B, 0, st, dn, h->n_exp, h->dc_dn)) !=
+            cudaSuccess ||
+        (e = launch_kernel(repack_router_decode_kernel, G, B, 0, st, (const uint16_t*)w->w_router,
+                           c.has_shared ? (const uint16_t*)w->w_shared_gate : nullptr, c.E, c.d,
+                           decode_router_pitch(c.E), h->dc_router_t)) != cudaSuccess)
+      return e;
   }
-  cudaError_t e = cudaMemcpyAsync(h->w_router, w->w_router, (size_t)c.E * c.d * 2,
-                                  cudaMemcpyDeviceToDevice, st);
+  e = cudaMemcpyAsync(h->w_router, w->w_router, (size_t)c.E * c.d * 2, cudaMemcpyDeviceToDevice,
+                      st);
   if (e != cudaSuccess) return e;
-  if (c.has_shared) {
-    e = cudaMemcpyAsync(h->w_sg, w->w_shared_gate, (size_t)c.d * 2, cudaMemcpyDeviceToDevice, st);
-    if (e != cudaSuccess) return e;
-  } else {
-    e = cudaMemsetAsync(h->w_sg, 0, (size_t)c.d * 2, st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaGetLastError();
+  if (c.has_shared)
+    return cudaMemcpyAsync(h->w_sg, w->w_shared_gate, (size_t)c.d * 2, cudaMemcpyDeviceToDevice,
+                           st);
+  return cudaMemsetAsync(h->w_sg, 0, (size_t)c.d * 2, st);
 }
 
 }  // namespace moe

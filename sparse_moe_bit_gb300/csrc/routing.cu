@@ -911,12 +911,10 @@ cudaError_t launch_combine(const Handle* h, int T, uint16_t* y, cudaStream_t st)
   const int threads = c.d / 8 < 256 ? c.d / 8 : 256;
   const int k1 = c.k + (c.has_shared ? 1 : 0);
   if (k1 == 9)
-    combine_kernel<9><<<combine_grid<9>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y,
-                                                                          h->dev_err);
-  else
-    combine_kernel<0><<<combine_grid<0>(h, threads, T), threads, 0, st>>>(h->ws.Y, k1, c.d, T, y,
-                                                                          h->dev_err);
-  return cudaGetLastError();
+    return launch_kernel(combine_kernel<9>, dim3(combine_grid<9>(h, threads, T)), dim3(threads), 0,
+                         st, (const uint16_t*)h->ws.Y, k1, c.d, T, y, h->dev_err);
+  return launch_kernel(combine_kernel<0>, dim3(combine_grid<0>(h, threads, T)), dim3(threads), 0,
+                       st, (const uint16_t*)h->ws.Y, k1, c.d, T, y, h->dev_err);
 }
 
 
