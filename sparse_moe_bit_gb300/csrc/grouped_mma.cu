@@ -30,8 +30,9 @@
 // Warp roles (640 threads, one CTA per SM, persistent over the unit list):
 //   warp 0       B producer (TMA tiles, or the gate/up row gather) and, for
 //                the router, the A bulk copies
-//   warps 1, 3   lane 0 issues tcgen05.mma, one thread per weight tile (in a
-//                pair, the even CTA's); warp 1 owns the TMEM allocation
+//   warps 1, 3   issue tcgen05.mma (the whole warp runs the loop, one elected
+//                lane issues), one warp per weight tile (in a pair, the even
+//                CTA's); warp 1 owns the TMEM allocation
 //   warp 2       lane 0 issues the bulk copies of the code ring
 //   warps 4..11  dequantise the weight codes from the ring into fp16 A tiles
 //                in TMEM (gate/up one row per thread, every other K block;
@@ -632,11 +633,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
     }
   } else if (warp == 1 || (warp == 3 && C::NISS == 2)) {
     // ---------------------------------------------------------- MMA issuer
-    // With two weight tiles per unit, lane 0 of warp 1 issues tile 0's MMAs
-    // and lane 0 of warp 3 tile 1's: a single thread issues a tcgen05.mma
-    // no faster than one per ~56 cycles (measured), which bounded the small
-    // tiles; two issuers on separate accumulators overlap.
-    if (lane == 0 && leader) {
+    // With two weight tiles per unit, warp 1 issues tile 0's MMAs and warp 3
+    // tile 1's: two issuers on separate accumulators overlap.  The whole warp
+    // runs the loop (every wait and operand warp-uniform) and one elected
+    // lane issues each MMA and commit: issuing from one divergent lane cost
+    // ~100-150 cycles per MMA (per-K-block clock64 stamps), which bounded
+    // every tile narrower than ~256 columns.
+    if (leader) {
       const int q = (warp == 1) ? 0 : 1;  // this issuer's tile (two-tile units)
       uint32_t sa = 0, pa = 0, sb = 0, pb = 0;  // ring slots and phase parities
       Unit tn = get_unit(p, MODE, cunit(0) * CL + crank, kPad);
@@ -645,18 +648,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         if (i + 1 < nmy) tn = get_unit(p, MODE, cunit(i + 1) * CL + crank, kPad);
         const int ab = (C::NACC == 2) ? (int)(i & 1) : 0;
         const uint32_t aph = ((C::NACC == 2) ? (i >> 1) : i) & 1;
-        if (!thread_wait(S.acc_empty(ab), aph ^ 1, abort_flag, p.err)) break;
+        if (!warp_wait(S.acc_empty(ab), aph ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_f16(PAIR ? 256 : 128, t.npad, MODE == MMA_ROUTER ? 1 : 0);
         bool ok = true;
         for (int kb = 0; kb < kbs; ++kb) {
           // both operands' barriers tested at once (the two tests' latencies
-          // overlap; a test costs ~130 cycles even on a completed phase, and
-          // the issuing thread is the pipeline's bottleneck at small N)
+          // overlap), the outcome taken for the whole warp
           const bool ra = mbar_try_wait(S.a_full(sa), pa);
           const bool rb = mbar_try_wait(S.b_full(sb), pb);
-          if (!(ra && rb) && (!thread_wait(S.a_full(sa), pa, abort_flag, p.err) ||
-                              !thread_wait(S.b_full(sb), pb, abort_flag, p.err))) {
+          if (!__all_sync(0xffffffffu, ra && rb) &&
+              (!warp_wait(S.a_full(sa), pa, abort_flag, p.err) ||
+               !warp_wait(S.b_full(sb), pb, abort_flag, p.err))) {
             ok = false;
             break;
           }
@@ -678,41 +681,41 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   if constexpr (PAIR)
-                    tc_mma_f16_ts_pair(dcol, at + 8 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
+                    tc_mma_f16_ts_pair_w(dcol, at + 8 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
                   else
-                    tc_mma_f16_ts(dcol, at + 8 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
+                    tc_mma_f16_ts_w(dcol, at + 8 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
                 }
               } else {
                 const uint64_t ad = sdesc_k_sw128(S.a(sa) + j * 16384);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  tc_mma_f16(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
+                  tc_mma_f16_w(dcol, ad + 2 * kk, bd + 2 * kk, idesc, (acc | kk) ? 1u : 0u);
               }
             }
           }
           if constexpr (PAIR) {
             // one commit frees both stages: the dequantising warps wait on
             // the B slot's barrier (see dequant_kb)
-            tc_commit_pair_mc(S.b_empty(sb), 3);
+            tc_commit_pair_mc_w(S.b_empty(sb), 3);
           } else {
-            tc_commit(S.a_empty(sa));
-            tc_commit(S.b_empty(sb));
+            tc_commit_w(S.a_empty(sa));
+            tc_commit_w(S.b_empty(sb));
           }
           if (++sa == kAStages) { sa = 0; pa ^= 1; }
           if (++sb == (uint32_t)kBStages) { sb = 0; pb ^= 1; }
         }
         if (!ok) break;
         if constexpr (PAIR)
-          tc_commit_pair_mc(S.acc_full(ab), 3);
+          tc_commit_pair_mc_w(S.acc_full(ab), 3);
         else
-          tc_commit(S.acc_full(ab));
+          tc_commit_w(S.acc_full(ab));
       }
       // every issued MMA has finished before TMEM is released (in both CTAs
       // of a pair)
       if constexpr (PAIR)
-        tc_commit_pair_mc(S.drain(), 3);
+        tc_commit_pair_mc_w(S.drain(), 3);
       else
-        tc_commit(S.drain());
+        tc_commit_w(S.drain());
     }
     if (lane == 0) mbar_wait_bounded(S.drain(), 0, abort_flag, kWaitLimitNs);
   } else if (warp == 2 && MODE != MMA_ROUTER) {
