@@ -30,9 +30,9 @@
 // Warp roles (640 threads, one CTA per SM, persistent over the unit list):
 //   warp 0       B producer (TMA tiles, or the gate/up row gather) and, for
 //                the router, the A bulk copies
-//   warps 1, 3   issue tcgen05.mma (the whole warp runs the loop, one elected
-//                lane issues), one warp per weight tile (in a pair, the even
-//                CTA's); warp 1 owns the TMEM allocation
+//   warp 1       issues tcgen05.mma (the whole warp runs the loop, one
+//                elected lane issues; in a pair, the even CTA's) and owns the
+//                TMEM allocation
 //   warp 2       lane 0 issues the bulk copies of the code ring
 //   warps 4..11  dequantise the weight codes from the ring into fp16 A tiles
 //                in TMEM (gate/up one row per thread, every other K block;
@@ -91,7 +91,9 @@ struct Cfg {
   static constexpr bool TMEM_A = MODE != MMA_ROUTER;
   static constexpr int NA = (MODE == MMA_DOWN) ? 1 : 2;
   static constexpr int NACC = (MODE == MMA_DOWN) ? 2 : 1;
-  static constexpr int NISS = NA;  // MMA-issuing threads (one per weight tile)
+  // MMA-issuing warps: one.  (One per weight tile, on separate
+  // accumulators, was 1 % slower for gate/up once each warp issued warp-wide.)
+  static constexpr int NISS = 1;
   static constexpr int NMAX = TMEM_A ? kTileRows : 128;  // router token tiles: <= 128 rows
   // KPS: 64-wide K blocks per pipeline stage.  The down projection (one
   // weight tile, 4 MMAs per K block, one issuing thread) was bound by the
@@ -631,16 +633,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
         ++gb;
       }
     }
-  } else if (warp == 1 || (warp == 3 && C::NISS == 2)) {
+  } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // With two weight tiles per unit, warp 1 issues tile 0's MMAs and warp 3
-    // tile 1's: two issuers on separate accumulators overlap.  The whole warp
-    // runs the loop (every wait and operand warp-uniform) and one elected
-    // lane issues each MMA and commit: issuing from one divergent lane cost
-    // ~100-150 cycles per MMA (per-K-block clock64 stamps), which bounded
-    // every tile narrower than ~256 columns.
+    // The whole warp runs the loop (every wait and operand warp-uniform) and
+    // one elected lane issues each MMA and commit: issuing from one divergent
+    // lane cost ~100-150 cycles per MMA (per-K-block clock64 stamps).
     if (leader) {
-      const int q = (warp == 1) ? 0 : 1;  // this issuer's tile (two-tile units)
       uint32_t sa = 0, pa = 0, sb = 0, pb = 0;  // ring slots and phase parities
       Unit tn = get_unit(p, MODE, cunit(0) * CL + crank, kPad);
       for (int i = 0; i < nmy; ++i) {
@@ -672,7 +670,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mma_kernel(const __grid_c
             const uint32_t acc = (kb | k2) ? 1u : 0u;
 #pragma unroll
             for (int j = 0; j < C::NA; ++j) {
-              if (C::NISS == 2 && j != q) continue;
               // NA == 2: tile j -> columns NMAX j; NACC == 2: buffer ab -> columns NMAX ab
               const uint32_t dcol = tmem + C::NMAX * (C::NA == 2 ? j : ab);
               if constexpr (C::TMEM_A) {
